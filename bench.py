@@ -1,0 +1,382 @@
+#!/usr/bin/env python
+"""Throughput of one step of the A2ATS hot path on GB300.
+
+A step is one pass of the whole path over one batch of cached keys, each
+stage one C-ABI call of liba2ats.so: query second moment, Cholesky factor,
+windowed RoPE of the cache, retrieval split (proxy query), H-weighted
+assignment of the retrieval rows and plain nearest-centroid assignment of the
+bulk rows (the codebook transform runs inside the assignment calls).
+
+Default workload: one attention layer of a Llama-3.2-3B-shaped model
+(8 KV heads x 32768 cached keys x d=128, bf16; K=1024 centroids per head;
+H from 8192 calibration queries per head; window 512; retrieval fraction
+0.05), seeded synthetic data.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is keys assigned per second over all
+ranks with the inputs resident on the GPU; `e2e` repeats the measurement with
+the inputs copied from pinned host memory and the codes / split copied back
+inside the timed region.  The reference arm (`--impl reference`) times the
+fp64 CPU oracle on this machine's host cores on a bounded sample of the same
+workload.  Under torchrun each rank runs an independent replica of the
+workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of roofline"
+DEFAULT_WORKLOAD = "llama32_3b_layer"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        self.gpu = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _inputs(w, rank):
+    keys = synth.keys(w)
+    cb = synth.codebook(w)
+    queries = synth.queries(w) if (w.M and not w.h_given) else None
+    hg = synth.given_h(w) if w.h_given else None
+    return keys, cb, queries, hg
+
+
+def _work(w, count):
+    """Algorithmic work of each stage for one step (bytes or flops)."""
+    s = {"f32": 4, "bf16": 2, "f16": 2}[w.dtype]
+    keys = w.B * w.H * w.N
+    n_ret = int(count.sum())
+    n_bulk = keys - n_ret
+    return {
+        "second_moment": ("tensor", 2.0 * w.H * w.M * w.d * w.d),
+        "cholesky": ("alu", w.H * w.d ** 3 / 3.0),
+        "windowed_rope": ("hbm", keys * w.d * 2.0 * s),
+        "retrieval_split": ("hbm", keys * (w.d * s + 4.0)),
+        "assign_retrieval": ("tensor", n_ret * (2.0 * w.d * w.K + 2.0 * w.d * w.d)),
+        "assign_bulk": ("tensor", n_bulk * 2.0 * w.d * w.K),
+    }
+
+
+def run_ours(a):
+    import query_aware_vq_gb300 as q
+    from query_aware_vq_gb300.pipeline import A2ATSStep
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    keys, cb, queries, hg = _inputs(w, rank)
+    dt = synth.DTYPES[w.dtype]
+    step = A2ATSStep(w.B, w.H, w.N, w.d, w.K, dt, window=w.W, fraction=w.fraction,
+                     rope_base=w.rope_base, far_offset=w.far_offset, M=w.M, ridge=w.ridge,
+                     beta=w.betas[-1])
+    kd, cd = keys.cuda(), cb.cuda()
+    qd = queries.cuda() if queries is not None else None
+    hd = hg.cuda() if hg is not None else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(a.warmup):
+        step(kd, cd, queries=qd, h_given=hd)
+        flush.zero_()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps on resident inputs, L2 flushed between steps
+    events = {}
+    step_ev = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    t_wall = time.perf_counter()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(kd, cd, queries=qd, h_given=hd, events=events)
+        e1.record(stream)
+        step_ev.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    launches = q.kernel_launches() - launches0
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in step_ev]
+    ms = sum(step_ms) / len(step_ms)
+    ms = _max_over_ranks(ms, world)
+    keys_per_step = w.B * w.H * w.N
+    value = world * keys_per_step / (ms * 1e-3)
+    stage_ms = {k: sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in events.items()}
+
+    # ---- roofline of the dominant stage
+    hbm, bf16, src = _peaks()
+    work = _work(w, step.count.cpu())
+    dom = max(stage_ms, key=stage_ms.get)
+    bound, amount = work[dom]
+    sec = stage_ms[dom] * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = amount / sec / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = amount / sec / 1e12, bf16, "TFLOP/s"
+        bound = "tensor"
+    roof = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
+            "peak_source": f"{src} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'})"}
+    stages = {}
+    for k, v in stage_ms.items():
+        b, amt = work[k]
+        entry = {"ms": round(v, 4)}
+        if b == "hbm":
+            entry["GB/s"] = round(amt / (v * 1e-3) / 1e9, 1)
+        else:
+            entry["TFLOP/s"] = round(amt / (v * 1e-3) / 1e12, 3)
+        stages[k] = entry
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        hk = keys.pin_memory()
+        hc = cb.pin_memory()
+        hq = queries.pin_memory() if queries is not None else None
+        hh = hg.pin_memory() if hg is not None else None
+        out_codes = torch.empty(step.codes.shape, dtype=torch.int32).pin_memory()
+        out_perm = torch.empty(step.perm.shape, dtype=torch.int32).pin_memory()
+        out_count = torch.empty(step.count.shape, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hk, hc, hq, hh) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in (out_codes, out_perm, out_count))
+        e2e_ms = []
+        for i in range(a.warmup + a.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            kd.copy_(hk, non_blocking=True)
+            cd.copy_(hc, non_blocking=True)
+            if hq is not None:
+                qd.copy_(hq, non_blocking=True)
+            if hh is not None:
+                hd.copy_(hh, non_blocking=True)
+            step(kd, cd, queries=qd, h_given=hd)
+            out_codes.copy_(step.codes, non_blocking=True)
+            out_perm.copy_(step.perm, non_blocking=True)
+            out_count.copy_(step.count, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= a.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        em = _max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+        e2e = {"value": world * keys_per_step / (em * 1e-3), "unit": "keys/s",
+               "ms_per_step": round(em, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_baseline(w, keys, cb, queries, hg)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; correlated-Gaussian keys with outlier channels, "
+                    "queries and codebooks from the same generator; no model weights)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
+                       "M": w.M, "window": w.W, "fraction": w.fraction, "storage": w.dtype,
+                       "l2": "flushed between steps (256 MB write)",
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": roof, "stages": stages, "cpu_baseline": cpu, "clocks": clk,
+            "e2e": e2e, "gpu_launches": launches, "wall_s_timed": round(t_wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _oracle_sample(w, keys, cb, queries, hg, rows: int, h: int):
+    """One bounded sample of the workload on the oracle: the first `rows`
+    keys of head h (as a sequence of that length) through the whole step."""
+    import oracle
+    n = min(rows, w.N)
+    k = keys[0, h, :n]
+    L = None
+    if queries is not None:
+        hm = oracle.query_second_moment(queries[h], w.ridge)
+        L, _ = oracle.cholesky(hm.astype(np.float32).astype(np.float64))
+    elif hg is not None:
+        L, _ = oracle.cholesky(hg[h].double().numpy())
+    t0 = time.perf_counter()
+    oracle.pipeline_step(k, n - 1, cb[h], w.W, w.far_offset, w.rope_base, w.fraction, l=L,
+                         beta=w.betas[-1])
+    return n, time.perf_counter() - t0
+
+
+def cpu_baseline(w, keys, cb, queries, hg, rows: int = 8192, reps: int = 2):
+    n_done, t = 0, 0.0
+    for r in range(reps):
+        n, dt = _oracle_sample(w, keys, cb, queries, hg, rows, r % w.H)
+        n_done += n
+        t += dt
+    import oracle
+    return {"value": n_done / t, "unit": "keys/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} x the first {rows} keys of one head as a whole sequence "
+                      f"(all stages; calibration of L excluded from the time), fp64 C"}
+
+
+def run_reference(a):
+    rank, local, world = _dist()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[a.workload]
+    keys, cb, queries, hg = _inputs(w, rank)
+    rows = 4096
+    for i in range(a.warmup):
+        _oracle_sample(w, keys, cb, queries, hg, rows, i % w.H)
+    t, n_done, per = 0.0, 0, []
+    for i in range(a.steps):
+        n, dt = _oracle_sample(w, keys, cb, queries, hg, rows, i % w.H)
+        t += dt
+        n_done += n
+        per.append(dt)
+    value = n_done / t
+    import oracle
+    line = {
+        "metric": METRIC, "value": value, "unit": "keys/s", "impl": "reference",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(1e3 * t / a.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same generator)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K},
+        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": oracle.default_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: the first {rows} keys of one head as a whole "
+                                   "sequence through every stage, fp64 C oracle"},
+        "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)

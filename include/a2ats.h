@@ -1,0 +1,206 @@
+/*
+ * a2ats.h -- C ABI of the GB300 (sm_103a) library for the data-parallel hot path
+ * of A2ATS-style retrieval-based KV-cache compression: windowed RoPE, query
+ * second moment and its Cholesky factor, H-weighted and cosine-blend codebook
+ * assignment, and the retrieval-set split.
+ *
+ * Sources.  The operations follow the veloxquant-mlx documentation of its
+ * "A2ATS-adapted" method (after He et al., "A2ATS: Retrieval-Based KV Cache
+ * Reduction via Windowed Rotary Position Embedding and Query-Aware Vector
+ * Quantization", ACL 2025 Findings):
+ *   [API]  "veloxquant_mlx.quantizers.a2ats module" (readthedocs API page):
+ *          the five functions a2ats_query_second_moment, a2ats_cholesky_factor,
+ *          a2ats_h_weighted_assignment, a2ats_query_aware_assignment,
+ *          a2ats_select_retrieval_set;
+ *   [ALG]  "A2ATS-adapted" algorithm page (deploy-preview build), section
+ *          "For contributors -- paper fidelity": windowed RoPE (Eq. 11-12),
+ *          query-aware VQ (Eq. 13-18), per-step re-rotation;
+ *   [V039] the v0.39.0 algorithm page, "How it works" (steps 1-5).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array argument is DEVICE memory owned by the caller; the library
+ *   keeps no pointer after the call returns and allocates no device memory.
+ *   Calls that need scratch take a caller-owned `workspace` of at least the
+ *   size the matching *_workspace_size() function returns.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *   stream) and runs asynchronously: a call returns after enqueueing.
+ * - Keys are laid out [B, H, Ncap, d] row-major: B sequences, H heads,
+ *   Ncap cached rows of width d per (sequence, head).  Sequence b holds
+ *   len[b] valid rows (len: device int32 [B]; NULL means every row is
+ *   valid).  Row j of sequence b is at position j; its decode position is
+ *   t = len[b] - 1.  Rows j >= len[b] are neither read nor written.
+ * - Codebooks are [H, K, d] in the same dtype as the keys, shared by the
+ *   batch.  H and L matrices are [H, d, d] fp32 row-major.
+ * - Pointers to key, query, codebook and output arrays must be 16-byte
+ *   aligned; d must be a multiple of 8 with 8 <= d <= 256.
+ * - Return value: A2ATS_OK, or a negative a2ats_status found on the host
+ *   before anything is enqueued (bad argument, shape, dtype, alignment,
+ *   workspace), or A2ATS_ERR_CUDA when a launch fails
+ *   (a2ats_last_error() then gives CUDA's message).
+ * - Results are deterministic: the same inputs give the same bits.
+ */
+#ifndef A2ATS_H
+#define A2ATS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    A2ATS_OK = 0,
+    A2ATS_ERR_INVALID_ARG = -1, /* a parameter out of its range, or a NULL array */
+    A2ATS_ERR_SHAPE = -2,       /* sizes the kernels do not support */
+    A2ATS_ERR_DTYPE = -3,       /* dtype code not in a2ats_dtype */
+    A2ATS_ERR_ALIGN = -4,       /* an array not 16-byte aligned */
+    A2ATS_ERR_CUDA = -5,        /* a kernel launch failed */
+    A2ATS_ERR_WORKSPACE = -6    /* workspace NULL or smaller than required */
+} a2ats_status;
+
+typedef enum { A2ATS_F32 = 0, A2ATS_BF16 = 1, A2ATS_F16 = 2 } a2ats_dtype;
+
+/* Which rows an assignment call visits (routing of [V039] step 2). */
+typedef enum {
+    A2ATS_ROWS_ALL = 0,       /* rows 0 .. len-1 */
+    A2ATS_ROWS_RETRIEVAL = 1, /* rows perm[0 .. count-1] of a retrieval split */
+    A2ATS_ROWS_BULK = 2       /* rows perm[count .. len-1] of a retrieval split */
+} a2ats_rows;
+
+/* Windowed RoPE ([ALG] Eq. 11-12; [V039] step 4).  Row p with decode
+ * position t is rotated at its own position p when 0 <= t - p < window, and
+ * at the one shared position far_offset otherwise.  far_offset = 0 leaves far
+ * keys unrotated, which is the paper's Eq. 12.  window <= 0: every row is far;
+ * window >= len: every row is exact.  Pair i of d/2 is (i, i + d/2) when
+ * interleaved = 0 and (2i, 2i+1) otherwise; its angle is
+ * position * rope_base^(-2i/d).  Positions must stay below 2^24. */
+typedef struct {
+    int32_t window;
+    int32_t far_offset;
+    double rope_base;
+    int32_t interleaved;
+} a2ats_rope_params;
+
+/* --------------------------------------------------------------------------
+ * a2ats_windowed_rope -- [ALG] "Windowed RoPE (Eq. 11-12)" and "Per-step
+ * re-rotation": re-rotate every cached key against the current decode
+ * position.
+ *   k_in   [B, H, Ncap, d] in in_dtype (pre-RoPE keys)
+ *   k_out  [B, H, Ncap, d] in out_dtype; may alias k_in when the dtypes match
+ * Arithmetic is fp32; the fp32 output is within 1e-6 relative of the exact
+ * rotation, a bf16/fp16 output is the fp32 result rounded to nearest even.
+ * ------------------------------------------------------------------------ */
+int a2ats_windowed_rope(const void* k_in, int32_t in_dtype, void* k_out, int32_t out_dtype,
+                        int64_t B, int64_t H, int64_t Ncap, int64_t d, const int32_t* len,
+                        const a2ats_rope_params* rope, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_query_second_moment -- [API] a2ats_query_second_moment (paper Eq. 10):
+ *   H_h = (1/M) Q_h^T Q_h + ridge * I, not mean-centred.
+ *   queries [H, M, d] in dtype;  h_out [H, d, d] fp32, exactly symmetric.
+ * ridge >= 0 (the page's default is 1e-4).  M >= 1.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_query_second_moment_workspace_size(int64_t H, int64_t M, int64_t d);
+int a2ats_query_second_moment(const void* queries, int32_t dtype, int64_t H, int64_t M,
+                              int64_t d, double ridge, float* h_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_cholesky_factor -- [API] a2ats_cholesky_factor (paper Eq. 15):
+ * lower-triangular L with H = L L^T, per head.
+ *   h [H, d, d] fp32 (symmetric positive definite);  l_out [H, d, d] fp32
+ *   (zeros above the diagonal);  info [H] int32: 0, or j >= 1 when the
+ *   leading minor of order j of that head is not positive definite (L of that
+ *   head is then unspecified).  A non-PD input is reported, never trapped.
+ * ------------------------------------------------------------------------ */
+int a2ats_cholesky_factor(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
+                          void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_h_weighted_assign -- [API] a2ats_h_weighted_assignment (paper
+ * Eq. 14 through the Eq. 15-18 Cholesky identity):
+ *   code = argmin_j (k~ - c_j) H (k~ - c_j)^T = argmin_j |k~ L - c_j L|^2,
+ * ties to the lowest j.
+ *   x        [B, H, Ncap, d] in dtype: k~ itself, or pre-RoPE keys when
+ *            fused_rope != NULL (windowed RoPE is then applied on the fly)
+ *   codebook [H, K, d] in dtype (untransformed centroids)
+ *   L        [H, d, d] fp32 Cholesky factor; NULL = identity, which is plain
+ *            nearest-centroid VQ ([V039] step 2, bulk rows)
+ *   rows     which rows to assign; RETRIEVAL / BULK read perm [B, H, Ncap]
+ *            and count [B, H] as written by a2ats_select_retrieval_set
+ *   codes    [B, H, Ncap] int32; only the visited rows are written
+ * Exactness: the code equals the exact argmin except possibly on rows whose
+ * two best distances differ by less than 1e-5 of the second best.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_h_weighted_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                              int64_t K);
+int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                            int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                            const float* L, const a2ats_rope_params* fused_rope,
+                            int32_t rows, const int32_t* perm, const int32_t* count,
+                            int32_t* codes, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_query_aware_assign -- [API] a2ats_query_aware_assignment (cosine
+ * blend):  e_j = |x - c_j|^2,  m = max_j e_j,
+ *   score_j = -beta * e_j / m + (1 - beta) * cos(query, c_j),
+ *   code = argmax_j score_j (ties to the lowest j);  e_j / m is 0 when m = 0
+ *   and a cosine with a zero-norm vector is 0.  beta = 1 is exactly plain
+ *   nearest-centroid VQ (argmin_j e_j).
+ *   query  [B, H, d] in dtype, one query per (sequence, head); NULL = the
+ *          proxy query of [V039] honesty point 1: the key at the decode
+ *          position t after windowed RoPE (the same proxy the retrieval split
+ *          uses; with fused_rope == NULL, x at t as given).
+ *   beta in [0, 1]; other arguments as a2ats_h_weighted_assign.
+ * Exactness: the exact argmax except possibly on rows whose two best scores
+ * differ by less than 1e-5.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                               int64_t K);
+int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                             int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                             const void* query, double beta,
+                             const a2ats_rope_params* fused_rope, int32_t rows,
+                             const int32_t* perm, const int32_t* count, int32_t* codes,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_select_retrieval_set -- [API] a2ats_select_retrieval_set: per
+ * (sequence, head), score s_i = cos(k~_i, query) (0 when a norm is 0) and
+ * keep the top n_r = ceil(fraction * len) rows, ordered by (score desc,
+ * index asc), with fraction * len evaluated in IEEE double.
+ *   keys   [B, H, Ncap, d] in dtype: k~, or pre-RoPE keys with fused_rope
+ *   query  [B, H, d] in dtype; NULL = the proxy query: the key at the decode
+ *          position t as it stands after windowed RoPE
+ *   fraction in [0, 1] (the page's default is 0.2)
+ *   perm   [B, H, Ncap] int32: perm[0:n_r] the retrieval rows ascending,
+ *          perm[n_r:len] the bulk rows ascending (disjoint, covering 0..len-1)
+ *   count  [B, H] int32: n_r
+ * Exactness: the exact set except possibly for rows whose score is within
+ * 1e-5 of the n_r-th largest score; the set size is always exactly n_r.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_select_retrieval_set_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d);
+int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                               int64_t Ncap, int64_t d, const int32_t* len, const void* query,
+                               double fraction, const a2ats_rope_params* fused_rope,
+                               int32_t* perm, int32_t* count, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Number of kernels this library has enqueued since it was loaded, over all
+ * host threads (diagnostics: lets a caller count the launches of a region). */
+uint64_t a2ats_kernel_launches(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* a2ats_status_string(int32_t status);
+
+/* CUDA's message for the last A2ATS_ERR_CUDA returned on this host thread
+ * (static per-thread storage; "" when there was none). */
+const char* a2ats_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* A2ATS_H */

@@ -1,0 +1,291 @@
+"""Python binding of liba2ats.so -- the GB300 (sm_103a) library for the hot
+path of A2ATS-style retrieval-based KV-cache compression.
+
+Every function here has the name of the C entry point it wraps (see
+include/a2ats.h) and only marshals arguments: tensor pointers, sizes, the
+current CUDA stream, and a scratch workspace tensor when the caller gives none.
+All arithmetic runs in the library's CUDA kernels.  There is no CPU path: the
+functions raise when the library is missing or a tensor is not on a CUDA
+device.
+
+Layouts: keys [B, H, N, d] (a 2-D [N, d] array is taken as B = H = 1),
+codebooks [H, K, d], H / L matrices [H, d, d] fp32, per-(b, h) queries
+[B, H, d]; dtypes fp32, bf16 or fp16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liba2ats.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "a2ats.h")
+
+A2ATS_ROWS = {"all": 0, "retrieval": 1, "bulk": 2}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
+class A2ATSError(RuntimeError):
+    """A non-zero status from the library."""
+
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        name = _load().a2ats_status_string(status).decode()
+        super().__init__(f"{fn}: {name} ({status}){': ' + detail if detail else ''}")
+
+
+class RopeParams(ctypes.Structure):
+    """a2ats_rope_params: windowed RoPE (window, far_offset, base, pairing)."""
+
+    _fields_ = [("window", ctypes.c_int32), ("far_offset", ctypes.c_int32),
+                ("rope_base", ctypes.c_double), ("interleaved", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32, _I64, _D, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
+_SIGS = {
+    "a2ats_windowed_rope": [_P, _I32, _P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P],
+    "a2ats_query_second_moment_workspace_size": [_I64, _I64, _I64],
+    "a2ats_query_second_moment": [_P, _I32, _I64, _I64, _I64, _D, _P, _P, _SZ, _P],
+    "a2ats_cholesky_factor": [_P, _I64, _I64, _P, _P, _P],
+    "a2ats_h_weighted_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_h_weighted_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I32, _P,
+                                _P, _P, _P, _SZ, _P],
+    "a2ats_query_aware_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_query_aware_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _D, _P,
+                                 _I32, _P, _P, _P, _P, _SZ, _P],
+    "a2ats_select_retrieval_set_workspace_size": [_I64, _I64, _I64, _I64],
+    "a2ats_select_retrieval_set": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P, _P, _P,
+                                   _SZ, _P],
+    "a2ats_status_string": [_I32],
+    "a2ats_last_error": [],
+    "a2ats_kernel_launches": [],
+}
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/a2ats.h declares."""
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(a2ats_\w+)\s*\(", text)))
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m query_aware_vq_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        for name in ("a2ats_query_second_moment_workspace_size",
+                     "a2ats_h_weighted_assign_workspace_size",
+                     "a2ats_query_aware_assign_workspace_size",
+                     "a2ats_select_retrieval_set_workspace_size"):
+            getattr(lib, name).restype = ctypes.c_size_t
+        lib.a2ats_kernel_launches.restype = ctypes.c_uint64
+        lib.a2ats_status_string.restype = ctypes.c_char_p
+        lib.a2ats_last_error.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def library():
+    """The loaded ctypes handle of liba2ats.so."""
+    return _load()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(_load().a2ats_kernel_launches())
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        detail = _load().a2ats_last_error().decode() if status == -5 else ""
+        raise A2ATSError(fn, status, detail)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device (the library has no CPU path)")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _as4(k: torch.Tensor) -> torch.Tensor:
+    if k.dim() == 2:
+        return k.view(1, 1, *k.shape)
+    if k.dim() != 4:
+        raise ValueError("keys must be [N, d] or [B, H, N, d]")
+    return k
+
+
+def _rope(rope):
+    """None, a RopeParams, or a dict with window / far_offset / rope_base / interleaved."""
+    if rope is None or isinstance(rope, RopeParams):
+        return rope
+    return RopeParams(int(rope["window"]), int(rope.get("far_offset", 0)),
+                      float(rope.get("rope_base", 10000.0)), int(bool(rope.get("interleaved", 0))))
+
+
+def _workspace(nbytes: int, device, ws):
+    if ws is not None:
+        return ws, ws.numel() * ws.element_size()
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device), int(nbytes)
+
+
+def _lens(lengths):
+    if lengths is not None and lengths.dtype != torch.int32:
+        raise TypeError("lengths must be int32")
+    return lengths
+
+
+def a2ats_windowed_rope(k, *, window: int, far_offset: int = 0, rope_base: float = 10000.0,
+                        interleaved: bool = False, lengths=None, out=None, out_dtype=None,
+                        stream=None):
+    """Windowed RoPE of every valid cached key against its sequence's decode
+    position; returns `out` (same shape as k)."""
+    _dev(k, lengths, out)
+    k4 = _as4(k)
+    if out is None:
+        out = torch.empty(k.shape, dtype=out_dtype or k.dtype, device=k.device)
+    o4 = _as4(out)
+    p = RopeParams(int(window), int(far_offset), float(rope_base), int(bool(interleaved)))
+    B, H, N, d = k4.shape
+    _check("a2ats_windowed_rope", _load().a2ats_windowed_rope(
+        _ptr(k4), _dt(k4), _ptr(o4), _dt(o4), B, H, N, d, _ptr(_lens(lengths)),
+        ctypes.byref(p), _stream(stream)))
+    return out
+
+
+def a2ats_query_second_moment(queries, ridge: float = 1e-4, *, out=None, workspace=None,
+                              stream=None):
+    """H = (1/M) Q^T Q + ridge I per head; queries [H, M, d] (or [M, d])."""
+    _dev(queries, out)
+    q = queries if queries.dim() == 3 else queries.unsqueeze(0)
+    Hh, M, d = q.shape
+    if out is None:
+        out = torch.empty((Hh, d, d), dtype=torch.float32, device=q.device)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_query_second_moment_workspace_size(Hh, M, d), q.device,
+                        workspace)
+    _check("a2ats_query_second_moment", lib.a2ats_query_second_moment(
+        _ptr(q), _dt(q), Hh, M, d, float(ridge), _ptr(out), _ptr(ws), nb, _stream(stream)))
+    return out if queries.dim() == 3 else out[0]
+
+
+def a2ats_cholesky_factor(h, *, out=None, info=None, stream=None):
+    """Lower-triangular L with H = L L^T per head; returns (L, info)."""
+    _dev(h, out, info)
+    h3 = h if h.dim() == 3 else h.unsqueeze(0)
+    Hh, d, _ = h3.shape
+    if out is None:
+        out = torch.empty_like(h3, dtype=torch.float32)
+    if info is None:
+        info = torch.empty(Hh, dtype=torch.int32, device=h.device)
+    _check("a2ats_cholesky_factor", _load().a2ats_cholesky_factor(
+        _ptr(h3), Hh, d, _ptr(out), _ptr(info), _stream(stream)))
+    return (out, info) if h.dim() == 3 else (out[0], info)
+
+
+def _assign_common(x, codebook, codes):
+    x4 = _as4(x)
+    B, H, N, d = x4.shape
+    cb = codebook if codebook.dim() == 3 else codebook.unsqueeze(0)
+    if cb.dtype != x4.dtype:
+        raise TypeError("codebook and keys must share a dtype")
+    K = cb.shape[1]
+    if codes is None:
+        codes = torch.empty((B, H, N), dtype=torch.int32, device=x.device)
+    return x4, cb, K, codes
+
+
+def a2ats_h_weighted_assign(x, codebook, L=None, *, lengths=None, rope=None, rows="all",
+                            perm=None, count=None, codes=None, workspace=None, stream=None):
+    """argmin_j |x~ L - c_j L|^2 per visited row (L None: plain VQ)."""
+    _dev(x, codebook, L, lengths, perm, count, codes)
+    x4, cb, K, codes = _assign_common(x, codebook, codes)
+    B, H, N, d = x4.shape
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K), x.device,
+                        workspace)
+    rp = _rope(rope)
+    _check("a2ats_h_weighted_assign", lib.a2ats_h_weighted_assign(
+        _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), _ptr(cb), K, _ptr(L),
+        ctypes.byref(rp) if rp is not None else None, A2ATS_ROWS[rows], _ptr(perm), _ptr(count),
+        _ptr(codes), _ptr(ws), nb, _stream(stream)))
+    return codes
+
+
+def a2ats_query_aware_assign(x, codebook, query=None, beta: float = 0.5, *, lengths=None,
+                             rope=None, rows="all", perm=None, count=None, codes=None,
+                             workspace=None, stream=None):
+    """Cosine-blend assignment; query [B, H, d], or None for the proxy query
+    (the key at the decode position after windowed RoPE)."""
+    _dev(x, codebook, query, lengths, perm, count, codes)
+    x4, cb, K, codes = _assign_common(x, codebook, codes)
+    B, H, N, d = x4.shape
+    if query is not None and query.dtype != x4.dtype:
+        raise TypeError("query and keys must share a dtype")
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K), x.device,
+                        workspace)
+    rp = _rope(rope)
+    _check("a2ats_query_aware_assign", lib.a2ats_query_aware_assign(
+        _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), _ptr(cb), K, _ptr(query),
+        float(beta), ctypes.byref(rp) if rp is not None else None, A2ATS_ROWS[rows], _ptr(perm),
+        _ptr(count), _ptr(codes), _ptr(ws), nb, _stream(stream)))
+    return codes
+
+
+def a2ats_select_retrieval_set(keys, query=None, fraction: float = 0.2, *, lengths=None,
+                               rope=None, perm=None, count=None, workspace=None, stream=None):
+    """Retrieval split; returns (perm [B, H, N] int32, count [B, H] int32).
+    perm[..., :count] are the retrieval rows ascending, the rest the bulk."""
+    _dev(keys, query, lengths, perm, count)
+    k4 = _as4(keys)
+    B, H, N, d = k4.shape
+    if query is not None and query.dtype != k4.dtype:
+        raise TypeError("query and keys must share a dtype")
+    if perm is None:
+        perm = torch.empty((B, H, N), dtype=torch.int32, device=keys.device)
+    if count is None:
+        count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d), keys.device,
+                        workspace)
+    rp = _rope(rope)
+    _check("a2ats_select_retrieval_set", lib.a2ats_select_retrieval_set(
+        _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
+        ctypes.byref(rp) if rp is not None else None, _ptr(perm), _ptr(count), _ptr(ws), nb,
+        _stream(stream)))
+    return perm, count
+
+
+def split_views(perm, count, b: int = 0, h: int = 0, n: int | None = None):
+    """(retrieval_idx, bulk_idx) of one (b, h), as the API page returns them."""
+    c = int(count[b, h])
+    p = perm[b, h] if n is None else perm[b, h, :n]
+    return p[:c], p[c:]

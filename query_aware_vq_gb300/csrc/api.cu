@@ -1,0 +1,337 @@
+// api.cu -- the extern "C" entry points declared in include/a2ats.h.
+//
+// Each entry point checks its arguments on the host (nothing is enqueued when
+// a check fails), carves its workspace, and enqueues the kernels on the
+// caller's stream.  The operations follow the API page
+// "veloxquant_mlx.quantizers.a2ats module" and the "A2ATS-adapted" algorithm
+// pages; see include/a2ats.h for the contract of each call.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "../../include/a2ats.h"
+#include "kernels.cuh"
+
+using namespace a2ats;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void a2ats::note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return A2ATS_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool dtype_ok(int32_t dt) { return dt == A2ATS_F32 || dt == A2ATS_BF16 || dt == A2ATS_F16; }
+
+size_t dtype_bytes(int32_t dt) { return dt == A2ATS_F32 ? 4 : 2; }
+
+// d multiple of 8 in [8, 256]; positions below 2^24 (exact in fp32).
+int check_shape(int64_t B, int64_t H, int64_t Ncap, int64_t d) {
+    if (B < 0 || H < 0 || Ncap < 0) return A2ATS_ERR_SHAPE;
+    if (d < 8 || d > kMaxD || d % 8 != 0) return A2ATS_ERR_SHAPE;
+    if (Ncap >= (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if (B > (int64_t(1) << 20) || H > 4096 || B * H > 65535) return A2ATS_ERR_SHAPE;
+    return A2ATS_OK;
+}
+
+bool unit_interval(double v) { return v >= 0.0 && v <= 1.0; }  // false for NaN
+
+// Fill the device-side RoPE constants.  enabled = 0 when p is null.
+int make_rope(const a2ats_rope_params* p, int64_t d, RopeArgs& ra) {
+    memset(&ra, 0, sizeof(ra));
+    if (!p) return A2ATS_OK;
+    if (!(p->rope_base > 0.0) || !isfinite(p->rope_base)) return A2ATS_ERR_INVALID_ARG;
+    if (p->far_offset <= -(1 << 24) || p->far_offset >= (1 << 24)) return A2ATS_ERR_INVALID_ARG;
+    if (d % 2 != 0) return A2ATS_ERR_SHAPE;
+    ra.enabled = 1;
+    ra.window = p->window;
+    ra.far_offset = p->far_offset;
+    ra.interleaved = p->interleaved ? 1 : 0;
+    const double two_pi = 6.283185307179586476925286766559;
+    const float a = (float)two_pi;
+    const float b = (float)(two_pi - (double)a);
+    const float c = (float)(two_pi - (double)a - (double)b);
+    ra.two_pi_a = a;
+    ra.two_pi_b = b;
+    ra.two_pi_c = c;
+    ra.inv_2pi = (float)(1.0 / two_pi);
+    for (int64_t i = 0; i < d / 2; i++) {
+        const double om = pow(p->rope_base, -2.0 * (double)i / (double)d);
+        ra.omega_hi[i] = (float)om;
+        ra.omega_lo[i] = (float)(om - (double)ra.omega_hi[i]);
+    }
+    return A2ATS_OK;
+}
+
+// Bump allocator over the caller's workspace (256-byte aligned pieces).
+struct Carve {
+    char* base;
+    size_t used = 0;
+    explicit Carve(void* p) : base((char*)p) {}
+    template <class T>
+    T* take(size_t count) {
+        used = (used + 255) & ~size_t(255);
+        T* p = base ? (T*)(base + used) : nullptr;
+        used += sizeof(T) * count;
+        return p;
+    }
+};
+
+struct AssignWs {
+    float* cp;         // [H, K, d] transformed (or decoded) centroids
+    float* half_norm;  // [H, K]
+    float* cnorm;      // [H, K]
+    float* q;          // [B*H, d]
+    float* qnorm;      // [B*H]
+};
+
+AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t d, int64_t K) {
+    AssignWs w;
+    w.cp = c.take<float>((size_t)(H * K * d));
+    w.half_norm = c.take<float>((size_t)(H * K));
+    w.cnorm = c.take<float>((size_t)(H * K));
+    w.q = c.take<float>((size_t)(B * H * d));
+    w.qnorm = c.take<float>((size_t)(B * H));
+    return w;
+}
+
+struct SelectWs {
+    float* q;
+    float* qnorm;
+    float* scores;
+};
+
+SelectWs carve_select(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d) {
+    SelectWs w;
+    w.q = c.take<float>((size_t)(B * H * d));
+    w.qnorm = c.take<float>((size_t)(B * H));
+    w.scores = c.take<float>((size_t)(B * H * Ncap));
+    return w;
+}
+
+int check_rows(int32_t rows, const int32_t* perm, const int32_t* count) {
+    if (rows != A2ATS_ROWS_ALL && rows != A2ATS_ROWS_RETRIEVAL && rows != A2ATS_ROWS_BULK)
+        return A2ATS_ERR_INVALID_ARG;
+    if (rows != A2ATS_ROWS_ALL && (!perm || !count)) return A2ATS_ERR_INVALID_ARG;
+    return A2ATS_OK;
+}
+
+int check_assign_common(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                        int64_t d, const void* codebook, int64_t K, int32_t rows,
+                        const int32_t* perm, const int32_t* count, const int32_t* codes) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if ((st = check_rows(rows, perm, count))) return st;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (!x || !codebook || !codes) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codebook) || !aligned16(codes)) return A2ATS_ERR_ALIGN;
+    return A2ATS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* a2ats_status_string(int32_t status) {
+    switch (status) {
+        case A2ATS_OK: return "A2ATS_OK";
+        case A2ATS_ERR_INVALID_ARG: return "A2ATS_ERR_INVALID_ARG";
+        case A2ATS_ERR_SHAPE: return "A2ATS_ERR_SHAPE";
+        case A2ATS_ERR_DTYPE: return "A2ATS_ERR_DTYPE";
+        case A2ATS_ERR_ALIGN: return "A2ATS_ERR_ALIGN";
+        case A2ATS_ERR_CUDA: return "A2ATS_ERR_CUDA";
+        case A2ATS_ERR_WORKSPACE: return "A2ATS_ERR_WORKSPACE";
+        default: return "A2ATS_ERR_UNKNOWN";
+    }
+}
+
+const char* a2ats_last_error(void) { return g_last_error; }
+
+uint64_t a2ats_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int a2ats_windowed_rope(const void* k_in, int32_t in_dtype, void* k_out, int32_t out_dtype,
+                        int64_t B, int64_t H, int64_t Ncap, int64_t d, const int32_t* len,
+                        const a2ats_rope_params* rope, void* stream) {
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (!rope) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(rope, d, ra))) return st;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (!k_in || !k_out) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(k_in) || !aligned16(k_out)) return A2ATS_ERR_ALIGN;
+    if (k_in == k_out && in_dtype != out_dtype) return A2ATS_ERR_INVALID_ARG;
+    cudaError_t e = launch_windowed_rope(k_in, in_dtype, k_out, out_dtype, Shape{B, H, Ncap, d},
+                                         len, ra, (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_query_second_moment_workspace_size(int64_t H, int64_t M, int64_t d) {
+    if (H < 0 || M < 1 || d < 1) return 0;
+    Carve c(nullptr);
+    c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
+    return c.used + 256;
+}
+
+int a2ats_query_second_moment(const void* queries, int32_t dtype, int64_t H, int64_t M,
+                              int64_t d, double ridge, float* h_out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    if (H < 0 || H > 4096 || M < 1 || M >= (int64_t(1) << 31) || d < 8 || d > kMaxD || d % 8)
+        return A2ATS_ERR_SHAPE;
+    if (!(ridge >= 0.0) || !isfinite(ridge)) return A2ATS_ERR_INVALID_ARG;
+    if (H == 0) return A2ATS_OK;
+    if (!queries || !h_out) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(queries) || !aligned16(h_out)) return A2ATS_ERR_ALIGN;
+    if (!workspace || workspace_bytes < a2ats_query_second_moment_workspace_size(H, M, d))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    float* partial = c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
+    cudaError_t e = launch_second_moment(queries, dtype, H, M, d, ridge, partial, h_out,
+                                         (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+int a2ats_cholesky_factor(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
+                          void* stream) {
+    if (H < 0 || H > 4096 || d < 8 || d > kMaxD || d % 8) return A2ATS_ERR_SHAPE;
+    if (H == 0) return A2ATS_OK;
+    if (!h || !l_out || !info) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(l_out)) return A2ATS_ERR_ALIGN;
+    cudaError_t e = launch_cholesky(h, H, d, l_out, info, (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_h_weighted_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                              int64_t K) {
+    (void)Ncap;
+    Carve c(nullptr);
+    carve_assign(c, B, H, d, K);
+    return c.used + 256;
+}
+
+int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                            int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                            const float* L, const a2ats_rope_params* fused_rope, int32_t rows,
+                            const int32_t* perm, const int32_t* count, int32_t* codes,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_assign_common(x, dtype, B, H, Ncap, d, codebook, K, rows, perm, count, codes);
+    if (st) return st;
+    RopeArgs ra;
+    if ((st = make_rope(fused_rope, d, ra))) return st;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (L && !aligned16(L)) return A2ATS_ERR_ALIGN;
+    if (!workspace ||
+        workspace_bytes < a2ats_h_weighted_assign_workspace_size(B, H, Ncap, d, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    AssignWs w = carve_assign(c, B, H, d, K);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, L, w.cp, w.half_norm, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_assign_exact(x, dtype, Shape{B, H, Ncap, d}, len, ra, RowSel{rows, perm, count}, L,
+                            w.cp, w.half_norm, K, codes, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                               int64_t K) {
+    return a2ats_h_weighted_assign_workspace_size(B, H, Ncap, d, K);
+}
+
+int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                             int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                             const void* query, double beta, const a2ats_rope_params* fused_rope,
+                             int32_t rows, const int32_t* perm, const int32_t* count,
+                             int32_t* codes, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    int st = check_assign_common(x, dtype, B, H, Ncap, d, codebook, K, rows, perm, count, codes);
+    if (st) return st;
+    if (!unit_interval(beta)) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(fused_rope, d, ra))) return st;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (query && !aligned16(query)) return A2ATS_ERR_ALIGN;
+    if (!workspace ||
+        workspace_bytes < a2ats_query_aware_assign_workspace_size(B, H, Ncap, d, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    AssignWs w = carve_assign(c, B, H, d, K);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    // decoded fp32 centroids (and |c|^2 / 2) for either rule
+    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, w.cp,
+                                              w.half_norm, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (beta == 1.0) {
+        // beta = 1 is plain nearest-centroid VQ: the same argmin as the
+        // H-weighted rule with L = I, so it reduces exactly by construction
+        e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, nullptr, w.cp,
+                                w.half_norm, K, codes, s);
+        return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+    }
+    e = launch_centroid_norms(codebook, dtype, H, K, d, w.cnorm, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // the per-(b, h) query: decoded as given, or the proxy k~ at t
+    e = launch_prepare_query(x, query, dtype, sh, len, ra, w.q, w.qnorm, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_assign_blend(x, w.cp, dtype, sh, len, ra, RowSel{rows, perm, count}, w.q,
+                            w.qnorm, (float)beta, K, w.cnorm, codes, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_select_retrieval_set_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d) {
+    Carve c(nullptr);
+    carve_select(c, B, H, Ncap, d);
+    return c.used + 256;
+}
+
+int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                               int64_t Ncap, int64_t d, const int32_t* len, const void* query,
+                               double fraction, const a2ats_rope_params* fused_rope,
+                               int32_t* perm, int32_t* count, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(fused_rope, d, ra))) return st;
+    if (B * H == 0) return A2ATS_OK;
+    if (!count || (Ncap > 0 && (!keys || !perm))) return A2ATS_ERR_INVALID_ARG;
+    if ((keys && !aligned16(keys)) || (query && !aligned16(query)) || (perm && !aligned16(perm)))
+        return A2ATS_ERR_ALIGN;
+    if (!workspace || workspace_bytes < a2ats_select_retrieval_set_workspace_size(B, H, Ncap, d))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    SelectWs w = carve_select(c, B, H, Ncap, d);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    cudaError_t e = cudaSuccess;
+    if (Ncap > 0) {
+        e = launch_prepare_query(keys, query, dtype, sh, len, ra, w.q, w.qnorm, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = launch_cosine_scores(keys, dtype, sh, len, ra, w.q, w.qnorm, w.scores, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_select(w.scores, sh, len, fraction, perm, count, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,323 @@
+// calib.cu -- query second moment, Cholesky factor, codebook transform.
+//
+// API page "veloxquant_mlx.quantizers.a2ats module":
+//   a2ats_query_second_moment  H = E[q^T q] + ridge I        (paper Eq. 10)
+//   a2ats_cholesky_factor      H = L L^T                     (paper Eq. 15)
+//   a2ats_h_weighted_assignment, Eq. 16-18: centroids are mapped once into the
+//   space z = kL (c' = cL, |c'|^2) so the assignment is a Euclidean argmin.
+//
+// GB300 executes fp64 at a small fraction of its fp32 rate, so the extra
+// precision these small, latency-bound kernels need comes from compensated
+// fp32 (TwoSum / TwoProduct) rather than from doubles.
+#include "kernels.cuh"
+
+namespace a2ats {
+namespace {
+
+// ----------------------------------------------------- second moment --
+constexpr int kSmTile = 32;    // output tile edge
+constexpr int kSmChunk = 64;   // query rows per plain-fp32 partial sum
+constexpr int kSmThreads = 256;
+
+// Partial second moment of one 32x32 tile of H over one slice of the M
+// queries.  Each thread owns 4 outputs; 64-row plain fp32 partials are folded
+// into a compensated accumulator, so the result is within a few units of
+// fp32 rounding of the exact slice sum.
+template <int DT>
+__global__ void __launch_bounds__(kSmThreads)
+second_moment_partial_kernel(const void* __restrict__ q, int64_t M, int32_t d, int64_t splits,
+                             float* __restrict__ partial) {
+    __shared__ float qa[kSmChunk][kSmTile + 1];
+    __shared__ float qb[kSmChunk][kSmTile + 1];
+    // decode the lower-triangular tile pair (ti >= tj) from blockIdx.x
+    int ti = 0, rem = blockIdx.x;
+    while (rem > ti) { rem -= ti + 1; ti++; }
+    const int tj = rem;
+    const int split = blockIdx.y;
+    const int h = blockIdx.z;
+    const int64_t m0 = M * split / splits, m1 = M * (split + 1) / splits;
+    const int tid = threadIdx.x;
+    const int ra = tid / 8;            // row of the tile (a index)
+    const int rb = (tid % 8) * 4;      // first of 4 columns (b index)
+    Dot2 acc[4];
+    const int64_t qbase = (int64_t)h * M * d;
+    for (int64_t mc = m0; mc < m1; mc += kSmChunk) {
+        const int rows = (int)(m1 - mc < (int64_t)(kSmChunk) ? m1 - mc : (int64_t)(kSmChunk));
+        for (int e = tid; e < kSmChunk * kSmTile; e += kSmThreads) {
+            const int r = e / kSmTile, c = e % kSmTile;
+            float va = 0.f, vb = 0.f;
+            if (r < rows && ti * kSmTile + c < d) va = load1<DT>(q, qbase + (mc + r) * d + ti * kSmTile + c);
+            if (r < rows && tj * kSmTile + c < d) vb = load1<DT>(q, qbase + (mc + r) * d + tj * kSmTile + c);
+            qa[r][c] = va;
+            qb[r][c] = vb;
+        }
+        __syncthreads();
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < rows; r++) {
+            const float a = qa[r][ra];
+#pragma unroll
+            for (int k = 0; k < 4; k++) p[k] = fmaf(a, qb[r][rb + k], p[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) acc[k].add(p[k]);
+        __syncthreads();
+    }
+    float* out = partial + ((int64_t)split * gridDim.z + h) * d * d;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        // store hi and lo in two planes so the final sum stays compensated
+        if (ti * kSmTile + ra >= d || tj * kSmTile + rb + k >= d) continue;
+        const int64_t idx = (int64_t)(ti * kSmTile + ra) * d + tj * kSmTile + rb + k;
+        out[idx] = acc[k].s;
+        out[idx + (int64_t)splits * gridDim.z * d * d] = acc[k].c;
+    }
+}
+
+// H[h][a][b] = H[h][b][a] = (sum over slices) / M + ridge [a == b], a >= b.
+__global__ void second_moment_reduce_kernel(const float* __restrict__ partial, int64_t H,
+                                            int64_t M, int32_t d, int64_t splits, float ridge,
+                                            float* __restrict__ h_out) {
+    const int64_t n = H * d * d;
+    const int64_t plane = splits * H * d * d;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t h = idx / ((int64_t)d * d);
+        const int a = (int)((idx / d) % d), b = (int)(idx % d);
+        if (a < b) continue;
+        Dot2 acc;
+        for (int64_t s = 0; s < splits; s++) {
+            const int64_t p = (s * H + h) * d * d + (int64_t)a * d + b;
+            acc.add(partial[p]);
+            acc.add(partial[p + plane]);
+        }
+        float v = __fdiv_rn(acc.value(), (float)M);
+        if (a == b) v = __fadd_rn(v, ridge);
+        h_out[(h * d + a) * d + b] = v;
+        h_out[(h * d + b) * d + a] = v;
+    }
+}
+
+// ----------------------------------------------------------- Cholesky --
+constexpr int kCholThreads = 1024;
+
+__device__ __forceinline__ int tri(int i, int k) { return i * (i + 1) / 2 + k; }
+
+// One block per head.  Column-by-column (Crout order) Cholesky with the
+// factor held packed in shared memory; every entry is
+// (H_ij - sum_{k<j} L_ik L_jk) / L_jj with the sum formed by a compensated
+// dot product over one warp, so each entry is accurate to about one fp32
+// rounding of the values it depends on.
+__global__ void __launch_bounds__(kCholThreads)
+cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_out,
+                int32_t* __restrict__ info) {
+    extern __shared__ float smem[];
+    float* Lp = smem;                        // d(d+1)/2 packed lower triangle
+    float* tmp = smem + d * (d + 1) / 2;     // d residuals of the current column
+    const int h = blockIdx.x;
+    const float* Hh = hm + (int64_t)h * d * d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    int failed = 0;
+    for (int j = 0; j < d; j++) {
+        for (int i = j + warp; i < d; i += nwarps) {
+            Dot2 acc;
+            const float* Li = Lp + tri(i, 0);
+            const float* Lj = Lp + tri(j, 0);
+            for (int k = lane; k < j; k += 32) acc.add_prod(Li[k], Lj[k]);
+            for (int m = 16; m; m >>= 1) acc.merge(shfl_xor(acc, m));
+            if (lane == 0) {
+                acc.s = -acc.s;
+                acc.c = -acc.c;
+                acc.add(Hh[(int64_t)i * d + j]);
+                tmp[i] = acc.value();
+            }
+        }
+        __syncthreads();
+        const float pivot = tmp[j];
+        if (!(pivot > 0.f)) {  // not positive definite (or NaN)
+            failed = j + 1;
+            break;
+        }
+        const float diag = sqrtf(pivot);
+        for (int i = j + threadIdx.x; i < d; i += blockDim.x)
+            Lp[tri(i, j)] = (i == j) ? diag : __fdiv_rn(tmp[i], diag);
+        __syncthreads();
+    }
+    float* Lh = l_out + (int64_t)h * d * d;
+    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+        const int i = e / d, k = e % d;
+        float v = 0.f;
+        if (k <= i && (!failed || k < failed - 1)) v = Lp[tri(i, k)];
+        Lh[e] = v;
+    }
+    if (threadIdx.x == 0) info[h] = failed;
+}
+
+// ------------------------------------------------ codebook transform --
+constexpr int kCtCent = 8;  // centroids per block
+
+// cp[h][j] = c[h][j] L[h] (compensated), half_norm[h][j] = |cp[h][j]|^2 / 2.
+// blockDim.x = d rounded up to a multiple of 32: thread b < d owns output
+// column b of kCtCent centroids; the others only take part in reductions.
+template <int DT>
+__global__ void codebook_transform_kernel(const void* __restrict__ c, int64_t K, int32_t d,
+                                          const float* __restrict__ L, float* __restrict__ cp,
+                                          float* __restrict__ half_norm) {
+    __shared__ float cs[kCtCent][kMaxD];
+    __shared__ Dot2 red[kCtCent][kMaxD / 32];
+    const int h = blockIdx.y;
+    const int64_t j0 = (int64_t)blockIdx.x * kCtCent;
+    const int b = threadIdx.x;
+    const int nc = (int)(K - j0 < (int64_t)(kCtCent) ? K - j0 : (int64_t)(kCtCent));
+    const bool col = b < d;
+    for (int k = 0; k < kCtCent; k++)
+        if (col) cs[k][b] = k < nc ? load1<DT>(c, ((int64_t)h * K + j0 + k) * d + b) : 0.f;
+    __syncthreads();
+    float out[kCtCent];
+    if (!col) {
+#pragma unroll
+        for (int k = 0; k < kCtCent; k++) out[k] = 0.f;
+    } else if (L) {
+        Dot2 acc[kCtCent];
+        const float* Lh = L + (int64_t)h * d * d;
+        for (int a = 0; a < d; a++) {
+            const float l = Lh[(int64_t)a * d + b];
+#pragma unroll
+            for (int k = 0; k < kCtCent; k++) acc[k].add_prod(cs[k][a], l);
+        }
+#pragma unroll
+        for (int k = 0; k < kCtCent; k++) out[k] = acc[k].value();
+    } else {
+#pragma unroll
+        for (int k = 0; k < kCtCent; k++) out[k] = cs[k][b];
+    }
+    const int lane = b & 31, w = b >> 5;
+#pragma unroll
+    for (int k = 0; k < kCtCent; k++) {
+        if (k < nc && col) cp[((int64_t)h * K + j0 + k) * d + b] = out[k];
+        Dot2 n;
+        n.add_prod(out[k], out[k]);
+        for (int m = 16; m; m >>= 1) n.merge(shfl_xor(n, m));
+        if (lane == 0) red[k][w] = n;
+    }
+    __syncthreads();
+    if (b < nc) {
+        Dot2 t = red[b][0];
+        for (int ww = 1; ww < (int)(blockDim.x >> 5); ww++) t.merge(red[b][ww]);
+        half_norm[(int64_t)h * K + j0 + b] = 0.5f * t.value();
+    }
+}
+
+// cnorm[h][j] = |c[h][j]| (compensated sum of squares); one warp per centroid.
+template <int DT>
+__global__ void centroid_norm_kernel(const void* __restrict__ c, int64_t HK, int32_t d,
+                                     float* __restrict__ cnorm) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < HK;
+         j += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        Dot2 n;
+        for (int a = lane; a < d; a += 32) {
+            const float v = load1<DT>(c, j * d + a);
+            n.add_prod(v, v);
+        }
+        for (int m = 16; m; m >>= 1) n.merge(shfl_xor(n, m));
+        if (lane == 0) cnorm[j] = sqrtf(n.value());
+    }
+}
+
+}  // namespace
+
+int64_t second_moment_splits(int64_t M) {
+    int64_t s = M / 512;
+    return s < 1 ? 1 : (s > 64 ? 64 : s);
+}
+
+cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, int64_t d,
+                                 double ridge, float* partial, float* h_out, cudaStream_t st) {
+    const int64_t splits = second_moment_splits(M);
+    // tiles past the edge of H (d not a multiple of 32) read zeros and write nothing
+    const int Tt = (int)((d + kSmTile - 1) / kSmTile);
+    dim3 grid(Tt * (Tt + 1) / 2, (unsigned)splits, (unsigned)H);
+    switch (dt) {
+        case kF32:
+            second_moment_partial_kernel<kF32><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
+                                                                            splits, partial);
+                                                                            note_launches(1);
+            break;
+        case kBF16:
+            second_moment_partial_kernel<kBF16><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
+                                                                             splits, partial);
+                                                                             note_launches(1);
+            break;
+        default:
+            second_moment_partial_kernel<kF16><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
+                                                                            splits, partial);
+                                                                            note_launches(1);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t n = H * d * d;
+    second_moment_reduce_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096),
+                                  256, 0, st>>>(partial, H, M, (int32_t)d, splits, (float)ridge,
+                                                h_out);
+                                                note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
+                            cudaStream_t st) {
+    if (H == 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * (size_t)(d * (d + 1) / 2 + d);
+    cudaError_t e = cudaFuncSetAttribute(cholesky_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cholesky_kernel<<<(unsigned)H, kCholThreads, smem, st>>>(h, (int32_t)d, l_out, info);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_codebook_transform(const void* c, int dt, int64_t H, int64_t K, int64_t d,
+                                      const float* L, float* cp, float* half_norm,
+                                      cudaStream_t st) {
+    dim3 grid((unsigned)((K + kCtCent - 1) / kCtCent), (unsigned)H);
+    const unsigned threads = (unsigned)((d + 31) / 32 * 32);
+    switch (dt) {
+        case kF32:
+            codebook_transform_kernel<kF32><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
+                                                                       half_norm);
+                                                                       note_launches(1);
+            break;
+        case kBF16:
+            codebook_transform_kernel<kBF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
+                                                                        half_norm);
+                                                                        note_launches(1);
+            break;
+        default:
+            codebook_transform_kernel<kF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
+                                                                       half_norm);
+                                                                       note_launches(1);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
+                                  float* cnorm, cudaStream_t st) {
+    const int64_t HK = H * K;
+    const unsigned blocks = (unsigned)((HK * 32 + 255) / 256 < 2048 ? (HK * 32 + 255) / 256 : 2048);
+    switch (dt) {
+        case kF32:
+            centroid_norm_kernel<kF32><<<blocks, 256, 0, st>>>(c, HK, (int32_t)d, cnorm);
+            note_launches(1);
+            break;
+        case kBF16:
+            centroid_norm_kernel<kBF16><<<blocks, 256, 0, st>>>(c, HK, (int32_t)d, cnorm);
+            note_launches(1);
+            break;
+        default:
+            centroid_norm_kernel<kF16><<<blocks, 256, 0, st>>>(c, HK, (int32_t)d, cnorm);
+            note_launches(1);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace a2ats

@@ -1,0 +1,76 @@
+// kernels.cuh -- host-side launch functions of the A2ATS kernels.  Each .cu
+// file implements the launches for its kernels; api.cu validates arguments,
+// lays out the workspace and calls these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace a2ats {
+
+// Count of kernels enqueued by this library (see a2ats_kernel_launches).
+void note_launches(int n);
+
+struct Shape {
+    int64_t B, H, Ncap, d;
+};
+
+// rope_split.cu ----------------------------------------------------------
+cudaError_t launch_windowed_rope(const void* k_in, int in_dt, void* k_out, int out_dt,
+                                 const Shape& s, const int32_t* len, const RopeArgs& ra,
+                                 cudaStream_t st);
+
+// q_out [B*H, d] fp32 and qnorm [B*H]: the given query (decoded), or the key
+// at the decode position after windowed RoPE when query == nullptr.
+cudaError_t launch_prepare_query(const void* keys, const void* query, int dt, const Shape& s,
+                                 const int32_t* len, const RopeArgs& ra, float* q_out,
+                                 float* qnorm, cudaStream_t st);
+
+// scores [B*H*Ncap] fp32 cosine of every valid row with its (b, h) query.
+cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
+                                 const RopeArgs& ra, const float* q, const float* qnorm,
+                                 float* scores, cudaStream_t st);
+
+cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* len,
+                          double fraction, int32_t* perm, int32_t* count, cudaStream_t st);
+
+// calib.cu ---------------------------------------------------------------
+int64_t second_moment_splits(int64_t M);
+cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, int64_t d,
+                                 double ridge, float* partial, float* h_out, cudaStream_t st);
+
+cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
+                            cudaStream_t st);
+
+// Transformed codebook for the assignment: cp [H, K, d] fp32 = c L (c when L
+// is null) and half_norm [H, K] fp32 = |cp_j|^2 / 2.
+cudaError_t launch_codebook_transform(const void* c, int dt, int64_t H, int64_t K, int64_t d,
+                                      const float* L, float* cp, float* half_norm,
+                                      cudaStream_t st);
+
+// assign.cu --------------------------------------------------------------
+struct RowSel {
+    int32_t mode;  // a2ats_rows
+    const int32_t* perm;
+    const int32_t* count;
+};
+
+// Exact z-space assignment (SIMT, compensated fp32): code = argmin_j
+// |x~ L - cp_j|^2.  L null = identity.
+cudaError_t launch_assign_exact(const void* x, int dt, const Shape& s, const int32_t* len,
+                                const RopeArgs& ra, const RowSel& sel, const float* L,
+                                const float* cp, const float* half_norm, int64_t K,
+                                int32_t* codes, cudaStream_t st);
+
+// Cosine blend (SIMT): q [B*H, d] fp32 per-(b, h) query and its norm.
+cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shape& s,
+                                const int32_t* len, const RopeArgs& ra, const RowSel& sel,
+                                const float* q, const float* qnorm, float beta, int64_t K,
+                                const float* cnorm, int32_t* codes, cudaStream_t st);
+
+cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
+                                  float* cnorm, cudaStream_t st);
+
+}  // namespace a2ats

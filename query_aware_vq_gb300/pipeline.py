@@ -1,0 +1,100 @@
+"""One step of the A2ATS hot path, composed from the C-ABI calls.
+
+The order is the one the pages' cache wrapper runs every step (v0.39.0 page,
+"How it works"; deploy-preview page, "Per-step re-rotation" and "Query-aware
+VQ (Eq. 13-18)"), with the calibration of H and L in front:
+
+  1. H = E[q^T q] + ridge I            a2ats_query_second_moment
+  2. L = chol(H)                       a2ats_cholesky_factor
+  3. k~ = windowed RoPE of the cache   a2ats_windowed_rope
+  4. retrieval split, proxy query k~_t a2ats_select_retrieval_set (RoPE fused)
+  5. retrieval rows: H-weighted rule   a2ats_h_weighted_assign (RoPE fused)
+     (or the cosine blend when no H is calibrated)
+  6. bulk rows: plain nearest centroid a2ats_h_weighted_assign, L = identity
+
+Steps 4-6 apply the windowed RoPE on the fly in fp32 to the pre-RoPE keys, so
+their decisions are taken on the unrounded rotated keys; step 3 writes the
+rotated cache in the storage dtype for the attention that follows.
+
+All buffers are allocated once in the constructor; a step allocates nothing.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (a2ats_cholesky_factor, a2ats_h_weighted_assign, a2ats_query_aware_assign,
+               a2ats_query_second_moment, a2ats_select_retrieval_set, a2ats_windowed_rope,
+               library)
+
+
+class A2ATSStep:
+    def __init__(self, B: int, H: int, N: int, d: int, K: int, dtype: torch.dtype, *,
+                 window: int, fraction: float, rope_base: float, far_offset: int = 0,
+                 M: int = 0, ridge: float = 1e-4, beta: float = 0.5, interleaved: bool = False,
+                 device="cuda"):
+        self.B, self.H, self.N, self.d, self.K, self.M = B, H, N, d, K, M
+        self.dtype, self.fraction, self.ridge, self.beta = dtype, fraction, ridge, beta
+        self.rope = dict(window=window, far_offset=far_offset, rope_base=rope_base,
+                         interleaved=interleaved)
+        dev = torch.device(device)
+        lib = library()
+        self.k_tilde = torch.empty((B, H, N, d), dtype=dtype, device=dev)
+        self.perm = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.count = torch.empty((B, H), dtype=torch.int32, device=dev)
+        self.codes = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.Hm = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+        self.L = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+        self.info = torch.empty((H,), dtype=torch.int32, device=dev)
+        ws = max(lib.a2ats_query_second_moment_workspace_size(H, max(M, 1), d),
+                 lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
+                 lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
+                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def __call__(self, keys, codebook, queries=None, h_given=None, lengths=None, stream=None,
+                 events=None):
+        """keys [B, H, N, d] pre-RoPE; codebook [H, K, d]; queries [H, M, d]
+        (calibration) or h_given [H, d, d] fp32 or neither (cosine-blend path).
+        events: optional dict; each stage appends a (start, end) CUDA event
+        pair recorded on the launching stream around its call."""
+        ws = self.workspace
+        st = stream if stream is not None else torch.cuda.current_stream()
+
+        def stage(name, fn, *a, **kw):
+            if events is None:
+                return fn(*a, **kw)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            r = fn(*a, **kw)
+            e1.record(st)
+            events.setdefault(name, []).append((e0, e1))
+            return r
+
+        L = None
+        if queries is not None:
+            stage("second_moment", a2ats_query_second_moment, queries, self.ridge, out=self.Hm,
+                  workspace=ws, stream=st)
+            h_given = self.Hm
+        if h_given is not None:
+            stage("cholesky", a2ats_cholesky_factor, h_given, out=self.L, info=self.info,
+                  stream=st)
+            L = self.L
+        stage("windowed_rope", a2ats_windowed_rope, keys, lengths=lengths, out=self.k_tilde,
+              stream=st, **self.rope)
+        stage("retrieval_split", a2ats_select_retrieval_set, keys, None, self.fraction,
+              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws,
+              stream=st)
+        if L is not None:
+            stage("assign_retrieval", a2ats_h_weighted_assign, keys, codebook, L,
+                  lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
+                  count=self.count, codes=self.codes, workspace=ws, stream=st)
+        else:
+            # no calibrated H: the cosine blend against the same proxy query
+            # (the key at t after windowed RoPE) the split used
+            stage("assign_retrieval", a2ats_query_aware_assign, keys, codebook, None, self.beta,
+                  lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
+                  count=self.count, codes=self.codes, workspace=ws, stream=st)
+        stage("assign_bulk", a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
+              rope=self.rope, rows="bulk", perm=self.perm, count=self.count, codes=self.codes,
+              workspace=ws, stream=st)
+        return self

@@ -1,0 +1,97 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch
+(CPU only: nothing here reaches a kernel)."""
+import ctypes
+
+import pytest
+
+import query_aware_vq_gb300 as q
+from query_aware_vq_gb300 import build as qbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return q.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = q.declared_symbols()
+    assert len(names) >= 12
+    for n in ("a2ats_query_second_moment", "a2ats_cholesky_factor", "a2ats_windowed_rope",
+              "a2ats_h_weighted_assign", "a2ats_query_aware_assign",
+              "a2ats_select_retrieval_set"):
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.a2ats_status_string(0) == b"A2ATS_OK"
+    assert lib.a2ats_status_string(-2) == b"A2ATS_ERR_SHAPE"
+    assert lib.a2ats_status_string(-6) == b"A2ATS_ERR_WORKSPACE"
+    assert lib.a2ats_status_string(12345) == b"A2ATS_ERR_UNKNOWN"
+
+
+def test_workspace_sizes_grow_with_shape(lib):
+    a = lib.a2ats_h_weighted_assign_workspace_size(1, 8, 32768, 128, 1024)
+    b = lib.a2ats_h_weighted_assign_workspace_size(1, 8, 32768, 128, 4096)
+    assert 0 < a < b
+    assert lib.a2ats_select_retrieval_set_workspace_size(1, 8, 32768, 128) >= 8 * 32768 * 4
+    assert lib.a2ats_query_second_moment_workspace_size(8, 8192, 128) >= 8 * 128 * 128 * 4
+
+
+FAKE = 0x1000  # a 16-byte aligned address that is never dereferenced
+
+
+def _rope(window=64, far=0, base=10000.0, inter=0):
+    return ctypes.byref(q.RopeParams(window, far, base, inter))
+
+
+def test_rope_validation(lib):
+    f = lib.a2ats_windowed_rope
+    assert f(FAKE, 7, FAKE, 0, 1, 1, 16, 128, None, _rope(), None) == -3      # dtype
+    assert f(FAKE, 1, FAKE, 1, 1, 1, 16, 130, None, _rope(), None) == -2      # d % 8
+    assert f(FAKE, 1, FAKE, 1, 1, 1, 16, 264, None, _rope(), None) == -2      # d > 256
+    assert f(FAKE, 1, FAKE, 1, 1, 1, 1 << 24, 128, None, _rope(), None) == -2  # positions
+    assert f(FAKE, 1, FAKE, 1, 1, 1, 16, 128, None, None, None) == -1          # no params
+    assert f(FAKE, 1, FAKE, 1, 1, 1, 16, 128, None, _rope(base=-1.0), None) == -1
+    assert f(FAKE + 8, 1, FAKE, 1, 1, 1, 16, 128, None, _rope(), None) == -4   # alignment
+    assert f(None, 1, FAKE, 1, 1, 1, 16, 128, None, _rope(), None) == -1
+    assert f(FAKE, 1, FAKE, 0, 1, 1, 16, 128, None, _rope(), None) == -1      # alias, dtypes differ
+    assert f(None, 1, None, 1, 0, 1, 16, 128, None, _rope(), None) == 0       # empty: no-op
+
+
+def test_assign_validation(lib):
+    f = lib.a2ats_h_weighted_assign
+    args = lambda **kw: [kw.get("x", FAKE), kw.get("dt", 1), 1, 2, 64, kw.get("d", 128), None,
+                         FAKE, kw.get("K", 16), None, None, kw.get("rows", 0), kw.get("perm"),
+                         kw.get("count"), FAKE, kw.get("ws", FAKE), kw.get("wsb", 1 << 30), None]
+    assert f(*args(dt=9)) == -3
+    assert f(*args(K=0)) == -2
+    assert f(*args(d=12)) == -2
+    assert f(*args(rows=5)) == -1
+    assert f(*args(rows=1)) == -1                  # retrieval rows need perm and count
+    assert f(*args(x=FAKE + 4)) == -4
+    assert f(*args(ws=None)) == -6
+    assert f(*args(wsb=16)) == -6
+    g = lib.a2ats_query_aware_assign
+    base = [FAKE, 1, 1, 2, 64, 128, None, FAKE, 16, None]
+    tail = [None, 0, None, None, FAKE, FAKE, 1 << 30, None]
+    for beta in (-0.1, 1.5, float("nan")):
+        assert g(*base, beta, *tail) == -1
+
+
+def test_split_and_calibration_validation(lib):
+    s = lib.a2ats_select_retrieval_set
+    for frac in (-0.01, 1.01, float("nan")):
+        assert s(FAKE, 1, 1, 2, 64, 128, None, None, frac, None, FAKE, FAKE, FAKE, 1 << 30,
+                 None) == -1
+    assert s(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, None, FAKE, FAKE, None, 0, None) == -6
+    m = lib.a2ats_query_second_moment
+    assert m(FAKE, 1, 2, 0, 128, 1e-4, FAKE, FAKE, 1 << 30, None) == -2       # M = 0
+    assert m(FAKE, 1, 2, 10, 128, -1.0, FAKE, FAKE, 1 << 30, None) == -1      # ridge < 0
+    assert m(FAKE, 1, 2, 10, 128, 1e-4, FAKE, None, 0, None) == -6
+    c = lib.a2ats_cholesky_factor
+    assert c(FAKE, 2, 100, FAKE, FAKE, None) == -2
+    assert c(FAKE, 2, 128, FAKE, None, None) == -1

@@ -1,0 +1,141 @@
+"""GPU parity: H-weighted and cosine-blend assignment against the oracle
+(API page, a2ats_h_weighted_assignment and a2ats_query_aware_assignment).
+Codes must equal the oracle's except where its top-2 gap is below 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import query_aware_vq_gb300 as q
+import synth
+from _parity import check_codes, dev, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _spd(rng, d, cond):
+    Qm, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    lam = np.exp(np.linspace(0, np.log(cond), d))
+    return (Qm * lam) @ Qm.T
+
+
+def _L(H, d, cond, seed):
+    rng = np.random.default_rng(seed)
+    Ls = []
+    for _ in range(H):
+        l, _ = oracle.cholesky(_spd(rng, d, cond))
+        Ls.append(l)
+    return torch.from_numpy(np.stack(Ls).astype(np.float32))
+
+
+def _rows(x, lens, rope):
+    """Per (b, h): the oracle's k~ of the valid rows (fp64)."""
+    B, H, N, d = x.shape
+    out = {}
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(H):
+            v = f64(x[b, h, :n])
+            if rope is not None:
+                v = oracle.windowed_rope(v, np.arange(n), n - 1, rope["window"],
+                                         rope.get("far_offset", 0), rope["rope_base"])
+            out[b, h] = v
+    return out
+
+
+CASES = [
+    # B, H, N, d, K, dtype, with L, rope
+    (2, 2, 300, 128, 100, "bf16", True, None),
+    (1, 3, 129, 64, 33, "f32", False, None),
+    (2, 1, 200, 128, 64, "f16", True, dict(window=40, far_offset=0, rope_base=500000.0)),
+    (1, 2, 150, 256, 40, "bf16", True, dict(window=20, far_offset=9, rope_base=10000.0)),
+    (1, 1, 70, 24, 17, "f32", True, None),
+    (1, 1, 5, 16, 1, "bf16", False, None),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_h_weighted_matches_oracle(case):
+    B, H, N, d, K, dt, withL, rope = case
+    x = synth.gaussian((B, H, N, d), seed=N, dtype=dt, scale=2.0)
+    c = synth.gaussian((H, K, d), seed=K + 1, dtype=dt, scale=2.0)
+    L = _L(H, d, 30.0, seed=d) if withL else None
+    lens = torch.tensor([N - 11 * b for b in range(B)], dtype=torch.int32)
+    codes = q.a2ats_h_weighted_assign(dev(x), dev(c), dev(L) if withL else None,
+                                      lengths=dev(lens), rope=rope)
+    got = codes.cpu().numpy()
+    kt = _rows(x, lens, rope)
+    for (b, h), v in kt.items():
+        code, d1, d2 = oracle.assign_cholesky(v, c[h], L[h] if withL else None)
+        check_codes(got[b, h, :len(v)], code, (d2 - d1) / np.maximum(d2, 1e-300))
+
+
+@pytest.mark.parametrize("mode", ["retrieval", "bulk"])
+def test_row_selection_writes_only_its_rows(mode):
+    B, H, N, d, K = 1, 2, 300, 128, 50
+    x = synth.gaussian((B, H, N, d), seed=7, dtype="bf16")
+    c = synth.gaussian((H, K, d), seed=8, dtype="bf16")
+    perm = np.zeros((B, H, N), np.int32)
+    count = np.zeros((B, H), np.int32)
+    for h in range(H):
+        p, cnt, _, _ = oracle.select_retrieval_set(x[0, h], f64(x[0, h, -1]), 0.2)
+        perm[0, h], count[0, h] = p, cnt
+    codes = torch.full((B, H, N), -7, dtype=torch.int32, device="cuda")
+    q.a2ats_h_weighted_assign(dev(x), dev(c), None, rows=mode, perm=dev(torch.from_numpy(perm)),
+                              count=dev(torch.from_numpy(count)), codes=codes)
+    got = codes.cpu().numpy()
+    for h in range(H):
+        sel = perm[0, h, :count[0, h]] if mode == "retrieval" else perm[0, h, count[0, h]:]
+        other = np.setdiff1d(np.arange(N), sel)
+        assert (got[0, h, other] == -7).all()
+        code, d1, d2 = oracle.assign_cholesky(x[0, h, sel], c[h], None)
+        check_codes(got[0, h, sel], code, (d2 - d1) / d2)
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.3, 0.7, 1.0])
+@pytest.mark.parametrize("qmode", ["given", "proxy"])
+def test_blend_matches_oracle(beta, qmode):
+    B, H, N, d, K = 2, 2, 260, 128, 90
+    x = synth.gaussian((B, H, N, d), seed=11, dtype="bf16", scale=2.0)
+    c = synth.gaussian((H, K, d), seed=12, dtype="bf16", scale=2.0)
+    lens = torch.tensor([N, N - 40], dtype=torch.int32)
+    rope = dict(window=32, far_offset=0, rope_base=500000.0)
+    query = synth.gaussian((B, H, d), seed=13, dtype="bf16") if qmode == "given" else None
+    codes = q.a2ats_query_aware_assign(dev(x), dev(c), dev(query) if query is not None else None,
+                                       beta, lengths=dev(lens), rope=rope)
+    got = codes.cpu().numpy()
+    kt = _rows(x, lens, rope)
+    for (b, h), v in kt.items():
+        qv = f64(query[b, h]) if query is not None else v[-1]
+        code, s1, s2 = oracle.assign_blend(v, c[h], qv, beta)
+        gap = (s2 - s1) / np.maximum(s2, 1e-300) if beta == 1.0 else (s1 - s2)
+        check_codes(got[b, h, :len(v)], code, gap)
+
+
+def test_beta_one_equals_plain_vq_bitwise():
+    x = dev(synth.gaussian((1, 2, 300, 128), seed=21, dtype="bf16"))
+    c = dev(synth.gaussian((2, 64, 128), seed=22, dtype="bf16"))
+    a = q.a2ats_query_aware_assign(x, c, None, 1.0)
+    b = q.a2ats_h_weighted_assign(x, c, None)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["llama32_3b_layer"])
+def test_h_weighted_full_size_sampled(name):
+    w = synth.WORKLOADS[name]
+    k, c = synth.keys(w), synth.codebook(w)
+    Q = synth.queries(w)
+    Ls = []
+    for h in range(w.H):
+        hm = oracle.query_second_moment(Q[h], w.ridge).astype(np.float32)
+        Ls.append(oracle.cholesky(hm.astype(np.float64))[0].astype(np.float32))
+    L = torch.from_numpy(np.stack(Ls))
+    rope = dict(window=w.W, far_offset=w.far_offset, rope_base=w.rope_base)
+    got = q.a2ats_h_weighted_assign(dev(k), dev(c), dev(L), rope=rope).cpu().numpy()
+    rng = np.random.default_rng(1)
+    for h in range(w.H):
+        rows = np.unique(np.concatenate([rng.choice(w.N, 512, replace=False),
+                                         np.arange(w.N - 64, w.N)]))
+        v = oracle.windowed_rope(k[0, h, rows], rows, w.N - 1, w.W, 0, w.rope_base)
+        code, d1, d2 = oracle.assign_cholesky(v, c[h], L[h])
+        check_codes(got[0, h, rows], code, (d2 - d1) / d2)
