@@ -77,9 +77,12 @@ assign_exact_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
     const int64_t bh = blockIdx.y;
     const int32_t Ls = seq_len(len, (int32_t)(bh / H), ncap);
     const int32_t r0 = blockIdx.x * kRB;
-    if (threadIdx.x < kRB) rows[threadIdx.x] = list_row(sel, bh, ncap, Ls, r0 + threadIdx.x);
-    __syncthreads();
-    if (r0 >= Ls) return;  // past the end of every row list of this (b, h)
+    bool any = false;
+    if (threadIdx.x < kRB) {
+        rows[threadIdx.x] = list_row(sel, bh, ncap, Ls, r0 + threadIdx.x);
+        any = rows[threadIdx.x] >= 0;
+    }
+    if (!__syncthreads_or(any)) return;  // this slice of the row list is empty
     load_rows<DT>(x, bh, ncap, d, Ls, ra, rows, xs, ld);
     const float* Z = xs;
     if (L) {
@@ -154,9 +157,12 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
     const int64_t h = bh % H;
     const int32_t Ls = seq_len(len, (int32_t)(bh / H), ncap);
     const int32_t r0 = blockIdx.x * kRB;
-    if (threadIdx.x < kRB) rows[threadIdx.x] = list_row(sel, bh, ncap, Ls, r0 + threadIdx.x);
-    __syncthreads();
-    if (r0 >= Ls) return;
+    bool any = false;
+    if (threadIdx.x < kRB) {
+        rows[threadIdx.x] = list_row(sel, bh, ncap, Ls, r0 + threadIdx.x);
+        any = rows[threadIdx.x] >= 0;
+    }
+    if (!__syncthreads_or(any)) return;
     load_rows<DT>(x, bh, ncap, d, Ls, ra, rows, xs, ld);
     for (int a = threadIdx.x; a < d; a += blockDim.x) qs[a] = q[bh * d + a];
     const int r = threadIdx.x / kSlots, slot = threadIdx.x % kSlots;

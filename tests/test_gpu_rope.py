@@ -54,8 +54,10 @@ def test_rope_matches_oracle(case):
         worst = assert_rows_close(got[b, :, :n].reshape(-1, d), want[b, :, :n].reshape(-1, d))
         assert worst < 2e-6
         assert (got[b, :, n:] == 7.0).all()  # rows past the length are untouched
-    # storage-dtype output: at most one unit in the last place from the
-    # oracle rounded to nearest even
+    # half-precision storage output: at most one unit in the last place from
+    # the oracle rounded to nearest even (fp32 storage is the check above)
+    if dt == "f32":
+        return
     out2 = q.a2ats_windowed_rope(kd, window=W, far_offset=far, rope_base=base,
                                  interleaved=inter, lengths=ld)
     g2 = f64(out2)
