@@ -96,16 +96,53 @@ struct AssignWs {
     float* cnorm;      // [H, K]
     float* q;          // [B*H, d]
     float* qnorm;      // [B*H]
+    TcCall tc;         // buffers of the tensor-core path
 };
 
-AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t d, int64_t K) {
+AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, int64_t K) {
     AssignWs w;
     w.cp = c.take<float>((size_t)(H * K * d));
     w.half_norm = c.take<float>((size_t)(H * K));
     w.cnorm = c.take<float>((size_t)(H * K));
     w.q = c.take<float>((size_t)(B * H * d));
     w.qnorm = c.take<float>((size_t)(B * H));
+    const size_t rows = (size_t)(B * H * Ncap);
+    memset(&w.tc, 0, sizeof(w.tc));
+    w.tc.Lt = c.take<float>((size_t)(H * d * d));
+    w.tc.chat = c.take<float>((size_t)(H * K * d));
+    w.tc.scratch_norm = c.take<float>((size_t)(H * K));
+    w.tc.head_bits = c.take<uint32_t>((size_t)(H * 4));
+    w.tc.head = c.take<float>((size_t)(H * 4));
+    w.tc.scale = c.take<float>((size_t)H);
+    w.tc.planes = c.take<uint16_t>((size_t)(H * 3 * K * d));
+    w.tc.compact = c.take<uint16_t>(rows * (size_t)d);
+    w.tc.row_map = c.take<int32_t>(rows);
+    w.tc.skip = c.take<uint8_t>(rows);
+    w.tc.exact_list = c.take<int64_t>(rows);
+    w.tc.exact_count = c.take<int32_t>(2);
     return w;
+}
+
+// The tensor-core route for bf16 / fp16 keys (d a multiple of 64); cp and
+// half_norm must hold c L and |c L|^2 / 2.
+cudaError_t assign_on_tensor_cores(AssignWs& w, int32_t dtype, const Shape& sh,
+                                   const int32_t* len, const void* x, const void* codebook,
+                                   int64_t K, const float* L, const RopeArgs& ra,
+                                   const RowSel& sel, int32_t* codes, cudaStream_t s) {
+    TcCall& c = w.tc;
+    c.dt = dtype;
+    c.s = sh;
+    c.K = K;
+    c.x = x;
+    c.codebook = codebook;
+    c.L = L;
+    c.ra = ra;
+    c.sel = sel;
+    c.len = len;
+    c.cp = w.cp;
+    c.half_norm = w.half_norm;
+    c.codes = codes;
+    return launch_assign_tc(c, s);
 }
 
 struct SelectWs {
@@ -220,9 +257,8 @@ int a2ats_cholesky_factor(const float* h, int64_t H, int64_t d, float* l_out, in
 
 size_t a2ats_h_weighted_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
                                               int64_t K) {
-    (void)Ncap;
     Carve c(nullptr);
-    carve_assign(c, B, H, d, K);
+    carve_assign(c, B, H, Ncap, d, K);
     return c.used + 256;
 }
 
@@ -241,12 +277,17 @@ int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, 
         workspace_bytes < a2ats_h_weighted_assign_workspace_size(B, H, Ncap, d, K))
         return A2ATS_ERR_WORKSPACE;
     Carve c(workspace);
-    AssignWs w = carve_assign(c, B, H, d, K);
+    AssignWs w = carve_assign(c, B, H, Ncap, d, K);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, L, w.cp, w.half_norm, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_assign_exact(x, dtype, Shape{B, H, Ncap, d}, len, ra, RowSel{rows, perm, count}, L,
-                            w.cp, w.half_norm, K, codes, s);
+    const Shape sh{B, H, Ncap, d};
+    if (tc_supported(dtype, d))
+        e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, L, ra,
+                                   RowSel{rows, perm, count}, codes, s);
+    else
+        e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, L, w.cp,
+                                w.half_norm, K, codes, s);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
@@ -272,7 +313,7 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
         workspace_bytes < a2ats_query_aware_assign_workspace_size(B, H, Ncap, d, K))
         return A2ATS_ERR_WORKSPACE;
     Carve c(workspace);
-    AssignWs w = carve_assign(c, B, H, d, K);
+    AssignWs w = carve_assign(c, B, H, Ncap, d, K);
     cudaStream_t s = (cudaStream_t)stream;
     const Shape sh{B, H, Ncap, d};
     // decoded fp32 centroids (and |c|^2 / 2) for either rule
@@ -282,8 +323,12 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
     if (beta == 1.0) {
         // beta = 1 is plain nearest-centroid VQ: the same argmin as the
         // H-weighted rule with L = I, so it reduces exactly by construction
-        e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, nullptr, w.cp,
-                                w.half_norm, K, codes, s);
+        if (tc_supported(dtype, d))
+            e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, nullptr, ra,
+                                       RowSel{rows, perm, count}, codes, s);
+        else
+            e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, nullptr,
+                                    w.cp, w.half_norm, K, codes, s);
         return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
     }
     e = launch_centroid_norms(codebook, dtype, H, K, d, w.cnorm, s);

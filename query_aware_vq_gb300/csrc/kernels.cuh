@@ -70,6 +70,42 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
                                 const float* q, const float* qnorm, float beta, int64_t K,
                                 const float* cnorm, int32_t* codes, cudaStream_t st);
 
+// assign_tc.cu ----------------------------------------------------------
+// Tensor-core assignment (argmin_j |x~ L - c_j L|^2, L null = identity) for
+// bf16 / fp16 keys with d a multiple of 64.  cp / half_norm must already hold
+// c L and |c L|^2 / 2 (launch_codebook_transform).  Rows inside the RoPE
+// window and rows whose top two the contraction cannot separate are decided
+// by the exact kernel.
+struct TcCall {
+    int dt;
+    Shape s;
+    int64_t K;
+    const void* x;
+    const void* codebook;
+    const float* L;
+    RopeArgs ra;
+    RowSel sel;
+    const int32_t* len;
+    const float* cp;
+    const float* half_norm;
+    int32_t* codes;
+    // workspace
+    float* Lt;            // [H, d, d]
+    float* chat;          // [H, K, d]
+    float* scratch_norm;  // [H, K]
+    uint32_t* head_bits;  // [H, 4]
+    float* head;          // [H, 4]
+    float* scale;         // [H]
+    uint16_t* planes;     // [H, 3, K, d]
+    void* compact;        // [B*H*Ncap, d] 16-bit
+    int32_t* row_map;     // [B*H*Ncap]
+    uint8_t* skip;        // [B*H*Ncap]
+    int64_t* exact_list;  // [B*H*Ncap]
+    int32_t* exact_count; // [2]: count, status
+};
+bool tc_supported(int dt, int64_t d);
+cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st);
+
 cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
                                   float* cnorm, cudaStream_t st);
 
