@@ -108,15 +108,19 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.qnorm = c.take<float>((size_t)(B * H));
     const size_t rows = (size_t)(B * H * Ncap);
     memset(&w.tc, 0, sizeof(w.tc));
+    const int64_t kpad = (K + 255) / 256 * 256;
     w.tc.Lt = c.take<float>((size_t)(H * d * d));
     w.tc.chat = c.take<float>((size_t)(H * K * d));
+    w.tc.chat_rot = c.take<float>((size_t)(H * K * d));
     w.tc.scratch_norm = c.take<float>((size_t)(H * K));
-    w.tc.head_bits = c.take<uint32_t>((size_t)(H * 4));
-    w.tc.head = c.take<float>((size_t)(H * 4));
-    w.tc.scale = c.take<float>((size_t)H);
-    w.tc.planes = c.take<uint16_t>((size_t)(H * 3 * K * d));
-    w.tc.compact = c.take<uint16_t>(rows * (size_t)d);
+    w.tc.hneg = c.take<float>((size_t)(H * kpad));
+    w.tc.head_bits = c.take<uint32_t>((size_t)(2 * H * 4));
+    w.tc.head = c.take<float>((size_t)(2 * H * 4));
+    w.tc.scale = c.take<float>((size_t)(2 * H));
+    w.tc.planes = c.take<uint16_t>((size_t)(2 * H * 3 * K * d));
+    w.tc.compact = c.take<uint16_t>(2 * rows * (size_t)d);
     w.tc.row_map = c.take<int32_t>(rows);
+    w.tc.ccount = c.take<int32_t>((size_t)(B * H));
     w.tc.skip = c.take<uint8_t>(rows);
     w.tc.exact_list = c.take<int64_t>(rows);
     w.tc.exact_count = c.take<int32_t>(2);
@@ -282,7 +286,7 @@ int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, 
     cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, L, w.cp, w.half_norm, s);
     if (e != cudaSuccess) return cuda_fail(e);
     const Shape sh{B, H, Ncap, d};
-    if (tc_supported(dtype, d))
+    if (tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30))
         e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, L, ra,
                                    RowSel{rows, perm, count}, codes, s);
     else
@@ -323,7 +327,7 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
     if (beta == 1.0) {
         // beta = 1 is plain nearest-centroid VQ: the same argmin as the
         // H-weighted rule with L = I, so it reduces exactly by construction
-        if (tc_supported(dtype, d))
+        if (tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30))
             e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, nullptr, ra,
                                        RowSel{rows, perm, count}, codes, s);
         else

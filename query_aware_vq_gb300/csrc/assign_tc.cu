@@ -44,17 +44,21 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
 
 struct Params {
-    int32_t H, ncap, d, K, P;
-    int32_t num_bh, tiles_per_bh, nchunks;
+    int32_t H, d, K, P;
+    int32_t num_bh, seg, tiles_per_bh, nchunks, kpad;
+    int32_t out_ncap;          // rows per (b, h) of the keys and of codes
+    int64_t plane_rows;        // rows of one A plane in the A tensor map
     const int32_t* len;        // [B] or null
-    const int32_t* count;      // compact mode: rows per (b, h); null = natural mode
-    const int32_t* row_map;    // compact mode: original row of each compact row
+    const int32_t* count;      // compact list: rows per (b, h); null = natural order
+    const int32_t* row_map;    // compact list: row of the keys each entry stands for
     const uint8_t* skip;       // rows to leave untouched (bulk mode), or null
-    int32_t window;            // rows with t - j < window go to the exact list
-    const float* half_norm;    // [H, K]
+    int32_t skip_near;         // natural order: rows with t - j < skip_near belong to
+                               // the compact pass (0 = none)
+    const float* hneg;         // [H, kpad]: -|c_j L|^2 / 2, -FLT_MAX past K
     const float* head;         // [H, 4]: max |chat_j|, max h_j, 1/scale, abs error
-    float err_coef;            // relative error of the contraction (see host)
-    int32_t* codes;            // [num_bh * ncap]
+    float err_coef;            // relative error bound of the contraction (host)
+    float norm_slack;          // |x| from plane 0 times this bounds |x|
+    int32_t* codes;            // [num_bh * out_ncap]
     int64_t* exact_list;       // rows for the exact kernel
     int32_t* exact_count;
     int32_t* status;           // 0, or the code of a timed-out wait
@@ -168,7 +172,22 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Top two of a 32-value chunk by a merge tree of (max, second) pairs.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// (bits & ~31) | pos in one logic op: the column position rides in the five
+// low mantissa bits of the key.
+__device__ __forceinline__ float embed_pos(float v, uint32_t pos) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(__float_as_uint(v)), "r"(0xFFFFFFE0u),
+        "r"(pos));
+    return __uint_as_float(r);
+}
+
+// Top two of 32 keys: min/max of pairs, then a merge tree of (max, second)
+// pairs where each merge is max(h1, h2) and max3(min(h1, h2), l1, l2).
 __device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
     float hi[16], lo[16];
 #pragma unroll
@@ -181,9 +200,8 @@ __device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
 #pragma unroll
         for (int i = 0; i < w; i++) {
             const float h = fmaxf(hi[i], hi[i + w]);
-            const float l = fmaxf(fminf(hi[i], hi[i + w]), fmaxf(lo[i], lo[i + w]));
+            lo[i] = max3f(fminf(hi[i], hi[i + w]), lo[i], lo[i + w]);
             hi[i] = h;
-            lo[i] = l;
         }
     }
     t1 = hi[0];
@@ -199,34 +217,41 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int t) {
     TileInfo ti;
     ti.bh = t / p.tiles_per_bh;
     ti.r0 = (t % p.tiles_per_bh) * BM;
-    ti.nvalid = seq_len(p.len, ti.bh / p.H, p.ncap);
-    if (p.count) ti.nvalid = min(max(p.count[ti.bh], 0), ti.nvalid);
+    if (p.count) {
+        ti.nvalid = min(max(p.count[ti.bh], 0), p.seg);
+    } else {
+        ti.nvalid = seq_len(p.len, ti.bh / p.H, p.out_ncap);
+        // rows of the compact pass never enter this tile
+        if (p.skip_near > 0) ti.nvalid = max(ti.nvalid - p.skip_near, 0);
+    }
     ti.skip = ti.r0 >= ti.nvalid;
     return ti;
 }
 
-template <int DK, int AST, int BST>
+template <int DK, int PA, int AST, int BST>
 struct Smem {
-    static constexpr int kA = BM * 128;        // bytes of one 64-element k-block of A
-    static constexpr int kB = BN * 128;        // bytes of one B stage
-    static constexpr int kABytes = AST * DK * kA;
+    static constexpr int kA = BM * 128;        // one 64-element k-block of one A plane
+    static constexpr int kB = BN * 128;        // one B stage
+    static constexpr int kABytes = AST * PA * DK * kA;
     static constexpr int kBBytes = BST * kB;
-    static constexpr int kBarOff = kABytes + kBBytes;
-    static constexpr int kBars = 2 * AST + 2 * BST + 6;
+    static constexpr int kHOff = kABytes + kBBytes;          // 2 x 256 floats of -h
+    static constexpr int kBarOff = kHOff + 2 * BN * 4;
+    static constexpr int kBars = 2 * AST + 2 * BST + 10;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
     static constexpr int kTotal = kMergeOff + 4 * 32 * 16 + 1024;  // + alignment slack
 };
 
-template <bool BF16, int DK, int AST, int BST>
+template <bool BF16, int DK, int PA, int AST, int BST>
 __global__ void __launch_bounds__(kThreads, 1)
 assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const Params p) {
-    using S = Smem<DK, AST, BST>;
+    using S = Smem<DK, PA, AST, BST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     uint8_t* smA = sm;
     uint8_t* smB = sm + S::kABytes;
+    float* smH = reinterpret_cast<float*>(sm + S::kHOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBarOff);
     uint64_t* a_full = bars;
     uint64_t* a_empty = bars + AST;
@@ -234,8 +259,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* b_empty = bars + 2 * AST + BST;
     uint64_t* acc_full = bars + 2 * AST + 2 * BST;
     uint64_t* acc_empty = acc_full + 2;
-    uint64_t* merge_full = acc_full + 4;   // column-half 1 -> half 0 handoff per tile
-    uint64_t* merge_empty = acc_full + 5;
+    uint64_t* h_full = acc_full + 4;
+    uint64_t* h_empty = acc_full + 6;
+    uint64_t* merge_full = acc_full + 8;   // column-half handoff, after the h ring
+    uint64_t* merge_empty = acc_full + 9;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
 
@@ -254,6 +281,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int i = 0; i < 2; i++) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], kEpiWarps);
+            mbar_init(&h_full[i], 1);
+            mbar_init(&h_empty[i], kEpiWarps);
         }
         mbar_init(merge_full, kEpiWarps / 2);
         mbar_init(merge_empty, kEpiWarps / 2);
@@ -274,7 +303,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
-            uint32_t a_it = 0, b_it = 0;
+            uint32_t a_it = 0, b_it = 0, h_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info(p, t);
@@ -282,14 +311,28 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_empty[sa], ((a_it / AST) & 1) ^ 1, p.status, 1);
                 if (!ok) break;
-                mbar_expect_tx(&a_full[sa], DK * S::kA);
-                const int row0 = ti.bh * p.ncap + ti.r0;
+                mbar_expect_tx(&a_full[sa], PA * DK * S::kA);
+                const int row0 = ti.bh * p.seg + ti.r0;
 #pragma unroll
-                for (int kb = 0; kb < DK; kb++)
-                    tma_2d(smA + (sa * DK + kb) * S::kA, &tmA, &a_full[sa], kb * BK, row0);
+                for (int pa = 0; pa < PA; pa++)
+#pragma unroll
+                    for (int kb = 0; kb < DK; kb++)
+                        tma_2d(smA + ((sa * PA + pa) * DK + kb) * S::kA, &tmA, &a_full[sa], kb * BK,
+                               (int)(pa * p.plane_rows) + row0);
                 a_it++;
                 const int h = ti.bh % p.H;
-                for (int c = 0; c < p.nchunks && ok; c++)
+                for (int c = 0; c < p.nchunks && ok; c++) {
+                    const int hs = h_it & 1;
+                    ok = mbar_wait(&h_empty[hs], ((h_it >> 1) & 1) ^ 1, p.status, 11);
+                    if (!ok) break;
+                    mbar_expect_tx(&h_full[hs], BN * 4);
+                    asm volatile(
+                        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                        "%2, [%3];" ::"r"(su32(smH + hs * BN)),
+                        "l"(p.hneg + (int64_t)h * p.kpad + c * BN), "r"(BN * 4),
+                        "r"(su32(&h_full[hs]))
+                        : "memory");
+                    h_it++;
                     for (int pl = 0; pl < p.P && ok; pl++)
                         for (int kb = 0; kb < DK; kb++) {
                             const int sb = b_it % BST;
@@ -300,6 +343,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                    h * p.P + pl);
                             b_it++;
                         }
+                }
             }
             // every issued copy has landed before the CTA may leave
             for (int s = 0; s < BST; s++)
@@ -311,6 +355,11 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (a_it > (uint32_t)s) {
                     const uint32_t last = a_it - 1 - ((a_it - 1 - s) % AST);
                     mbar_wait(&a_full[last % AST], (last / AST) & 1, p.status, 3);
+                }
+            for (int s = 0; s < 2; s++)
+                if (h_it > (uint32_t)s) {
+                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % 2);
+                    mbar_wait(&h_full[last % 2], (last / 2) & 1, p.status, 3);
                 }
         }
     } else if (warp == 1) {
@@ -340,13 +389,19 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             ok = mbar_wait(&b_full[sb], (b_it / BST) & 1, p.status, 6);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t a_base = su32(smA + (sa * DK + kb) * S::kA);
                             const uint32_t b_base = su32(smB + sb * S::kB);
 #pragma unroll
-                            for (int ks = 0; ks < BK / 16; ks++) {
-                                tc_mma(d_tmem, sw128_desc(a_base + ks * 32),
-                                       sw128_desc(b_base + ks * 32), idesc, accumulate);
-                                accumulate = 1;
+                            for (int pa = 0; pa < PA; pa++) {
+                                // products of order pa + pl > 2 are below 2^-24
+                                if (pa + pl > 2) continue;
+                                const uint32_t a_base =
+                                    su32(smA + ((sa * PA + pa) * DK + kb) * S::kA);
+#pragma unroll
+                                for (int ks = 0; ks < BK / 16; ks++) {
+                                    tc_mma(d_tmem, sw128_desc(a_base + ks * 32),
+                                           sw128_desc(b_base + ks * 32), idesc, accumulate);
+                                    accumulate = 1;
+                                }
                             }
                             tc_commit(&b_empty[sb]);
                             b_it++;
@@ -373,12 +428,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int sa = a_it % AST;
             ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 7);
             if (!ok) break;
-            // |x|^2 of this row from the swizzled tile (order does not matter)
+            // |x|^2 of this row from the swizzled tile of plane 0 (order does not matter)
             float nrm = 0.f;
             if (half == 0) {
 #pragma unroll
                 for (int kb = 0; kb < DK; kb++) {
-                    const uint8_t* rowp = smA + (sa * DK + kb) * S::kA + row_in_tile * 128;
+                    const uint8_t* rowp = smA + (sa * PA * DK + kb) * S::kA + row_in_tile * 128;
 #pragma unroll
                     for (int c = 0; c < 8; c++) {
                         const uint4 raw = *reinterpret_cast<const uint4*>(
@@ -408,13 +463,15 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
             float m1 = -FLT_MAX, m2 = -FLT_MAX;
             int32_t c1 = 0;
-            const float* hn = p.half_norm + (int64_t)h * p.K;
             const float inv_scale = p.head[h * 4 + 2];
+            const float2 inv2 = make_float2(inv_scale, inv_scale);
             for (int c = 0; c < p.nchunks && ok; c++) {
                 const int acc = acc_it & 1;
-                ok = mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
+                ok = mbar_wait(&h_full[acc], (acc_it >> 1) & 1, p.status, 12) &&
+                     mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
+                const float2* hrow = reinterpret_cast<const float2*>(smH + acc * BN);
 #pragma unroll 1
                 for (int sub = 0; sub < 4; sub++) {
                     const int col = half * 128 + sub * 32;
@@ -422,38 +479,28 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     A2ATS_TMEM_LD32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + col),
                                     r);
                     tmem_wait_ld();
-                    const int j0 = c * BN + col;
                     float key[32];
-                    if (j0 + 32 <= p.K && (p.K & 3) == 0) {
-                        const float4* h4 = reinterpret_cast<const float4*>(hn + j0);
 #pragma unroll
-                        for (int u = 0; u < 8; u++) {
-                            const float4 hv = __ldg(h4 + u);
-                            key[4 * u + 0] = fmaf(__uint_as_float(r[4 * u + 0]), inv_scale, -hv.x);
-                            key[4 * u + 1] = fmaf(__uint_as_float(r[4 * u + 1]), inv_scale, -hv.y);
-                            key[4 * u + 2] = fmaf(__uint_as_float(r[4 * u + 2]), inv_scale, -hv.z);
-                            key[4 * u + 3] = fmaf(__uint_as_float(r[4 * u + 3]), inv_scale, -hv.w);
-                        }
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 32; u++)
-                            key[u] = (j0 + u < p.K)
-                                         ? fmaf(__uint_as_float(r[u]), inv_scale, -hn[j0 + u])
-                                         : -FLT_MAX;
+                    for (int u = 0; u < 16; u++) {
+                        const float2 a2 =
+                            make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+                        const float2 v2 = __ffma2_rn(a2, inv2, hrow[(col >> 1) + u]);
+                        key[2 * u] = embed_pos(v2.x, 31u - 2 * u);
+                        key[2 * u + 1] = embed_pos(v2.y, 30u - 2 * u);
                     }
-#pragma unroll
-                    for (int u = 0; u < 32; u++)
-                        key[u] = __uint_as_float((__float_as_uint(key[u]) & ~31u) | (31u - u));
                     float t1, t2;
                     top2_32(key, t1, t2);
+                    const int j0 = c * BN + col;
                     if (t1 > m1) c1 = j0 >> 5;
-                    const float n1 = fmaxf(m1, t1);
-                    m2 = fmaxf(fminf(m1, t1), fmaxf(m2, t2));
-                    m1 = n1;
+                    m2 = max3f(fminf(m1, t1), m2, t2);
+                    m1 = fmaxf(m1, t1);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[acc]);
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[acc]);
+                    mbar_arrive(&h_empty[acc]);
+                }
                 acc_it++;
             }
             if (!ok) break;
@@ -471,7 +518,6 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_empty);
                 const int32_t oc = __float_as_int(o.z);
-                // keys are distinct (column bits), so only the order matters
                 if (o.x > m1) {
                     m2 = fmaxf(m1, o.y);
                     m1 = o.x;
@@ -481,25 +527,25 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 const int32_t ri = ti.r0 + row_in_tile;
                 if (ri < ti.nvalid) {
-                    const int32_t j = p.row_map ? p.row_map[(int64_t)ti.bh * p.ncap + ri] : ri;
-                    const int32_t Lb = seq_len(p.len, ti.bh / p.H, p.ncap);
+                    const int32_t j = p.row_map ? p.row_map[(int64_t)ti.bh * p.seg + ri] : ri;
+                    const int32_t Lb = seq_len(p.len, ti.bh / p.H, p.out_ncap);
                     if (j >= 0 && j < Lb) {
-                        const int64_t out = (int64_t)ti.bh * p.ncap + j;
+                        const int64_t out = (int64_t)ti.bh * p.out_ncap + j;
                         const bool skip = p.skip && p.skip[out];
-                        const bool near = p.window > 0 && (Lb - 1 - j) < p.window;
                         // bound on |v_hat - v| for every centroid, plus the
                         // perturbation of the column bits in both keys
+                        const float xn = sqrtf(nrm) * p.norm_slack;
                         const float cmax = p.head[h * 4 + 0], hmax = p.head[h * 4 + 1];
-                        const float e = p.err_coef * (sqrtf(nrm) * 1.0001f * cmax + hmax) +
-                                        p.head[h * 4 + 3] * sqrtf(nrm);
+                        const float e = p.err_coef * (xn * cmax + hmax) + p.head[h * 4 + 3] * xn;
                         const float mag = fmaxf(fabsf(m1), fabsf(m2));
                         const float tau = 2.f * e + 64.f * mag * 1.1920929e-07f;
                         if (!skip) {
-                            if (near || !(m1 - m2 > tau)) {
+                            if (!(m1 - m2 > tau)) {
                                 const int32_t slot = atomicAdd(p.exact_count, 1);
                                 p.exact_list[slot] = out;
                             } else {
-                                p.codes[out] = c1 * 32 + (31 - (int32_t)(__float_as_uint(m1) & 31u));
+                                p.codes[out] =
+                                    c1 * 32 + (31 - (int32_t)(__float_as_uint(m1) & 31u));
                             }
                         }
                     }
@@ -519,31 +565,34 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 // -------------------------------------------------- codebook preparation --
-// In place on chat [H, K, d] fp32: optional rotation by -far_offset (so far
-// keys can enter the contraction unrotated), then per-head maxima into
-// head_bits [H, 4] (uint bits of non-negative floats; zeroed by the caller):
-// max |chat_j|, max h_j, max |element|.
-__global__ void codebook_stats_kernel(float* __restrict__ chat, int64_t HK, int64_t K,
-                                      int32_t d, const RopeArgs ra, int32_t rotate,
-                                      const float* __restrict__ half_norm,
+// rot = RoPE(chat, -far_offset) for every centroid (far keys enter the
+// contraction unrotated, so their shared rotation moves to the codebook).
+__global__ void rotate_rows_kernel(const float* __restrict__ in, int64_t rows, int32_t d,
+                                   const RopeArgs ra, float* __restrict__ out) {
+    const int halfd = d / 2;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < rows * halfd;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = e / halfd;
+        const int i = (int)(e % halfd);
+        const int a = ra.interleaved ? 2 * i : i;
+        const int b = ra.interleaved ? 2 * i + 1 : i + halfd;
+        float s, c;
+        rope_angle(-ra.far_offset, ra.omega_hi[i], ra.omega_lo[i], ra, s, c);
+        const float xa = in[r * d + a], xb = in[r * d + b];
+        out[r * d + a] = fmaf(xa, c, -__fmul_rn(xb, s));
+        out[r * d + b] = fmaf(xa, s, __fmul_rn(xb, c));
+    }
+}
+
+// Per-head maxima into head_bits [H, 4] (uint bits of non-negative floats,
+// zeroed by the caller): max |chat_j|, max h_j, max |element|.
+__global__ void codebook_stats_kernel(const float* __restrict__ chat, int64_t HK, int64_t K,
+                                      int32_t d, const float* __restrict__ half_norm,
                                       uint32_t* __restrict__ head_bits) {
     const int lane = threadIdx.x & 31;
     for (int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < HK;
          j += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-        float* row = chat + j * d;
-        if (rotate) {
-            const int halfd = d / 2;
-            for (int i = lane; i < halfd; i += 32) {
-                float s, c;
-                rope_angle(-ra.far_offset, ra.omega_hi[i], ra.omega_lo[i], ra, s, c);
-                const int a = ra.interleaved ? 2 * i : i;
-                const int b = ra.interleaved ? 2 * i + 1 : i + halfd;
-                const float xa = row[a], xb = row[b];
-                row[a] = fmaf(xa, c, -__fmul_rn(xb, s));
-                row[b] = fmaf(xa, s, __fmul_rn(xb, c));
-            }
-            __syncwarp();
-        }
+        const float* row = chat + j * d;
         Dot2 n;
         float mx = 0.f;
         for (int a = lane; a < d; a += 32) {
@@ -565,9 +614,10 @@ __global__ void codebook_stats_kernel(float* __restrict__ chat, int64_t HK, int6
 }
 
 // head [H, 4] floats from the raw maxima: max |chat|, max h, 1/scale, abs err.
-// bf16 planes: scale 1.  fp16 planes: a power of two that puts the largest
-// element near 2^14; elements that fall into the fp16 subnormal range are
-// covered by the absolute error term (per unit of |x|).
+// unit_scale: planes are bf16 or the raw 16-bit codebook (scale 1).  fp16
+// planes: a power of two that puts the largest element near 2^14; elements in
+// the fp16 subnormal range are covered by the absolute error term (per unit
+// of |x|).
 __global__ void head_finish_kernel(const uint32_t* __restrict__ head_bits, int32_t H, int32_t d,
                                    int32_t unit_scale, float* __restrict__ head,
                                    float* __restrict__ scale) {
@@ -591,6 +641,16 @@ __global__ void head_finish_kernel(const uint32_t* __restrict__ head_bits, int32
     head[h * 4 + 2] = 1.f / sc;
     head[h * 4 + 3] = abs_err;
     scale[h] = sc;
+}
+
+// hneg [H, kpad] = -half_norm, and -FLT_MAX past K (those columns never win).
+__global__ void pad_half_norm_kernel(const float* __restrict__ half_norm, int64_t H, int64_t K,
+                                     int64_t kpad, float* __restrict__ hneg) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < H * kpad;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t h = i / kpad, j = i % kpad;
+        hneg[i] = j < K ? -half_norm[h * K + j] : -FLT_MAX;
+    }
 }
 
 // planes [H, P, K, d] (16-bit) of chat * scale: plane p is the rounding of
@@ -623,28 +683,85 @@ __global__ void codebook_planes_kernel(const float* __restrict__ chat, int64_t K
     }
 }
 
-// ------------------------------------------------------- row gathering --
-// Compact copy of the retrieval rows of each (b, h): row i of the compact
-// block is row perm[i] of the keys (16-byte vectors), row_map[i] = perm[i].
-__global__ void gather_rows_kernel(const void* __restrict__ x, int32_t esize, int32_t H,
-                                   int32_t ncap, int32_t d, const int32_t* __restrict__ len,
-                                   const int32_t* __restrict__ perm,
-                                   const int32_t* __restrict__ count, void* __restrict__ compact,
-                                   int32_t* __restrict__ row_map) {
+// ------------------------------------------------------ compact rows --
+// The rows of one pass that cannot use the stored keys as they are: rows
+// inside the RoPE window (natural order), or every retrieval row (routed
+// mode).  Each is rotated in fp32 and split into two 16-bit planes
+// hi = rn(k~), lo = rn(k~ - hi); planes [2][nbh * ncap][d].  Rows whose fp16
+// planes would overflow go to the exact list instead.
+template <int DT>
+__global__ void __launch_bounds__(256)
+compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
+                    const int32_t* __restrict__ len, const RopeArgs ra, int32_t mode,
+                    const int32_t* __restrict__ perm, const int32_t* __restrict__ count,
+                    uint16_t* __restrict__ planes, int32_t* __restrict__ row_map,
+                    int32_t* __restrict__ ccount, int64_t* __restrict__ exact_list,
+                    int32_t* __restrict__ exact_count) {
+    using T = typename Elem<DT>::T;
     const int bh = blockIdx.y;
     const int32_t L = seq_len(len, bh / H, ncap);
-    const int32_t cnt = min(max(count[bh], 0), L);
-    const int vec = d * esize / 16;  // 16-byte vectors per row
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    uint4* dst = reinterpret_cast<uint4*>(compact);
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < (int64_t)cnt * vec;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t i = (int32_t)(e / vec), v = (int32_t)(e % vec);
-        int32_t j = perm[(int64_t)bh * ncap + i];
-        const bool valid = j >= 0 && j < L;
-        if (v == 0) row_map[(int64_t)bh * ncap + i] = valid ? j : -1;
-        dst[((int64_t)bh * ncap + i) * vec + v] =
-            valid ? src[((int64_t)bh * ncap + j) * vec + v] : make_uint4(0, 0, 0, 0);
+    int32_t n;
+    if (mode == 1) {
+        n = min(max(count[bh], 0), L);
+    } else {
+        n = (ra.enabled && ra.window > 0) ? min(L, ra.window) : 0;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) ccount[bh] = n;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int halfd = d / 2;
+    const int64_t plane_rows = (int64_t)gridDim.y * ncap;
+    for (int32_t i = blockIdx.x * 8 + w; i < n; i += gridDim.x * 8) {
+        int32_t j = mode == 1 ? perm[(int64_t)bh * ncap + i] : L - n + i;
+        if (j < 0 || j >= L) {
+            if (lane == 0) row_map[(int64_t)bh * ncap + i] = -1;
+            continue;
+        }
+        const int64_t src = ((int64_t)bh * ncap + j) * d;
+        const int64_t dst = ((int64_t)bh * ncap + i) * d;
+        const int32_t pos = ra.enabled ? rope_position(j, L - 1, ra) : 0;
+        bool over = false;
+        for (int pi = lane; pi < halfd; pi += 32) {
+            const int a = ra.interleaved ? 2 * pi : pi;
+            const int b = ra.interleaved ? 2 * pi + 1 : pi + halfd;
+            float xa = load1<DT>(x, src + a), xb = load1<DT>(x, src + b);
+            if (pos != 0) {
+                float s, c;
+                rope_angle(pos, ra.omega_hi[pi], ra.omega_lo[pi], ra, s, c);
+                const float ya = fmaf(xa, c, -__fmul_rn(xb, s));
+                const float yb = fmaf(xa, s, __fmul_rn(xb, c));
+                xa = ya;
+                xb = yb;
+            }
+            const float vals[2] = {xa, xb};
+            const int idx[2] = {a, b};
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                uint16_t hb, lb;
+                if (DT == kBF16) {
+                    const __nv_bfloat16 hv = __float2bfloat16_rn(vals[u]);
+                    const __nv_bfloat16 lv = __float2bfloat16_rn(vals[u] - __bfloat162float(hv));
+                    hb = __bfloat16_as_ushort(hv);
+                    lb = __bfloat16_as_ushort(lv);
+                } else {
+                    const __half hv = __float2half_rn(vals[u]);
+                    const __half lv = __float2half_rn(vals[u] - __half2float(hv));
+                    over |= !(fabsf(vals[u]) <= 65504.f);
+                    hb = __half_as_ushort(hv);
+                    lb = __half_as_ushort(lv);
+                }
+                planes[dst + idx[u]] = hb;
+                planes[plane_rows * d + dst + idx[u]] = lb;
+            }
+        }
+        over = __any_sync(0xffffffffu, over);
+        if (lane == 0) {
+            if (over) {
+                row_map[(int64_t)bh * ncap + i] = -1;
+                exact_list[atomicAdd(exact_count, 1)] = (int64_t)bh * ncap + j;
+            } else {
+                row_map[(int64_t)bh * ncap + i] = j;
+            }
+        }
     }
 }
 
@@ -771,11 +888,17 @@ int sm_count() {
     return n;
 }
 
-template <bool BF16, int DK, int AST, int BST>
+unsigned blocks_for(int64_t n, int per, unsigned cap) {
+    const int64_t b = (n + per - 1) / per;
+    return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+template <bool BF16, int DK, int PA, int AST, int BST>
 cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                           cudaStream_t st) {
-    using S = Smem<DK, AST, BST>;
-    auto k = assign_tc_kernel<BF16, DK, AST, BST>;
+    using S = Smem<DK, PA, AST, BST>;
+    static_assert(S::kTotal <= 232448, "shared memory budget");
+    auto k = assign_tc_kernel<BF16, DK, PA, AST, BST>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
     if (e != cudaSuccess) return e;
     const int tiles = p.num_bh * p.tiles_per_bh;
@@ -785,15 +908,135 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const Pa
     return cudaGetLastError();
 }
 
-template <bool BF16>
+template <bool BF16, int PA>
 cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                             cudaStream_t st) {
-    switch (p.d) {
-        case 64: return launch_kernel<BF16, 1, 2, 4>(ta, tb, p, st);
-        case 128: return launch_kernel<BF16, 2, 2, 4>(ta, tb, p, st);
-        case 192: return launch_kernel<BF16, 3, 1, 4>(ta, tb, p, st);
-        default: return launch_kernel<BF16, 4, 1, 4>(ta, tb, p, st);
+    if constexpr (PA == 1) {
+        switch (p.d) {
+            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 2, 4>(ta, tb, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 4>(ta, tb, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 4>(ta, tb, p, st);
+        }
     }
+    else {
+        switch (p.d) {
+            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, p, st);
+        }
+    }
+}
+
+bool encode(CUtensorMap* m, bool bf16, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                       (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One codebook operand: the planes (or the raw codebook) and its head table.
+struct BSide {
+    const void* src;
+    int P;
+    bool exact;           // products exact without planes (raw 16-bit codebook)
+    const float* head;
+};
+
+cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide& out,
+                      cudaStream_t st) {
+    const bool bf16 = c.dt == kBF16;
+    const int64_t H = c.s.H, K = c.K, d = c.s.d;
+    codebook_stats_kernel<<<blocks_for(H * K * 32, 256, 4096), 256, 0, st>>>(
+        chat, H * K, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
+    note_launches(1);
+    head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
+        c.head_bits + v * H * 4, (int32_t)H, (int32_t)d, (bf16 || raw) ? 1 : 0, c.head + v * H * 4,
+        c.scale + v * H);
+    note_launches(1);
+    out.head = c.head + v * H * 4;
+    out.exact = raw;
+    if (raw) {
+        out.src = c.codebook;
+        out.P = 1;
+    } else {
+        out.P = bf16 ? 3 : 2;
+        uint16_t* planes = c.planes + (size_t)v * H * 3 * K * d;
+        if (bf16)
+            codebook_planes_kernel<true><<<blocks_for(H * K * d, 256, 8192), 256, 0, st>>>(
+                chat, K, (int32_t)d, out.P, (int32_t)H, c.scale + v * H, planes);
+        else
+            codebook_planes_kernel<false><<<blocks_for(H * K * d, 256, 8192), 256, 0, st>>>(
+                chat, K, (int32_t)d, out.P, (int32_t)H, c.scale + v * H, planes);
+        note_launches(1);
+        out.src = planes;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, int64_t plane_rows,
+                     const int32_t* count, const int32_t* row_map, const uint8_t* skip,
+                     int32_t skip_near, cudaStream_t st) {
+    const bool bf16 = c.dt == kBF16;
+    const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
+    CUtensorMap ta, tb;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(PA * nbh * ncap)};
+        const cuuint64_t strides[1] = {(cuuint64_t)(d * 2)};
+        const cuuint32_t box[2] = {BK, BM};
+        if (!encode(&ta, bf16, 2, asrc, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)K, (cuuint64_t)(H * b.P)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(K * d * 2)};
+        const cuuint32_t box[3] = {BK, BN, 1};
+        if (!encode(&tb, bf16, 3, b.src, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.H = (int32_t)H;
+    p.d = (int32_t)d;
+    p.K = (int32_t)K;
+    p.P = b.P;
+    p.num_bh = (int32_t)nbh;
+    p.seg = (int32_t)ncap;
+    p.tiles_per_bh = (int32_t)((ncap + BM - 1) / BM);
+    p.nchunks = (int32_t)((K + BN - 1) / BN);
+    p.kpad = p.nchunks * BN;
+    p.out_ncap = (int32_t)ncap;
+    p.plane_rows = plane_rows;
+    p.len = c.len;
+    p.count = count;
+    p.row_map = row_map;
+    p.skip = skip;
+    p.skip_near = skip_near;
+    p.hneg = c.hneg;
+    p.head = b.head;
+    // The products are exact; the tensor core adds (d/16 per operand pair)
+    // partial sums into fp32, each addition off by at most 2^-23 of the
+    // running magnitude, which |x| max|chat| + max h bounds; plus the rounding
+    // of chat and of the planes that are dropped, of the two-plane row
+    // operand, and of h and of acc - h.
+    int pairs = 0;
+    for (int pb = 0; pb < b.P; pb++)
+        for (int pa = 0; pa < PA; pa++)
+            if (pa + pb <= 2) pairs++;
+    double coef = ((double)pairs * (double)(d / 16) + 8.0) * 0x1p-22;
+    if (!b.exact) coef += bf16 ? 0x1p-21 : 0x1p-20;
+    if (PA == 2) coef += bf16 ? 0x1p-15 : 0x1p-20;
+    p.err_coef = (float)coef;
+    p.norm_slack = PA == 2 ? 1.01f : 1.0001f;
+    p.codes = c.codes;
+    p.exact_list = c.exact_list;
+    p.exact_count = c.exact_count;
+    p.status = c.exact_count + 1;
+    if (p.num_bh * p.tiles_per_bh == 0) return cudaSuccess;
+    if (PA == 1)
+        return bf16 ? launch_by_width<true, 1>(ta, tb, p, st) : launch_by_width<false, 1>(ta, tb, p, st);
+    return bf16 ? launch_by_width<true, 2>(ta, tb, p, st) : launch_by_width<false, 2>(ta, tb, p, st);
 }
 
 }  // namespace tc
@@ -803,24 +1046,27 @@ bool tc_supported(int dt, int64_t d) {
            tc::encode_fn() != nullptr;
 }
 
-size_t tc_workspace_floats(int64_t H, int64_t K, int64_t d) {
-    return (size_t)(H * K * d);  // chat
-}
-
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     using namespace tc;
-    const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
-    const size_t esz = 2;
+    const int64_t kpad = (K + BN - 1) / BN * BN;
+    const bool rot = c.ra.enabled && c.ra.far_offset != 0;
+    const bool natural = c.sel.mode != 1;
+    const bool compact = c.sel.mode == 1 || (c.ra.enabled && c.ra.window > 0);
+    const bool need_u = compact || (natural && !rot);
+    const bool need_r = natural && rot;
     cudaError_t e;
-    // 1. transformed codebook chat (fp32) unless the raw codebook is exact
-    const bool exact_plain = !c.L && !(c.ra.enabled && c.ra.far_offset != 0);
-    const int P = exact_plain ? 1 : (bf16 ? 3 : 2);
-    e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 4 * H, st);
+
+    e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
     if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 2, st);  // count and status
+    if (e != cudaSuccess) return e;
+    pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K, kpad,
+                                                                         c.hneg);
+    note_launches(1);
+    // chat = c L L^T (the codebook side of the contraction), fp32
     if (c.L) {
-        transpose_kernel<<<(unsigned)((H * d * d + 255) / 256 < 4096 ? (H * d * d + 255) / 256 : 4096),
-                           256, 0, st>>>(c.L, H, (int32_t)d, c.Lt);
+        transpose_kernel<<<blocks_for(H * d * d, 256, 4096), 256, 0, st>>>(c.L, H, (int32_t)d, c.Lt);
         note_launches(1);
         e = launch_codebook_transform(c.cp, kF32, H, K, d, c.Lt, c.chat, c.scratch_norm, st);
         if (e != cudaSuccess) return e;
@@ -828,118 +1074,50 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         e = cudaMemcpyAsync(c.chat, c.cp, sizeof(float) * H * K * d, cudaMemcpyDeviceToDevice, st);
         if (e != cudaSuccess) return e;
     }
-    {
-        const int64_t HK = H * K;
-        const unsigned blocks = (unsigned)((HK * 32 + 255) / 256 < 4096 ? (HK * 32 + 255) / 256 : 4096);
-        codebook_stats_kernel<<<blocks, 256, 0, st>>>(c.chat, HK, K, (int32_t)d, c.ra,
-                                                      c.ra.enabled && c.ra.far_offset != 0,
-                                                      c.half_norm, c.head_bits);
+    BSide bu{}, br{};
+    if (need_u && (e = prepare_b(c, c.chat, 0, c.L == nullptr, bu, st)) != cudaSuccess) return e;
+    if (need_r) {
+        rotate_rows_kernel<<<blocks_for(H * K * (d / 2), 256, 8192), 256, 0, st>>>(
+            c.chat, H * K, (int32_t)d, c.ra, c.chat_rot);
         note_launches(1);
-        head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
-            c.head_bits, (int32_t)H, (int32_t)d, (bf16 || exact_plain) ? 1 : 0, c.head, c.scale);
-        note_launches(1);
+        if ((e = prepare_b(c, c.chat_rot, 1, false, br, st)) != cudaSuccess) return e;
     }
-    const void* bsrc = c.codebook;
-    if (!exact_plain) {
-        const int64_t n = H * K * d;
-        const unsigned blocks = (unsigned)((n + 255) / 256 < 8192 ? (n + 255) / 256 : 8192);
-        if (bf16)
-            codebook_planes_kernel<true><<<blocks, 256, 0, st>>>(c.chat, K, (int32_t)d, P,
-                                                                 (int32_t)H, c.scale, c.planes);
-        else
-            codebook_planes_kernel<false><<<blocks, 256, 0, st>>>(c.chat, K, (int32_t)d, P,
-                                                                  (int32_t)H, c.scale, c.planes);
-        note_launches(1);
-        bsrc = c.planes;
-    }
-    // 2. row selection
-    const void* asrc = c.x;
-    const int32_t* row_map = nullptr;
-    const int32_t* count = nullptr;
     const uint8_t* skip = nullptr;
-    if (c.sel.mode == 1) {
-        dim3 g((unsigned)((ncap * (d * esz / 16) + 255) / 256 < 256 ? (ncap * (d * esz / 16) + 255) / 256 : 256),
-               (unsigned)nbh);
-        gather_rows_kernel<<<g, 256, 0, st>>>(c.x, (int32_t)esz, (int32_t)H, (int32_t)ncap,
-                                              (int32_t)d, c.len, c.sel.perm, c.sel.count,
-                                              c.compact, c.row_map);
-        note_launches(1);
-        asrc = c.compact;
-        row_map = c.row_map;
-        count = c.sel.count;
-    } else if (c.sel.mode == 2) {
+    if (c.sel.mode == 2) {
         e = cudaMemsetAsync(c.skip, 0, (size_t)(nbh * ncap), st);
         if (e != cudaSuccess) return e;
-        dim3 g((unsigned)((ncap + 255) / 256 < 64 ? (ncap + 255) / 256 : 64), (unsigned)nbh);
+        dim3 g(blocks_for(ncap, 256, 64), (unsigned)nbh);
         mark_rows_kernel<<<g, 256, 0, st>>>((int32_t)H, (int32_t)ncap, c.len, c.sel.perm,
                                             c.sel.count, c.skip);
         note_launches(1);
         skip = c.skip;
     }
-    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 2, st);  // count and status
-    if (e != cudaSuccess) return e;
-    // 3. tensor maps
-    CUtensorMap ta, tb;
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(nbh * ncap)};
-        const cuuint64_t strides[1] = {(cuuint64_t)(d * esz)};
-        const cuuint32_t box[2] = {BK, BM};
-        const cuuint32_t es[2] = {1, 1};
-        if (encode_fn()(&ta, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        2, const_cast<void*>(asrc), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)K, (cuuint64_t)(H * P)};
-        const cuuint64_t strides[2] = {(cuuint64_t)(d * esz), (cuuint64_t)(K * d * esz)};
-        const cuuint32_t box[3] = {BK, BN, 1};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (encode_fn()(&tb, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void*>(bsrc), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    // 4. the contraction
-    Params p;
-    p.H = (int32_t)H;
-    p.ncap = (int32_t)ncap;
-    p.d = (int32_t)d;
-    p.K = (int32_t)K;
-    p.P = P;
-    p.num_bh = (int32_t)nbh;
-    p.tiles_per_bh = (int32_t)((ncap + BM - 1) / BM);
-    p.nchunks = (int32_t)((K + BN - 1) / BN);
-    p.len = c.len;
-    p.count = count;
-    p.row_map = row_map;
-    p.skip = skip;
-    p.window = c.ra.enabled ? c.ra.window : 0;
-    p.half_norm = c.half_norm;
-    p.head = c.head;
-    // products are exact; the tensor core adds (d/16 per plane) partial sums
-    // into fp32, each addition off by at most 2^-23 of the running magnitude,
-    // which |x| max|chat| bounds; plus the rounding of chat (fp32) and of the
-    // planes that are dropped, and of h and of acc - h.
-    const double steps = (double)P * (double)(d / 16);
-    double coef = (steps + 8.0) * 0x1p-22;
-    if (!exact_plain) coef += bf16 ? 0x1p-20 : (0x1p-21 + 0x1p-20);
-    p.err_coef = (float)coef;
-    p.codes = c.codes;
-    p.exact_list = c.exact_list;
-    p.exact_count = c.exact_count;
-    p.status = c.exact_count + 1;
-    if (p.num_bh * p.tiles_per_bh > 0) {
-        e = bf16 ? launch_by_width<true>(ta, tb, p, st) : launch_by_width<false>(ta, tb, p, st);
+    // far rows in stored order: the keys themselves are the row operand
+    if (natural) {
+        const int32_t skip_near = (c.ra.enabled && c.ra.window > 0) ? c.ra.window : 0;
+        e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, st);
         if (e != cudaSuccess) return e;
     }
-    // 5. rows the contraction could not decide
+    // rotated rows (the RoPE window, or every routed row) as two 16-bit planes
+    if (compact) {
+        dim3 g(blocks_for(ncap, 8, 1024), (unsigned)nbh);
+        if (c.dt == kBF16)
+            compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
+                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 1 ? 1 : 0,
+                c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
+                c.exact_count);
+        else
+            compact_rows_kernel<kF16><<<g, 256, 0, st>>>(
+                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 1 ? 1 : 0,
+                c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
+                c.exact_count);
+        note_launches(1);
+        e = run_pass(c, bu, 2, c.compact, nbh * ncap, c.ccount, c.row_map, skip, 0, st);
+        if (e != cudaSuccess) return e;
+    }
+    // rows the contraction could not decide
     const unsigned lg = (unsigned)(sm_count() * 4);
-    if (bf16)
+    if (c.dt == kBF16)
         exact_list_kernel<kBF16><<<lg, 256, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
                                                      c.len, c.ra, c.L, c.cp, K, c.exact_list,
                                                      c.exact_count, c.codes);

@@ -91,14 +91,17 @@ struct TcCall {
     int32_t* codes;
     // workspace
     float* Lt;            // [H, d, d]
-    float* chat;          // [H, K, d]
+    float* chat;          // [H, K, d]  c L L^T
+    float* chat_rot;      // [H, K, d]  the same, rotated by -far_offset
     float* scratch_norm;  // [H, K]
-    uint32_t* head_bits;  // [H, 4]
-    float* head;          // [H, 4]
-    float* scale;         // [H]
-    uint16_t* planes;     // [H, 3, K, d]
-    void* compact;        // [B*H*Ncap, d] 16-bit
+    float* hneg;          // [H, Kpad]  -|c L|^2 / 2, padded to 256 columns
+    uint32_t* head_bits;  // [2, H, 4]
+    float* head;          // [2, H, 4]
+    float* scale;         // [2, H]
+    uint16_t* planes;     // [2, H, 3, K, d]
+    uint16_t* compact;    // [2, B*H*Ncap, d] two 16-bit planes of rotated rows
     int32_t* row_map;     // [B*H*Ncap]
+    int32_t* ccount;      // [B*H]
     uint8_t* skip;        // [B*H*Ncap]
     int64_t* exact_list;  // [B*H*Ncap]
     int32_t* exact_count; // [2]: count, status

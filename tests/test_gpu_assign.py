@@ -51,6 +51,12 @@ CASES = [
     (1, 2, 150, 256, 40, "bf16", True, dict(window=20, far_offset=9, rope_base=10000.0)),
     (1, 1, 70, 24, 17, "f32", True, None),
     (1, 1, 5, 16, 1, "bf16", False, None),
+    # every row inside the window: all rows take the two-plane pass
+    (1, 2, 600, 128, 700, "bf16", True, dict(window=10 ** 6, far_offset=0, rope_base=500000.0)),
+    # far rows rotated at a fixed offset (rotated codebook) next to exact in-window rows
+    (2, 1, 300, 64, 257, "f16", False, dict(window=50, far_offset=3, rope_base=10000.0)),
+    (1, 2, 400, 128, 33, "bf16", False, dict(window=128, far_offset=11, rope_base=500000.0)),
+    (1, 1, 1000, 256, 513, "f16", True, dict(window=300, far_offset=0, rope_base=10000.0)),
 ]
 
 
@@ -71,7 +77,8 @@ def test_h_weighted_matches_oracle(case):
 
 
 @pytest.mark.parametrize("mode", ["retrieval", "bulk"])
-def test_row_selection_writes_only_its_rows(mode):
+@pytest.mark.parametrize("rope", [None, dict(window=40, far_offset=5, rope_base=10000.0)])
+def test_row_selection_writes_only_its_rows(mode, rope):
     B, H, N, d, K = 1, 2, 300, 128, 50
     x = synth.gaussian((B, H, N, d), seed=7, dtype="bf16")
     c = synth.gaussian((H, K, d), seed=8, dtype="bf16")
@@ -81,14 +88,16 @@ def test_row_selection_writes_only_its_rows(mode):
         p, cnt, _, _ = oracle.select_retrieval_set(x[0, h], f64(x[0, h, -1]), 0.2)
         perm[0, h], count[0, h] = p, cnt
     codes = torch.full((B, H, N), -7, dtype=torch.int32, device="cuda")
-    q.a2ats_h_weighted_assign(dev(x), dev(c), None, rows=mode, perm=dev(torch.from_numpy(perm)),
+    q.a2ats_h_weighted_assign(dev(x), dev(c), None, rope=rope, rows=mode,
+                              perm=dev(torch.from_numpy(perm)),
                               count=dev(torch.from_numpy(count)), codes=codes)
     got = codes.cpu().numpy()
+    kt = _rows(x, torch.tensor([N], dtype=torch.int32), rope)
     for h in range(H):
         sel = perm[0, h, :count[0, h]] if mode == "retrieval" else perm[0, h, count[0, h]:]
         other = np.setdiff1d(np.arange(N), sel)
         assert (got[0, h, other] == -7).all()
-        code, d1, d2 = oracle.assign_cholesky(x[0, h, sel], c[h], None)
+        code, d1, d2 = oracle.assign_cholesky(kt[0, h][sel], c[h], None)
         check_codes(got[0, h, sel], code, (d2 - d1) / d2)
 
 
