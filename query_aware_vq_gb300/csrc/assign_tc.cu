@@ -779,65 +779,68 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
 }
 
 // ------------------------------------------------------ exact list kernel --
-// One warp per listed row: windowed RoPE in fp32, z = x L (compensated), then
-// the direct distance to every cp_j = c_j L, ties to the lowest index.
+// One block per listed row: windowed RoPE in fp32, z = x L (compensated),
+// then the direct distance to every cp_j = c_j L spread over the block's
+// threads, ties to the lowest index.
+constexpr int kExactThreads = 256;
+
 template <int DT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kExactThreads)
 exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
                   const int32_t* __restrict__ len, const RopeArgs ra, const float* __restrict__ L,
                   const float* __restrict__ cp, int64_t K, const int64_t* __restrict__ list,
                   const int32_t* __restrict__ list_count, int32_t* __restrict__ codes) {
-    __shared__ float xs[8][kMaxD];
-    __shared__ float zs[8][kMaxD];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ __align__(16) float xv[kMaxD];
+    __shared__ __align__(16) float zv[kMaxD];
+    __shared__ float wbest[kExactThreads / 32];
+    __shared__ int32_t wj[kExactThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int n = *list_count;
-    for (int e = blockIdx.x * 8 + w; e < n; e += gridDim.x * 8) {
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int64_t out = list[e];
         const int64_t bh = out / ncap;
         const int32_t j = (int32_t)(out % ncap);
         const int64_t h = bh % H;
         const int32_t Lb = seq_len(len, (int32_t)(bh / H), ncap);
-        float* xv = xs[w];
-        float* zv = zs[w];
-        for (int a = lane; a < d; a += 32) xv[a] = load1<DT>(x, out * d + a);
-        __syncwarp();
+        for (int a = tid; a < d; a += blockDim.x) xv[a] = load1<DT>(x, out * d + a);
+        __syncthreads();
         if (ra.enabled) {
             const int32_t pos = rope_position(j, Lb - 1, ra);
-            if (pos != 0) {
-                const int halfd = d / 2;
-                for (int i = lane; i < halfd; i += 32) {
-                    float s, c;
-                    rope_angle(pos, ra.omega_hi[i], ra.omega_lo[i], ra, s, c);
-                    const int a = ra.interleaved ? 2 * i : i;
-                    const int b = ra.interleaved ? 2 * i + 1 : i + halfd;
-                    const float xa = xv[a], xb = xv[b];
-                    xv[a] = fmaf(xa, c, -__fmul_rn(xb, s));
-                    xv[b] = fmaf(xa, s, __fmul_rn(xb, c));
-                }
+            const int halfd = d / 2;
+            if (pos != 0 && tid < halfd) {
+                float s, c;
+                rope_angle(pos, ra.omega_hi[tid], ra.omega_lo[tid], ra, s, c);
+                const int a = ra.interleaved ? 2 * tid : tid;
+                const int b = ra.interleaved ? 2 * tid + 1 : tid + halfd;
+                const float xa = xv[a], xb = xv[b];
+                xv[a] = fmaf(xa, c, -__fmul_rn(xb, s));
+                xv[b] = fmaf(xa, s, __fmul_rn(xb, c));
             }
-            __syncwarp();
+            __syncthreads();
         }
         const float* zr = xv;
         if (L) {
             const float* Lh = L + h * d * d;
-            for (int b = lane; b < d; b += 32) {
+            for (int b = tid; b < d; b += blockDim.x) {
                 Dot2 acc;
                 for (int a = 0; a < d; a++) acc.add_prod(xv[a], Lh[(int64_t)a * d + b]);
                 zv[b] = acc.value();
             }
-            __syncwarp();
+            __syncthreads();
             zr = zv;
         }
         float best = INFINITY;
         int32_t bj = 0;
         const float* cph = cp + h * K * d;
-        for (int64_t jj = lane; jj < K; jj += 32) {
+        const float4* z4 = reinterpret_cast<const float4*>(zr);
+        for (int64_t jj = tid; jj < K; jj += blockDim.x) {
             const float4* c4 = reinterpret_cast<const float4*>(cph + jj * d);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int a = 0; a < d / 4; a++) {
                 const float4 cv = __ldg(c4 + a);
-                const float t0 = zr[4 * a] - cv.x, t1 = zr[4 * a + 1] - cv.y;
-                const float t2 = zr[4 * a + 2] - cv.z, t3 = zr[4 * a + 3] - cv.w;
+                const float4 zz = z4[a];
+                const float t0 = zz.x - cv.x, t1 = zz.y - cv.y;
+                const float t2 = zz.z - cv.z, t3 = zz.w - cv.w;
                 acc[0] = fmaf(t0, t0, acc[0]);
                 acc[1] = fmaf(t1, t1, acc[1]);
                 acc[2] = fmaf(t2, t2, acc[2]);
@@ -851,8 +854,17 @@ exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
             const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
             if (ov < best || (ov == best && oj < bj)) { best = ov; bj = oj; }
         }
-        if (lane == 0) codes[out] = bj;
-        __syncwarp();
+        if (lane == 0) { wbest[w] = best; wj[w] = bj; }
+        __syncthreads();
+        if (tid == 0) {
+            for (int ww = 1; ww < (int)(blockDim.x >> 5); ww++)
+                if (wbest[ww] < best || (wbest[ww] == best && wj[ww] < bj)) {
+                    best = wbest[ww];
+                    bj = wj[ww];
+                }
+            codes[out] = bj;
+        }
+        __syncthreads();
     }
 }
 
@@ -1118,11 +1130,11 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     // rows the contraction could not decide
     const unsigned lg = (unsigned)(sm_count() * 4);
     if (c.dt == kBF16)
-        exact_list_kernel<kBF16><<<lg, 256, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
+        exact_list_kernel<kBF16><<<lg, kExactThreads, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
                                                      c.len, c.ra, c.L, c.cp, K, c.exact_list,
                                                      c.exact_count, c.codes);
     else
-        exact_list_kernel<kF16><<<lg, 256, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
+        exact_list_kernel<kF16><<<lg, kExactThreads, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
                                                     c.len, c.ra, c.L, c.cp, K, c.exact_list,
                                                     c.exact_count, c.codes);
     note_launches(1);

@@ -98,59 +98,133 @@ __global__ void second_moment_reduce_kernel(const float* __restrict__ partial, i
 }
 
 // ----------------------------------------------------------- Cholesky --
-constexpr int kCholThreads = 1024;
+constexpr int kCholThreads = 512;
+constexpr int kPanel = 32;
 
 __device__ __forceinline__ int tri(int i, int k) { return i * (i + 1) / 2 + k; }
 
-// One block per head.  Column-by-column (Crout order) Cholesky with the
-// factor held packed in shared memory; every entry is
-// (H_ij - sum_{k<j} L_ik L_jk) / L_jj with the sum formed by a compensated
-// dot product over one warp, so each entry is accurate to about one fp32
-// rounding of the values it depends on.
+// double-float helpers on (hi, lo) pairs
+struct DF {
+    float hi, lo;
+};
+__device__ __forceinline__ DF df_from(float hi, float lo) {
+    float s, e;
+    two_sum(hi, lo, s, e);
+    return DF{s, e};
+}
+// a - b * c with b, c plain floats
+__device__ __forceinline__ DF df_sub_prod(DF a, float b, float c) {
+    const float p = __fmul_rn(b, c);
+    const float pe = fmaf(b, c, -p);
+    float s, e;
+    two_sum(a.hi, -p, s, e);
+    e = __fadd_rn(e, __fsub_rn(a.lo, pe));
+    return df_from(s, e);
+}
+// a / b (b a plain positive float): q = rn(a/b), then one correction step
+__device__ __forceinline__ float df_div(DF a, float b) {
+    const float q = __fdiv_rn(a.hi, b);
+    const float r = fmaf(-q, b, a.hi);  // exact remainder of a.hi - q b
+    return __fadd_rn(q, __fdiv_rn(__fadd_rn(r, a.lo), b));
+}
+// sqrt of a positive double-float, rounded to float
+__device__ __forceinline__ float df_sqrt(DF a) {
+    const float s = sqrtf(a.hi);
+    const float r = fmaf(-s, s, a.hi);  // exact a.hi - s^2
+    return __fadd_rn(s, __fdiv_rn(__fadd_rn(r, a.lo), __fmul_rn(2.f, s)));
+}
+
+// One block per head; the factor lives packed in shared memory.  Columns are
+// taken 32 at a time (left-looking, Crout order):
+//   1. every entry of the panel, H_ij - sum_{k<j0} L_ik L_jk, with a
+//      compensated dot product (all entries in parallel);
+//   2. the panel is factored in double-float registers, one row per thread,
+//      with two barriers per column.
+// Each entry of L is within about one fp32 rounding of the factor of the
+// values it depends on; a non-positive pivot stops the head and is reported.
 __global__ void __launch_bounds__(kCholThreads)
 cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_out,
                 int32_t* __restrict__ info) {
     extern __shared__ float smem[];
-    float* Lp = smem;                        // d(d+1)/2 packed lower triangle
-    float* tmp = smem + d * (d + 1) / 2;     // d residuals of the current column
+    float* Lp = smem;                                     // d(d+1)/2 packed factor
+    float2* panel = reinterpret_cast<float2*>(smem + ((d * (d + 1) / 2 + 1) & ~1));  // [d][32]
+    __shared__ float colbuf[kPanel];
+    __shared__ float s_diag;
+    __shared__ int s_fail;
     const int h = blockIdx.x;
     const float* Hh = hm + (int64_t)h * d * d;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_fail = 0;
     int failed = 0;
-    for (int j = 0; j < d; j++) {
-        for (int i = j + warp; i < d; i += nwarps) {
+    for (int j0 = 0; j0 < d && !failed; j0 += kPanel) {
+        const int pw = min(kPanel, d - j0);
+        const int rows = d - j0;
+        // 1. panel entries from the columns already factored
+        for (int e = tid; e < rows * pw; e += blockDim.x) {
+            const int ii = e / pw, jj = e % pw;
+            const int i = j0 + ii, j = j0 + jj;
+            if (jj > ii) continue;
             Dot2 acc;
             const float* Li = Lp + tri(i, 0);
             const float* Lj = Lp + tri(j, 0);
-            for (int k = lane; k < j; k += 32) acc.add_prod(Li[k], Lj[k]);
-            for (int m = 16; m; m >>= 1) acc.merge(shfl_xor(acc, m));
-            if (lane == 0) {
-                acc.s = -acc.s;
-                acc.c = -acc.c;
-                acc.add(Hh[(int64_t)i * d + j]);
-                tmp[i] = acc.value();
+            for (int k = 0; k < j0; k++) acc.add_prod(Li[k], Lj[k]);
+            acc.s = -acc.s;
+            acc.c = -acc.c;
+            acc.add(Hh[(int64_t)i * d + j]);
+            const DF v = df_from(acc.s, acc.c);
+            panel[ii * kPanel + jj] = make_float2(v.hi, v.lo);
+        }
+        __syncthreads();
+        // 2. factor the panel: thread t owns row j0 + t
+        DF row[kPanel];
+        const bool mine = tid < rows;
+#pragma unroll
+        for (int jj = 0; jj < kPanel; jj++) {
+            row[jj] = DF{0.f, 0.f};
+            if (mine && jj < pw && jj <= tid) {
+                const float2 v = panel[tid * kPanel + jj];
+                row[jj] = DF{v.x, v.y};
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < kPanel; jj++) {
+            if (jj >= pw) break;
+            if (tid == jj) {
+                if (!(row[jj].hi > 0.f)) {
+                    s_fail = j0 + jj + 1;
+                } else {
+                    s_diag = df_sqrt(row[jj]);
+                }
+            }
+            __syncthreads();
+            if (s_fail) {
+                failed = s_fail;
+                break;
+            }
+            const float diag = s_diag;
+            float l = 0.f;
+            if (mine && tid >= jj) {
+                l = (tid == jj) ? diag : df_div(row[jj], diag);
+                Lp[tri(j0 + tid, j0 + jj)] = l;
+                if (tid < pw) colbuf[tid] = l;
+            }
+            __syncthreads();
+            if (mine && tid > jj) {
+#pragma unroll
+                for (int kk = 0; kk < kPanel; kk++)
+                    if (kk > jj && kk < pw && kk <= tid) row[kk] = df_sub_prod(row[kk], l, colbuf[kk]);
             }
         }
         __syncthreads();
-        const float pivot = tmp[j];
-        if (!(pivot > 0.f)) {  // not positive definite (or NaN)
-            failed = j + 1;
-            break;
-        }
-        const float diag = sqrtf(pivot);
-        for (int i = j + threadIdx.x; i < d; i += blockDim.x)
-            Lp[tri(i, j)] = (i == j) ? diag : __fdiv_rn(tmp[i], diag);
-        __syncthreads();
     }
     float* Lh = l_out + (int64_t)h * d * d;
-    for (int e = threadIdx.x; e < d * d; e += blockDim.x) {
+    for (int e = tid; e < d * d; e += blockDim.x) {
         const int i = e / d, k = e % d;
         float v = 0.f;
         if (k <= i && (!failed || k < failed - 1)) v = Lp[tri(i, k)];
         Lh[e] = v;
     }
-    if (threadIdx.x == 0) info[h] = failed;
+    if (tid == 0) info[h] = failed;
 }
 
 // ------------------------------------------------ codebook transform --
@@ -267,7 +341,8 @@ cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, in
 cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
                             cudaStream_t st) {
     if (H == 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * (size_t)(d * (d + 1) / 2 + d);
+    const size_t packed = (size_t)((d * (d + 1) / 2 + 1) & ~1);
+    const size_t smem = sizeof(float) * packed + sizeof(float2) * (size_t)(d * kPanel);
     cudaError_t e = cudaFuncSetAttribute(cholesky_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
