@@ -836,6 +836,7 @@ exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
         for (int64_t jj = tid; jj < K; jj += blockDim.x) {
             const float4* c4 = reinterpret_cast<const float4*>(cph + jj * d);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
             for (int a = 0; a < d / 4; a++) {
                 const float4 cv = __ldg(c4 + a);
                 const float4 zz = z4[a];

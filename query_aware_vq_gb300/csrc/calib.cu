@@ -137,23 +137,28 @@ __device__ __forceinline__ float df_sqrt(DF a) {
 // One block per head; the factor lives packed in shared memory.  Columns are
 // taken 32 at a time (left-looking, Crout order):
 //   1. every entry of the panel, H_ij - sum_{k<j0} L_ik L_jk, with a
-//      compensated dot product (all entries in parallel);
-//   2. the panel is factored in double-float registers, one row per thread,
-//      with two barriers per column.
+//      compensated dot product (all entries in parallel), kept as a
+//      double-float in shared memory;
+//   2. the panel is factored column by column: one thread takes the pivot,
+//      all rows are scaled in parallel, and the rank-1 update of the panel is
+//      spread over the block (lanes over columns, warps over rows).
 // Each entry of L is within about one fp32 rounding of the factor of the
 // values it depends on; a non-positive pivot stops the head and is reported.
+constexpr int kPS = kPanel + 1;  // padded panel row stride (float2), conflict-free
+
 __global__ void __launch_bounds__(kCholThreads)
 cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_out,
                 int32_t* __restrict__ info) {
     extern __shared__ float smem[];
     float* Lp = smem;                                     // d(d+1)/2 packed factor
-    float2* panel = reinterpret_cast<float2*>(smem + ((d * (d + 1) / 2 + 1) & ~1));  // [d][32]
-    __shared__ float colbuf[kPanel];
+    float2* panel = reinterpret_cast<float2*>(smem + ((d * (d + 1) / 2 + 1) & ~1));  // [d][kPS]
+    float* colL = reinterpret_cast<float*>(panel + (size_t)d * kPS);                  // [d]
     __shared__ float s_diag;
     __shared__ int s_fail;
     const int h = blockIdx.x;
     const float* Hh = hm + (int64_t)h * d * d;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
     if (tid == 0) s_fail = 0;
     int failed = 0;
     for (int j0 = 0; j0 < d && !failed; j0 += kPanel) {
@@ -162,39 +167,26 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
         // 1. panel entries from the columns already factored
         for (int e = tid; e < rows * pw; e += blockDim.x) {
             const int ii = e / pw, jj = e % pw;
-            const int i = j0 + ii, j = j0 + jj;
             if (jj > ii) continue;
+            const int i = j0 + ii, j = j0 + jj;
             Dot2 acc;
             const float* Li = Lp + tri(i, 0);
             const float* Lj = Lp + tri(j, 0);
+#pragma unroll 4
             for (int k = 0; k < j0; k++) acc.add_prod(Li[k], Lj[k]);
             acc.s = -acc.s;
             acc.c = -acc.c;
             acc.add(Hh[(int64_t)i * d + j]);
             const DF v = df_from(acc.s, acc.c);
-            panel[ii * kPanel + jj] = make_float2(v.hi, v.lo);
+            panel[ii * kPS + jj] = make_float2(v.hi, v.lo);
         }
         __syncthreads();
-        // 2. factor the panel: thread t owns row j0 + t
-        DF row[kPanel];
-        const bool mine = tid < rows;
-#pragma unroll
-        for (int jj = 0; jj < kPanel; jj++) {
-            row[jj] = DF{0.f, 0.f};
-            if (mine && jj < pw && jj <= tid) {
-                const float2 v = panel[tid * kPanel + jj];
-                row[jj] = DF{v.x, v.y};
-            }
-        }
-#pragma unroll
-        for (int jj = 0; jj < kPanel; jj++) {
-            if (jj >= pw) break;
-            if (tid == jj) {
-                if (!(row[jj].hi > 0.f)) {
-                    s_fail = j0 + jj + 1;
-                } else {
-                    s_diag = df_sqrt(row[jj]);
-                }
+        // 2. factor the panel
+        for (int jj = 0; jj < pw; jj++) {
+            if (tid == 0) {
+                const float2 pv = panel[jj * kPS + jj];
+                if (!(pv.x > 0.f)) s_fail = j0 + jj + 1;
+                else s_diag = df_sqrt(DF{pv.x, pv.y});
             }
             __syncthreads();
             if (s_fail) {
@@ -202,20 +194,25 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
                 break;
             }
             const float diag = s_diag;
-            float l = 0.f;
-            if (mine && tid >= jj) {
-                l = (tid == jj) ? diag : df_div(row[jj], diag);
-                Lp[tri(j0 + tid, j0 + jj)] = l;
-                if (tid < pw) colbuf[tid] = l;
+            for (int ii = jj + tid; ii < rows; ii += blockDim.x) {
+                const float2 pv = panel[ii * kPS + jj];
+                const float l = (ii == jj) ? diag : df_div(DF{pv.x, pv.y}, diag);
+                Lp[tri(j0 + ii, j0 + jj)] = l;
+                colL[ii] = l;
             }
             __syncthreads();
-            if (mine && tid > jj) {
-#pragma unroll
-                for (int kk = 0; kk < kPanel; kk++)
-                    if (kk > jj && kk < pw && kk <= tid) row[kk] = df_sub_prod(row[kk], l, colbuf[kk]);
+            const int kk = jj + 1 + lane;
+            if (kk < pw) {
+                const float lk = colL[kk];
+                for (int ii = jj + 1 + warp; ii < rows; ii += nwarps) {
+                    if (kk > ii) continue;
+                    const float2 pv = panel[ii * kPS + kk];
+                    const DF r = df_sub_prod(DF{pv.x, pv.y}, colL[ii], lk);
+                    panel[ii * kPS + kk] = make_float2(r.hi, r.lo);
+                }
             }
+            __syncthreads();
         }
-        __syncthreads();
     }
     float* Lh = l_out + (int64_t)h * d * d;
     for (int e = tid; e < d * d; e += blockDim.x) {
@@ -228,16 +225,19 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
 }
 
 // ------------------------------------------------ codebook transform --
-constexpr int kCtCent = 8;  // centroids per block
+constexpr int kCtCent = 16;  // centroids per block
+constexpr int kCtSlab = 16;  // rows of L staged in shared memory at a time
 
 // cp[h][j] = c[h][j] L[h] (compensated), half_norm[h][j] = |cp[h][j]|^2 / 2.
 // blockDim.x = d rounded up to a multiple of 32: thread b < d owns output
 // column b of kCtCent centroids; the others only take part in reductions.
+// L is read through shared memory in slabs of kCtSlab rows.
 template <int DT>
 __global__ void codebook_transform_kernel(const void* __restrict__ c, int64_t K, int32_t d,
                                           const float* __restrict__ L, float* __restrict__ cp,
                                           float* __restrict__ half_norm) {
     __shared__ float cs[kCtCent][kMaxD];
+    __shared__ float Ls[kCtSlab][kMaxD];
     __shared__ Dot2 red[kCtCent][kMaxD / 32];
     const int h = blockIdx.y;
     const int64_t j0 = (int64_t)blockIdx.x * kCtCent;
@@ -248,22 +248,28 @@ __global__ void codebook_transform_kernel(const void* __restrict__ c, int64_t K,
         if (col) cs[k][b] = k < nc ? load1<DT>(c, ((int64_t)h * K + j0 + k) * d + b) : 0.f;
     __syncthreads();
     float out[kCtCent];
-    if (!col) {
-#pragma unroll
-        for (int k = 0; k < kCtCent; k++) out[k] = 0.f;
-    } else if (L) {
+    if (L) {
         Dot2 acc[kCtCent];
         const float* Lh = L + (int64_t)h * d * d;
-        for (int a = 0; a < d; a++) {
-            const float l = Lh[(int64_t)a * d + b];
+        for (int a0 = 0; a0 < d; a0 += kCtSlab) {
+            const int na = min(kCtSlab, d - a0);
+            if (col)
+                for (int r = 0; r < na; r++) Ls[r][b] = Lh[(int64_t)(a0 + r) * d + b];
+            __syncthreads();
+            if (col) {
+                for (int r = 0; r < na; r++) {
+                    const float l = Ls[r][b];
 #pragma unroll
-            for (int k = 0; k < kCtCent; k++) acc[k].add_prod(cs[k][a], l);
+                    for (int k = 0; k < kCtCent; k++) acc[k].add_prod(cs[k][a0 + r], l);
+                }
+            }
+            __syncthreads();
         }
 #pragma unroll
-        for (int k = 0; k < kCtCent; k++) out[k] = acc[k].value();
+        for (int k = 0; k < kCtCent; k++) out[k] = col ? acc[k].value() : 0.f;
     } else {
 #pragma unroll
-        for (int k = 0; k < kCtCent; k++) out[k] = cs[k][b];
+        for (int k = 0; k < kCtCent; k++) out[k] = col ? cs[k][b] : 0.f;
     }
     const int lane = b & 31, w = b >> 5;
 #pragma unroll
@@ -342,7 +348,8 @@ cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, 
                             cudaStream_t st) {
     if (H == 0) return cudaSuccess;
     const size_t packed = (size_t)((d * (d + 1) / 2 + 1) & ~1);
-    const size_t smem = sizeof(float) * packed + sizeof(float2) * (size_t)(d * kPanel);
+    const size_t smem = sizeof(float) * packed + sizeof(float2) * (size_t)(d * kPS) +
+                        sizeof(float) * (size_t)d;
     cudaError_t e = cudaFuncSetAttribute(cholesky_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
