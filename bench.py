@@ -207,6 +207,8 @@ def run_ours(a):
     _barrier(world)
     torch.cuda.synchronize()
     launches0 = q.kernel_launches()
+    q.set_kernel_timing(True)
+    q.timed_kernels_ms()
     t_wall = time.perf_counter()
     for _ in range(a.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -219,6 +221,8 @@ def run_ours(a):
     _barrier(world)
     t_wall = time.perf_counter() - t_wall
     launches = q.kernel_launches() - launches0
+    tc_ms, tc_launches = q.timed_kernels_ms()
+    q.set_kernel_timing(False)
     clk = clocks.stop()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in step_ev]
     ms = sum(step_ms) / len(step_ms)
@@ -227,20 +231,33 @@ def run_ours(a):
     value = world * keys_per_step / (ms * 1e-3)
     stage_ms = {k: sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in events.items()}
 
-    # ---- roofline of the dominant stage
+    # ---- roofline of the dominant kernel: the tensor-core contraction over
+    # the keys in stored order (every key outside the RoPE window), timed by
+    # the library's CUDA events on the launching stream
     hbm, bf16, src = _peaks()
     work = _work(w, step.count.cpu())
-    dom = max(stage_ms, key=stage_ms.get)
-    bound, amount = work[dom]
-    sec = stage_ms[dom] * 1e-3
-    if bound == "hbm":
-        achieved, peak, unit = amount / sec / 1e9, hbm, "GB/s"
+    if tc_launches > 0:
+        per_launch = tc_ms / tc_launches
+        far_rows = w.B * w.H * max(w.N - max(w.W, 0), 0)
+        amount = far_rows * 2.0 * w.d * w.K
+        achieved = amount / (per_launch * 1e-3) / 1e12
+        roof = {"kernel": "assign_tc_kernel (stored-order pass, bulk rows)", "bound": "tensor",
+                "achieved": round(achieved, 3), "peak": bf16, "unit": "TFLOP/s",
+                "frac": round(achieved / bf16, 5), "traffic": None,
+                "flop_per_launch": amount, "ms_per_launch": round(per_launch, 5),
+                "launches": tc_launches, "peak_source": f"{src} (bf16_tflops, burst)"}
     else:
-        achieved, peak, unit = amount / sec / 1e12, bf16, "TFLOP/s"
-        bound = "tensor"
-    roof = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
-            "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
-            "peak_source": f"{src} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'})"}
+        dom = max(stage_ms, key=stage_ms.get)
+        bound, amount = work[dom]
+        sec = stage_ms[dom] * 1e-3
+        if bound == "hbm":
+            achieved, peak, unit = amount / sec / 1e9, hbm, "GB/s"
+        else:
+            achieved, peak, unit = amount / sec / 1e12, bf16, "TFLOP/s"
+            bound = "tensor"
+        roof = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
+                "unit": unit, "frac": round(achieved / peak, 5), "traffic": None,
+                "peak_source": f"{src} ({'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops'})"}
     stages = {}
     for k, v in stage_ms.items():
         b, amt = work[k]

@@ -193,6 +193,16 @@ int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64
  * host threads (diagnostics: lets a caller count the launches of a region). */
 uint64_t a2ats_kernel_launches(void);
 
+/* Diagnostics for benchmarks.  With timing on, every assignment call records
+ * a pair of CUDA events on its stream around each tensor-core contraction
+ * over keys in stored order (the pass that does almost all of the work).
+ * a2ats_timed_kernels_ms() waits for the recorded events, returns the summed
+ * milliseconds, writes the number of timed launches to *launches (if not
+ * NULL) and clears the record.  Timing is off after loading; not for
+ * concurrent use from several host threads. */
+int a2ats_set_kernel_timing(int32_t enable);
+double a2ats_timed_kernels_ms(int64_t* launches);
+
 /* Human-readable name of a status code (static storage). */
 const char* a2ats_status_string(int32_t status);
 

@@ -64,6 +64,8 @@ _SIGS = {
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
+    "a2ats_set_kernel_timing": [_I32],
+    "a2ats_timed_kernels_ms": [_P],
 }
 
 
@@ -91,6 +93,7 @@ def _load():
                      "a2ats_select_retrieval_set_workspace_size"):
             getattr(lib, name).restype = ctypes.c_size_t
         lib.a2ats_kernel_launches.restype = ctypes.c_uint64
+        lib.a2ats_timed_kernels_ms.restype = ctypes.c_double
         lib.a2ats_status_string.restype = ctypes.c_char_p
         lib.a2ats_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -105,6 +108,18 @@ def library():
 def kernel_launches() -> int:
     """Kernels the library has enqueued since it was loaded."""
     return int(_load().a2ats_kernel_launches())
+
+
+def set_kernel_timing(enable: bool) -> None:
+    """Record CUDA events around each stored-order tensor-core contraction."""
+    _load().a2ats_set_kernel_timing(int(bool(enable)))
+
+
+def timed_kernels_ms():
+    """(summed milliseconds, number of timed launches) since the last call."""
+    n = ctypes.c_int64(0)
+    ms = _load().a2ats_timed_kernels_ms(ctypes.byref(n))
+    return ms, n.value
 
 
 def _check(fn: str, status: int):

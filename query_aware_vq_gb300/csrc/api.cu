@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <vector>
 
 #include "../../include/a2ats.h"
 #include "kernels.cuh"
@@ -21,6 +22,38 @@ std::atomic<uint64_t> g_launches{0};
 }  // namespace
 
 void a2ats::note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+struct TimingPool {
+    bool on = false;
+    std::vector<cudaEvent_t> ev;  // pairs
+    size_t used = 0;
+};
+TimingPool g_timing;
+}  // namespace
+
+bool a2ats::kernel_timing_on() { return g_timing.on; }
+
+static cudaEvent_t timing_event() {
+    if (g_timing.used == g_timing.ev.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        g_timing.ev.push_back(e);
+    }
+    return g_timing.ev[g_timing.used++];
+}
+
+void a2ats::timing_begin(cudaStream_t st) {
+    if (!g_timing.on || (g_timing.used & 1)) return;
+    cudaEvent_t e = timing_event();
+    if (e) cudaEventRecord(e, st);
+}
+
+void a2ats::timing_end(cudaStream_t st) {
+    if (!g_timing.on || !(g_timing.used & 1)) return;
+    cudaEvent_t e = timing_event();
+    if (e) cudaEventRecord(e, st);
+}
 
 namespace {
 
@@ -204,6 +237,28 @@ const char* a2ats_status_string(int32_t status) {
 const char* a2ats_last_error(void) { return g_last_error; }
 
 uint64_t a2ats_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int a2ats_set_kernel_timing(int32_t enable) {
+    g_timing.on = enable != 0;
+    g_timing.used = 0;
+    return A2ATS_OK;
+}
+
+double a2ats_timed_kernels_ms(int64_t* launches) {
+    double total = 0.0;
+    int64_t n = 0;
+    for (size_t i = 0; i + 1 < g_timing.used; i += 2) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(g_timing.ev[i + 1]) == cudaSuccess &&
+            cudaEventElapsedTime(&ms, g_timing.ev[i], g_timing.ev[i + 1]) == cudaSuccess) {
+            total += ms;
+            n++;
+        }
+    }
+    g_timing.used = 0;
+    if (launches) *launches = n;
+    return total;
+}
 
 int a2ats_windowed_rope(const void* k_in, int32_t in_dtype, void* k_out, int32_t out_dtype,
                         int64_t B, int64_t H, int64_t Ncap, int64_t d, const int32_t* len,

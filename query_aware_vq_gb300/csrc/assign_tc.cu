@@ -1108,7 +1108,9 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     // far rows in stored order: the keys themselves are the row operand
     if (natural) {
         const int32_t skip_near = (c.ra.enabled && c.ra.window > 0) ? c.ra.window : 0;
+        timing_begin(st);
         e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, st);
+        timing_end(st);
         if (e != cudaSuccess) return e;
     }
     // rotated rows (the RoPE window, or every routed row) as two 16-bit planes

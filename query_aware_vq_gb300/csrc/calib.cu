@@ -15,20 +15,21 @@ namespace a2ats {
 namespace {
 
 // ----------------------------------------------------- second moment --
-constexpr int kSmTile = 32;    // output tile edge
-constexpr int kSmChunk = 64;   // query rows per plain-fp32 partial sum
+constexpr int kSmTile = 64;    // output tile edge
+constexpr int kSmChunk = 32;   // query rows per plain-fp32 partial sum
 constexpr int kSmThreads = 256;
 
-// Partial second moment of one 32x32 tile of H over one slice of the M
-// queries.  Each thread owns 4 outputs; 64-row plain fp32 partials are folded
-// into a compensated accumulator, so the result is within a few units of
-// fp32 rounding of the exact slice sum.
+// Partial second moment of one 64x64 tile of H over one slice of the M
+// queries.  Each thread owns a 4x4 block of outputs fed by 16-byte shared
+// memory reads; 32-row plain fp32 partials are folded into compensated
+// accumulators, so the result is within a few units of fp32 rounding of the
+// exact slice sum.
 template <int DT>
 __global__ void __launch_bounds__(kSmThreads)
 second_moment_partial_kernel(const void* __restrict__ q, int64_t M, int32_t d, int64_t splits,
                              float* __restrict__ partial) {
-    __shared__ float qa[kSmChunk][kSmTile + 1];
-    __shared__ float qb[kSmChunk][kSmTile + 1];
+    __shared__ __align__(16) float qa[kSmChunk][kSmTile];
+    __shared__ __align__(16) float qb[kSmChunk][kSmTile];
     // decode the lower-triangular tile pair (ti >= tj) from blockIdx.x
     int ti = 0, rem = blockIdx.x;
     while (rem > ti) { rem -= ti + 1; ti++; }
@@ -37,40 +38,59 @@ second_moment_partial_kernel(const void* __restrict__ q, int64_t M, int32_t d, i
     const int h = blockIdx.z;
     const int64_t m0 = M * split / splits, m1 = M * (split + 1) / splits;
     const int tid = threadIdx.x;
-    const int ra = tid / 8;            // row of the tile (a index)
-    const int rb = (tid % 8) * 4;      // first of 4 columns (b index)
-    Dot2 acc[4];
+    const int ty = tid >> 4, tx = tid & 15;   // 4x4 block (rows ty*4.., cols tx*4..)
+    float p[4][4];
+    Dot2 acc[4][4];
     const int64_t qbase = (int64_t)h * M * d;
     for (int64_t mc = m0; mc < m1; mc += kSmChunk) {
-        const int rows = (int)(m1 - mc < (int64_t)(kSmChunk) ? m1 - mc : (int64_t)(kSmChunk));
+        const int rows = (int)(m1 - mc < kSmChunk ? m1 - mc : kSmChunk);
+        // stage 32 rows x 64 columns of both column blocks as fp32
         for (int e = tid; e < kSmChunk * kSmTile; e += kSmThreads) {
             const int r = e / kSmTile, c = e % kSmTile;
+            const int ca = ti * kSmTile + c, cb = tj * kSmTile + c;
             float va = 0.f, vb = 0.f;
-            if (r < rows && ti * kSmTile + c < d) va = load1<DT>(q, qbase + (mc + r) * d + ti * kSmTile + c);
-            if (r < rows && tj * kSmTile + c < d) vb = load1<DT>(q, qbase + (mc + r) * d + tj * kSmTile + c);
+            if (r < rows) {
+                const int64_t row = qbase + (mc + r) * d;
+                if (ca < d) va = load1<DT>(q, row + ca);
+                if (cb < d) vb = load1<DT>(q, row + cb);
+            }
             qa[r][c] = va;
             qb[r][c] = vb;
         }
         __syncthreads();
-        float p[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int r = 0; r < rows; r++) {
-            const float a = qa[r][ra];
 #pragma unroll
-            for (int k = 0; k < 4; k++) p[k] = fmaf(a, qb[r][rb + k], p[k]);
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) p[i][j] = 0.f;
+        for (int r = 0; r < rows; r++) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&qa[r][ty * 4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&qb[r][tx * 4]);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) p[i][j] = fmaf(av[i], bv[j], p[i][j]);
         }
 #pragma unroll
-        for (int k = 0; k < 4; k++) acc[k].add(p[k]);
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[i][j].add(p[i][j]);
         __syncthreads();
     }
     float* out = partial + ((int64_t)split * gridDim.z + h) * d * d;
+    const int64_t plane = (int64_t)splits * gridDim.z * d * d;
 #pragma unroll
-    for (int k = 0; k < 4; k++) {
-        // store hi and lo in two planes so the final sum stays compensated
-        if (ti * kSmTile + ra >= d || tj * kSmTile + rb + k >= d) continue;
-        const int64_t idx = (int64_t)(ti * kSmTile + ra) * d + tj * kSmTile + rb + k;
-        out[idx] = acc[k].s;
-        out[idx + (int64_t)splits * gridDim.z * d * d] = acc[k].c;
-    }
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int a = ti * kSmTile + ty * 4 + i, b = tj * kSmTile + tx * 4 + j;
+            if (a >= d || b >= d) continue;
+            // hi and lo in two planes so the final sum stays compensated
+            const int64_t idx = (int64_t)a * d + b;
+            out[idx] = acc[i][j].s;
+            out[idx + plane] = acc[i][j].c;
+        }
 }
 
 // H[h][a][b] = H[h][b][a] = (sum over slices) / M + ridge [a == b], a >= b.
@@ -308,7 +328,7 @@ __global__ void centroid_norm_kernel(const void* __restrict__ c, int64_t HK, int
 }  // namespace
 
 int64_t second_moment_splits(int64_t M) {
-    int64_t s = M / 512;
+    int64_t s = M / 256;
     return s < 1 ? 1 : (s > 64 ? 64 : s);
 }
 

@@ -13,6 +13,11 @@ namespace a2ats {
 // Count of kernels enqueued by this library (see a2ats_kernel_launches).
 void note_launches(int n);
 
+// Event pairs around the stored-order contraction (see a2ats_set_kernel_timing).
+bool kernel_timing_on();
+void timing_begin(cudaStream_t st);
+void timing_end(cudaStream_t st);
+
 struct Shape {
     int64_t B, H, Ncap, d;
 };

@@ -10,6 +10,8 @@
 // thread moves 16-byte vectors, a row of d elements is handled by d/16
 // (half-split) or d/8 (interleaved) consecutive threads so every warp touches
 // whole 128-byte lines, and the grid is a multiple of the SM count.
+#include <cooperative_groups.h>
+
 #include "kernels.cuh"
 
 namespace a2ats {
@@ -373,7 +375,8 @@ cosine_score_warp_kernel(const void* __restrict__ keys, int64_t rows, int32_t H,
     }
 }
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;
+constexpr int kSelCluster = 8;
 
 // Exclusive block-wide scan of one flag per thread; returns the block total.
 __device__ __forceinline__ int block_scan_flag(bool f, int& excl, int* warp_tot) {
@@ -403,20 +406,28 @@ __device__ __forceinline__ int block_scan_flag(bool f, int& excl, int* warp_tot)
 // Exact top-n_r per (b, h) by radix select on order-preserving keys of the
 // scores, ties on the threshold broken by lower index, then a stable
 // two-sided compaction: retrieval rows ascending, then bulk rows ascending.
-__global__ void __launch_bounds__(kSelThreads)
+// One cluster of kSelCluster CTAs per (b, h): each CTA owns a contiguous
+// segment of the row; the per-pass histograms and the compaction offsets are
+// combined through distributed shared memory.
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
               const int32_t* __restrict__ len, double fraction, int32_t* __restrict__ perm,
               int32_t* __restrict__ count) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
     __shared__ uint32_t hist[256];
-    __shared__ uint32_t sel_prefix, sel_need;
+    __shared__ int seg_counts[2];   // this CTA's rows above the threshold, equal to it
     __shared__ int warp_tot[65];
-    const int bh = blockIdx.x;
+    const int rank = (int)cluster.block_rank();
+    const int bh = blockIdx.x / kSelCluster;
     const int32_t n = seq_len(len, bh / H, ncap);
     const float* s = scores + (int64_t)bh * ncap;
     int32_t* out = perm + (int64_t)bh * ncap;
-    double kd = ceil(fraction * (double)n);
-    int32_t k = kd < 0.0 ? 0 : (kd > (double)n ? n : (int32_t)kd);
-    if (threadIdx.x == 0) count[bh] = k;
+    const double kd = ceil(fraction * (double)n);
+    const int32_t k = kd < 0.0 ? 0 : (kd > (double)n ? n : (int32_t)kd);
+    if (rank == 0 && threadIdx.x == 0) count[bh] = k;
+    const int32_t seg = (n + kSelCluster - 1) / kSelCluster;
+    const int32_t lo = min(n, rank * seg), hi = min(n, lo + seg);
 
     uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
     const bool partial = k > 0 && k < n;
@@ -424,35 +435,73 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
             __syncthreads();
-            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
                 const uint32_t u = ordered_key(s[i]);
                 if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
             }
-            __syncthreads();
+            cluster.sync();
+            // every CTA sums the cluster's histograms and takes the same digit
+            __shared__ uint32_t tot[256];
+            for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+                uint32_t t = 0;
+                for (int r = 0; r < kSelCluster; r++) t += cluster.map_shared_rank(hist, r)[i];
+                tot[i] = t;
+            }
+            cluster.sync();  // no CTA resets its histogram while another reads it
+            __shared__ uint32_t sel_prefix, sel_need;
             if (threadIdx.x == 0) {
                 uint32_t cum = 0;
                 for (int dg = 255; dg >= 0; --dg) {
-                    const uint32_t h = hist[dg];
-                    if (cum + h >= need) {
+                    const uint32_t hcount = tot[dg];
+                    if (cum + hcount >= need) {
                         sel_prefix = prefix | ((uint32_t)dg << shift);
                         sel_need = need - cum;
                         break;
                     }
-                    cum += h;
+                    cum += hcount;
                 }
             }
             __syncthreads();
             prefix = sel_prefix;
             need = sel_need;
             mask |= 255u << shift;
+            __syncthreads();
         }
     }
-    // prefix is now the key of the n_r-th largest score; `need` of the rows
-    // equal to it (lowest indices first) complete the set.
-    int carry_eq = 0, carry_take = 0;
-    for (int base = 0; base < n; base += blockDim.x) {
+    // per-CTA counts of rows above and equal to the threshold, then prefixes
+    // over the CTAs of lower rank
+    int gt_local = 0, eq_local = 0;
+    if (partial) {
+        for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+            const uint32_t u = ordered_key(s[i]);
+            gt_local += u > prefix;
+            eq_local += u == prefix;
+        }
+    }
+    gt_local = __reduce_add_sync(0xffffffffu, gt_local);
+    eq_local = __reduce_add_sync(0xffffffffu, eq_local);
+    if (threadIdx.x == 0) { seg_counts[0] = 0; seg_counts[1] = 0; }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&seg_counts[0], gt_local);
+        atomicAdd(&seg_counts[1], eq_local);
+    }
+    cluster.sync();
+    int gt_before = 0, eq_before = 0;
+    for (int r = 0; r < rank; r++) {
+        const int* other = cluster.map_shared_rank(seg_counts, r);
+        gt_before += other[0];
+        eq_before += other[1];
+    }
+    cluster.sync();  // the counts stay readable until every CTA has them
+    // rows taken before this segment: those above the threshold plus the
+    // equal ones that fit in `need`, in index order
+    const int eq_taken_before = min(eq_before, (int)need);
+    int carry_take = partial ? gt_before + eq_taken_before : (k == n ? lo : 0);
+    int carry_eq = eq_before;
+    for (int base = lo; base < hi; base += blockDim.x) {
         const int i = base + threadIdx.x;
-        const bool valid = i < n;
+        const bool valid = i < hi;
         uint32_t u = 0;
         if (valid && partial) u = ordered_key(s[i]);
         const bool eq = valid && partial && u == prefix;
@@ -554,8 +603,9 @@ cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* le
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st) {
     const int nbh = (int)(s.B * s.H);
     if (nbh == 0) return cudaSuccess;
-    select_kernel<<<nbh, kSelThreads, 0, st>>>(scores, (int32_t)s.H, (int32_t)s.Ncap, len,
-                                               fraction, perm, count);
+    select_kernel<<<nbh * kSelCluster, kSelThreads, 0, st>>>(scores, (int32_t)s.H,
+                                                             (int32_t)s.Ncap, len, fraction, perm,
+                                                             count);
                                                note_launches(1);
     return cudaGetLastError();
 }
