@@ -57,7 +57,8 @@ typedef enum {
     A2ATS_ERR_DTYPE = -3,       /* dtype code not in a2ats_dtype */
     A2ATS_ERR_ALIGN = -4,       /* an array not 16-byte aligned */
     A2ATS_ERR_CUDA = -5,        /* a kernel launch failed */
-    A2ATS_ERR_WORKSPACE = -6    /* workspace NULL or smaller than required */
+    A2ATS_ERR_WORKSPACE = -6,   /* workspace NULL or smaller than required */
+    A2ATS_ERR_CAPACITY = -7     /* shape beyond a fixed library-owned scratch array */
 } a2ats_status;
 
 typedef enum { A2ATS_F32 = 0, A2ATS_BF16 = 1, A2ATS_F16 = 2 } a2ats_dtype;
@@ -188,6 +189,31 @@ int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64
                                double fraction, const a2ats_rope_params* fused_rope,
                                int32_t* perm, int32_t* count, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_select_retrieval_set_static -- the same retrieval split as
+ * a2ats_select_retrieval_set, for callers that cannot allocate device memory
+ * (no counterpart on the pages: this is a packaging variant).  Some callers
+ * have every byte of device memory owned by another allocator, or run on
+ * paths that must never risk an allocation failure or its latency; they
+ * cannot provide a workspace.  This entry point allocates nothing: its
+ * scratch is one fixed array compiled into the library, which every GPU that
+ * loads the library holds (about 5.3 MB) until the process exits.
+ *   Limits: B*H <= 1024 and B*H*Ncap <= 1048576, else A2ATS_ERR_CAPACITY
+ *   (before anything is enqueued).  Arguments and results are otherwise those
+ *   of a2ats_select_retrieval_set, and the results are identical.
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents
+ *   (every word a call reads is written earlier in the same call): calls
+ *   that may overlap on the GPU -- on different streams, or from different
+ *   host threads -- race and must be serialised by the caller.
+ * ------------------------------------------------------------------------ */
+int a2ats_select_retrieval_set_static(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                                      int64_t Ncap, int64_t d, const int32_t* len,
+                                      const void* query, double fraction,
+                                      const a2ats_rope_params* fused_rope, int32_t* perm,
+                                      int32_t* count, void* stream);
 
 /* Number of kernels this library has enqueued since it was loaded, over all
  * host threads (diagnostics: lets a caller count the launches of a region). */

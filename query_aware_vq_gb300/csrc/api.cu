@@ -230,6 +230,7 @@ const char* a2ats_status_string(int32_t status) {
         case A2ATS_ERR_ALIGN: return "A2ATS_ERR_ALIGN";
         case A2ATS_ERR_CUDA: return "A2ATS_ERR_CUDA";
         case A2ATS_ERR_WORKSPACE: return "A2ATS_ERR_WORKSPACE";
+        case A2ATS_ERR_CAPACITY: return "A2ATS_ERR_CAPACITY";
         default: return "A2ATS_ERR_UNKNOWN";
     }
 }
