@@ -67,7 +67,8 @@ typedef enum { A2ATS_F32 = 0, A2ATS_BF16 = 1, A2ATS_F16 = 2 } a2ats_dtype;
 typedef enum {
     A2ATS_ROWS_ALL = 0,       /* rows 0 .. len-1 */
     A2ATS_ROWS_RETRIEVAL = 1, /* rows perm[0 .. count-1] of a retrieval split */
-    A2ATS_ROWS_BULK = 2       /* rows perm[count .. len-1] of a retrieval split */
+    A2ATS_ROWS_BULK = 2,      /* rows perm[count .. len-1] of a retrieval split */
+    A2ATS_ROWS_LAST = 3       /* the decode row t = len-1 only (the key just appended) */
 } a2ats_rows;
 
 /* Windowed RoPE ([ALG] Eq. 11-12; [V039] step 4).  Row p with decode
@@ -96,6 +97,18 @@ typedef struct {
 int a2ats_windowed_rope(const void* k_in, int32_t in_dtype, void* k_out, int32_t out_dtype,
                         int64_t B, int64_t H, int64_t Ncap, int64_t d, const int32_t* len,
                         const a2ats_rope_params* rope, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_append_rows -- the cache step of a decode ([V039] "How it works": every
+ * call stores the incoming keys, pre-RoPE, and the whole cache is re-rotated
+ * against the new position): row len[b] of every (b, h) receives
+ * rows[b, h, :], then len[b] += 1.
+ *   cache [B, H, Ncap, d] in dtype;  rows [B, H, d] in dtype;
+ *   len   [B] int32 device, read and updated in place (required).
+ * A sequence already holding Ncap rows is left unchanged (len stays Ncap).
+ * ------------------------------------------------------------------------ */
+int a2ats_append_rows(void* cache, int32_t dtype, int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                      int32_t* len, const void* rows, void* stream);
 
 /* --------------------------------------------------------------------------
  * a2ats_query_second_moment -- [API] a2ats_query_second_moment (paper Eq. 10):
@@ -130,7 +143,8 @@ int a2ats_cholesky_factor(const float* h, int64_t H, int64_t d, float* l_out, in
  *   L        [H, d, d] fp32 Cholesky factor; NULL = identity, which is plain
  *            nearest-centroid VQ ([V039] step 2, bulk rows)
  *   rows     which rows to assign; RETRIEVAL / BULK read perm [B, H, Ncap]
- *            and count [B, H] as written by a2ats_select_retrieval_set
+ *            and count [B, H] as written by a2ats_select_retrieval_set;
+ *            LAST assigns the decode row t = len-1 of each (b, h)
  *   codes    [B, H, Ncap] int32; only the visited rows are written
  * Exactness: the code equals the exact argmin except possibly on rows whose
  * two best distances differ by less than 1e-5 of the second best.

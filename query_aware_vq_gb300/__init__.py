@@ -24,7 +24,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "liba2ats.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "a2ats.h")
 
-A2ATS_ROWS = {"all": 0, "retrieval": 1, "bulk": 2}
+A2ATS_ROWS = {"all": 0, "retrieval": 1, "bulk": 2, "last": 3}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 
@@ -49,6 +49,7 @@ _P = ctypes.c_void_p
 _I32, _I64, _D, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
 _SIGS = {
     "a2ats_windowed_rope": [_P, _I32, _P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P],
+    "a2ats_append_rows": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P],
     "a2ats_query_second_moment_workspace_size": [_I64, _I64, _I64],
     "a2ats_query_second_moment": [_P, _I32, _I64, _I64, _I64, _D, _P, _P, _SZ, _P],
     "a2ats_cholesky_factor": [_P, _I64, _I64, _P, _P, _P],
@@ -193,6 +194,20 @@ def a2ats_windowed_rope(k, *, window: int, far_offset: int = 0, rope_base: float
         _ptr(k4), _dt(k4), _ptr(o4), _dt(o4), B, H, N, d, _ptr(_lens(lengths)),
         ctypes.byref(p), _stream(stream)))
     return out
+
+
+def a2ats_append_rows(cache, lengths, rows, *, stream=None):
+    """Store rows [B, H, d] at position lengths[b] of every (b, h) of the
+    cache [B, H, Ncap, d] and advance lengths (int32, device) by one."""
+    _dev(cache, lengths, rows)
+    if lengths is None or lengths.dtype != torch.int32:
+        raise TypeError("lengths must be an int32 device tensor")
+    if rows.dtype != cache.dtype:
+        raise TypeError("rows and cache must share a dtype")
+    B, H, N, d = cache.shape
+    _check("a2ats_append_rows", _load().a2ats_append_rows(
+        _ptr(cache), _dt(cache), B, H, N, d, _ptr(lengths), _ptr(rows), _stream(stream)))
+    return cache
 
 
 def a2ats_query_second_moment(queries, ridge: float = 1e-4, *, out=None, workspace=None,

@@ -197,9 +197,11 @@ SelectWs carve_select(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d) {
 }
 
 int check_rows(int32_t rows, const int32_t* perm, const int32_t* count) {
-    if (rows != A2ATS_ROWS_ALL && rows != A2ATS_ROWS_RETRIEVAL && rows != A2ATS_ROWS_BULK)
+    if (rows != A2ATS_ROWS_ALL && rows != A2ATS_ROWS_RETRIEVAL && rows != A2ATS_ROWS_BULK &&
+        rows != A2ATS_ROWS_LAST)
         return A2ATS_ERR_INVALID_ARG;
-    if (rows != A2ATS_ROWS_ALL && (!perm || !count)) return A2ATS_ERR_INVALID_ARG;
+    if ((rows == A2ATS_ROWS_RETRIEVAL || rows == A2ATS_ROWS_BULK) && (!perm || !count))
+        return A2ATS_ERR_INVALID_ARG;
     return A2ATS_OK;
 }
 
@@ -276,6 +278,19 @@ int a2ats_windowed_rope(const void* k_in, int32_t in_dtype, void* k_out, int32_t
     if (k_in == k_out && in_dtype != out_dtype) return A2ATS_ERR_INVALID_ARG;
     cudaError_t e = launch_windowed_rope(k_in, in_dtype, k_out, out_dtype, Shape{B, H, Ncap, d},
                                          len, ra, (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+int a2ats_append_rows(void* cache, int32_t dtype, int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                      int32_t* len, const void* rows, void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (B * H == 0 || Ncap == 0) return A2ATS_OK;
+    if (!cache || !len || !rows) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(cache) || !aligned16(rows)) return A2ATS_ERR_ALIGN;
+    cudaError_t e = launch_append_rows(cache, dtype, Shape{B, H, Ncap, d}, len, rows,
+                                       (cudaStream_t)stream);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 

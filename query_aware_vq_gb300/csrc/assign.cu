@@ -21,6 +21,7 @@ constexpr int kAThreads = kRB * kSlots;
 __device__ __forceinline__ int32_t list_row(const RowSel& sel, int64_t bh, int32_t ncap, int32_t L,
                                             int32_t r) {
     if (sel.mode == 0) return r < L ? r : -1;
+    if (sel.mode == 3) return (r == 0 && L > 0) ? L - 1 : -1;
     const int32_t cnt = min(max(sel.count[bh], 0), L);
     int32_t j = -1;
     if (sel.mode == 1) j = r < cnt ? sel.perm[bh * ncap + r] : -1;
@@ -235,7 +236,8 @@ cudaError_t launch_assign_exact(const void* x, int dt, const Shape& s, const int
                                 const float* cp, const float* half_norm, int64_t K,
                                 int32_t* codes, cudaStream_t st) {
     if (s.B * s.H * s.Ncap == 0) return cudaSuccess;
-    dim3 grid((unsigned)((s.Ncap + kRB - 1) / kRB), (unsigned)(s.B * s.H));
+    // the decode-row selection has one row per (b, h)
+    dim3 grid(sel.mode == 3 ? 1u : (unsigned)((s.Ncap + kRB - 1) / kRB), (unsigned)(s.B * s.H));
     const size_t smem = exact_smem((int)s.d);
     cudaError_t e = cudaSuccess;
 #define A2ATS_LAUNCH_EXACT(DTV)                                                               \
@@ -260,7 +262,7 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
                                 const float* q, const float* qnorm, float beta, int64_t K,
                                 const float* cnorm, int32_t* codes, cudaStream_t st) {
     if (s.B * s.H * s.Ncap == 0) return cudaSuccess;
-    dim3 grid((unsigned)((s.Ncap + kRB - 1) / kRB), (unsigned)(s.B * s.H));
+    dim3 grid(sel.mode == 3 ? 1u : (unsigned)((s.Ncap + kRB - 1) / kRB), (unsigned)(s.B * s.H));
     const size_t smem = blend_smem((int)s.d);
     const float* cf = reinterpret_cast<const float*>(c);  // fp32 copy of the codebook
     cudaError_t e = cudaSuccess;

@@ -177,13 +177,10 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
-// (bits & ~31) | pos in one logic op: the column position rides in the five
-// low mantissa bits of the key.
+// (bits & ~31) | pos: the column position rides in the five low mantissa
+// bits of the key (pos is a compile-time constant at every use).
 __device__ __forceinline__ float embed_pos(float v, uint32_t pos) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(__float_as_uint(v)), "r"(0xFFFFFFE0u),
-        "r"(pos));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(v) & 0xFFFFFFE0u) | pos);
 }
 
 // Top two of 32 keys: min/max of pairs, then a merge tree of (max, second)
@@ -471,22 +468,32 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                      mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
-                const float2* hrow = reinterpret_cast<const float2*>(smH + acc * BN);
-#pragma unroll 1
+                const float* hrow = smH + acc * BN;
+                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+                // TMEM loads run one sub-chunk ahead of the arithmetic
+                uint32_t rbuf[2][32];
+                A2ATS_TMEM_LD32(tbase + (uint32_t)(half * 128), rbuf[0]);
+                tmem_wait_ld();
+#pragma unroll
                 for (int sub = 0; sub < 4; sub++) {
                     const int col = half * 128 + sub * 32;
-                    uint32_t r[32];
-                    A2ATS_TMEM_LD32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + col),
-                                    r);
-                    tmem_wait_ld();
+                    if (sub < 3) A2ATS_TMEM_LD32(tbase + (uint32_t)(col + 32), rbuf[(sub + 1) & 1]);
+                    const uint32_t* r = rbuf[sub & 1];
+                    const float4* h4 = reinterpret_cast<const float4*>(hrow + col);
                     float key[32];
 #pragma unroll
-                    for (int u = 0; u < 16; u++) {
-                        const float2 a2 =
-                            make_float2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-                        const float2 v2 = __ffma2_rn(a2, inv2, hrow[(col >> 1) + u]);
-                        key[2 * u] = embed_pos(v2.x, 31u - 2 * u);
-                        key[2 * u + 1] = embed_pos(v2.y, 30u - 2 * u);
+                    for (int u = 0; u < 8; u++) {
+                        const float4 hv = h4[u];
+                        const float2 v01 = __ffma2_rn(
+                            make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
+                            inv2, make_float2(hv.x, hv.y));
+                        const float2 v23 = __ffma2_rn(
+                            make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                            inv2, make_float2(hv.z, hv.w));
+                        key[4 * u + 0] = embed_pos(v01.x, 31u - 4 * u);
+                        key[4 * u + 1] = embed_pos(v01.y, 30u - 4 * u);
+                        key[4 * u + 2] = embed_pos(v23.x, 29u - 4 * u);
+                        key[4 * u + 3] = embed_pos(v23.y, 28u - 4 * u);
                     }
                     float t1, t2;
                     top2_32(key, t1, t2);
@@ -494,6 +501,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (t1 > m1) c1 = j0 >> 5;
                     m2 = max3f(fminf(m1, t1), m2, t2);
                     m1 = fmaxf(m1, t1);
+                    if (sub < 3) tmem_wait_ld();
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -685,8 +693,8 @@ __global__ void codebook_planes_kernel(const float* __restrict__ chat, int64_t K
 
 // ------------------------------------------------------ compact rows --
 // The rows of one pass that cannot use the stored keys as they are: rows
-// inside the RoPE window (natural order), or every retrieval row (routed
-// mode).  Each is rotated in fp32 and split into two 16-bit planes
+// inside the RoPE window (natural order), every retrieval row (routed mode 1)
+// or the decode row (mode 3).  Each is rotated in fp32 and split into two 16-bit planes
 // hi = rn(k~), lo = rn(k~ - hi); planes [2][nbh * ncap][d].  Rows whose fp16
 // planes would overflow go to the exact list instead.
 template <int DT>
@@ -703,6 +711,8 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
     int32_t n;
     if (mode == 1) {
         n = min(max(count[bh], 0), L);
+    } else if (mode == 3) {
+        n = L > 0 ? 1 : 0;  // the decode row
     } else {
         n = (ra.enabled && ra.window > 0) ? min(L, ra.window) : 0;
     }
@@ -711,7 +721,7 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
     const int halfd = d / 2;
     const int64_t plane_rows = (int64_t)gridDim.y * ncap;
     for (int32_t i = blockIdx.x * 8 + w; i < n; i += gridDim.x * 8) {
-        int32_t j = mode == 1 ? perm[(int64_t)bh * ncap + i] : L - n + i;
+        int32_t j = mode == 1 ? perm[(int64_t)bh * ncap + i] : L - n + i;  // mode 3: L - 1
         if (j < 0 || j >= L) {
             if (lane == 0) row_map[(int64_t)bh * ncap + i] = -1;
             continue;
@@ -1064,8 +1074,8 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
     const int64_t kpad = (K + BN - 1) / BN * BN;
     const bool rot = c.ra.enabled && c.ra.far_offset != 0;
-    const bool natural = c.sel.mode != 1;
-    const bool compact = c.sel.mode == 1 || (c.ra.enabled && c.ra.window > 0);
+    const bool natural = c.sel.mode == 0 || c.sel.mode == 2;
+    const bool compact = !natural || (c.ra.enabled && c.ra.window > 0);
     const bool need_u = compact || (natural && !rot);
     const bool need_r = natural && rot;
     cudaError_t e;
@@ -1118,12 +1128,12 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         dim3 g(blocks_for(ncap, 8, 1024), (unsigned)nbh);
         if (c.dt == kBF16)
             compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
-                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 1 ? 1 : 0,
+                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,
                 c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
                 c.exact_count);
         else
             compact_rows_kernel<kF16><<<g, 256, 0, st>>>(
-                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 1 ? 1 : 0,
+                c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,
                 c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
                 c.exact_count);
         note_launches(1);

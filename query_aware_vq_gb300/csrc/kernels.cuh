@@ -38,6 +38,10 @@ cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const
                                  const RopeArgs& ra, const float* q, const float* qnorm,
                                  float* scores, cudaStream_t st);
 
+// row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)
+cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
+                               cudaStream_t st);
+
 cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* len,
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st);
 

@@ -521,6 +521,23 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     }
 }
 
+// One block per sequence: every head's new row is copied into slot len[b]
+// (16-byte vectors), then one thread advances len[b].
+__global__ void append_rows_kernel(uint4* __restrict__ cache, int32_t H, int32_t ncap,
+                                   int32_t vec, int32_t* __restrict__ len,
+                                   const uint4* __restrict__ rows) {
+    const int b = blockIdx.x;
+    const int32_t L = len[b];
+    if (L >= 0 && L < ncap) {
+        for (int e = threadIdx.x; e < H * vec; e += blockDim.x) {
+            const int h = e / vec, v = e % vec;
+            cache[(((int64_t)b * H + h) * ncap + L) * vec + v] = rows[((int64_t)b * H + h) * vec + v];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && L >= 0 && L < ncap) len[b] = L + 1;
+}
+
 template <int DT>
 cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
                            const RopeArgs& ra, const float* q, const float* qnorm,
@@ -597,6 +614,16 @@ cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const
         case kBF16: return score_dispatch<kBF16>(keys, s, len, ra, q, qnorm, scores, st);
         default: return score_dispatch<kF16>(keys, s, len, ra, q, qnorm, scores, st);
     }
+}
+
+cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
+                               cudaStream_t st) {
+    const int32_t vec = (int32_t)(s.d * (dt == kF32 ? 4 : 2) / 16);
+    append_rows_kernel<<<(unsigned)s.B, 256, 0, st>>>(reinterpret_cast<uint4*>(cache),
+                                                      (int32_t)s.H, (int32_t)s.Ncap, vec, len,
+                                                      reinterpret_cast<const uint4*>(rows));
+    note_launches(1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* len,

@@ -22,9 +22,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (a2ats_cholesky_factor, a2ats_h_weighted_assign, a2ats_query_aware_assign,
-               a2ats_query_second_moment, a2ats_select_retrieval_set, a2ats_windowed_rope,
-               library)
+from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_h_weighted_assign,
+               a2ats_query_aware_assign, a2ats_query_second_moment, a2ats_select_retrieval_set,
+               a2ats_windowed_rope, library)
 
 
 class A2ATSStep:
@@ -97,4 +97,67 @@ class A2ATSStep:
         stage("assign_bulk", a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
               rope=self.rope, rows="bulk", perm=self.perm, count=self.count, codes=self.codes,
               workspace=ws, stream=st)
+        return self
+
+
+class A2ATSDecodeStep:
+    """One decode step over a batch of growing caches (v0.39.0 page, "How it
+    works", with one incoming key per (sequence, head)):
+
+      1. append the new pre-RoPE keys at position len[b]   a2ats_append_rows
+      2. windowed RoPE of the whole cache against the new
+         decode position (the per-step re-rotation)        a2ats_windowed_rope
+      3. retrieval split of every cached key, proxy query
+         = the new key after windowed RoPE                 a2ats_select_retrieval_set
+      4. the new keys assigned by the cosine blend against
+         that proxy (each new key is its own query)        a2ats_query_aware_assign
+         (or by the H-weighted rule when L is given)
+
+    cache [B, H, Ncap, d] and lengths [B] int32 are updated in place; the
+    rotated cache, split and codes are written to buffers allocated once."""
+
+    def __init__(self, B: int, H: int, N: int, d: int, K: int, dtype: torch.dtype, *,
+                 window: int, fraction: float, rope_base: float, beta: float,
+                 far_offset: int = 0, interleaved: bool = False, device="cuda"):
+        self.fraction, self.beta = fraction, beta
+        self.rope = dict(window=window, far_offset=far_offset, rope_base=rope_base,
+                         interleaved=interleaved)
+        dev = torch.device(device)
+        lib = library()
+        self.k_tilde = torch.empty((B, H, N, d), dtype=dtype, device=dev)
+        self.perm = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.count = torch.empty((B, H), dtype=torch.int32, device=dev)
+        self.codes = torch.full((B, H, N), -1, dtype=torch.int32, device=dev)
+        ws = max(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
+                 lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
+                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def __call__(self, cache, lengths, new_keys, codebook, L=None, stream=None, events=None):
+        st = stream if stream is not None else torch.cuda.current_stream()
+        ws = self.workspace
+
+        def stage(name, fn, *a, **kw):
+            if events is None:
+                return fn(*a, **kw)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            r = fn(*a, **kw)
+            e1.record(st)
+            events.setdefault(name, []).append((e0, e1))
+            return r
+
+        stage("append", a2ats_append_rows, cache, lengths, new_keys, stream=st)
+        stage("windowed_rope", a2ats_windowed_rope, cache, lengths=lengths, out=self.k_tilde,
+              stream=st, **self.rope)
+        stage("retrieval_split", a2ats_select_retrieval_set, cache, None, self.fraction,
+              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws,
+              stream=st)
+        if L is not None:
+            stage("assign_new", a2ats_h_weighted_assign, cache, codebook, L, lengths=lengths,
+                  rope=self.rope, rows="last", codes=self.codes, workspace=ws, stream=st)
+        else:
+            stage("assign_new", a2ats_query_aware_assign, cache, codebook, None, self.beta,
+                  lengths=lengths, rope=self.rope, rows="last", codes=self.codes, workspace=ws,
+                  stream=st)
         return self
