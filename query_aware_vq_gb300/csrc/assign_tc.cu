@@ -833,7 +833,13 @@ exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
             const float* Lh = L + h * d * d;
             for (int b = tid; b < d; b += blockDim.x) {
                 Dot2 acc;
-                for (int a = 0; a < d; a++) acc.add_prod(xv[a], Lh[(int64_t)a * d + b]);
+                for (int a0 = 0; a0 < d; a0 += 16) {
+                    float l[16];
+#pragma unroll
+                    for (int u = 0; u < 16; u++) l[u] = __ldg(Lh + (int64_t)(a0 + u) * d + b);
+#pragma unroll
+                    for (int u = 0; u < 16; u++) acc.add_prod(xv[a0 + u], l[u]);
+                }
                 zv[b] = acc.value();
             }
             __syncthreads();

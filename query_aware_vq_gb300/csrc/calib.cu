@@ -28,6 +28,10 @@ template <int DT>
 __global__ void __launch_bounds__(kSmThreads)
 second_moment_partial_kernel(const void* __restrict__ q, int64_t M, int32_t d, int64_t splits,
                              float* __restrict__ partial) {
+    using T = typename Elem<DT>::T;
+    constexpr int VE = 16 / (int)sizeof(T);                   // elements per 16-byte vector
+    constexpr int VPR = kSmTile / VE;                         // vectors per 64-column row
+    constexpr int NV = 2 * kSmChunk * VPR / kSmThreads;       // vectors per thread per chunk
     __shared__ __align__(16) float qa[kSmChunk][kSmTile];
     __shared__ __align__(16) float qb[kSmChunk][kSmTile];
     // decode the lower-triangular tile pair (ti >= tj) from blockIdx.x
@@ -41,23 +45,37 @@ second_moment_partial_kernel(const void* __restrict__ q, int64_t M, int32_t d, i
     const int ty = tid >> 4, tx = tid & 15;   // 4x4 block (rows ty*4.., cols tx*4..)
     float p[4][4];
     Dot2 acc[4][4];
-    const int64_t qbase = (int64_t)h * M * d;
+    const T* qh = reinterpret_cast<const T*>(q) + (int64_t)h * M * d;
+    uint4 buf[NV];
+    // 16-byte loads of one chunk into registers (zeros past M or d)
+    auto fetch = [&](int64_t mc) {
+#pragma unroll
+        for (int v = 0; v < NV; v++) {
+            const int e = tid + v * kSmThreads;
+            const int tile = e / (kSmChunk * VPR), r = (e / VPR) % kSmChunk, cv = e % VPR;
+            const int col = (tile ? tj : ti) * kSmTile + cv * VE;
+            buf[v] = make_uint4(0, 0, 0, 0);
+            if (mc + r < m1 && col < d)
+                buf[v] = __ldg(reinterpret_cast<const uint4*>(qh + (mc + r) * d + col));
+        }
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int v = 0; v < NV; v++) {
+            const int e = tid + v * kSmThreads;
+            const int tile = e / (kSmChunk * VPR), r = (e / VPR) % kSmChunk, cv = e % VPR;
+            const T* el = reinterpret_cast<const T*>(&buf[v]);
+            float* dst = tile ? &qb[r][cv * VE] : &qa[r][cv * VE];
+#pragma unroll
+            for (int u = 0; u < VE; u++) dst[u] = to_f32<DT>(el[u]);
+        }
+    };
+    if (m0 < m1) fetch(m0);
     for (int64_t mc = m0; mc < m1; mc += kSmChunk) {
         const int rows = (int)(m1 - mc < kSmChunk ? m1 - mc : kSmChunk);
-        // stage 32 rows x 64 columns of both column blocks as fp32
-        for (int e = tid; e < kSmChunk * kSmTile; e += kSmThreads) {
-            const int r = e / kSmTile, c = e % kSmTile;
-            const int ca = ti * kSmTile + c, cb = tj * kSmTile + c;
-            float va = 0.f, vb = 0.f;
-            if (r < rows) {
-                const int64_t row = qbase + (mc + r) * d;
-                if (ca < d) va = load1<DT>(q, row + ca);
-                if (cb < d) vb = load1<DT>(q, row + cb);
-            }
-            qa[r][c] = va;
-            qb[r][c] = vb;
-        }
+        stage();
         __syncthreads();
+        if (mc + kSmChunk < m1) fetch(mc + kSmChunk);  // overlaps the arithmetic below
 #pragma unroll
         for (int i = 0; i < 4; i++)
 #pragma unroll
@@ -159,9 +177,9 @@ __device__ __forceinline__ float df_sqrt(DF a) {
 //   1. every entry of the panel, H_ij - sum_{k<j0} L_ik L_jk, with a
 //      compensated dot product (all entries in parallel), kept as a
 //      double-float in shared memory;
-//   2. the panel is factored column by column: one thread takes the pivot,
-//      all rows are scaled in parallel, and the rank-1 update of the panel is
-//      spread over the block (lanes over columns, warps over rows).
+//   2. the panel is factored column by column, left-looking: each row's
+//      entry loses its compensated dot with the panel columns already done,
+//      then every row is scaled by the pivot (two barriers per column).
 // Each entry of L is within about one fp32 rounding of the factor of the
 // values it depends on; a non-positive pivot stops the head and is reported.
 constexpr int kPS = kPanel + 1;  // padded panel row stride (float2), conflict-free
@@ -172,14 +190,9 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
     extern __shared__ float smem[];
     float* Lp = smem;                                     // d(d+1)/2 packed factor
     float2* panel = reinterpret_cast<float2*>(smem + ((d * (d + 1) / 2 + 1) & ~1));  // [d][kPS]
-    float* colL = reinterpret_cast<float*>(panel + (size_t)d * kPS);                  // [d]
-    __shared__ float s_diag;
-    __shared__ int s_fail;
     const int h = blockIdx.x;
     const float* Hh = hm + (int64_t)h * d * d;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
-    if (tid == 0) s_fail = 0;
+    const int tid = threadIdx.x;
     int failed = 0;
     for (int j0 = 0; j0 < d && !failed; j0 += kPanel) {
         const int pw = min(kPanel, d - j0);
@@ -201,35 +214,32 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
             panel[ii * kPS + jj] = make_float2(v.hi, v.lo);
         }
         __syncthreads();
-        // 2. factor the panel
+        // 2. factor the panel, left-looking: column jj of every row is its
+        // panel entry minus the dot with the panel columns already done
+        // (compensated), then scaled by the pivot every thread recomputes.
         for (int jj = 0; jj < pw; jj++) {
-            if (tid == 0) {
-                const float2 pv = panel[jj * kPS + jj];
-                if (!(pv.x > 0.f)) s_fail = j0 + jj + 1;
-                else s_diag = df_sqrt(DF{pv.x, pv.y});
+            const int ii = jj + tid;
+            if (ii < rows) {
+                const float2 pv = panel[ii * kPS + jj];
+                Dot2 acc;
+                acc.s = pv.x;
+                acc.c = pv.y;
+                const float* Li = Lp + tri(j0 + ii, j0);
+                const float* Lj = Lp + tri(j0 + jj, j0);
+                for (int kk = 0; kk < jj; kk++) acc.add_prod(-Li[kk], Lj[kk]);
+                const DF v = df_from(acc.s, acc.c);
+                panel[ii * kPS + jj] = make_float2(v.hi, v.lo);
             }
             __syncthreads();
-            if (s_fail) {
-                failed = s_fail;
+            const float2 pvt = panel[jj * kPS + jj];
+            if (!(pvt.x > 0.f)) {
+                failed = j0 + jj + 1;
                 break;
             }
-            const float diag = s_diag;
-            for (int ii = jj + tid; ii < rows; ii += blockDim.x) {
+            const float diag = df_sqrt(DF{pvt.x, pvt.y});
+            if (ii < rows) {
                 const float2 pv = panel[ii * kPS + jj];
-                const float l = (ii == jj) ? diag : df_div(DF{pv.x, pv.y}, diag);
-                Lp[tri(j0 + ii, j0 + jj)] = l;
-                colL[ii] = l;
-            }
-            __syncthreads();
-            const int kk = jj + 1 + lane;
-            if (kk < pw) {
-                const float lk = colL[kk];
-                for (int ii = jj + 1 + warp; ii < rows; ii += nwarps) {
-                    if (kk > ii) continue;
-                    const float2 pv = panel[ii * kPS + kk];
-                    const DF r = df_sub_prod(DF{pv.x, pv.y}, colL[ii], lk);
-                    panel[ii * kPS + kk] = make_float2(r.hi, r.lo);
-                }
+                Lp[tri(j0 + ii, j0 + jj)] = (ii == jj) ? diag : df_div(DF{pv.x, pv.y}, diag);
             }
             __syncthreads();
         }
