@@ -140,8 +140,10 @@ int a2ats_cholesky_factor(const float* h, int64_t H, int64_t d, float* l_out, in
  *   x        [B, H, Ncap, d] in dtype: k~ itself, or pre-RoPE keys when
  *            fused_rope != NULL (windowed RoPE is then applied on the fly)
  *   codebook [H, K, d] in dtype (untransformed centroids)
- *   L        [H, d, d] fp32 Cholesky factor; NULL = identity, which is plain
- *            nearest-centroid VQ ([V039] step 2, bulk rows)
+ *   L        [H, d, d] fp32 Cholesky factor; only its lower triangle (with
+ *            the diagonal) is read, entries above the diagonal are ignored;
+ *            NULL = identity, which is plain nearest-centroid VQ ([V039]
+ *            step 2, bulk rows)
  *   rows     which rows to assign; RETRIEVAL / BULK read perm [B, H, Ncap]
  *            and count [B, H] as written by a2ats_select_retrieval_set;
  *            LAST assigns the decode row t = len-1 of each (b, h)

@@ -124,6 +124,7 @@ struct Carve {
 };
 
 struct AssignWs {
+    float* Lc;         // [H, d, d] lower triangle of L
     float* cp;         // [H, K, d] transformed (or decoded) centroids
     float* half_norm;  // [H, K]
     float* cnorm;      // [H, K]
@@ -134,6 +135,7 @@ struct AssignWs {
 
 AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, int64_t K) {
     AssignWs w;
+    w.Lc = c.take<float>((size_t)(H * d * d));
     w.cp = c.take<float>((size_t)(H * K * d));
     w.half_norm = c.take<float>((size_t)(H * K));
     w.cnorm = c.take<float>((size_t)(H * K));
@@ -145,7 +147,6 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.Lt = c.take<float>((size_t)(H * d * d));
     w.tc.chat = c.take<float>((size_t)(H * K * d));
     w.tc.chat_rot = c.take<float>((size_t)(H * K * d));
-    w.tc.scratch_norm = c.take<float>((size_t)(H * K));
     w.tc.hneg = c.take<float>((size_t)(H * kpad));
     w.tc.head_bits = c.take<uint32_t>((size_t)(2 * H * 4));
     w.tc.head = c.take<float>((size_t)(2 * H * 4));
@@ -156,6 +157,7 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.ccount = c.take<int32_t>((size_t)(B * H));
     w.tc.skip = c.take<uint8_t>(rows);
     w.tc.exact_list = c.take<int64_t>(rows);
+    w.tc.exact_best = c.take<unsigned long long>(rows);
     w.tc.exact_count = c.take<int32_t>(2);
     return w;
 }
@@ -354,14 +356,23 @@ int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, 
     Carve c(workspace);
     AssignWs w = carve_assign(c, B, H, Ncap, d, K);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, L, w.cp, w.half_norm, s);
+    cudaError_t e;
+    // only the lower triangle of L is read: every kernel uses the masked copy
+    const float* Lc = nullptr;
+    if (L) {
+        if ((e = launch_factor_prep(L, H, d, w.Lc, w.tc.Lt, s)) != cudaSuccess) return cuda_fail(e);
+        Lc = w.Lc;
+    }
+    const bool tc = tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30);
+    e = launch_codebook_transform(codebook, dtype, H, K, d, Lc, w.tc.Lt, w.cp, w.half_norm,
+                                  tc ? w.tc.chat : nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e);
     const Shape sh{B, H, Ncap, d};
-    if (tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30))
-        e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, L, ra,
+    if (tc)
+        e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, Lc, ra,
                                    RowSel{rows, perm, count}, codes, s);
     else
-        e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, L, w.cp,
+        e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, Lc, w.cp,
                                 w.half_norm, K, codes, s);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
@@ -392,8 +403,8 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
     cudaStream_t s = (cudaStream_t)stream;
     const Shape sh{B, H, Ncap, d};
     // decoded fp32 centroids (and |c|^2 / 2) for either rule
-    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, w.cp,
-                                              w.half_norm, s);
+    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, nullptr, w.cp,
+                                              w.half_norm, nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (beta == 1.0) {
         // beta = 1 is plain nearest-centroid VQ: the same argmin as the

@@ -788,23 +788,28 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
     }
 }
 
-// ------------------------------------------------------ exact list kernel --
-// One block per listed row: windowed RoPE in fp32, z = x L (compensated),
-// then the direct distance to every cp_j = c_j L spread over the block's
-// threads, ties to the lowest index.
+// ------------------------------------------------------ exact list kernels --
+// Rows the contraction could not decide, in three short launches so that a
+// handful of rows still spreads over the whole GPU:
+//   exact_rows_kernel   one block per listed row: windowed RoPE in fp32 and
+//                       z = x L (compensated) into zbuf; best <- +inf
+//   exact_scan_kernel   one block per (row, slice of 128 centroids): the
+//                       direct distance sum_b (z_b - cp_jb)^2 to each cp_j =
+//                       c_j L, folded into best by a 64-bit atomicMin on
+//                       (distance bits, j), so ties go to the lowest index
+//   exact_write_kernel  codes <- the index half of best
 constexpr int kExactThreads = 256;
+constexpr int kScanCents = 128;  // centroids per scan block (8 warps x 16)
 
 template <int DT>
 __global__ void __launch_bounds__(kExactThreads)
-exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
+exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
                   const int32_t* __restrict__ len, const RopeArgs ra, const float* __restrict__ L,
-                  const float* __restrict__ cp, int64_t K, const int64_t* __restrict__ list,
-                  const int32_t* __restrict__ list_count, int32_t* __restrict__ codes) {
+                  const int64_t* __restrict__ list, const int32_t* __restrict__ list_count,
+                  float* __restrict__ zbuf, unsigned long long* __restrict__ best) {
     __shared__ __align__(16) float xv[kMaxD];
-    __shared__ __align__(16) float zv[kMaxD];
-    __shared__ float wbest[kExactThreads / 32];
-    __shared__ int32_t wj[kExactThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    __shared__ Dot2 part[kExactThreads];
+    const int tid = threadIdx.x;
     const int n = *list_count;
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int64_t out = list[e];
@@ -818,82 +823,124 @@ exact_list_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
             const int32_t pos = rope_position(j, Lb - 1, ra);
             const int halfd = d / 2;
             if (pos != 0 && tid < halfd) {
-                float s, c;
-                rope_angle(pos, ra.omega_hi[tid], ra.omega_lo[tid], ra, s, c);
+                float sn, cs;
+                rope_angle(pos, ra.omega_hi[tid], ra.omega_lo[tid], ra, sn, cs);
                 const int a = ra.interleaved ? 2 * tid : tid;
                 const int b = ra.interleaved ? 2 * tid + 1 : tid + halfd;
                 const float xa = xv[a], xb = xv[b];
-                xv[a] = fmaf(xa, c, -__fmul_rn(xb, s));
-                xv[b] = fmaf(xa, s, __fmul_rn(xb, c));
+                xv[a] = fmaf(xa, cs, -__fmul_rn(xb, sn));
+                xv[b] = fmaf(xa, sn, __fmul_rn(xb, cs));
             }
             __syncthreads();
         }
-        const float* zr = xv;
+        float* z = zbuf + (int64_t)e * d;
         if (L) {
-            const float* Lh = L + h * d * d;
-            for (int b = tid; b < d; b += blockDim.x) {
+            // P groups of threads split the rows of L into spans of a
+            // multiple of 32 rows; group g sums rows [g d / P, (g + 1) d / P)
+            // of column b (d % 32 == 0)
+            const int P = min((int)blockDim.x / d, d / 32);
+            const int g = tid / d, b = tid - g * d;
+            const int span = d / P;
+            if (g < P) {
+                const float* Lh = L + h * d * d + b;
                 Dot2 acc;
-                for (int a0 = 0; a0 < d; a0 += 16) {
-                    float l[16];
+                for (int a0 = g * span; a0 < (g + 1) * span; a0 += 32) {
+                    float l[32];
 #pragma unroll
-                    for (int u = 0; u < 16; u++) l[u] = __ldg(Lh + (int64_t)(a0 + u) * d + b);
+                    for (int u = 0; u < 32; u++) l[u] = __ldg(Lh + (int64_t)(a0 + u) * d);
 #pragma unroll
-                    for (int u = 0; u < 16; u++) acc.add_prod(xv[a0 + u], l[u]);
+                    for (int u = 0; u < 32; u++) acc.add_prod(xv[a0 + u], l[u]);
                 }
-                zv[b] = acc.value();
+                part[g * d + b] = acc;
             }
             __syncthreads();
-            zr = zv;
-        }
-        float best = INFINITY;
-        int32_t bj = 0;
-        const float* cph = cp + h * K * d;
-        const float4* z4 = reinterpret_cast<const float4*>(zr);
-        for (int64_t jj = tid; jj < K; jj += blockDim.x) {
-            const float4* c4 = reinterpret_cast<const float4*>(cph + jj * d);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-            for (int a = 0; a < d / 4; a++) {
-                const float4 cv = __ldg(c4 + a);
-                const float4 zz = z4[a];
-                const float t0 = zz.x - cv.x, t1 = zz.y - cv.y;
-                const float t2 = zz.z - cv.z, t3 = zz.w - cv.w;
-                acc[0] = fmaf(t0, t0, acc[0]);
-                acc[1] = fmaf(t1, t1, acc[1]);
-                acc[2] = fmaf(t2, t2, acc[2]);
-                acc[3] = fmaf(t3, t3, acc[3]);
+            if (tid < d) {
+                Dot2 acc = part[tid];
+                for (int gg = 1; gg < P; gg++) acc.merge(part[gg * d + tid]);
+                z[tid] = acc.value();
             }
-            const float v = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            if (v < best) { best = v; bj = (int32_t)jj; }
+        } else {
+            for (int b = tid; b < d; b += blockDim.x) z[b] = xv[b];
         }
-        for (int m = 16; m; m >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, m);
-            const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
-            if (ov < best || (ov == best && oj < bj)) { best = ov; bj = oj; }
-        }
-        if (lane == 0) { wbest[w] = best; wj[w] = bj; }
-        __syncthreads();
-        if (tid == 0) {
-            for (int ww = 1; ww < (int)(blockDim.x >> 5); ww++)
-                if (wbest[ww] < best || (wbest[ww] == best && wj[ww] < bj)) {
-                    best = wbest[ww];
-                    bj = wj[ww];
-                }
-            codes[out] = bj;
-        }
+        if (tid == 0) best[e] = ~0ull;
         __syncthreads();
     }
 }
 
-__global__ void transpose_kernel(const float* __restrict__ in, int64_t H, int32_t d,
-                                 float* __restrict__ out) {
-    const int64_t n = H * d * d;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t h = i / ((int64_t)d * d);
-        const int a = (int)((i / d) % d), b = (int)(i % d);
-        out[(h * d + b) * d + a] = in[i];
+// 8 lanes share a centroid, each summing every 8th group of four elements
+// (VPL = d / 32 groups per lane); a warp covers 16 centroids in four rounds
+// of four, with the loads of RB rounds issued together.
+template <int VPL>
+__global__ void __launch_bounds__(kExactThreads)
+exact_scan_kernel(int32_t H, int32_t ncap, const float* __restrict__ cp, int64_t K,
+                  const int64_t* __restrict__ list, const int32_t* __restrict__ list_count,
+                  const float* __restrict__ zbuf, unsigned long long* __restrict__ best) {
+    constexpr int d = VPL * 32, vpr = d / 4;
+    constexpr int RB = VPL <= 4 ? 4 : 2;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int grp = lane >> 3, seg = lane & 7;
+    const int64_t slices = (K + kScanCents - 1) / kScanCents;
+    const int64_t items = (int64_t)(*list_count) * slices;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t e = it / slices;
+        const int64_t j0 = (it % slices) * kScanCents + w * 16;
+        const int64_t h = (list[e] / ncap) % H;
+        const float4* z4 = reinterpret_cast<const float4*>(zbuf + e * d) + seg;
+        const float4* c4 = reinterpret_cast<const float4*>(cp + h * K * d) + seg;
+        float4 zz[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; i++) zz[i] = z4[8 * i];
+        float bv = INFINITY;
+        int32_t bj = 0;
+#pragma unroll
+        for (int r0 = 0; r0 < 4; r0 += RB) {
+            float4 cv[RB][VPL];
+#pragma unroll
+            for (int r = 0; r < RB; r++) {
+                // past the end, reload the last centroid (its value is unused)
+                int64_t jj = j0 + 4 * (r0 + r) + grp;
+                jj = jj < K ? jj : K - 1;
+#pragma unroll
+                for (int i = 0; i < VPL; i++) cv[r][i] = __ldg(c4 + jj * vpr + 8 * i);
+            }
+#pragma unroll
+            for (int r = 0; r < RB; r++) {
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < VPL; i++) {
+                    const float t0 = zz[i].x - cv[r][i].x, t1 = zz[i].y - cv[r][i].y;
+                    const float t2 = zz[i].z - cv[r][i].z, t3 = zz[i].w - cv[r][i].w;
+                    acc0 = fmaf(t0, t0, acc0);
+                    acc1 = fmaf(t1, t1, acc1);
+                    acc0 = fmaf(t2, t2, acc0);
+                    acc1 = fmaf(t3, t3, acc1);
+                }
+                float v = acc0 + acc1;
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                const int64_t jj = j0 + 4 * (r0 + r) + grp;
+                if (jj < K && v < bv) { bv = v; bj = (int32_t)jj; }
+            }
+        }
+        // rounds run in increasing j, so a strict < keeps the lowest index
+        for (int m = 8; m < 32; m <<= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
+            const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
+            if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        if (lane == 0 && bv < INFINITY)
+            atomicMin(best + e, ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
     }
+}
+
+__global__ void exact_write_kernel(const int64_t* __restrict__ list,
+                                   const int32_t* __restrict__ list_count,
+                                   const unsigned long long* __restrict__ best,
+                                   int32_t* __restrict__ codes) {
+    const int n = *list_count;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x)
+        codes[list[e]] = (int32_t)(uint32_t)(best[e] & 0xffffffffull);
 }
 
 // ------------------------------------------------------------ host side --
@@ -1093,21 +1140,14 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K, kpad,
                                                                          c.hneg);
     note_launches(1);
-    // chat = c L L^T (the codebook side of the contraction), fp32
-    if (c.L) {
-        transpose_kernel<<<blocks_for(H * d * d, 256, 4096), 256, 0, st>>>(c.L, H, (int32_t)d, c.Lt);
-        note_launches(1);
-        e = launch_codebook_transform(c.cp, kF32, H, K, d, c.Lt, c.chat, c.scratch_norm, st);
-        if (e != cudaSuccess) return e;
-    } else {
-        e = cudaMemcpyAsync(c.chat, c.cp, sizeof(float) * H * K * d, cudaMemcpyDeviceToDevice, st);
-        if (e != cudaSuccess) return e;
-    }
+    // chat = c L L^T, the codebook side of the contraction (c itself when L
+    // is the identity)
+    const float* chat = c.L ? c.chat : c.cp;
     BSide bu{}, br{};
-    if (need_u && (e = prepare_b(c, c.chat, 0, c.L == nullptr, bu, st)) != cudaSuccess) return e;
+    if (need_u && (e = prepare_b(c, chat, 0, c.L == nullptr, bu, st)) != cudaSuccess) return e;
     if (need_r) {
         rotate_rows_kernel<<<blocks_for(H * K * (d / 2), 256, 8192), 256, 0, st>>>(
-            c.chat, H * K, (int32_t)d, c.ra, c.chat_rot);
+            chat, H * K, (int32_t)d, c.ra, c.chat_rot);
         note_launches(1);
         if ((e = prepare_b(c, c.chat_rot, 1, false, br, st)) != cudaSuccess) return e;
     }
@@ -1147,16 +1187,26 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     // rows the contraction could not decide
-    const unsigned lg = (unsigned)(sm_count() * 4);
+    const unsigned sms = (unsigned)sm_count();
+    float* zbuf = reinterpret_cast<float*>(c.compact);  // the planes are no longer read
     if (c.dt == kBF16)
-        exact_list_kernel<kBF16><<<lg, kExactThreads, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
-                                                     c.len, c.ra, c.L, c.cp, K, c.exact_list,
-                                                     c.exact_count, c.codes);
+        exact_rows_kernel<kBF16><<<sms * 4, kExactThreads, 0, st>>>(
+            c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
+            c.exact_count, zbuf, c.exact_best);
     else
-        exact_list_kernel<kF16><<<lg, kExactThreads, 0, st>>>(c.x, (int32_t)H, (int32_t)ncap, (int32_t)d,
-                                                    c.len, c.ra, c.L, c.cp, K, c.exact_list,
-                                                    c.exact_count, c.codes);
-    note_launches(1);
+        exact_rows_kernel<kF16><<<sms * 4, kExactThreads, 0, st>>>(
+            c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
+            c.exact_count, zbuf, c.exact_best);
+    {
+        auto scan = d == 64    ? exact_scan_kernel<2>
+                    : d == 128 ? exact_scan_kernel<4>
+                    : d == 192 ? exact_scan_kernel<6>
+                               : exact_scan_kernel<8>;
+        scan<<<sms * 8, kExactThreads, 0, st>>>((int32_t)H, (int32_t)ncap, c.cp, K, c.exact_list,
+                                                c.exact_count, zbuf, c.exact_best);
+    }
+    exact_write_kernel<<<sms, 256, 0, st>>>(c.exact_list, c.exact_count, c.exact_best, c.codes);
+    note_launches(3);
     return cudaGetLastError();
 }
 

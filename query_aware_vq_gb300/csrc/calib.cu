@@ -255,66 +255,149 @@ cholesky_kernel(const float* __restrict__ hm, int32_t d, float* __restrict__ l_o
 }
 
 // ------------------------------------------------ codebook transform --
-constexpr int kCtCent = 16;  // centroids per block
-constexpr int kCtSlab = 16;  // rows of L staged in shared memory at a time
+constexpr int kCtCent = 16;  // centroids per block (8 packed pairs)
+constexpr int kCtVs = 20;    // row stride of the operand rows (float4-aligned, fewer conflicts)
 
-// cp[h][j] = c[h][j] L[h] (compensated), half_norm[h][j] = |cp[h][j]|^2 / 2.
-// blockDim.x = d rounded up to a multiple of 32: thread b < d owns output
-// column b of kCtCent centroids; the others only take part in reductions.
-// L is read through shared memory in slabs of kCtSlab rows.
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+// Dot2 on two independent sums at once (packed fp32 instructions).
+struct Dot2x2 {
+    float2 s = {0.f, 0.f}, c = {0.f, 0.f};
+    __device__ __forceinline__ void add_prod(float2 a, float2 b) {
+        const float2 p = __fmul2_rn(a, b);
+        const float2 pe = __ffma2_rn(a, b, neg2(p));
+        const float2 t = __fadd2_rn(s, p);
+        const float2 bp = __fadd2_rn(t, neg2(s));
+        const float2 te = __fadd2_rn(__fadd2_rn(s, neg2(__fadd2_rn(t, neg2(bp)))),
+                                     __fadd2_rn(p, neg2(bp)));
+        s = t;
+        c = __fadd2_rn(c, __fadd2_rn(pe, te));
+    }
+    __device__ __forceinline__ float2 value() const { return __fadd2_rn(s, c); }
+};
+
+// cp[h][j] = c[h][j] Lc[h] and half_norm[h][j] = |cp[h][j]|^2 / 2, and when
+// chat is given chat[h][j] = cp[h][j] Lc[h]^T, all compensated (Dot2).  Lc is
+// lower triangular (zeros above the diagonal) and Lt its transpose, so output
+// column b of c Lc sums rows a >= b only, and column a of cp Lc^T rows b <= a:
+// each warp starts or stops at the first or last row its 32 columns need.
+// Without Lc, cp is the decoded codebook.  A block holds 16 centroids and
+// 2 x dr threads (dr = d rounded up to 32): thread (half, b) owns output
+// column b of centroids 8 half .. 8 half + 7, as four packed pairs.  The
+// factor is read straight from L1/L2 (no barriers in the loops); the
+// centroid rows sit in shared memory.
 template <int DT>
-__global__ void codebook_transform_kernel(const void* __restrict__ c, int64_t K, int32_t d,
-                                          const float* __restrict__ L, float* __restrict__ cp,
-                                          float* __restrict__ half_norm) {
-    __shared__ float cs[kCtCent][kMaxD];
-    __shared__ float Ls[kCtSlab][kMaxD];
-    __shared__ Dot2 red[kCtCent][kMaxD / 32];
+__global__ void __launch_bounds__(2 * kMaxD)
+codebook_transform_kernel(const void* __restrict__ c, int64_t K, int32_t d,
+                          const float* __restrict__ Lc, const float* __restrict__ Lt,
+                          float* __restrict__ cp, float* __restrict__ half_norm,
+                          float* __restrict__ chat) {
+    __shared__ __align__(16) float vs[kMaxD][kCtVs];  // operand rows (c, then cp)
+    __shared__ Dot2 red[kCtCent][2 * kMaxD / 32];
     const int h = blockIdx.y;
     const int64_t j0 = (int64_t)blockIdx.x * kCtCent;
-    const int b = threadIdx.x;
+    const int dr = (d + 31) / 32 * 32;
+    const int t = threadIdx.x, half = t >= dr ? 1 : 0, b = t - half * dr;
+    const int lane = t & 31, w = t >> 5;
+    const int wcol = b & ~31;      // first column of this warp
+    const int kb = half * (kCtCent / 2);
     const int nc = (int)(K - j0 < (int64_t)(kCtCent) ? K - j0 : (int64_t)(kCtCent));
     const bool col = b < d;
-    for (int k = 0; k < kCtCent; k++)
-        if (col) cs[k][b] = k < nc ? load1<DT>(c, ((int64_t)h * K + j0 + k) * d + b) : 0.f;
+    for (int i = t; i < d * kCtCent; i += blockDim.x) {
+        const int k = i / d, a = i - k * d;
+        vs[a][k] = k < nc ? load1<DT>(c, ((int64_t)h * K + j0 + k) * d + a) : 0.f;
+    }
     __syncthreads();
-    float out[kCtCent];
-    if (L) {
-        Dot2 acc[kCtCent];
-        const float* Lh = L + (int64_t)h * d * d;
-        for (int a0 = 0; a0 < d; a0 += kCtSlab) {
-            const int na = min(kCtSlab, d - a0);
-            if (col)
-                for (int r = 0; r < na; r++) Ls[r][b] = Lh[(int64_t)(a0 + r) * d + b];
-            __syncthreads();
-            if (col) {
-                for (int r = 0; r < na; r++) {
-                    const float l = Ls[r][b];
+    float out[kCtCent / 2];
+    if (Lc) {
+        Dot2x2 acc[kCtCent / 4];
+        if (col) {
+            const float* Lb = Lc + (int64_t)h * d * d + b;
+            for (int a0 = wcol; a0 < d; a0 += 8) {  // d % 8 == 0
+                float l[8];
 #pragma unroll
-                    for (int k = 0; k < kCtCent; k++) acc[k].add_prod(cs[k][a0 + r], l);
+                for (int u = 0; u < 8; u++) l[u] = __ldg(Lb + (int64_t)(a0 + u) * d);
+#pragma unroll
+                for (int u = 0; u < 8; u++) {
+                    const float2 l2 = make_float2(l[u], l[u]);
+                    const float4* v4 = reinterpret_cast<const float4*>(&vs[a0 + u][kb]);
+                    const float4 v0 = v4[0], v1 = v4[1];
+                    acc[0].add_prod(make_float2(v0.x, v0.y), l2);
+                    acc[1].add_prod(make_float2(v0.z, v0.w), l2);
+                    acc[2].add_prod(make_float2(v1.x, v1.y), l2);
+                    acc[3].add_prod(make_float2(v1.z, v1.w), l2);
                 }
             }
-            __syncthreads();
         }
 #pragma unroll
-        for (int k = 0; k < kCtCent; k++) out[k] = col ? acc[k].value() : 0.f;
+        for (int k = 0; k < kCtCent / 4; k++) {
+            const float2 v = acc[k].value();
+            out[2 * k] = col ? v.x : 0.f;
+            out[2 * k + 1] = col ? v.y : 0.f;
+        }
     } else {
 #pragma unroll
-        for (int k = 0; k < kCtCent; k++) out[k] = col ? cs[k][b] : 0.f;
+        for (int k = 0; k < kCtCent / 2; k++) out[k] = col ? vs[b][kb + k] : 0.f;
     }
-    const int lane = b & 31, w = b >> 5;
 #pragma unroll
-    for (int k = 0; k < kCtCent; k++) {
-        if (k < nc && col) cp[((int64_t)h * K + j0 + k) * d + b] = out[k];
+    for (int k = 0; k < kCtCent / 2; k++) {
+        if (kb + k < nc && col) cp[((int64_t)h * K + j0 + kb + k) * d + b] = out[k];
         Dot2 n;
         n.add_prod(out[k], out[k]);
         for (int m = 16; m; m >>= 1) n.merge(shfl_xor(n, m));
-        if (lane == 0) red[k][w] = n;
+        if (lane == 0) red[kb + k][w - half * (dr >> 5)] = n;
     }
     __syncthreads();
-    if (b < nc) {
-        Dot2 t = red[b][0];
-        for (int ww = 1; ww < (int)(blockDim.x >> 5); ww++) t.merge(red[b][ww]);
-        half_norm[(int64_t)h * K + j0 + b] = 0.5f * t.value();
+    if (t < nc) {
+        Dot2 s2 = red[t][0];
+        for (int ww = 1; ww < (dr >> 5); ww++) s2.merge(red[t][ww]);
+        half_norm[(int64_t)h * K + j0 + t] = 0.5f * s2.value();
+    }
+    if (!Lc || !chat) return;
+    // second factor: the operand rows become cp (every read of c is done)
+    if (col)
+#pragma unroll
+        for (int k = 0; k < kCtCent / 2; k++) vs[b][kb + k] = out[k];
+    __syncthreads();
+    Dot2x2 acc[kCtCent / 4];
+    if (col) {
+        const float* Tb = Lt + (int64_t)h * d * d + b;
+        const int aend = wcol + 32 < d ? wcol + 32 : d;
+        for (int a0 = 0; a0 < aend; a0 += 8) {
+            float l[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) l[u] = __ldg(Tb + (int64_t)(a0 + u) * d);
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const float2 l2 = make_float2(l[u], l[u]);
+                const float4* v4 = reinterpret_cast<const float4*>(&vs[a0 + u][kb]);
+                const float4 v0 = v4[0], v1 = v4[1];
+                acc[0].add_prod(make_float2(v0.x, v0.y), l2);
+                acc[1].add_prod(make_float2(v0.z, v0.w), l2);
+                acc[2].add_prod(make_float2(v1.x, v1.y), l2);
+                acc[3].add_prod(make_float2(v1.z, v1.w), l2);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kCtCent / 4; k++) {
+            const float2 v = acc[k].value();
+            if (kb + 2 * k < nc) chat[((int64_t)h * K + j0 + kb + 2 * k) * d + b] = v.x;
+            if (kb + 2 * k + 1 < nc) chat[((int64_t)h * K + j0 + kb + 2 * k + 1) * d + b] = v.y;
+        }
+    }
+}
+
+// Lc = the lower triangle of L with zeros above the diagonal, Lt = Lc^T.
+__global__ void factor_prep_kernel(const float* __restrict__ L, int64_t H, int32_t d,
+                                   float* __restrict__ Lc, float* __restrict__ Lt) {
+    const int64_t n = H * d * d;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t h = i / ((int64_t)d * d);
+        const int a = (int)((i / d) % d), b = (int)(i % d);
+        const float v = b <= a ? L[i] : 0.f;
+        Lc[i] = v;
+        Lt[(h * d + b) * d + a] = v;
     }
 }
 
@@ -388,27 +471,37 @@ cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_factor_prep(const float* L, int64_t H, int64_t d, float* Lc, float* Lt,
+                               cudaStream_t st) {
+    const int64_t n = H * d * d;
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    factor_prep_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(
+        L, H, (int32_t)d, Lc, Lt);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_codebook_transform(const void* c, int dt, int64_t H, int64_t K, int64_t d,
-                                      const float* L, float* cp, float* half_norm,
-                                      cudaStream_t st) {
+                                      const float* Lc, const float* Lt, float* cp,
+                                      float* half_norm, float* chat, cudaStream_t st) {
+    if (H * K == 0) return cudaSuccess;
     dim3 grid((unsigned)((K + kCtCent - 1) / kCtCent), (unsigned)H);
-    const unsigned threads = (unsigned)((d + 31) / 32 * 32);
+    const unsigned threads = (unsigned)(2 * ((d + 31) / 32 * 32));
     switch (dt) {
         case kF32:
-            codebook_transform_kernel<kF32><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
-                                                                       half_norm);
-                                                                       note_launches(1);
+            codebook_transform_kernel<kF32><<<grid, threads, 0, st>>>(c, K, (int32_t)d, Lc, Lt, cp,
+                                                                       half_norm, chat);
             break;
         case kBF16:
-            codebook_transform_kernel<kBF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
-                                                                        half_norm);
-                                                                        note_launches(1);
+            codebook_transform_kernel<kBF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, Lc, Lt,
+                                                                        cp, half_norm, chat);
             break;
         default:
-            codebook_transform_kernel<kF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, L, cp,
-                                                                       half_norm);
-                                                                       note_launches(1);
+            codebook_transform_kernel<kF16><<<grid, threads, 0, st>>>(c, K, (int32_t)d, Lc, Lt, cp,
+                                                                       half_norm, chat);
     }
+    note_launches(1);
     return cudaGetLastError();
 }
 

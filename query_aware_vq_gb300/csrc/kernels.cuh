@@ -53,11 +53,17 @@ cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, in
 cudaError_t launch_cholesky(const float* h, int64_t H, int64_t d, float* l_out, int32_t* info,
                             cudaStream_t st);
 
-// Transformed codebook for the assignment: cp [H, K, d] fp32 = c L (c when L
-// is null) and half_norm [H, K] fp32 = |cp_j|^2 / 2.
+// Lc [H, d, d] = the lower triangle of L (zeros above the diagonal, which
+// is all of L the library reads) and Lt [H, d, d] = Lc^T.
+cudaError_t launch_factor_prep(const float* L, int64_t H, int64_t d, float* Lc, float* Lt,
+                               cudaStream_t st);
+
+// Transformed codebook for the assignment: cp [H, K, d] fp32 = c Lc (c when
+// Lc is null) and half_norm [H, K] fp32 = |cp_j|^2 / 2; with Lc and chat
+// given, also chat [H, K, d] fp32 = cp Lc^T (Lt = Lc^T).
 cudaError_t launch_codebook_transform(const void* c, int dt, int64_t H, int64_t K, int64_t d,
-                                      const float* L, float* cp, float* half_norm,
-                                      cudaStream_t st);
+                                      const float* Lc, const float* Lt, float* cp,
+                                      float* half_norm, float* chat, cudaStream_t st);
 
 // assign.cu --------------------------------------------------------------
 struct RowSel {
@@ -82,7 +88,8 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
 // assign_tc.cu ----------------------------------------------------------
 // Tensor-core assignment (argmin_j |x~ L - c_j L|^2, L null = identity) for
 // bf16 / fp16 keys with d a multiple of 64.  cp / half_norm must already hold
-// c L and |c L|^2 / 2 (launch_codebook_transform).  Rows inside the RoPE
+// c L and |c L|^2 / 2, and with L given chat must hold c L L^T
+// (launch_codebook_transform; L is the lower-triangular copy).  Rows inside the RoPE
 // window and rows whose top two the contraction cannot separate are decided
 // by the exact kernel.
 struct TcCall {
@@ -99,10 +106,9 @@ struct TcCall {
     const float* half_norm;
     int32_t* codes;
     // workspace
-    float* Lt;            // [H, d, d]
+    float* Lt;            // [H, d, d]  L^T
     float* chat;          // [H, K, d]  c L L^T
     float* chat_rot;      // [H, K, d]  the same, rotated by -far_offset
-    float* scratch_norm;  // [H, K]
     float* hneg;          // [H, Kpad]  -|c L|^2 / 2, padded to 256 columns
     uint32_t* head_bits;  // [2, H, 4]
     float* head;          // [2, H, 4]
@@ -113,6 +119,7 @@ struct TcCall {
     int32_t* ccount;      // [B*H]
     uint8_t* skip;        // [B*H*Ncap]
     int64_t* exact_list;  // [B*H*Ncap]
+    unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
     int32_t* exact_count; // [2]: count, status
 };
 bool tc_supported(int dt, int64_t d);

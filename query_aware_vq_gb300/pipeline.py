@@ -16,6 +16,12 @@ Steps 4-6 apply the windowed RoPE on the fly in fp32 to the pre-RoPE keys, so
 their decisions are taken on the unrounded rotated keys; step 3 writes the
 rotated cache in the storage dtype for the attention that follows.
 
+Steps 1-2 depend on the queries only and steps 3, 4 and 6 on the keys only,
+so the calibration runs on a second stream beside them, and step 5 (which
+needs L and the split) follows it there once the split is done, while the
+bulk rows of step 6 are assigned on the caller's stream; the two write
+disjoint codes.  The caller's stream waits for the second before returning.
+
 All buffers are allocated once in the constructor; a step allocates nothing.
 """
 from __future__ import annotations
@@ -45,58 +51,74 @@ class A2ATSStep:
         self.Hm = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.L = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.info = torch.empty((H,), dtype=torch.int32, device=dev)
-        ws = max(lib.a2ats_query_second_moment_workspace_size(H, max(M, 1), d),
-                 lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
+        ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
                  lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
                  lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # the second stream (calibration, then the retrieval rows) and its
+        # own workspace, so that it can run beside the caller's stream
+        side = max(lib.a2ats_query_second_moment_workspace_size(H, max(M, 1), d),
+                   lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
+                   lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K))
+        self.side_workspace = torch.empty(side, dtype=torch.uint8, device=dev)
+        self.side_stream = torch.cuda.Stream(device=dev)
+        self._inputs_ready = torch.cuda.Event()
+        self._split_done = torch.cuda.Event()
+        self._side_done = torch.cuda.Event()
 
     def __call__(self, keys, codebook, queries=None, h_given=None, lengths=None, stream=None,
                  events=None):
         """keys [B, H, N, d] pre-RoPE; codebook [H, K, d]; queries [H, M, d]
         (calibration) or h_given [H, d, d] fp32 or neither (cosine-blend path).
-        events: optional dict; each stage appends a (start, end) CUDA event
-        pair recorded on the launching stream around its call."""
-        ws = self.workspace
+        Every output is complete, in the order of `stream`, when the call's
+        work on `stream` is.  events: optional dict; each stage appends a
+        (start, end) CUDA event pair recorded around its call on the stream
+        that runs it (stages on the two streams overlap)."""
+        ws, sws = self.workspace, self.side_workspace
         st = stream if stream is not None else torch.cuda.current_stream()
+        side = self.side_stream
 
-        def stage(name, fn, *a, **kw):
+        def stage(name, on, fn, *a, **kw):
             if events is None:
-                return fn(*a, **kw)
+                return fn(*a, stream=on, **kw)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            r = fn(*a, **kw)
-            e1.record(st)
+            e0.record(on)
+            r = fn(*a, stream=on, **kw)
+            e1.record(on)
             events.setdefault(name, []).append((e0, e1))
             return r
 
+        self._inputs_ready.record(st)
+        side.wait_event(self._inputs_ready)
         L = None
         if queries is not None:
-            stage("second_moment", a2ats_query_second_moment, queries, self.ridge, out=self.Hm,
-                  workspace=ws, stream=st)
+            stage("second_moment", side, a2ats_query_second_moment, queries, self.ridge,
+                  out=self.Hm, workspace=sws)
             h_given = self.Hm
         if h_given is not None:
-            stage("cholesky", a2ats_cholesky_factor, h_given, out=self.L, info=self.info,
-                  stream=st)
+            stage("cholesky", side, a2ats_cholesky_factor, h_given, out=self.L, info=self.info)
             L = self.L
-        stage("windowed_rope", a2ats_windowed_rope, keys, lengths=lengths, out=self.k_tilde,
-              stream=st, **self.rope)
-        stage("retrieval_split", a2ats_select_retrieval_set, keys, None, self.fraction,
-              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws,
-              stream=st)
+        stage("windowed_rope", st, a2ats_windowed_rope, keys, lengths=lengths, out=self.k_tilde,
+              **self.rope)
+        stage("retrieval_split", st, a2ats_select_retrieval_set, keys, None, self.fraction,
+              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws)
+        self._split_done.record(st)
+        side.wait_event(self._split_done)
         if L is not None:
-            stage("assign_retrieval", a2ats_h_weighted_assign, keys, codebook, L,
+            stage("assign_retrieval", side, a2ats_h_weighted_assign, keys, codebook, L,
                   lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
-                  count=self.count, codes=self.codes, workspace=ws, stream=st)
+                  count=self.count, codes=self.codes, workspace=sws)
         else:
             # no calibrated H: the cosine blend against the same proxy query
             # (the key at t after windowed RoPE) the split used
-            stage("assign_retrieval", a2ats_query_aware_assign, keys, codebook, None, self.beta,
-                  lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
-                  count=self.count, codes=self.codes, workspace=ws, stream=st)
-        stage("assign_bulk", a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
+            stage("assign_retrieval", side, a2ats_query_aware_assign, keys, codebook, None,
+                  self.beta, lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
+                  count=self.count, codes=self.codes, workspace=sws)
+        self._side_done.record(side)
+        stage("assign_bulk", st, a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
               rope=self.rope, rows="bulk", perm=self.perm, count=self.count, codes=self.codes,
-              workspace=ws, stream=st)
+              workspace=ws)
+        st.wait_event(self._side_done)
         return self
 
 

@@ -76,6 +76,22 @@ def test_h_weighted_matches_oracle(case):
         check_codes(got[b, h, :len(v)], code, (d2 - d1) / np.maximum(d2, 1e-300))
 
 
+@pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 48)])
+def test_entries_above_the_diagonal_are_ignored(dt, d):
+    """Only the lower triangle of L is read: filling the rest with noise
+    changes no code, on the tensor-core route and on the SIMT route."""
+    B, H, N, K = 1, 2, 300, 70
+    x = dev(synth.gaussian((B, H, N, d), seed=31, dtype=dt, scale=2.0))
+    c = dev(synth.gaussian((H, K, d), seed=32, dtype=dt, scale=2.0))
+    L = _L(H, d, 30.0, seed=33)
+    noisy = L + torch.triu(torch.from_numpy(
+        np.random.default_rng(34).standard_normal((H, d, d)).astype(np.float32)), diagonal=1)
+    rope = dict(window=40, far_offset=0, rope_base=500000.0)
+    a = q.a2ats_h_weighted_assign(x, c, dev(L), rope=rope)
+    b = q.a2ats_h_weighted_assign(x, c, dev(noisy), rope=rope)
+    assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("mode", ["retrieval", "bulk"])
 @pytest.mark.parametrize("rope", [None, dict(window=40, far_offset=5, rope_base=10000.0)])
 def test_row_selection_writes_only_its_rows(mode, rope):
