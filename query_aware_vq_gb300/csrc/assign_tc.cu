@@ -594,30 +594,41 @@ __global__ void rotate_rows_kernel(const float* __restrict__ in, int64_t rows, i
 
 // Per-head maxima into head_bits [H, 4] (uint bits of non-negative floats,
 // zeroed by the caller): max |chat_j|, max h_j, max |element|.
-__global__ void codebook_stats_kernel(const float* __restrict__ chat, int64_t HK, int64_t K,
-                                      int32_t d, const float* __restrict__ half_norm,
-                                      uint32_t* __restrict__ head_bits) {
-    const int lane = threadIdx.x & 31;
-    for (int64_t j = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; j < HK;
-         j += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-        const float* row = chat + j * d;
+__global__ void __launch_bounds__(256)
+codebook_stats_kernel(const float* __restrict__ chat, int64_t K, int32_t d,
+                      const float* __restrict__ half_norm, uint32_t* __restrict__ head_bits) {
+    // one warp per centroid, one head per block row; the block's maxima are
+    // combined in shared memory first, so a head takes one atomic per block
+    __shared__ float red[3][8];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t h = blockIdx.y;
+    const int64_t j = (int64_t)blockIdx.x * 8 + w;
+    float cm = 0.f, hm = 0.f, em = 0.f;
+    if (j < K) {
+        const float* row = chat + (h * K + j) * d;
         Dot2 n;
-        float mx = 0.f;
         for (int a = lane; a < d; a += 32) {
             const float v = row[a];
             n.add_prod(v, v);
-            mx = fmaxf(mx, fabsf(v));
+            em = fmaxf(em, fabsf(v));
         }
         for (int m = 16; m; m >>= 1) {
             n.merge(shfl_xor(n, m));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            em = fmaxf(em, __shfl_xor_sync(0xffffffffu, em, m));
         }
-        if (lane == 0) {
-            const int64_t h = j / K;
-            atomicMax(&head_bits[h * 4 + 0], __float_as_uint(sqrtf(n.value()) * 1.000001f));
-            atomicMax(&head_bits[h * 4 + 1], __float_as_uint(fmaxf(half_norm[j], 0.f)));
-            atomicMax(&head_bits[h * 4 + 2], __float_as_uint(mx));
-        }
+        cm = sqrtf(n.value()) * 1.000001f;
+        hm = fmaxf(half_norm[h * K + j], 0.f);
+    }
+    if (lane == 0) {
+        red[0][w] = cm;
+        red[1][w] = hm;
+        red[2][w] = em;
+    }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        float v = 0.f;
+        for (int ww = 0; ww < 8; ww++) v = fmaxf(v, red[threadIdx.x][ww]);
+        atomicMax(&head_bits[h * 4 + threadIdx.x], __float_as_uint(v));
     }
 }
 
@@ -1027,8 +1038,8 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
                       cudaStream_t st) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d;
-    codebook_stats_kernel<<<blocks_for(H * K * 32, 256, 4096), 256, 0, st>>>(
-        chat, H * K, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
+    codebook_stats_kernel<<<dim3((unsigned)((K + 7) / 8), (unsigned)H), 256, 0, st>>>(
+        chat, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
     note_launches(1);
     head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
         c.head_bits + v * H * 4, (int32_t)H, (int32_t)d, (bf16 || raw) ? 1 : 0, c.head + v * H * 4,
@@ -1171,7 +1182,13 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     }
     // rotated rows (the RoPE window, or every routed row) as two 16-bit planes
     if (compact) {
-        dim3 g(blocks_for(ncap, 8, 1024), (unsigned)nbh);
+        // rows per (b, h): at most the window (natural order), one (decode),
+        // or the retrieval count (not known here; grid-stride)
+        const int cmode = c.sel.mode == 2 ? 0 : c.sel.mode;
+        const int64_t most = cmode == 0 ? (c.ra.window < ncap ? c.ra.window : ncap)
+                                        : (cmode == 3 ? 1 : ncap);
+        const int64_t per_bh = 4 * (int64_t)sm_count() / (nbh > 0 ? nbh : 1);
+        dim3 g(blocks_for(most, 8, (unsigned)(per_bh > 1 ? per_bh : 1)), (unsigned)nbh);
         if (c.dt == kBF16)
             compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
                 c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,

@@ -88,21 +88,33 @@ windowed_rope_kernel(const void* __restrict__ kin, void* __restrict__ kout, int6
     if (far_rot) angles8<INTERLEAVED>(ra.far_offset, pair0, ra, fc, fs);
     if ((int)threadIdx.x >= rpb * lpr) return;  // lpr need not divide the block
 
-    for (int64_t row = (int64_t)blockIdx.x * rpb + threadIdx.x / lpr; row < rows;
-         row += (int64_t)gridDim.x * rpb) {
-        const int32_t j = (int32_t)(row % ncap);
-        const int32_t b = (int32_t)(row / ncap / H);
-        const int32_t L = seq_len(len, b, ncap);
-        if (j >= L) continue;
+    // grid-stride over rows; (bh, j) of the thread's row advance by the
+    // stride (qs whole sequences plus rs rows) without 64-bit divisions
+    const int64_t stride = (int64_t)gridDim.x * rpb;
+    const int64_t qs = stride / ncap;
+    const int32_t rs = (int32_t)(stride - qs * ncap);
+    int64_t row = (int64_t)blockIdx.x * rpb + threadIdx.x / lpr;
+    int64_t bh = row / ncap;
+    int32_t j = (int32_t)(row - bh * ncap);
+    for (; row < rows; row += stride) {
+        const int32_t L = seq_len(len, (int32_t)bh / H, ncap);
+        const int32_t jr = j;
+        j += rs;
+        bh += qs;
+        if (j >= ncap) {
+            j -= ncap;
+            bh++;
+        }
+        if (jr >= L) continue;
         const int64_t base = row * d;
         float v0[8], v1[8];
         load8<IN>(kin, base + e0, v0);
         if (!INTERLEAVED) load8<IN>(kin, base + e1, v1);
         if (ra.enabled) {
-            const bool near = ra.window > 0 && (L - 1 - j) < ra.window;
+            const bool near = ra.window > 0 && (L - 1 - jr) < ra.window;
             if (near) {
                 float c[8], s[8];
-                angles8<INTERLEAVED>(j, pair0, ra, c, s);
+                angles8<INTERLEAVED>(jr, pair0, ra, c, s);
                 rotate8<INTERLEAVED>(v0, v1, c, s);
             } else if (far_rot) {
                 rotate8<INTERLEAVED>(v0, v1, fc, fs);
@@ -254,71 +266,97 @@ prepare_query_kernel(const void* __restrict__ keys, const void* __restrict__ que
 }
 
 // Cosine of every valid row with its query (fp32; fused windowed RoPE).
+// The lpr lanes of a row each take 16 (or 8) of its elements and leave their
+// partial dot and squared norm in shared memory; one thread per row then adds
+// the partials and divides, so the square root and the division run once per
+// row rather than once per lane group.  Grid-stride over rows, with (bh, j)
+// advanced by the stride without 64-bit divisions.
 template <int DT, bool INTERLEAVED>
 __global__ void __launch_bounds__(kRopeThreads)
 cosine_score_kernel(const void* __restrict__ keys, int64_t rows, int32_t H, int32_t ncap,
                     int32_t d, const int32_t* __restrict__ len, const RopeArgs ra,
                     const float* __restrict__ q, const float* __restrict__ qnorm,
                     float* __restrict__ scores) {
+    __shared__ float2 part[kRopeThreads];
+    __shared__ int32_t row_bh[kRopeThreads];  // (b, h) of a valid row, else -1
     const int lpr = INTERLEAVED ? d / 8 : d / 16;
     const int rpb = kRopeThreads / lpr;
     const int lane = threadIdx.x % lpr;
+    const int rl = threadIdx.x / lpr;
+    const bool active = (int)threadIdx.x < rpb * lpr;  // lpr need not divide the block
     const int e0 = lane * 8;
     const int e1 = e0 + d / 2;
     const int pair0 = INTERLEAVED ? e0 / 2 : e0;
     const bool far_rot = ra.enabled && ra.far_offset != 0;
-    float fc[8], fs[8];
-    if (far_rot) angles8<INTERLEAVED>(ra.far_offset, pair0, ra, fc, fs);
-    for (int64_t row0 = (int64_t)blockIdx.x * rpb; row0 < rows; row0 += (int64_t)gridDim.x * rpb) {
-        const int64_t row = row0 + threadIdx.x / lpr;
-        bool valid = row < rows;
-        int32_t j = 0, L = 0;
-        int64_t bh = 0;
+    const int64_t stride = (int64_t)gridDim.x * rpb;
+    const int64_t qs = stride / ncap;
+    const int32_t rs = (int32_t)(stride - qs * ncap);
+    int64_t bh = ((int64_t)blockIdx.x * rpb + rl) / ncap;
+    int32_t j = (int32_t)(((int64_t)blockIdx.x * rpb + rl) - bh * ncap);
+    // the loop bounds are uniform over the block (it synchronises)
+    for (int64_t base = (int64_t)blockIdx.x * rpb; base < rows; base += stride) {
+        const int64_t row = base + rl;
+        bool valid = active && row < rows;
+        int32_t L = 0;
         if (valid) {
-            j = (int32_t)(row % ncap);
-            bh = row / ncap;
-            L = seq_len(len, (int32_t)(bh / H), ncap);
+            L = seq_len(len, (int32_t)bh / H, ncap);
             valid = j < L;
         }
         float dot = 0.f, nn = 0.f;
         if (valid) {
-            const int64_t base = row * d;
             float v0[8], v1[8];
-            load8<DT>(keys, base + e0, v0);
-            if (!INTERLEAVED) load8<DT>(keys, base + e1, v1);
+            load8<DT>(keys, row * d + e0, v0);
+            if (!INTERLEAVED) load8<DT>(keys, row * d + e1, v1);
             if (ra.enabled) {
                 const bool near = ra.window > 0 && (L - 1 - j) < ra.window;
-                if (near) {
-                    float c[8], s[8];
-                    angles8<INTERLEAVED>(j, pair0, ra, c, s);
-                    rotate8<INTERLEAVED>(v0, v1, c, s);
-                } else if (far_rot) {
-                    rotate8<INTERLEAVED>(v0, v1, fc, fs);
+                if (near || far_rot) {
+                    float c[8], sn[8];
+                    angles8<INTERLEAVED>(near ? j : ra.far_offset, pair0, ra, c, sn);
+                    rotate8<INTERLEAVED>(v0, v1, c, sn);
                 }
             }
-            const float* qq = q + bh * d;
+            const float4* qa = reinterpret_cast<const float4*>(q + bh * d + e0);
+            const float4 a0 = __ldg(qa), a1 = __ldg(qa + 1);
+            const float qv0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                dot = fmaf(v0[k], qq[e0 + k], dot);
+                dot = fmaf(v0[k], qv0[k], dot);
                 nn = fmaf(v0[k], v0[k], nn);
             }
             if (!INTERLEAVED) {
+                const float4* qb = reinterpret_cast<const float4*>(q + bh * d + e1);
+                const float4 b0 = __ldg(qb), b1 = __ldg(qb + 1);
+                const float qv1[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
-                    dot = fmaf(v1[k], qq[e1 + k], dot);
+                    dot = fmaf(v1[k], qv1[k], dot);
                     nn = fmaf(v1[k], v1[k], nn);
                 }
             }
         }
-        // reduce over the lpr lanes of the row (lpr is a power of two <= 32)
-        for (int m = lpr >> 1; m; m >>= 1) {
-            dot += __shfl_xor_sync(0xffffffffu, dot, m);
-            nn += __shfl_xor_sync(0xffffffffu, nn, m);
+        part[threadIdx.x] = make_float2(dot, nn);
+        if (active && lane == 0) row_bh[rl] = valid ? (int32_t)bh : -1;
+        __syncthreads();
+        if ((int)threadIdx.x < rpb) {
+            const int32_t rbh = row_bh[threadIdx.x];
+            if (rbh >= 0) {
+                float dd = 0.f, n2 = 0.f;
+                for (int i = 0; i < lpr; i++) {
+                    const float2 pp = part[threadIdx.x * lpr + i];
+                    dd += pp.x;
+                    n2 += pp.y;
+                }
+                const float qn = qnorm[rbh];
+                const float kn = sqrtf(n2);
+                scores[base + threadIdx.x] = (kn > 0.f && qn > 0.f) ? dd / (kn * qn) : 0.f;
+            }
         }
-        if (valid && lane == 0) {
-            const float qn = qnorm[bh];
-            const float kn = sqrtf(nn);
-            scores[row] = (kn > 0.f && qn > 0.f) ? dot / (kn * qn) : 0.f;
+        __syncthreads();
+        j += rs;
+        bh += qs;
+        if (j >= ncap) {
+            j -= ncap;
+            bh++;
         }
     }
 }
@@ -377,27 +415,31 @@ cosine_score_warp_kernel(const void* __restrict__ keys, int64_t rows, int32_t H,
 
 constexpr int kSelThreads = 512;
 constexpr int kSelCluster = 8;
+constexpr int kSelCache = 16384;  // keys of a CTA's segment kept in shared memory (66 KB)
 
-// Exclusive block-wide scan of one flag per thread; returns the block total.
-__device__ __forceinline__ int block_scan_flag(bool f, int& excl, int* warp_tot) {
+// Exclusive block-wide scan of one count per thread; returns the block total.
+__device__ __forceinline__ int block_scan(int v, int& excl, int* warp_tot) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[w] = __popc(bal);
+    int inc = v;
+    for (int m = 1; m < 32; m <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, m);
+        if (lane >= m) inc += t;
+    }
+    if (lane == 31) warp_tot[w] = inc;
     __syncthreads();
     if (w == 0) {
         const int nw = blockDim.x >> 5;
-        int v = lane < nw ? warp_tot[lane] : 0;
-        int inc = v;
+        const int x = lane < nw ? warp_tot[lane] : 0;
+        int wi = x;
         for (int m = 1; m < 32; m <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, inc, m);
-            if (lane >= m) inc += t;
+            const int t = __shfl_up_sync(0xffffffffu, wi, m);
+            if (lane >= m) wi += t;
         }
-        warp_tot[32 + lane] = inc - v;  // exclusive prefix of warp totals
-        if (lane == 31) warp_tot[64] = inc;
+        warp_tot[32 + lane] = wi - x;  // exclusive prefix of warp totals
+        if (lane == 31) warp_tot[64] = wi;
     }
     __syncthreads();
-    excl = warp_tot[32 + w] + in_warp;
+    excl = warp_tot[32 + w] + inc - v;
     const int total = warp_tot[64];
     __syncthreads();
     return total;
@@ -407,117 +449,160 @@ __device__ __forceinline__ int block_scan_flag(bool f, int& excl, int* warp_tot)
 // scores, ties on the threshold broken by lower index, then a stable
 // two-sided compaction: retrieval rows ascending, then bulk rows ascending.
 // One cluster of kSelCluster CTAs per (b, h): each CTA owns a contiguous
-// segment of the row; the per-pass histograms and the compaction offsets are
-// combined through distributed shared memory.
+// segment of the row (its keys cached in shared memory when they fit); the
+// per-pass histograms and the compaction offsets are combined through
+// distributed shared memory.  In the compaction each thread owns a contiguous
+// run of the segment, so two block scans place every row.
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
               const int32_t* __restrict__ len, double fraction, int32_t* __restrict__ perm,
               int32_t* __restrict__ count) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ uint32_t ks[];  // [kSelCache] ordered keys of the segment
     __shared__ uint32_t hist[256];
-    __shared__ int seg_counts[2];   // this CTA's rows above the threshold, equal to it
+    __shared__ uint32_t tot[256];
+    __shared__ int seg_counts[2];     // this CTA's rows above the threshold, equal to it
     __shared__ int warp_tot[65];
+    __shared__ uint32_t sel_prefix, sel_need;
     const int rank = (int)cluster.block_rank();
     const int bh = blockIdx.x / kSelCluster;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int32_t n = seq_len(len, bh / H, ncap);
     const float* s = scores + (int64_t)bh * ncap;
     int32_t* out = perm + (int64_t)bh * ncap;
     const double kd = ceil(fraction * (double)n);
     const int32_t k = kd < 0.0 ? 0 : (kd > (double)n ? n : (int32_t)kd);
-    if (rank == 0 && threadIdx.x == 0) count[bh] = k;
+    if (rank == 0 && tid == 0) count[bh] = k;
     const int32_t seg = (n + kSelCluster - 1) / kSelCluster;
     const int32_t lo = min(n, rank * seg), hi = min(n, lo + seg);
+    const int32_t m = hi - lo;
+    // the launch gives ks room for a segment of the capacity when that fits
+    const bool cached = (ncap + kSelCluster - 1) / kSelCluster <= kSelCache;
+    const bool partial = k > 0 && k < n;
+    // key i of the segment sits at ks[i + i / 32], so the contiguous runs of
+    // the compaction (thread t reads t * per + e) fall on distinct banks
+    if (cached && partial)
+        for (int i = tid; i < m; i += blockDim.x) ks[i + (i >> 5)] = ordered_key(s[lo + i]);
+    auto key = [&](int32_t i) -> uint32_t {  // i relative to lo
+        return cached ? ks[i + (i >> 5)] : ordered_key(s[lo + i]);
+    };
 
     uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
-    const bool partial = k > 0 && k < n;
     if (partial) {
         for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+            for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
             __syncthreads();
-            for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-                const uint32_t u = ordered_key(s[i]);
+            for (int i = tid; i < m; i += blockDim.x) {
+                const uint32_t u = key(i);
                 if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
             }
             cluster.sync();
             // every CTA sums the cluster's histograms and takes the same digit
-            __shared__ uint32_t tot[256];
-            for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            if (tid < 256) {
+                uint32_t part[kSelCluster];
+#pragma unroll
+                for (int r = 0; r < kSelCluster; r++) part[r] = cluster.map_shared_rank(hist, r)[tid];
                 uint32_t t = 0;
-                for (int r = 0; r < kSelCluster; r++) t += cluster.map_shared_rank(hist, r)[i];
-                tot[i] = t;
+#pragma unroll
+                for (int r = 0; r < kSelCluster; r++) t += part[r];
+                tot[tid] = t;
             }
             cluster.sync();  // no CTA resets its histogram while another reads it
-            __shared__ uint32_t sel_prefix, sel_need;
-            if (threadIdx.x == 0) {
-                uint32_t cum = 0;
-                for (int dg = 255; dg >= 0; --dg) {
-                    const uint32_t hcount = tot[dg];
-                    if (cum + hcount >= need) {
-                        sel_prefix = prefix | ((uint32_t)dg << shift);
-                        sel_need = need - cum;
-                        break;
+            if (w == 0) {
+                // lane l holds digits 255 - 8l ... 248 - 8l (descending);
+                // suffix sums from the top digit find the one holding the
+                // need-th largest key
+                uint32_t c[8], local = 0;
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    c[e] = tot[255 - 8 * lane - e];
+                    local += c[e];
+                }
+                uint32_t incl = local;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const uint32_t before = incl - local;
+                const bool here = before < need && incl >= need;
+                if (here) {
+                    uint32_t cum = before;
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        if (cum + c[e] >= need) {
+                            sel_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
+                            sel_need = need - cum;
+                            break;
+                        }
+                        cum += c[e];
                     }
-                    cum += hcount;
                 }
             }
             __syncthreads();
             prefix = sel_prefix;
             need = sel_need;
             mask |= 255u << shift;
-            __syncthreads();
         }
     }
-    // per-CTA counts of rows above and equal to the threshold, then prefixes
-    // over the CTAs of lower rank
+    // each thread owns the contiguous run [r0, r1) of the segment
+    const int per = (m + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int r0 = min(m, tid * per), r1 = min(m, r0 + per);
     int gt_local = 0, eq_local = 0;
-    if (partial) {
-        for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-            const uint32_t u = ordered_key(s[i]);
+    if (partial)
+        for (int i = r0; i < r1; i++) {
+            const uint32_t u = key(i);
             gt_local += u > prefix;
             eq_local += u == prefix;
         }
-    }
-    gt_local = __reduce_add_sync(0xffffffffu, gt_local);
-    eq_local = __reduce_add_sync(0xffffffffu, eq_local);
-    if (threadIdx.x == 0) { seg_counts[0] = 0; seg_counts[1] = 0; }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
-        atomicAdd(&seg_counts[0], gt_local);
-        atomicAdd(&seg_counts[1], eq_local);
+    int eq_excl, gt_excl;
+    const int eq_cta = block_scan(eq_local, eq_excl, warp_tot);
+    const int gt_cta = block_scan(gt_local, gt_excl, warp_tot);
+    if (tid == 0) {
+        seg_counts[0] = gt_cta;
+        seg_counts[1] = eq_cta;
     }
     cluster.sync();
     int gt_before = 0, eq_before = 0;
-    for (int r = 0; r < rank; r++) {
-        const int* other = cluster.map_shared_rank(seg_counts, r);
-        gt_before += other[0];
-        eq_before += other[1];
+    {
+        int g[kSelCluster], q[kSelCluster];
+#pragma unroll
+        for (int r = 0; r < kSelCluster; r++) {
+            const int* other = cluster.map_shared_rank(seg_counts, r);
+            g[r] = r < rank ? other[0] : 0;
+            q[r] = r < rank ? other[1] : 0;
+        }
+#pragma unroll
+        for (int r = 0; r < kSelCluster; r++) {
+            gt_before += g[r];
+            eq_before += q[r];
+        }
     }
     cluster.sync();  // the counts stay readable until every CTA has them
-    // rows taken before this segment: those above the threshold plus the
-    // equal ones that fit in `need`, in index order
-    const int eq_taken_before = min(eq_before, (int)need);
-    int carry_take = partial ? gt_before + eq_taken_before : (k == n ? lo : 0);
-    int carry_eq = eq_before;
-    for (int base = lo; base < hi; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        const bool valid = i < hi;
-        uint32_t u = 0;
-        if (valid && partial) u = ordered_key(s[i]);
-        const bool eq = valid && partial && u == prefix;
-        int eq_excl;
-        const int eq_tot = block_scan_flag(eq, eq_excl, warp_tot);
-        const bool take = valid && (k == n || (partial && (u > prefix ||
-                                                           (eq && carry_eq + eq_excl < (int)need))));
-        int t_excl;
-        const int t_tot = block_scan_flag(take, t_excl, warp_tot);
-        if (valid) {
-            const int pos_r = carry_take + t_excl;
-            if (take) out[pos_r] = i;
-            else out[k + (i - pos_r)] = i;
+    // rows of this thread's run that are taken: all above the threshold, and
+    // the equal ones among the first `need` equal rows in index order
+    int eq_seen = eq_before + eq_excl;
+    int take_local = 0;
+    if (k == n) take_local = r1 - r0;
+    else if (partial) {
+        const int eq_take = max(0, min((int)need - eq_seen, eq_local));
+        take_local = gt_local + eq_take;
+    }
+    int take_excl;
+    block_scan(take_local, take_excl, warp_tot);
+    const int take_before_seg = partial ? gt_before + min(eq_before, (int)need) : (k == n ? lo : 0);
+    int pos_r = take_before_seg + take_excl;      // next retrieval slot
+    int pos_b = k + (lo + r0 - pos_r);            // next bulk slot: rows before minus taken
+    for (int i = r0; i < r1; i++) {
+        bool take = k == n;
+        if (partial) {
+            const uint32_t u = key(i);
+            const bool eq = u == prefix;
+            take = u > prefix || (eq && eq_seen < (int)need);
+            eq_seen += eq;
         }
-        carry_eq += eq_tot;
-        carry_take += t_tot;
+        if (take) out[pos_r++] = lo + i;
+        else out[pos_b++] = lo + i;
     }
 }
 
@@ -557,7 +642,7 @@ cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
         cosine_score_kernel<DT, false><<<grid_for(rows, kRopeThreads / (d / 16)), kRopeThreads,
                                          0, st>>>(keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d,
                                                   len, ra, q, qnorm, scores);
-                                                  note_launches(1);
+        note_launches(1);
     } else {
         cosine_score_warp_kernel<DT><<<grid_for(rows, kRopeThreads / 32), kRopeThreads, 0, st>>>(
             keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra, q, qnorm, scores);
@@ -630,7 +715,13 @@ cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* le
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st) {
     const int nbh = (int)(s.B * s.H);
     if (nbh == 0) return cudaSuccess;
-    select_kernel<<<nbh * kSelCluster, kSelThreads, 0, st>>>(scores, (int32_t)s.H,
+    const int64_t seg = (s.Ncap + kSelCluster - 1) / kSelCluster;
+    const size_t smem = seg <= kSelCache ? sizeof(uint32_t) * (size_t)(seg + seg / 32 + 1) : 0;
+    cudaError_t e = cudaFuncSetAttribute(select_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(uint32_t) * (kSelCache + kSelCache / 32 + 1)));
+    if (e != cudaSuccess) return e;
+    select_kernel<<<nbh * kSelCluster, kSelThreads, smem, st>>>(scores, (int32_t)s.H,
                                                              (int32_t)s.Ncap, len, fraction, perm,
                                                              count);
                                                note_launches(1);

@@ -22,6 +22,9 @@ needs L and the split) follows it there once the split is done, while the
 bulk rows of step 6 are assigned on the caller's stream; the two write
 disjoint codes.  The caller's stream waits for the second before returning.
 
+Steps 1-2 may also run once, ahead of the steps that reuse their L
+(A2ATSStep.calibrate), as the pages do when H is calibrated offline.
+
 All buffers are allocated once in the constructor; a step allocates nothing.
 """
 from __future__ import annotations
@@ -62,41 +65,65 @@ class A2ATSStep:
                    lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K))
         self.side_workspace = torch.empty(side, dtype=torch.uint8, device=dev)
         self.side_stream = torch.cuda.Stream(device=dev)
+        self.calibrated = False
         self._inputs_ready = torch.cuda.Event()
         self._split_done = torch.cuda.Event()
         self._side_done = torch.cuda.Event()
 
+    @staticmethod
+    def _stage(events, name, on, fn, *a, **kw):
+        if events is None:
+            return fn(*a, stream=on, **kw)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(on)
+        r = fn(*a, stream=on, **kw)
+        e1.record(on)
+        events.setdefault(name, []).append((e0, e1))
+        return r
+
+    def calibrate(self, queries=None, h_given=None, stream=None, events=None):
+        """H = E[q^T q] + ridge I from queries [H, M, d] (or h_given [H, d, d]
+        fp32 as is) and its Cholesky factor, kept in self.Hm / self.L / self.info
+        for the steps that follow (the pages calibrate H once per layer, ahead
+        of decoding).  Runs on `stream`."""
+        st = stream if stream is not None else torch.cuda.current_stream()
+        if queries is not None:
+            self._stage(events, "second_moment", st, a2ats_query_second_moment, queries,
+                        self.ridge, out=self.Hm, workspace=self.side_workspace)
+            h_given = self.Hm
+        if h_given is None:
+            raise ValueError("calibrate needs queries or h_given")
+        self._stage(events, "cholesky", st, a2ats_cholesky_factor, h_given, out=self.L,
+                    info=self.info)
+        self.calibrated = True
+        return self
+
     def __call__(self, keys, codebook, queries=None, h_given=None, lengths=None, stream=None,
-                 events=None):
-        """keys [B, H, N, d] pre-RoPE; codebook [H, K, d]; queries [H, M, d]
-        (calibration) or h_given [H, d, d] fp32 or neither (cosine-blend path).
-        Every output is complete, in the order of `stream`, when the call's
-        work on `stream` is.  events: optional dict; each stage appends a
-        (start, end) CUDA event pair recorded around its call on the stream
-        that runs it (stages on the two streams overlap)."""
+                 events=None, calibrated=False):
+        """keys [B, H, N, d] pre-RoPE; codebook [H, K, d].  The retrieval rows
+        take the H-weighted rule with an L calibrated inside the step from
+        queries [H, M, d] (or h_given [H, d, d] fp32), or, with
+        calibrated=True, the L of an earlier calibrate(); with neither, the
+        cosine blend.  Every output is complete, in the order of `stream`,
+        when the call's work on `stream` is.  events: optional dict; each stage
+        appends a (start, end) CUDA event pair recorded around its call on the
+        stream that runs it (stages on the two streams overlap)."""
         ws, sws = self.workspace, self.side_workspace
         st = stream if stream is not None else torch.cuda.current_stream()
         side = self.side_stream
 
         def stage(name, on, fn, *a, **kw):
-            if events is None:
-                return fn(*a, stream=on, **kw)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(on)
-            r = fn(*a, stream=on, **kw)
-            e1.record(on)
-            events.setdefault(name, []).append((e0, e1))
-            return r
+            return self._stage(events, name, on, fn, *a, **kw)
 
         self._inputs_ready.record(st)
         side.wait_event(self._inputs_ready)
         L = None
-        if queries is not None:
-            stage("second_moment", side, a2ats_query_second_moment, queries, self.ridge,
-                  out=self.Hm, workspace=sws)
-            h_given = self.Hm
-        if h_given is not None:
-            stage("cholesky", side, a2ats_cholesky_factor, h_given, out=self.L, info=self.info)
+        if queries is not None or h_given is not None:
+            self.calibrate(queries, h_given, stream=side, events=events)
+            L = self.L
+        elif calibrated:
+            if not getattr(self, "calibrated", False):
+                raise ValueError("calibrated=True before any calibrate()")
             L = self.L
         stage("windowed_rope", st, a2ats_windowed_rope, keys, lengths=lengths, out=self.k_tilde,
               **self.rope)

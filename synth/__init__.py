@@ -57,6 +57,7 @@ class Workload:
     keys: str = "gaussian"  # or "student_t"
     h_given: bool = False   # H drawn directly (ill-conditioned) instead of from queries
     decode_steps: int = 0
+    calibrate_in_step: bool = False  # H and L recomputed by every step (else once, ahead)
     extra: dict = field(default_factory=dict)
 
 
@@ -69,7 +70,8 @@ WORKLOADS = {
                                  K=1024, W=512, fraction=0.05, rope_base=500000.0, M=8192),
     # Llama-3-8B-shaped long context, batch 4
     "llama3_8b_long": Workload("llama3_8b_long", B=4, H=8, N=131072, d=128, dtype="bf16",
-                               K=4096, W=1024, fraction=0.02, rope_base=500000.0, M=65536),
+                               K=4096, W=1024, fraction=0.02, rope_base=500000.0, M=65536,
+                               calibrate_in_step=True),
     # decode streaming: 64 sequences, lengths U[8192, 32768], one new key per
     # (sequence, head) per step, 128 steps
     "decode_stream": Workload("decode_stream", B=64, H=8, N=32768 + 128, d=128, dtype="bf16",

@@ -23,6 +23,8 @@ CASES = [
     (1, 1, 10, 16, "bf16", 0.0, "proxy", None),
     (1, 1, 1, 16, "bf16", 0.5, "proxy", None),
     (1, 1, 70000, 128, "bf16", 0.02, "proxy", dict(window=100, rope_base=500000.0)),
+    # segments too long for the select kernel's shared-memory cache
+    (1, 1, 140000, 16, "bf16", 0.03, "proxy", None),
 ]
 
 
