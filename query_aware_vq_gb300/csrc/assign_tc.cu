@@ -14,17 +14,20 @@
 // codebook needs one plane.  Each plane is one more pass of tcgen05.mma into
 // the same TMEM accumulator.
 //
-// Kernel layout (one persistent CTA per SM, 10 warps):
+// Kernel layout (one persistent CTA per SM, 18 warps):
 //   warp 0     TMA producer: the 128-row key tile once per tile (kept for all
 //              centroids), then the codebook in 256 x 64-element stages;
 //   warp 1     TMEM allocation and tcgen05.mma issue (128 x 256 x 16,
 //              bf16/fp16 -> fp32), two accumulators of 256 columns so the
 //              epilogue of one centroid chunk overlaps the MMAs of the next;
-//   warps 2-9  epilogue: tcgen05.ld of the accumulator, v = acc - |c'|^2/2,
-//              branch-free top-2 per row with the column index carried in the
-//              5 low mantissa bits, and a rigorous error bound: rows whose top
-//              two are closer than the bound, and rows inside the RoPE window,
-//              go to the exact SIMT kernel through a list.
+//   warps 2-17 epilogue, one per (TMEM lane quarter, 64-column part):
+//              tcgen05.ld of the accumulator, v = acc - |c'|^2/2, branch-free
+//              top-2 per row with the column index carried in the 5 low
+//              mantissa bits; the parts of a row meet in shared memory, and a
+//              rigorous error bound sends rows whose top two are closer than
+//              the bound (and rows inside the RoPE window) to the exact SIMT
+//              kernels through a list.  Four epilogue warps per scheduler
+//              hide the TMEM and shared-memory latencies of each other.
 // Every mbarrier wait is bounded; on time-out the kernel records an error
 // code and leaves.
 #include <cuda.h>
@@ -39,7 +42,9 @@ namespace tc {
 constexpr int BM = 128;   // rows per tile (UMMA M)
 constexpr int BN = 256;   // centroids per accumulator (UMMA N)
 constexpr int BK = 64;    // 16-bit elements per 128-byte swizzle atom
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;                // 4 TMEM lane quarters x 4 column parts
+constexpr int kParts = kEpiWarps / 4;         // column parts of a 256-column chunk
+constexpr int kSubs = BN / 32 / kParts;       // 32-column sub-chunks per part
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
 
@@ -62,6 +67,7 @@ struct Params {
     int64_t* exact_list;       // rows for the exact kernel
     int32_t* exact_count;
     int32_t* status;           // 0, or the code of a timed-out wait
+    uint32_t shr5_mul, shl5_mul;  // 2^27 and 32 (see embed_pos)
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -178,9 +184,12 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 // (bits & ~31) | pos: the column position rides in the five low mantissa
-// bits of the key (pos is a compile-time constant at every use).
-__device__ __forceinline__ float embed_pos(float v, uint32_t pos) {
-    return __uint_as_float((__float_as_uint(v) & 0xFFFFFFE0u) | pos);
+// bits of the key (pos is a compile-time constant at every use).  It is
+// computed as hi(bits * 2^27) * 32 + pos with the two multipliers taken from
+// the kernel parameters, so that it runs as integer multiply-adds on the FMA
+// pipe and leaves the ALU pipe to the min/max network.
+__device__ __forceinline__ float embed_pos(float v, uint32_t pos, uint32_t m27, uint32_t m5) {
+    return __uint_as_float(__umulhi(__float_as_uint(v), m27) * m5 + pos);
 }
 
 // Top two of 32 keys: min/max of pairs, then a merge tree of (max, second)
@@ -235,7 +244,7 @@ struct Smem {
     static constexpr int kBarOff = kHOff + 2 * BN * 4;
     static constexpr int kBars = 2 * AST + 2 * BST + 10;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
-    static constexpr int kTotal = kMergeOff + 4 * 32 * 16 + 1024;  // + alignment slack
+    static constexpr int kTotal = kMergeOff + (kParts - 1) * 4 * 32 * 16 + 1024;  // + slack
 };
 
 template <bool BF16, int DK, int PA, int AST, int BST>
@@ -258,7 +267,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* h_full = acc_full + 4;
     uint64_t* h_empty = acc_full + 6;
-    uint64_t* merge_full = acc_full + 8;   // column-half handoff, after the h ring
+    uint64_t* merge_full = acc_full + 8;   // column-part handoff, after the h ring
     uint64_t* merge_empty = acc_full + 9;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
@@ -281,8 +290,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(&h_full[i], 1);
             mbar_init(&h_empty[i], kEpiWarps);
         }
-        mbar_init(merge_full, kEpiWarps / 2);
-        mbar_init(merge_empty, kEpiWarps / 2);
+        mbar_init(merge_full, kEpiWarps - 4);  // every warp of parts 1.. hands over
+        mbar_init(merge_empty, 4);             // the part-0 warps take the handoff
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -414,7 +423,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // ------------------------------------------------------ epilogue --
         const int ew = warp - 2;
         const int q = warp & 3;          // TMEM lane quarter this warp may access
-        const int half = ew >> 2;        // which 128 of the 256 accumulator columns
+        const int part = ew >> 2;        // which BN / kParts accumulator columns
         const int row_in_tile = 32 * q + lane;
         uint32_t a_it = 0, acc_it = 0, m_it = 0;
         bool ok = true;
@@ -427,7 +436,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!ok) break;
             // |x|^2 of this row from the swizzled tile of plane 0 (order does not matter)
             float nrm = 0.f;
-            if (half == 0) {
+            if (part == 0) {
 #pragma unroll
                 for (int kb = 0; kb < DK; kb++) {
                     const uint8_t* rowp = smA + (sa * PA * DK + kb) * S::kA + row_in_tile * 128;
@@ -462,6 +471,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int32_t c1 = 0;
             const float inv_scale = p.head[h * 4 + 2];
             const float2 inv2 = make_float2(inv_scale, inv_scale);
+            const uint32_t m27 = p.shr5_mul, m5 = p.shl5_mul;
             for (int c = 0; c < p.nchunks && ok; c++) {
                 const int acc = acc_it & 1;
                 ok = mbar_wait(&h_full[acc], (acc_it >> 1) & 1, p.status, 12) &&
@@ -470,15 +480,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 tc_fence_after();
                 const float* hrow = smH + acc * BN;
                 const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-                // TMEM loads run one sub-chunk ahead of the arithmetic
-                uint32_t rbuf[2][32];
-                A2ATS_TMEM_LD32(tbase + (uint32_t)(half * 128), rbuf[0]);
-                tmem_wait_ld();
 #pragma unroll
-                for (int sub = 0; sub < 4; sub++) {
-                    const int col = half * 128 + sub * 32;
-                    if (sub < 3) A2ATS_TMEM_LD32(tbase + (uint32_t)(col + 32), rbuf[(sub + 1) & 1]);
-                    const uint32_t* r = rbuf[sub & 1];
+                for (int sub = 0; sub < kSubs; sub++) {
+                    const int col = (part * kSubs + sub) * 32;
+                    uint32_t r[32];
+                    A2ATS_TMEM_LD32(tbase + (uint32_t)col, r);
+                    tmem_wait_ld();
                     const float4* h4 = reinterpret_cast<const float4*>(hrow + col);
                     float key[32];
 #pragma unroll
@@ -490,10 +497,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         const float2 v23 = __ffma2_rn(
                             make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
                             inv2, make_float2(hv.z, hv.w));
-                        key[4 * u + 0] = embed_pos(v01.x, 31u - 4 * u);
-                        key[4 * u + 1] = embed_pos(v01.y, 30u - 4 * u);
-                        key[4 * u + 2] = embed_pos(v23.x, 29u - 4 * u);
-                        key[4 * u + 3] = embed_pos(v23.y, 28u - 4 * u);
+                        key[4 * u + 0] = embed_pos(v01.x, 31u - 4 * u, m27, m5);
+                        key[4 * u + 1] = embed_pos(v01.y, 30u - 4 * u, m27, m5);
+                        key[4 * u + 2] = embed_pos(v23.x, 29u - 4 * u, m27, m5);
+                        key[4 * u + 3] = embed_pos(v23.y, 28u - 4 * u, m27, m5);
                     }
                     float t1, t2;
                     top2_32(key, t1, t2);
@@ -501,7 +508,6 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (t1 > m1) c1 = j0 >> 5;
                     m2 = max3f(fminf(m1, t1), m2, t2);
                     m1 = fmaxf(m1, t1);
-                    if (sub < 3) tmem_wait_ld();
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -512,26 +518,31 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 acc_it++;
             }
             if (!ok) break;
-            // merge the two column halves of each row, then decide the row
-            if (half == 1) {
+            // merge the column parts of each row, then decide the row
+            if (part != 0) {
                 ok = mbar_wait(merge_empty, (m_it & 1) ^ 1, p.status, 9);
                 if (!ok) break;
-                merge[q * 32 + lane] = make_float4(m1, m2, __int_as_float(c1), 0.f);
+                merge[(part - 1) * 128 + q * 32 + lane] = make_float4(m1, m2, __int_as_float(c1), 0.f);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_full);
             } else {
                 ok = mbar_wait(merge_full, m_it & 1, p.status, 10);
                 if (!ok) break;
-                const float4 o = merge[q * 32 + lane];
+                float4 o[kParts - 1];
+#pragma unroll
+                for (int pp = 0; pp < kParts - 1; pp++) o[pp] = merge[pp * 128 + q * 32 + lane];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_empty);
-                const int32_t oc = __float_as_int(o.z);
-                if (o.x > m1) {
-                    m2 = fmaxf(m1, o.y);
-                    m1 = o.x;
-                    c1 = oc;
-                } else {
-                    m2 = fmaxf(m2, o.x);
+#pragma unroll
+                for (int pp = 0; pp < kParts - 1; pp++) {
+                    const int32_t oc = __float_as_int(o[pp].z);
+                    if (o[pp].x > m1) {
+                        m2 = fmaxf(m1, o[pp].y);
+                        m1 = o[pp].x;
+                        c1 = oc;
+                    } else {
+                        m2 = fmaxf(m2, o[pp].x);
+                    }
                 }
                 const int32_t ri = ti.r0 + row_in_tile;
                 if (ri < ti.nvalid) {
@@ -1120,6 +1131,8 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.exact_list = c.exact_list;
     p.exact_count = c.exact_count;
     p.status = c.exact_count + 1;
+    p.shr5_mul = 1u << 27;
+    p.shl5_mul = 32u;
     if (p.num_bh * p.tiles_per_bh == 0) return cudaSuccess;
     if (PA == 1)
         return bf16 ? launch_by_width<true, 1>(ta, tb, p, st) : launch_by_width<false, 1>(ta, tb, p, st);
