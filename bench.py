@@ -45,6 +45,13 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of roofline"
+
+# DRAM bytes (read + write) of one stored-order contraction launch on the
+# default workload, from the ncu capture summarised in
+# profiles/assign_tc_kernel_llama32_3b_layer.md.  It holds only for the
+# contraction source it was taken on (the first 16 hex digits of the sha256 of
+# csrc/assign_tc.cu); for any other source the bench reports null.
+TC_TRAFFIC = {"llama32_3b_layer": ("1501ccfd809fb2f0", 69023744)}
 DEFAULT_WORKLOAD = "llama32_3b_layer"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -153,6 +160,17 @@ class Clocks:
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _tc_traffic(workload: str):
+    import hashlib
+    entry = TC_TRAFFIC.get(workload)
+    if entry is None:
+        return None
+    src = os.path.join(ROOT, "query_aware_vq_gb300", "csrc", "assign_tc.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    return entry[1] if digest == entry[0] else None
 
 
 def _inputs(w, rank):
@@ -266,7 +284,7 @@ def run_ours(a):
         achieved = amount / (per_launch * 1e-3) / 1e12
         roof = {"kernel": "assign_tc_kernel (stored-order pass, bulk rows)", "bound": "tensor",
                 "achieved": round(achieved, 3), "peak": bf16, "unit": "TFLOP/s",
-                "frac": round(achieved / bf16, 5), "traffic": None,
+                "frac": round(achieved / bf16, 5), "traffic": _tc_traffic(w.name),
                 "flop_per_launch": amount, "ms_per_launch": round(per_launch, 5),
                 "launches": tc_launches, "peak_source": f"{src} (bf16_tflops, burst)"}
     else:
