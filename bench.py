@@ -192,6 +192,9 @@ def _work(w, count):
         "cholesky": ("alu", w.H * w.d ** 3 / 3.0),
         "windowed_rope": ("hbm", keys * w.d * 2.0 * s),
         "retrieval_split": ("hbm", keys * (w.d * s + 4.0)),
+        # one read of the keys, the rotated keys written, the scores written
+        # and read back by the select, the split written
+        "rope_and_split": ("hbm", keys * (2.0 * w.d * s + 12.0)),
         "assign_retrieval": ("tensor", n_ret * (2.0 * w.d * w.K + 2.0 * w.d * w.d)),
         "assign_bulk": ("tensor", n_bulk * 2.0 * w.d * w.K),
     }

@@ -207,6 +207,28 @@ int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64
                                size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_select_retrieval_set_rotated -- a2ats_windowed_rope and
+ * a2ats_select_retrieval_set (fused_rope = rope) in one pass over the keys
+ * (no counterpart on the pages: it fuses two of their steps, the per-step
+ * re-rotation of [ALG] "Per-step re-rotation" and the split of [API]
+ * a2ats_select_retrieval_set, so the pre-RoPE cache is read once).
+ *   keys   [B, H, Ncap, d] pre-RoPE, in dtype
+ *   rope   required; k_out [B, H, Ncap, d] in out_dtype receives exactly what
+ *          a2ats_windowed_rope(keys, ..., rope) writes (rows j < len[b]);
+ *          k_out must not be keys
+ *   query, fraction, perm, count, workspace: as a2ats_select_retrieval_set,
+ *          and perm / count are exactly what it writes with fused_rope = rope
+ * Errors: those of both calls; the workspace size is
+ * a2ats_select_retrieval_set_workspace_size.
+ * ------------------------------------------------------------------------ */
+int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                                       int64_t Ncap, int64_t d, const int32_t* len,
+                                       const void* query, double fraction,
+                                       const a2ats_rope_params* rope, void* k_out,
+                                       int32_t out_dtype, int32_t* perm, int32_t* count,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_select_retrieval_set_static -- the same retrieval split as
  * a2ats_select_retrieval_set, for callers that cannot allocate device memory
  * (no counterpart on the pages: this is a packaging variant).  Some callers

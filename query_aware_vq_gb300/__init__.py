@@ -62,6 +62,8 @@ _SIGS = {
     "a2ats_select_retrieval_set_workspace_size": [_I64, _I64, _I64, _I64],
     "a2ats_select_retrieval_set": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P, _P, _P,
                                    _SZ, _P],
+    "a2ats_select_retrieval_set_rotated": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
+                                           _I32, _P, _P, _P, _SZ, _P],
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
@@ -312,6 +314,35 @@ def a2ats_select_retrieval_set(keys, query=None, fraction: float = 0.2, *, lengt
         ctypes.byref(rp) if rp is not None else None, _ptr(perm), _ptr(count), _ptr(ws), nb,
         _stream(stream)))
     return perm, count
+
+
+def a2ats_select_retrieval_set_rotated(keys, query=None, fraction: float = 0.2, *, rope,
+                                       lengths=None, out=None, out_dtype=None, perm=None,
+                                       count=None, workspace=None, stream=None):
+    """Windowed RoPE of the cache and the retrieval split in one pass over
+    the pre-RoPE keys; returns (out, perm, count), each exactly what
+    a2ats_windowed_rope and a2ats_select_retrieval_set(rope=rope) return."""
+    _dev(keys, query, lengths, out, perm, count)
+    k4 = _as4(keys)
+    B, H, N, d = k4.shape
+    if query is not None and query.dtype != k4.dtype:
+        raise TypeError("query and keys must share a dtype")
+    if out is None:
+        out = torch.empty(keys.shape, dtype=out_dtype or keys.dtype, device=keys.device)
+    o4 = _as4(out)
+    if perm is None:
+        perm = torch.empty((B, H, N), dtype=torch.int32, device=keys.device)
+    if count is None:
+        count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d), keys.device,
+                        workspace)
+    rp = _rope(rope)
+    _check("a2ats_select_retrieval_set_rotated", lib.a2ats_select_retrieval_set_rotated(
+        _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
+        ctypes.byref(rp), _ptr(o4), _dt(o4), _ptr(perm), _ptr(count), _ptr(ws), nb,
+        _stream(stream)))
+    return out, perm, count
 
 
 def split_views(perm, count, b: int = 0, h: int = 0, n: int | None = None):

@@ -465,4 +465,48 @@ int a2ats_select_retrieval_set(const void* keys, int32_t dtype, int64_t B, int64
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                                       int64_t Ncap, int64_t d, const int32_t* len,
+                                       const void* query, double fraction,
+                                       const a2ats_rope_params* rope, void* k_out,
+                                       int32_t out_dtype, int32_t* perm, int32_t* count,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
+    if (!rope) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(rope, d, ra))) return st;
+    if (B * H == 0) return A2ATS_OK;
+    if (!count || (Ncap > 0 && (!keys || !perm || !k_out))) return A2ATS_ERR_INVALID_ARG;
+    if ((keys && !aligned16(keys)) || (query && !aligned16(query)) || (perm && !aligned16(perm)) ||
+        (k_out && !aligned16(k_out)))
+        return A2ATS_ERR_ALIGN;
+    // the keys are read again after k_out is written, so they may not share memory
+    if (Ncap > 0 && k_out == keys) return A2ATS_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < a2ats_select_retrieval_set_workspace_size(B, H, Ncap, d))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    SelectWs w = carve_select(c, B, H, Ncap, d);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    cudaError_t e = cudaSuccess;
+    if (Ncap > 0) {
+        e = launch_prepare_query(keys, query, dtype, sh, len, ra, w.q, w.qnorm, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = launch_cosine_scores(keys, dtype, sh, len, ra, w.q, w.qnorm, w.scores, s, k_out,
+                                 out_dtype);
+        if (e == cudaErrorNotSupported) {
+            // no fused form for this width: rotate in a pass of its own
+            e = launch_cosine_scores(keys, dtype, sh, len, ra, w.q, w.qnorm, w.scores, s);
+            if (e == cudaSuccess)
+                e = launch_windowed_rope(keys, dtype, k_out, out_dtype, sh, len, ra, s);
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_select(w.scores, sh, len, fraction, perm, count, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
 }  // extern "C"

@@ -34,9 +34,13 @@ cudaError_t launch_prepare_query(const void* keys, const void* query, int dt, co
                                  float* qnorm, cudaStream_t st);
 
 // scores [B*H*Ncap] fp32 cosine of every valid row with its (b, h) query.
+// kout != null: the windowed-RoPE rows are stored too, in out_dt (the same
+// values launch_windowed_rope writes); cudaErrorNotSupported when the width
+// has no fused form (the caller then runs launch_windowed_rope).
 cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
                                  const RopeArgs& ra, const float* q, const float* qnorm,
-                                 float* scores, cudaStream_t st);
+                                 float* scores, cudaStream_t st, void* kout = nullptr,
+                                 int out_dt = -1);
 
 // row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)
 cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,

@@ -271,12 +271,14 @@ prepare_query_kernel(const void* __restrict__ keys, const void* __restrict__ que
 // the partials and divides, so the square root and the division run once per
 // row rather than once per lane group.  Grid-stride over rows, with (bh, j)
 // advanced by the stride without 64-bit divisions.
-template <int DT, bool INTERLEAVED>
+// OUT >= 0: the rotated rows are also stored in that dtype (the same values
+// windowed_rope_kernel writes), so one pass over the keys serves both.
+template <int DT, bool INTERLEAVED, int OUT>
 __global__ void __launch_bounds__(kRopeThreads)
 cosine_score_kernel(const void* __restrict__ keys, int64_t rows, int32_t H, int32_t ncap,
                     int32_t d, const int32_t* __restrict__ len, const RopeArgs ra,
                     const float* __restrict__ q, const float* __restrict__ qnorm,
-                    float* __restrict__ scores) {
+                    float* __restrict__ scores, void* __restrict__ kout) {
     __shared__ float2 part[kRopeThreads];
     __shared__ int32_t row_bh[kRopeThreads];  // (b, h) of a valid row, else -1
     const int lpr = INTERLEAVED ? d / 8 : d / 16;
@@ -314,6 +316,10 @@ cosine_score_kernel(const void* __restrict__ keys, int64_t rows, int32_t H, int3
                     angles8<INTERLEAVED>(near ? j : ra.far_offset, pair0, ra, c, sn);
                     rotate8<INTERLEAVED>(v0, v1, c, sn);
                 }
+            }
+            if constexpr (OUT >= 0) {
+                store8<OUT>(kout, row * d + e0, v0);
+                if (!INTERLEAVED) store8<OUT>(kout, row * d + e1, v1);
             }
             const float4* qa = reinterpret_cast<const float4*>(q + bh * d + e0);
             const float4 a0 = __ldg(qa), a1 = __ldg(qa + 1);
@@ -623,10 +629,10 @@ __global__ void append_rows_kernel(uint4* __restrict__ cache, int32_t H, int32_t
     if (threadIdx.x == 0 && L >= 0 && L < ncap) len[b] = L + 1;
 }
 
-template <int DT>
+template <int DT, int OUT>
 cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
                            const RopeArgs& ra, const float* q, const float* qnorm,
-                           float* scores, cudaStream_t st) {
+                           float* scores, void* kout, cudaStream_t st) {
     const int64_t rows = s.B * s.H * s.Ncap;
     const int d = (int)s.d;
     // the score kernel reduces a row over lpr lanes with xor shuffles, so lpr
@@ -634,21 +640,34 @@ cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
     const int lpr = ra.interleaved ? d / 8 : d / 16;
     const bool vec_ok = (ra.interleaved || d % 16 == 0) && lpr <= 32 && (lpr & (lpr - 1)) == 0;
     if (vec_ok && ra.interleaved) {
-        cosine_score_kernel<DT, true><<<grid_for(rows, kRopeThreads / (d / 8)), kRopeThreads, 0,
-                                        st>>>(keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d, len,
-                                              ra, q, qnorm, scores);
-                                              note_launches(1);
+        cosine_score_kernel<DT, true, OUT><<<grid_for(rows, kRopeThreads / (d / 8)), kRopeThreads,
+                                             0, st>>>(keys, rows, (int32_t)s.H, (int32_t)s.Ncap,
+                                                      d, len, ra, q, qnorm, scores, kout);
+        note_launches(1);
     } else if (vec_ok) {
-        cosine_score_kernel<DT, false><<<grid_for(rows, kRopeThreads / (d / 16)), kRopeThreads,
-                                         0, st>>>(keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d,
-                                                  len, ra, q, qnorm, scores);
+        cosine_score_kernel<DT, false, OUT><<<grid_for(rows, kRopeThreads / (d / 16)),
+                                              kRopeThreads, 0, st>>>(
+            keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra, q, qnorm, scores, kout);
         note_launches(1);
     } else {
+        if (OUT >= 0) return cudaErrorNotSupported;  // the caller rotates in a pass of its own
         cosine_score_warp_kernel<DT><<<grid_for(rows, kRopeThreads / 32), kRopeThreads, 0, st>>>(
             keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra, q, qnorm, scores);
-            note_launches(1);
+        note_launches(1);
     }
     return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t score_dispatch_out(const void* keys, const Shape& s, const int32_t* len,
+                               const RopeArgs& ra, const float* q, const float* qnorm,
+                               float* scores, void* kout, int out_dt, cudaStream_t st) {
+    switch (out_dt) {
+        case -1: return score_dispatch<DT, -1>(keys, s, len, ra, q, qnorm, scores, nullptr, st);
+        case kF32: return score_dispatch<DT, kF32>(keys, s, len, ra, q, qnorm, scores, kout, st);
+        case kBF16: return score_dispatch<DT, kBF16>(keys, s, len, ra, q, qnorm, scores, kout, st);
+        default: return score_dispatch<DT, kF16>(keys, s, len, ra, q, qnorm, scores, kout, st);
+    }
 }
 
 }  // namespace
@@ -692,12 +711,13 @@ cudaError_t launch_prepare_query(const void* keys, const void* query, int dt, co
 
 cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
                                  const RopeArgs& ra, const float* q, const float* qnorm,
-                                 float* scores, cudaStream_t st) {
+                                 float* scores, cudaStream_t st, void* kout, int out_dt) {
     if (s.B * s.H * s.Ncap == 0) return cudaSuccess;
+    if (!kout) out_dt = -1;
     switch (dt) {
-        case kF32: return score_dispatch<kF32>(keys, s, len, ra, q, qnorm, scores, st);
-        case kBF16: return score_dispatch<kBF16>(keys, s, len, ra, q, qnorm, scores, st);
-        default: return score_dispatch<kF16>(keys, s, len, ra, q, qnorm, scores, st);
+        case kF32: return score_dispatch_out<kF32>(keys, s, len, ra, q, qnorm, scores, kout, out_dt, st);
+        case kBF16: return score_dispatch_out<kBF16>(keys, s, len, ra, q, qnorm, scores, kout, out_dt, st);
+        default: return score_dispatch_out<kF16>(keys, s, len, ra, q, qnorm, scores, kout, out_dt, st);
     }
 }
 

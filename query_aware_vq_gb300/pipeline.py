@@ -6,15 +6,17 @@ VQ (Eq. 13-18)"), with the calibration of H and L in front:
 
   1. H = E[q^T q] + ridge I            a2ats_query_second_moment
   2. L = chol(H)                       a2ats_cholesky_factor
-  3. k~ = windowed RoPE of the cache   a2ats_windowed_rope
-  4. retrieval split, proxy query k~_t a2ats_select_retrieval_set (RoPE fused)
+  3. k~ = windowed RoPE of the cache   a2ats_windowed_rope  } one pass:
+  4. retrieval split, proxy query k~_t a2ats_select_retrieval_set  } ..._rotated
   5. retrieval rows: H-weighted rule   a2ats_h_weighted_assign (RoPE fused)
      (or the cosine blend when no H is calibrated)
   6. bulk rows: plain nearest centroid a2ats_h_weighted_assign, L = identity
 
 Steps 4-6 apply the windowed RoPE on the fly in fp32 to the pre-RoPE keys, so
 their decisions are taken on the unrounded rotated keys; step 3 writes the
-rotated cache in the storage dtype for the attention that follows.
+rotated cache in the storage dtype for the attention that follows.  Steps 3
+and 4 run as one call (a2ats_select_retrieval_set_rotated) that reads the
+pre-RoPE cache once.
 
 Steps 1-2 depend on the queries only and steps 3, 4 and 6 on the keys only,
 so the calibration runs on a second stream beside them, and step 5 (which
@@ -33,7 +35,7 @@ import torch
 
 from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_h_weighted_assign,
                a2ats_query_aware_assign, a2ats_query_second_moment, a2ats_select_retrieval_set,
-               a2ats_windowed_rope, library)
+               a2ats_select_retrieval_set_rotated, a2ats_windowed_rope, library)
 
 
 class A2ATSStep:
@@ -125,10 +127,10 @@ class A2ATSStep:
             if not getattr(self, "calibrated", False):
                 raise ValueError("calibrated=True before any calibrate()")
             L = self.L
-        stage("windowed_rope", st, a2ats_windowed_rope, keys, lengths=lengths, out=self.k_tilde,
-              **self.rope)
-        stage("retrieval_split", st, a2ats_select_retrieval_set, keys, None, self.fraction,
-              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws)
+        # steps 3 and 4 in one pass over the pre-RoPE cache
+        stage("rope_and_split", st, a2ats_select_retrieval_set_rotated, keys, None,
+              self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde, perm=self.perm,
+              count=self.count, workspace=ws)
         self._split_done.record(st)
         side.wait_event(self._split_done)
         if L is not None:
@@ -155,9 +157,10 @@ class A2ATSDecodeStep:
 
       1. append the new pre-RoPE keys at position len[b]   a2ats_append_rows
       2. windowed RoPE of the whole cache against the new
-         decode position (the per-step re-rotation)        a2ats_windowed_rope
-      3. retrieval split of every cached key, proxy query
-         = the new key after windowed RoPE                 a2ats_select_retrieval_set
+         decode position (the per-step re-rotation), and
+      3. the retrieval split of every cached key, proxy
+         query = the new key after windowed RoPE, in one
+         pass over the cache                               a2ats_select_retrieval_set_rotated
       4. the new keys assigned by the cosine blend against
          that proxy (each new key is its own query)        a2ats_query_aware_assign
          (or by the H-weighted rule when L is given)
@@ -197,11 +200,9 @@ class A2ATSDecodeStep:
             return r
 
         stage("append", a2ats_append_rows, cache, lengths, new_keys, stream=st)
-        stage("windowed_rope", a2ats_windowed_rope, cache, lengths=lengths, out=self.k_tilde,
-              stream=st, **self.rope)
-        stage("retrieval_split", a2ats_select_retrieval_set, cache, None, self.fraction,
-              lengths=lengths, rope=self.rope, perm=self.perm, count=self.count, workspace=ws,
-              stream=st)
+        stage("rope_and_split", a2ats_select_retrieval_set_rotated, cache, None, self.fraction,
+              rope=self.rope, lengths=lengths, out=self.k_tilde, perm=self.perm,
+              count=self.count, workspace=ws, stream=st)
         if L is not None:
             stage("assign_new", a2ats_h_weighted_assign, cache, codebook, L, lengths=lengths,
                   rope=self.rope, rows="last", codes=self.codes, workspace=ws, stream=st)

@@ -95,3 +95,22 @@ def test_split_and_calibration_validation(lib):
     c = lib.a2ats_cholesky_factor
     assert c(FAKE, 2, 100, FAKE, FAKE, None) == -2
     assert c(FAKE, 2, 128, FAKE, None, None) == -1
+
+
+def test_rotated_split_validation(lib):
+    r = lib.a2ats_select_retrieval_set_rotated
+    rope = q.RopeParams(64, 0, 500000.0, 0)
+    ws = 1 << 30
+    # rope is required, k_out may not alias keys, the out dtype is checked
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, None, FAKE + 4096, 1, FAKE, FAKE, FAKE,
+             ws, None) == -1
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, ctypes.byref(rope), FAKE, 1, FAKE, FAKE,
+             FAKE, ws, None) == -1
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, ctypes.byref(rope), FAKE + 4096, 7, FAKE,
+             FAKE, FAKE, ws, None) == -3
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 1.5, ctypes.byref(rope), FAKE + 4096, 1, FAKE,
+             FAKE, FAKE, ws, None) == -1
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, ctypes.byref(rope), FAKE + 4100, 1, FAKE,
+             FAKE, FAKE, ws, None) == -4
+    assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, ctypes.byref(rope), FAKE + 4096, 1, FAKE,
+             FAKE, None, 0, None) == -6

@@ -77,3 +77,31 @@ def test_split_full_size(name):
             v = oracle.windowed_rope(k[b, h], np.arange(w.N), w.N - 1, w.W, 0, w.rope_base)
             _, cnt, scores, kth = oracle.select_retrieval_set(v, v[-1], w.fraction)
             check_split(perm[b, h], int(count[b, h]), w.N, cnt, scores, kth)
+
+
+@pytest.mark.parametrize("case", [
+    # B, H, N, d, dtype, out dtype, fraction, rope
+    (2, 3, 1000, 128, "bf16", "bf16", 0.1, dict(window=64, rope_base=500000.0)),
+    (1, 2, 777, 64, "f16", "f32", 0.2, dict(window=16, far_offset=5, rope_base=10000.0)),
+    (2, 1, 300, 128, "bf16", "bf16", 0.3, dict(window=40, rope_base=10000.0, interleaved=1)),
+    (1, 2, 300, 24, "f32", "f32", 0.3, dict(window=8, rope_base=10000.0)),   # no fused form
+    (1, 1, 5, 16, "bf16", "bf16", 0.5, dict(window=2, rope_base=10000.0)),
+])
+def test_rotated_split_equals_the_two_calls(case):
+    """The one-pass call writes exactly what a2ats_windowed_rope and
+    a2ats_select_retrieval_set(rope=...) write, ragged lengths included."""
+    B, H, N, d, dt, odt, f, rope = case
+    k = dev(synth.gaussian((B, H, N, d), seed=N + 7, dtype=dt))
+    lens = dev(torch.tensor([max(N - 17 * b, 1) for b in range(B)], dtype=torch.int32))
+    want_out = torch.zeros((B, H, N, d), dtype=synth.DTYPES[odt], device="cuda")
+    q.a2ats_windowed_rope(k, lengths=lens, out=want_out, **rope)
+    want_perm, want_count = q.a2ats_select_retrieval_set(k, None, f, lengths=lens, rope=rope)
+    out = torch.zeros_like(want_out)
+    out, perm, count = q.a2ats_select_retrieval_set_rotated(k, None, f, rope=rope, lengths=lens,
+                                                            out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want_out)
+    assert torch.equal(count, want_count)
+    for b in range(B):
+        n = int(lens[b])
+        assert torch.equal(perm[b, :, :n], want_perm[b, :, :n])
