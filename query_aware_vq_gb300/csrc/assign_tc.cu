@@ -68,6 +68,7 @@ struct Params {
     int32_t* exact_count;
     int32_t* status;           // 0, or the code of a timed-out wait
     uint32_t shr5_mul, shl5_mul;  // 2^27 and 32 (see embed_pos)
+    const int32_t* max_rows;   // compact list: longest list over (b, h), or null
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -214,15 +215,40 @@ __device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
     t2 = lo[0];
 }
 
+// The decision for one row of a pass, from its top two (m1 with the column
+// bits, m2), the group index c1 of m1 and |x|^2 of its row operand: the code
+// when the gap clears the error bound, else the row joins the exact list.
+__device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int h,
+                                           float m1, float m2, int32_t c1, float nrm) {
+    const int32_t j = p.row_map ? p.row_map[(int64_t)bh * p.seg + ri] : ri;
+    const int32_t Lb = seq_len(p.len, bh / p.H, p.out_ncap);
+    if (j < 0 || j >= Lb) return;
+    const int64_t out = (int64_t)bh * p.out_ncap + j;
+    if (p.skip && p.skip[out]) return;
+    // bound on |v_hat - v| for every centroid, plus the perturbation of the
+    // column bits in both keys
+    const float xn = sqrtf(nrm) * p.norm_slack;
+    const float cmax = p.head[h * 4 + 0], hmax = p.head[h * 4 + 1];
+    const float e = p.err_coef * (xn * cmax + hmax) + p.head[h * 4 + 3] * xn;
+    const float mag = fmaxf(fabsf(m1), fabsf(m2));
+    const float tau = 2.f * e + 64.f * mag * 1.1920929e-07f;
+    if (!(m1 - m2 > tau)) {
+        const int32_t slot = atomicAdd(p.exact_count, 1);
+        p.exact_list[slot] = out;
+    } else {
+        p.codes[out] = c1 * 32 + (31 - (int32_t)(__float_as_uint(m1) & 31u));
+    }
+}
+
 struct TileInfo {
     int32_t bh, r0, nvalid;
     bool skip;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const Params& p, int t) {
+__device__ __forceinline__ TileInfo tile_info(const Params& p, int t, int tpb) {
     TileInfo ti;
-    ti.bh = t / p.tiles_per_bh;
-    ti.r0 = (t % p.tiles_per_bh) * BM;
+    ti.bh = t / tpb;
+    ti.r0 = (t % tpb) * BM;
     if (p.count) {
         ti.nvalid = min(max(p.count[ti.bh], 0), p.seg);
     } else {
@@ -273,7 +299,11 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total_tiles = p.num_bh * p.tiles_per_bh;
+    // tiles per (b, h): the host's bound, cut to the longest compact list
+    // when its length is on the device (the tiles past it hold no row)
+    int tpb = p.tiles_per_bh;
+    if (p.max_rows) tpb = min(tpb, (max(*p.max_rows, 0) + BM - 1) / BM);
+    const int total_tiles = p.num_bh * tpb;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < AST; i++) {
@@ -312,7 +342,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t a_it = 0, b_it = 0, h_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(p, t);
+                const TileInfo ti = tile_info(p, t, tpb);
                 if (ti.skip) continue;
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_empty[sa], ((a_it / AST) & 1) ^ 1, p.status, 1);
@@ -376,7 +406,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t a_it = 0, b_it = 0, acc_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(p, t);
+                const TileInfo ti = tile_info(p, t, tpb);
                 if (ti.skip) continue;
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 4);
@@ -428,7 +458,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t a_it = 0, acc_it = 0, m_it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = tile_info(p, t);
+            const TileInfo ti = tile_info(p, t, tpb);
             if (ti.skip) continue;
             const int h = ti.bh % p.H;
             const int sa = a_it % AST;
@@ -545,30 +575,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                 }
                 const int32_t ri = ti.r0 + row_in_tile;
-                if (ri < ti.nvalid) {
-                    const int32_t j = p.row_map ? p.row_map[(int64_t)ti.bh * p.seg + ri] : ri;
-                    const int32_t Lb = seq_len(p.len, ti.bh / p.H, p.out_ncap);
-                    if (j >= 0 && j < Lb) {
-                        const int64_t out = (int64_t)ti.bh * p.out_ncap + j;
-                        const bool skip = p.skip && p.skip[out];
-                        // bound on |v_hat - v| for every centroid, plus the
-                        // perturbation of the column bits in both keys
-                        const float xn = sqrtf(nrm) * p.norm_slack;
-                        const float cmax = p.head[h * 4 + 0], hmax = p.head[h * 4 + 1];
-                        const float e = p.err_coef * (xn * cmax + hmax) + p.head[h * 4 + 3] * xn;
-                        const float mag = fmaxf(fabsf(m1), fabsf(m2));
-                        const float tau = 2.f * e + 64.f * mag * 1.1920929e-07f;
-                        if (!skip) {
-                            if (!(m1 - m2 > tau)) {
-                                const int32_t slot = atomicAdd(p.exact_count, 1);
-                                p.exact_list[slot] = out;
-                            } else {
-                                p.codes[out] =
-                                    c1 * 32 + (31 - (int32_t)(__float_as_uint(m1) & 31u));
-                            }
-                        }
-                    }
-                }
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, m2, c1, nrm);
             }
             m_it++;
         }
@@ -738,7 +745,10 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
     } else {
         n = (ra.enabled && ra.window > 0) ? min(L, ra.window) : 0;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) ccount[bh] = n;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        ccount[bh] = n;
+        atomicMax(exact_count + 2, n);  // the longest list, for the contraction's tile bound
+    }
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int halfd = d / 2;
     const int64_t plane_rows = (int64_t)gridDim.y * ncap;
@@ -1018,9 +1028,11 @@ cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const 
         }
     }
     else {
+        // two-plane row operands: a second A stage (the next item's key
+        // tile loads while this one is in use) is worth more than B stages
         switch (p.d) {
             case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 2, 2>(ta, tb, p, st);
             case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, p, st);
             default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, p, st);
         }
@@ -1076,9 +1088,11 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
     return cudaGetLastError();
 }
 
+// max_rows: a bound on the rows of any (b, h) in this pass (the tiles past it
+// are not visited).
 cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, int64_t plane_rows,
                      const int32_t* count, const int32_t* row_map, const uint8_t* skip,
-                     int32_t skip_near, cudaStream_t st) {
+                     int32_t skip_near, int64_t max_rows, cudaStream_t st) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
     CUtensorMap ta, tb;
@@ -1101,7 +1115,7 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.P = b.P;
     p.num_bh = (int32_t)nbh;
     p.seg = (int32_t)ncap;
-    p.tiles_per_bh = (int32_t)((ncap + BM - 1) / BM);
+    p.tiles_per_bh = (int32_t)(((max_rows < ncap ? max_rows : ncap) + BM - 1) / BM);
     p.nchunks = (int32_t)((K + BN - 1) / BN);
     p.kpad = p.nchunks * BN;
     p.out_ncap = (int32_t)ncap;
@@ -1133,6 +1147,7 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.status = c.exact_count + 1;
     p.shr5_mul = 1u << 27;
     p.shl5_mul = 32u;
+    p.max_rows = count ? c.exact_count + 2 : nullptr;
     if (p.num_bh * p.tiles_per_bh == 0) return cudaSuccess;
     if (PA == 1)
         return bf16 ? launch_by_width<true, 1>(ta, tb, p, st) : launch_by_width<false, 1>(ta, tb, p, st);
@@ -1159,7 +1174,7 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
 
     e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 2, st);  // count and status
+    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 3, st);  // count, status, longest list
     if (e != cudaSuccess) return e;
     pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K, kpad,
                                                                          c.hneg);
@@ -1189,7 +1204,7 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     if (natural) {
         const int32_t skip_near = (c.ra.enabled && c.ra.window > 0) ? c.ra.window : 0;
         timing_begin(st);
-        e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, st);
+        e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, ncap, st);
         timing_end(st);
         if (e != cudaSuccess) return e;
     }
@@ -1213,7 +1228,7 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
                 c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
                 c.exact_count);
         note_launches(1);
-        e = run_pass(c, bu, 2, c.compact, nbh * ncap, c.ccount, c.row_map, skip, 0, st);
+        e = run_pass(c, bu, 2, c.compact, nbh * ncap, c.ccount, c.row_map, skip, 0, most, st);
         if (e != cudaSuccess) return e;
     }
     // rows the contraction could not decide

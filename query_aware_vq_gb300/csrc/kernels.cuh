@@ -124,7 +124,7 @@ struct TcCall {
     uint8_t* skip;        // [B*H*Ncap]
     int64_t* exact_list;  // [B*H*Ncap]
     unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
-    int32_t* exact_count; // [2]: count, status
+    int32_t* exact_count; // [3]: count, status, longest compact list
 };
 bool tc_supported(int dt, int64_t d);
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st);
