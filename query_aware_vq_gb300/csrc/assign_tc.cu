@@ -824,11 +824,14 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
 // Rows the contraction could not decide, in three short launches so that a
 // handful of rows still spreads over the whole GPU:
 //   exact_rows_kernel   one block per listed row: windowed RoPE in fp32 and
-//                       z = x L (compensated) into zbuf; best <- +inf
-//   exact_scan_kernel   one block per (row, slice of 128 centroids): the
-//                       direct distance sum_b (z_b - cp_jb)^2 to each cp_j =
-//                       c_j L, folded into best by a 64-bit atomicMin on
-//                       (distance bits, j), so ties go to the lowest index
+//                       z = x L (compensated) into zbuf; best <- +inf; the
+//                       row joins its head's list
+//   exact_scan_kernel   one block per (head, slice of centroids, chunk of the
+//                       head's rows): the slice is staged in shared memory
+//                       once and every row of the chunk takes the direct
+//                       distance sum_b (z_b - cp_jb)^2 to each cp_j = c_j L;
+//                       a 64-bit atomicMin on (distance bits, j) merges the
+//                       slices, so ties go to the lowest index
 //   exact_write_kernel  codes <- the index half of best
 constexpr int kExactThreads = 256;
 constexpr int kScanCents = 128;  // centroids per scan block (8 warps x 16)
@@ -838,7 +841,9 @@ __global__ void __launch_bounds__(kExactThreads)
 exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
                   const int32_t* __restrict__ len, const RopeArgs ra, const float* __restrict__ L,
                   const int64_t* __restrict__ list, const int32_t* __restrict__ list_count,
-                  float* __restrict__ zbuf, unsigned long long* __restrict__ best) {
+                  float* __restrict__ zbuf, unsigned long long* __restrict__ best,
+                  int32_t* __restrict__ head_count, int32_t* __restrict__ head_rows,
+                  int64_t head_cap) {
     __shared__ __align__(16) float xv[kMaxD];
     __shared__ Dot2 part[kExactThreads];
     const int tid = threadIdx.x;
@@ -894,75 +899,97 @@ exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
         } else {
             for (int b = tid; b < d; b += blockDim.x) z[b] = xv[b];
         }
-        if (tid == 0) best[e] = ~0ull;
+        if (tid == 0) {
+            best[e] = ~0ull;
+            head_rows[h * head_cap + atomicAdd(head_count + h, 1)] = e;
+        }
         __syncthreads();
     }
 }
 
-// 8 lanes share a centroid, each summing every 8th group of four elements
-// (VPL = d / 32 groups per lane); a warp covers 16 centroids in four rounds
-// of four, with the loads of RB rounds issued together.
-template <int VPL>
+constexpr int kScanRows = 8;   // rows of a head per chunk: one per warp
+
+// The slice [j0, j0 + S) of head h's cp is staged transposed, cT[a][c] with a
+// padded stride S + 1 (conflict-free both when it is written along a and when
+// lanes read along c).  Each warp takes rows of the chunk; lane l owns
+// centroids l, l + 32, ... of the slice.
+template <int S>
 __global__ void __launch_bounds__(kExactThreads)
-exact_scan_kernel(int32_t H, int32_t ncap, const float* __restrict__ cp, int64_t K,
-                  const int64_t* __restrict__ list, const int32_t* __restrict__ list_count,
-                  const float* __restrict__ zbuf, unsigned long long* __restrict__ best) {
-    constexpr int d = VPL * 32, vpr = d / 4;
-    constexpr int RB = VPL <= 4 ? 4 : 2;
+exact_scan_kernel(int32_t d, const float* __restrict__ cp, int64_t K,
+                  const int32_t* __restrict__ head_count, const int32_t* __restrict__ head_rows,
+                  int64_t head_cap, const float* __restrict__ zbuf,
+                  unsigned long long* __restrict__ best) {
+    extern __shared__ float cT[];  // [d][S + 1], then [warps][d] for the rows' z
+    const int h = blockIdx.y;
+    const int64_t j0 = (int64_t)blockIdx.x * S;
+    const int n = head_count[h];
+    const int nchunks = (n + kScanRows - 1) / kScanRows;
+    if ((int)blockIdx.z >= nchunks || j0 >= K) return;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int grp = lane >> 3, seg = lane & 7;
-    const int64_t slices = (K + kScanCents - 1) / kScanCents;
-    const int64_t items = (int64_t)(*list_count) * slices;
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t e = it / slices;
-        const int64_t j0 = (it % slices) * kScanCents + w * 16;
-        const int64_t h = (list[e] / ncap) % H;
-        const float4* z4 = reinterpret_cast<const float4*>(zbuf + e * d) + seg;
-        const float4* c4 = reinterpret_cast<const float4*>(cp + h * K * d) + seg;
-        float4 zz[VPL];
+    const int nc = (int)(K - j0 < S ? K - j0 : S);
+    // 16-byte loads, eight in flight per thread before their stores
+    const float4* src4 = reinterpret_cast<const float4*>(cp + ((int64_t)h * K + j0) * d);
+    const int d4 = d / 4, n4 = S * d4;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * kExactThreads) {
+        float4 v[8];
 #pragma unroll
-        for (int i = 0; i < VPL; i++) zz[i] = z4[8 * i];
-        float bv = INFINITY;
-        int32_t bj = 0;
+        for (int u = 0; u < 8; u++) {
+            const int i = i0 + u * kExactThreads;
+            const int c = i / d4;
+            v[u] = (i < n4 && c < nc) ? __ldg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-        for (int r0 = 0; r0 < 4; r0 += RB) {
-            float4 cv[RB][VPL];
-#pragma unroll
-            for (int r = 0; r < RB; r++) {
-                // past the end, reload the last centroid (its value is unused)
-                int64_t jj = j0 + 4 * (r0 + r) + grp;
-                jj = jj < K ? jj : K - 1;
-#pragma unroll
-                for (int i = 0; i < VPL; i++) cv[r][i] = __ldg(c4 + jj * vpr + 8 * i);
+        for (int u = 0; u < 8; u++) {
+            const int i = i0 + u * kExactThreads;
+            if (i < n4) {
+                const int c = i / d4, a = (i - c * d4) * 4;
+                float* dst = cT + a * (S + 1) + c;
+                dst[0] = v[u].x;
+                dst[S + 1] = v[u].y;
+                dst[2 * (S + 1)] = v[u].z;
+                dst[3 * (S + 1)] = v[u].w;
             }
+        }
+    }
+    __syncthreads();
+    const int32_t* rows = head_rows + (int64_t)h * head_cap;
+    float* zs = cT + d * (S + 1) + w * d;  // this warp's row, staged once
+    for (int chunk = blockIdx.z; chunk < nchunks; chunk += gridDim.z) {
+        const int r_end = min(n, (chunk + 1) * kScanRows);
+        for (int r = chunk * kScanRows + w; r < r_end; r += kExactThreads / 32) {
+            const int64_t e = rows[r];
+            for (int a = lane; a < d; a += 32) zs[a] = __ldg(zbuf + e * d + a);
+            __syncwarp();
+            float acc[S / 32];
 #pragma unroll
-            for (int r = 0; r < RB; r++) {
-                float acc0 = 0.f, acc1 = 0.f;
+            for (int k = 0; k < S / 32; k++) acc[k] = 0.f;
+#pragma unroll 4
+            for (int a = 0; a < d; a++) {
+                const float za = zs[a];
+                const float* col = cT + a * (S + 1) + lane;
 #pragma unroll
-                for (int i = 0; i < VPL; i++) {
-                    const float t0 = zz[i].x - cv[r][i].x, t1 = zz[i].y - cv[r][i].y;
-                    const float t2 = zz[i].z - cv[r][i].z, t3 = zz[i].w - cv[r][i].w;
-                    acc0 = fmaf(t0, t0, acc0);
-                    acc1 = fmaf(t1, t1, acc1);
-                    acc0 = fmaf(t2, t2, acc0);
-                    acc1 = fmaf(t3, t3, acc1);
+                for (int k = 0; k < S / 32; k++) {
+                    const float t = za - col[32 * k];
+                    acc[k] = fmaf(t, t, acc[k]);
                 }
-                float v = acc0 + acc1;
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                const int64_t jj = j0 + 4 * (r0 + r) + grp;
-                if (jj < K && v < bv) { bv = v; bj = (int32_t)jj; }
             }
+            __syncwarp();  // zs is rewritten by the warp's next row
+            float bv = INFINITY;
+            int32_t bj = 0;
+#pragma unroll
+            for (int k = 0; k < S / 32; k++)
+                if (lane + 32 * k < nc && acc[k] < bv) {  // ascending j: strict < keeps the lowest
+                    bv = acc[k];
+                    bj = (int32_t)(j0 + lane + 32 * k);
+                }
+            for (int m = 16; m; m >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
+                const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
+                if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+            }
+            if (lane == 0 && bv < INFINITY)
+                atomicMin(best + e, ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
         }
-        // rounds run in increasing j, so a strict < keeps the lowest index
-        for (int m = 8; m < 32; m <<= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
-            const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
-            if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
-        }
-        if (lane == 0 && bv < INFINITY)
-            atomicMin(best + e, ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
     }
 }
 
@@ -1176,6 +1203,8 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 3, st);  // count, status, longest list
     if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(c.head_count, 0, sizeof(int32_t) * H, st);
+    if (e != cudaSuccess) return e;
     pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K, kpad,
                                                                          c.hneg);
     note_launches(1);
@@ -1233,22 +1262,27 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     }
     // rows the contraction could not decide
     const unsigned sms = (unsigned)sm_count();
-    float* zbuf = reinterpret_cast<float*>(c.compact);  // the planes are no longer read
+    float* zbuf = reinterpret_cast<float*>(c.compact);   // the planes are no longer read
+    int32_t* head_rows = c.row_map;                      // nor the compact row map
+    const int64_t head_cap = c.s.B * ncap;
     if (c.dt == kBF16)
         exact_rows_kernel<kBF16><<<sms * 4, kExactThreads, 0, st>>>(
             c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
-            c.exact_count, zbuf, c.exact_best);
+            c.exact_count, zbuf, c.exact_best, c.head_count, head_rows, head_cap);
     else
         exact_rows_kernel<kF16><<<sms * 4, kExactThreads, 0, st>>>(
             c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
-            c.exact_count, zbuf, c.exact_best);
+            c.exact_count, zbuf, c.exact_best, c.head_count, head_rows, head_cap);
     {
-        auto scan = d == 64    ? exact_scan_kernel<2>
-                    : d == 128 ? exact_scan_kernel<4>
-                    : d == 192 ? exact_scan_kernel<6>
-                               : exact_scan_kernel<8>;
-        scan<<<sms * 8, kExactThreads, 0, st>>>((int32_t)H, (int32_t)ncap, c.cp, K, c.exact_list,
-                                                c.exact_count, zbuf, c.exact_best);
+        // slices of 128 centroids (64 at d > 128) keep the staged slice near 66 KB
+        const int S = d <= 128 ? 128 : 64;
+        const size_t smem = sizeof(float) * (size_t)d * (S + 1 + kExactThreads / 32);
+        auto scan = S == 128 ? exact_scan_kernel<128> : exact_scan_kernel<64>;
+        e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        dim3 g((unsigned)((K + S - 1) / S), (unsigned)H, 8);
+        scan<<<g, kExactThreads, smem, st>>>((int32_t)d, c.cp, K, c.head_count, head_rows, head_cap,
+                                             zbuf, c.exact_best);
     }
     exact_write_kernel<<<sms, 256, 0, st>>>(c.exact_list, c.exact_count, c.exact_best, c.codes);
     note_launches(3);

@@ -125,6 +125,7 @@ struct TcCall {
     int64_t* exact_list;  // [B*H*Ncap]
     unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
     int32_t* exact_count; // [3]: count, status, longest compact list
+    int32_t* head_count;  // [H] listed rows per head (the exact path)
 };
 bool tc_supported(int dt, int64_t d);
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st);
