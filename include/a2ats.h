@@ -161,6 +161,28 @@ int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, 
                             void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_h_weighted_assign_reuse -- a2ats_h_weighted_assign without the
+ * codebook side (no counterpart on the pages: the codebook and L are
+ * per-layer calibration artifacts, [ALG] "Optional: query-aware
+ * calibration", and the Eq. 16-18 route assigns against pre-transformed
+ * centroids, so a decode loop needs their transform once per layer).
+ * It takes the lower-triangle copy of L, c L, |c L|^2 / 2, c L L^T and their
+ * 16-bit planes and tables from the workspace, where the last
+ * a2ats_h_weighted_assign call on it left them.  The caller guarantees that
+ * that call had the same codebook and L contents, dtype, B, H, Ncap, d, K,
+ * fused_rope and rows, and that nothing but a2ats_h_weighted_assign_reuse
+ * calls has used the workspace since; otherwise the codes are unspecified
+ * (no error is detected).  Arguments, results and errors are otherwise those
+ * of a2ats_h_weighted_assign (codebook and L are only checked, not read).
+ * ------------------------------------------------------------------------ */
+int a2ats_h_weighted_assign_reuse(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                  int64_t Ncap, int64_t d, const int32_t* len,
+                                  const void* codebook, int64_t K, const float* L,
+                                  const a2ats_rope_params* fused_rope, int32_t rows,
+                                  const int32_t* perm, const int32_t* count, int32_t* codes,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_query_aware_assign -- [API] a2ats_query_aware_assignment (cosine
  * blend):  e_j = |x - c_j|^2,  m = max_j e_j,
  *   score_j = -beta * e_j / m + (1 - beta) * cos(query, c_j),

@@ -56,6 +56,8 @@ _SIGS = {
     "a2ats_h_weighted_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_h_weighted_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _P, _I32, _P,
                                 _P, _P, _P, _SZ, _P],
+    "a2ats_h_weighted_assign_reuse": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _P,
+                                      _I32, _P, _P, _P, _P, _SZ, _P],
     "a2ats_query_aware_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_query_aware_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _D, _P,
                                  _I32, _P, _P, _P, _P, _SZ, _P],
@@ -255,16 +257,23 @@ def _assign_common(x, codebook, codes):
 
 
 def a2ats_h_weighted_assign(x, codebook, L=None, *, lengths=None, rope=None, rows="all",
-                            perm=None, count=None, codes=None, workspace=None, stream=None):
-    """argmin_j |x~ L - c_j L|^2 per visited row (L None: plain VQ)."""
+                            perm=None, count=None, codes=None, workspace=None, stream=None,
+                            reuse=False):
+    """argmin_j |x~ L - c_j L|^2 per visited row (L None: plain VQ).
+    reuse=True calls a2ats_h_weighted_assign_reuse: the codebook side is
+    taken from `workspace` as the previous call with the same codebook, L,
+    shapes, rope and rows left it."""
     _dev(x, codebook, L, lengths, perm, count, codes)
     x4, cb, K, codes = _assign_common(x, codebook, codes)
     B, H, N, d = x4.shape
     lib = _load()
+    if reuse and workspace is None:
+        raise ValueError("reuse needs the workspace of the preparing call")
     ws, nb = _workspace(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K), x.device,
                         workspace)
     rp = _rope(rope)
-    _check("a2ats_h_weighted_assign", lib.a2ats_h_weighted_assign(
+    name = "a2ats_h_weighted_assign_reuse" if reuse else "a2ats_h_weighted_assign"
+    _check(name, getattr(lib, name)(
         _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), _ptr(cb), K, _ptr(L),
         ctypes.byref(rp) if rp is not None else None, A2ATS_ROWS[rows], _ptr(perm), _ptr(count),
         _ptr(codes), _ptr(ws), nb, _stream(stream)))

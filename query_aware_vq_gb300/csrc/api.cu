@@ -340,11 +340,15 @@ size_t a2ats_h_weighted_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap
     return c.used + 256;
 }
 
-int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
-                            int64_t d, const int32_t* len, const void* codebook, int64_t K,
-                            const float* L, const a2ats_rope_params* fused_rope, int32_t rows,
-                            const int32_t* perm, const int32_t* count, int32_t* codes,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// The H-weighted assignment; with reuse, the codebook side (the copy of L,
+// c L, |c L|^2 / 2, c L L^T, its planes and tables) is taken as an earlier
+// call on this workspace left it.
+int h_weighted(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap, int64_t d,
+               const int32_t* len, const void* codebook, int64_t K, const float* L,
+               const a2ats_rope_params* fused_rope, int32_t rows, const int32_t* perm,
+               const int32_t* count, int32_t* codes, void* workspace, size_t workspace_bytes,
+               void* stream, bool reuse) {
     int st = check_assign_common(x, dtype, B, H, Ncap, d, codebook, K, rows, perm, count, codes);
     if (st) return st;
     RopeArgs ra;
@@ -359,23 +363,45 @@ int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
     // only the lower triangle of L is read: every kernel uses the masked copy
-    const float* Lc = nullptr;
-    if (L) {
-        if ((e = launch_factor_prep(L, H, d, w.Lc, w.tc.Lt, s)) != cudaSuccess) return cuda_fail(e);
-        Lc = w.Lc;
-    }
+    const float* Lc = L ? w.Lc : nullptr;
     const bool tc = tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30);
-    e = launch_codebook_transform(codebook, dtype, H, K, d, Lc, w.tc.Lt, w.cp, w.half_norm,
-                                  tc ? w.tc.chat : nullptr, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (!reuse) {
+        if (L && (e = launch_factor_prep(L, H, d, w.Lc, w.tc.Lt, s)) != cudaSuccess)
+            return cuda_fail(e);
+        e = launch_codebook_transform(codebook, dtype, H, K, d, Lc, w.tc.Lt, w.cp, w.half_norm,
+                                      tc ? w.tc.chat : nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     const Shape sh{B, H, Ncap, d};
-    if (tc)
+    if (tc) {
+        w.tc.prepared = reuse;
         e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, Lc, ra,
                                    RowSel{rows, perm, count}, codes, s);
-    else
+    } else {
         e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, Lc, w.cp,
                                 w.half_norm, K, codes, s);
+    }
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+}  // namespace
+
+int a2ats_h_weighted_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                            int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                            const float* L, const a2ats_rope_params* fused_rope, int32_t rows,
+                            const int32_t* perm, const int32_t* count, int32_t* codes,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return h_weighted(x, dtype, B, H, Ncap, d, len, codebook, K, L, fused_rope, rows, perm, count,
+                      codes, workspace, workspace_bytes, stream, false);
+}
+
+int a2ats_h_weighted_assign_reuse(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                  int64_t Ncap, int64_t d, const int32_t* len,
+                                  const void* codebook, int64_t K, const float* L,
+                                  const a2ats_rope_params* fused_rope, int32_t rows,
+                                  const int32_t* perm, const int32_t* count, int32_t* codes,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    return h_weighted(x, dtype, B, H, Ncap, d, len, codebook, K, L, fused_rope, rows, perm, count,
+                      codes, workspace, workspace_bytes, stream, true);
 }
 
 size_t a2ats_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,

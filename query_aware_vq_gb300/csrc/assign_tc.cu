@@ -1084,17 +1084,23 @@ struct BSide {
     const float* head;
 };
 
+// The codebook operand (variant v: 0 as is, 1 rotated by -far_offset) and,
+// when launch is set, the launches that build it: per-head statistics, the
+// head table and the 16-bit planes.  Without launch only the description is
+// filled in, for a call that reuses an earlier call's preparation.
 cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide& out,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool launch = true) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d;
-    codebook_stats_kernel<<<dim3((unsigned)((K + 7) / 8), (unsigned)H), 256, 0, st>>>(
-        chat, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
-    note_launches(1);
-    head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
-        c.head_bits + v * H * 4, (int32_t)H, (int32_t)d, (bf16 || raw) ? 1 : 0, c.head + v * H * 4,
-        c.scale + v * H);
-    note_launches(1);
+    if (launch) {
+        codebook_stats_kernel<<<dim3((unsigned)((K + 7) / 8), (unsigned)H), 256, 0, st>>>(
+            chat, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
+        note_launches(1);
+        head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
+            c.head_bits + v * H * 4, (int32_t)H, (int32_t)d, (bf16 || raw) ? 1 : 0,
+            c.head + v * H * 4, c.scale + v * H);
+        note_launches(1);
+    }
     out.head = c.head + v * H * 4;
     out.exact = raw;
     if (raw) {
@@ -1103,6 +1109,8 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
     } else {
         out.P = bf16 ? 3 : 2;
         uint16_t* planes = c.planes + (size_t)v * H * 3 * K * d;
+        out.src = planes;
+        if (!launch) return cudaSuccess;
         if (bf16)
             codebook_planes_kernel<true><<<blocks_for(H * K * d, 256, 8192), 256, 0, st>>>(
                 chat, K, (int32_t)d, out.P, (int32_t)H, c.scale + v * H, planes);
@@ -1110,7 +1118,6 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
             codebook_planes_kernel<false><<<blocks_for(H * K * d, 256, 8192), 256, 0, st>>>(
                 chat, K, (int32_t)d, out.P, (int32_t)H, c.scale + v * H, planes);
         note_launches(1);
-        out.src = planes;
     }
     return cudaGetLastError();
 }
@@ -1199,25 +1206,32 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     const bool need_r = natural && rot;
     cudaError_t e;
 
-    e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
-    if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 3, st);  // count, status, longest list
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(c.head_count, 0, sizeof(int32_t) * H, st);
     if (e != cudaSuccess) return e;
-    pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K, kpad,
-                                                                         c.hneg);
-    note_launches(1);
-    // chat = c L L^T, the codebook side of the contraction (c itself when L
-    // is the identity)
+    // the codebook side, unless an earlier call left it in this workspace:
+    // chat = c L L^T (c itself when L is the identity), -|c L|^2 / 2 padded,
+    // and the operand planes
+    const bool build = !c.prepared;
+    if (build) {
+        e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
+        if (e != cudaSuccess) return e;
+        pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K,
+                                                                             kpad, c.hneg);
+        note_launches(1);
+    }
     const float* chat = c.L ? c.chat : c.cp;
     BSide bu{}, br{};
-    if (need_u && (e = prepare_b(c, chat, 0, c.L == nullptr, bu, st)) != cudaSuccess) return e;
+    if (need_u && (e = prepare_b(c, chat, 0, c.L == nullptr, bu, st, build)) != cudaSuccess)
+        return e;
     if (need_r) {
-        rotate_rows_kernel<<<blocks_for(H * K * (d / 2), 256, 8192), 256, 0, st>>>(
-            chat, H * K, (int32_t)d, c.ra, c.chat_rot);
-        note_launches(1);
-        if ((e = prepare_b(c, c.chat_rot, 1, false, br, st)) != cudaSuccess) return e;
+        if (build) {
+            rotate_rows_kernel<<<blocks_for(H * K * (d / 2), 256, 8192), 256, 0, st>>>(
+                chat, H * K, (int32_t)d, c.ra, c.chat_rot);
+            note_launches(1);
+        }
+        if ((e = prepare_b(c, c.chat_rot, 1, false, br, st, build)) != cudaSuccess) return e;
     }
     const uint8_t* skip = nullptr;
     if (c.sel.mode == 2) {

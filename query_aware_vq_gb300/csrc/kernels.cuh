@@ -109,6 +109,7 @@ struct TcCall {
     const float* cp;
     const float* half_norm;
     int32_t* codes;
+    bool prepared;        // the codebook side is already in the workspace
     // workspace
     float* Lt;            // [H, d, d]  L^T
     float* chat;          // [H, K, d]  c L L^T

@@ -57,9 +57,13 @@ class A2ATSStep:
         self.L = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.info = torch.empty((H,), dtype=torch.int32, device=dev)
         ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
-                 lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
-                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
+                 lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        # the split has its own workspace, so the bulk call's codebook side
+        # survives from one step to the next
+        self.split_workspace = torch.empty(
+            lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d), dtype=torch.uint8,
+            device=dev)
         # the second stream (calibration, then the retrieval rows) and its
         # own workspace, so that it can run beside the caller's stream
         side = max(lib.a2ats_query_second_moment_workspace_size(H, max(M, 1), d),
@@ -101,15 +105,19 @@ class A2ATSStep:
         return self
 
     def __call__(self, keys, codebook, queries=None, h_given=None, lengths=None, stream=None,
-                 events=None, calibrated=False):
+                 events=None, calibrated=False, reuse_codebook=False):
         """keys [B, H, N, d] pre-RoPE; codebook [H, K, d].  The retrieval rows
         take the H-weighted rule with an L calibrated inside the step from
         queries [H, M, d] (or h_given [H, d, d] fp32), or, with
         calibrated=True, the L of an earlier calibrate(); with neither, the
-        cosine blend.  Every output is complete, in the order of `stream`,
-        when the call's work on `stream` is.  events: optional dict; each stage
-        appends a (start, end) CUDA event pair recorded around its call on the
-        stream that runs it (stages on the two streams overlap)."""
+        cosine blend.  reuse_codebook=True takes the codebook side of both
+        assignments (the transform by L, its norms and planes) from the
+        previous step, which must have had the same codebook, L and shapes
+        (the codebook and L are per-layer constants).  Every output is
+        complete, in the order of `stream`, when the call's work on `stream`
+        is.  events: optional dict; each stage appends a (start, end) CUDA
+        event pair recorded around its call on the stream that runs it
+        (stages on the two streams overlap)."""
         ws, sws = self.workspace, self.side_workspace
         st = stream if stream is not None else torch.cuda.current_stream()
         side = self.side_stream
@@ -130,13 +138,14 @@ class A2ATSStep:
         # steps 3 and 4 in one pass over the pre-RoPE cache
         stage("rope_and_split", st, a2ats_select_retrieval_set_rotated, keys, None,
               self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde, perm=self.perm,
-              count=self.count, workspace=ws)
+              count=self.count, workspace=self.split_workspace)
         self._split_done.record(st)
         side.wait_event(self._split_done)
         if L is not None:
             stage("assign_retrieval", side, a2ats_h_weighted_assign, keys, codebook, L,
                   lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
-                  count=self.count, codes=self.codes, workspace=sws)
+                  count=self.count, codes=self.codes, workspace=sws,
+                  reuse=reuse_codebook and queries is None and h_given is None)
         else:
             # no calibrated H: the cosine blend against the same proxy query
             # (the key at t after windowed RoPE) the split used
@@ -146,7 +155,7 @@ class A2ATSStep:
         self._side_done.record(side)
         stage("assign_bulk", st, a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
               rope=self.rope, rows="bulk", perm=self.perm, count=self.count, codes=self.codes,
-              workspace=ws)
+              workspace=ws, reuse=reuse_codebook)
         st.wait_event(self._side_done)
         return self
 

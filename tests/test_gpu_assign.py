@@ -164,3 +164,40 @@ def test_h_weighted_full_size_sampled(name):
         v = oracle.windowed_rope(k[0, h, rows], rows, w.N - 1, w.W, 0, w.rope_base)
         code, d1, d2 = oracle.assign_cholesky(v, c[h], L[h])
         check_codes(got[0, h, rows], code, (d2 - d1) / d2)
+
+
+@pytest.mark.parametrize("dt,d,withL,rows,rope", [
+    ("bf16", 128, True, "retrieval", dict(window=40, far_offset=0, rope_base=500000.0)),
+    ("bf16", 128, False, "bulk", dict(window=40, far_offset=0, rope_base=500000.0)),
+    ("f16", 64, True, "all", dict(window=30, far_offset=3, rope_base=10000.0)),
+    ("f32", 48, True, "retrieval", None),   # the SIMT route
+])
+def test_reuse_takes_the_codebook_side_from_the_workspace(dt, d, withL, rows, rope):
+    """A call with reuse gives, on new keys, the codes a full call gives."""
+    B, H, N, K = 2, 2, 400, 90
+    c = dev(synth.gaussian((H, K, d), seed=41, dtype=dt, scale=2.0))
+    L = dev(_L(H, d, 30.0, seed=42)) if withL else None
+    lens = dev(torch.tensor([N, N - 33], dtype=torch.int32))
+    perm = count = None
+    lib = q.library()
+    ws = torch.empty(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K), dtype=torch.uint8,
+                     device="cuda")
+    for step, seed in enumerate((43, 44, 45)):
+        x = dev(synth.gaussian((B, H, N, d), seed=seed, dtype=dt, scale=2.0))
+        if rows in ("retrieval", "bulk"):
+            perm, count = q.a2ats_select_retrieval_set(x, None, 0.1, lengths=lens, rope=rope)
+        kw = dict(lengths=lens, rope=rope, rows=rows, perm=perm, count=count)
+        want = q.a2ats_h_weighted_assign(x, c, L, **kw)
+        got = torch.full_like(want, -5)
+        got = q.a2ats_h_weighted_assign(x, c, L, codes=got, workspace=ws, reuse=step > 0, **kw)
+        torch.cuda.synchronize()
+        if rows == "all":
+            for b in range(B):
+                n = int(lens[b])
+                assert torch.equal(got[b, :, :n], want[b, :, :n])
+        else:
+            for b in range(B):
+                for h in range(H):
+                    n, cnt = int(lens[b]), int(count[b, h])
+                    sel = perm[b, h, :cnt] if rows == "retrieval" else perm[b, h, cnt:n]
+                    assert torch.equal(got[b, h, sel.long()], want[b, h, sel.long()])

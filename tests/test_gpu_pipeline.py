@@ -83,3 +83,26 @@ def test_step_is_deterministic():
                                          step.Hm, step.L)])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_calibrated_steps_reuse_the_codebook_side():
+    """calibrate() once, a first step that builds the codebook side, then
+    steps that reuse it on new keys: the same codes, split and rotated keys as
+    a step object that rebuilds everything for those keys."""
+    w = synth.scaled(synth.WORKLOADS["llama32_3b_layer"], H=2, N=4096, K=256, W=128, M=1024)
+    c, Q = dev(synth.codebook(w)), dev(synth.queries(w))
+    mk = lambda: A2ATSStep(w.B, w.H, w.N, w.d, w.K, synth.DTYPES[w.dtype], window=w.W,
+                           fraction=w.fraction, rope_base=w.rope_base, M=w.M, ridge=w.ridge)
+    step = mk().calibrate(queries=Q)
+    for i, seed in enumerate((0, 1, 2)):
+        k = dev(synth.keys(w) if seed == 0 else synth.gaussian((w.B, w.H, w.N, w.d), seed=seed,
+                                                                dtype=w.dtype))
+        step(k, c, calibrated=True, reuse_codebook=i > 0)
+        fresh = mk()
+        fresh(k, c, queries=Q)
+        torch.cuda.synchronize()
+        assert torch.equal(step.L, fresh.L)
+        assert torch.equal(step.count, fresh.count)
+        assert torch.equal(step.perm, fresh.perm)
+        assert torch.equal(step.k_tilde, fresh.k_tilde)
+        assert torch.equal(step.codes, fresh.codes)
