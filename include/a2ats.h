@@ -251,6 +251,22 @@ int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t 
                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
+ * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
+ * pages: it joins the two halves of [V039] step 2's routing when they are
+ * computed at the same time, the bulk rule over every row into dst and the
+ * retrieval rule into src).
+ *   src, dst  [B, H, Ncap] int32 device arrays (e.g. codes)
+ *   len       [B] int32 device, or NULL for Ncap everywhere
+ *   perm, count as written by a2ats_select_retrieval_set
+ * Errors: SHAPE for negative sizes or B*H > 65535; INVALID_ARG for a NULL
+ * array when B*H*Ncap > 0.
+ * ------------------------------------------------------------------------ */
+int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64_t H,
+                              int64_t Ncap, const int32_t* len, const int32_t* perm,
+                              const int32_t* count, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_select_retrieval_set_static -- the same retrieval split as
  * a2ats_select_retrieval_set, for callers that cannot allocate device memory
  * (no counterpart on the pages: this is a packaging variant).  Some callers

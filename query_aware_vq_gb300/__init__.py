@@ -66,6 +66,7 @@ _SIGS = {
                                    _SZ, _P],
     "a2ats_select_retrieval_set_rotated": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
                                            _I32, _P, _P, _P, _SZ, _P],
+    "a2ats_copy_retrieval_rows": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
@@ -352,6 +353,19 @@ def a2ats_select_retrieval_set_rotated(keys, query=None, fraction: float = 0.2, 
         ctypes.byref(rp), _ptr(o4), _dt(o4), _ptr(perm), _ptr(count), _ptr(ws), nb,
         _stream(stream)))
     return out, perm, count
+
+
+def a2ats_copy_retrieval_rows(src, dst, perm, count, *, lengths=None, stream=None):
+    """dst[b, h, j] = src[b, h, j] on the retrieval rows of the split;
+    returns dst (int32 [B, H, N] device tensors)."""
+    _dev(src, dst, perm, count, lengths)
+    if src.dtype != torch.int32 or dst.dtype != torch.int32 or src.shape != dst.shape:
+        raise TypeError("src and dst must be int32 tensors of one shape")
+    B, H, N = dst.shape
+    _check("a2ats_copy_retrieval_rows", _load().a2ats_copy_retrieval_rows(
+        _ptr(src), _ptr(dst), B, H, N, _ptr(_lens(lengths)), _ptr(perm), _ptr(count),
+        _stream(stream)))
+    return dst
 
 
 def split_views(perm, count, b: int = 0, h: int = 0, n: int | None = None):

@@ -536,4 +536,16 @@ int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t 
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64_t H,
+                              int64_t Ncap, const int32_t* len, const int32_t* perm,
+                              const int32_t* count, void* stream) {
+    if (B < 0 || H < 0 || Ncap < 0 || Ncap >= (int64_t(1) << 31) || B * H > 65535)
+        return A2ATS_ERR_SHAPE;
+    if (B * H == 0 || Ncap == 0) return A2ATS_OK;
+    if (!src || !dst || !perm || !count) return A2ATS_ERR_INVALID_ARG;
+    cudaError_t e = launch_copy_retrieval_rows(src, dst, Shape{B, H, Ncap, 8}, len, perm, count,
+                                               (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
 }  // extern "C"

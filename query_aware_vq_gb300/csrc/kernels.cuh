@@ -46,6 +46,10 @@ cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const
 cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
                                cudaStream_t st);
 
+// dst <- src on the retrieval rows of the split (perm[:count], within len).
+cudaError_t launch_copy_retrieval_rows(const int32_t* src, int32_t* dst, const Shape& s,
+                                       const int32_t* len, const int32_t* perm,
+                                       const int32_t* count, cudaStream_t st);
 cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* len,
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st);
 

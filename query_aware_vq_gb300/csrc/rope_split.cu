@@ -629,6 +629,23 @@ __global__ void append_rows_kernel(uint4* __restrict__ cache, int32_t H, int32_t
     if (threadIdx.x == 0 && L >= 0 && L < ncap) len[b] = L + 1;
 }
 
+// dst[b, h, j] = src[b, h, j] for the retrieval rows j = perm[b, h, i],
+// i < count[b, h], j < len[b].
+__global__ void copy_retrieval_rows_kernel(const int32_t* __restrict__ src,
+                                           int32_t* __restrict__ dst, int32_t H, int32_t ncap,
+                                           const int32_t* __restrict__ len,
+                                           const int32_t* __restrict__ perm,
+                                           const int32_t* __restrict__ count) {
+    const int bh = blockIdx.y;
+    const int32_t L = seq_len(len, bh / H, ncap);
+    const int32_t n = min(max(count[bh], 0), L);
+    const int64_t base = (int64_t)bh * ncap;
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int32_t j = perm[base + i];
+        if (j >= 0 && j < L) dst[base + j] = src[base + j];
+    }
+}
+
 template <int DT, int OUT>
 cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
                            const RopeArgs& ra, const float* q, const float* qnorm,
@@ -727,6 +744,19 @@ cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len
     append_rows_kernel<<<(unsigned)s.B, 256, 0, st>>>(reinterpret_cast<uint4*>(cache),
                                                       (int32_t)s.H, (int32_t)s.Ncap, vec, len,
                                                       reinterpret_cast<const uint4*>(rows));
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_retrieval_rows(const int32_t* src, int32_t* dst, const Shape& s,
+                                       const int32_t* len, const int32_t* perm,
+                                       const int32_t* count, cudaStream_t st) {
+    const int64_t nbh = s.B * s.H;
+    if (nbh == 0 || s.Ncap == 0) return cudaSuccess;
+    const int64_t blocks = (s.Ncap + 255) / 256;
+    dim3 g((unsigned)(blocks < 32 ? blocks : 32), (unsigned)nbh);
+    copy_retrieval_rows_kernel<<<g, 256, 0, st>>>(src, dst, (int32_t)s.H, (int32_t)s.Ncap, len,
+                                                  perm, count);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -18,11 +18,13 @@ rotated cache in the storage dtype for the attention that follows.  Steps 3
 and 4 run as one call (a2ats_select_retrieval_set_rotated) that reads the
 pre-RoPE cache once.
 
-Steps 1-2 depend on the queries only and steps 3, 4 and 6 on the keys only,
-so the calibration runs on a second stream beside them, and step 5 (which
-needs L and the split) follows it there once the split is done, while the
-bulk rows of step 6 are assigned on the caller's stream; the two write
-disjoint codes.  The caller's stream waits for the second before returning.
+The routing is computed as two halves at the same time.  The caller's
+stream assigns every row by the bulk rule (plain VQ needs neither the split
+nor L); a second stream runs the calibration when it is part of the step,
+steps 3-4, and the retrieval rule on the retrieval rows into a buffer of its
+own.  The caller's stream then waits for the second and copies the
+retrieval rows' codes over the bulk ones (a2ats_copy_retrieval_rows), which
+gives exactly step 5 on the retrieval rows and step 6 on the others.
 
 Steps 1-2 may also run once, ahead of the steps that reuse their L
 (A2ATSStep.calibrate), as the pages do when H is calibrated offline.
@@ -33,7 +35,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_h_weighted_assign,
+from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_copy_retrieval_rows,
+               a2ats_h_weighted_assign,
                a2ats_query_aware_assign, a2ats_query_second_moment, a2ats_select_retrieval_set,
                a2ats_select_retrieval_set_rotated, a2ats_windowed_rope, library)
 
@@ -53,6 +56,7 @@ class A2ATSStep:
         self.perm = torch.empty((B, H, N), dtype=torch.int32, device=dev)
         self.count = torch.empty((B, H), dtype=torch.int32, device=dev)
         self.codes = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.codes_retrieval = torch.empty((B, H, N), dtype=torch.int32, device=dev)
         self.Hm = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.L = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.info = torch.empty((H,), dtype=torch.int32, device=dev)
@@ -73,7 +77,6 @@ class A2ATSStep:
         self.side_stream = torch.cuda.Stream(device=dev)
         self.calibrated = False
         self._inputs_ready = torch.cuda.Event()
-        self._split_done = torch.cuda.Event()
         self._side_done = torch.cuda.Event()
 
     @staticmethod
@@ -135,28 +138,31 @@ class A2ATSStep:
             if not getattr(self, "calibrated", False):
                 raise ValueError("calibrated=True before any calibrate()")
             L = self.L
-        # steps 3 and 4 in one pass over the pre-RoPE cache
-        stage("rope_and_split", st, a2ats_select_retrieval_set_rotated, keys, None,
+        in_step = queries is not None or h_given is not None
+        # second stream: steps 3-4 in one pass over the pre-RoPE cache, then
+        # the retrieval rows into a buffer of their own
+        stage("rope_and_split", side, a2ats_select_retrieval_set_rotated, keys, None,
               self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde, perm=self.perm,
               count=self.count, workspace=self.split_workspace)
-        self._split_done.record(st)
-        side.wait_event(self._split_done)
         if L is not None:
             stage("assign_retrieval", side, a2ats_h_weighted_assign, keys, codebook, L,
                   lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
-                  count=self.count, codes=self.codes, workspace=sws,
-                  reuse=reuse_codebook and queries is None and h_given is None)
+                  count=self.count, codes=self.codes_retrieval, workspace=sws,
+                  reuse=reuse_codebook and not in_step)
         else:
             # no calibrated H: the cosine blend against the same proxy query
             # (the key at t after windowed RoPE) the split used
             stage("assign_retrieval", side, a2ats_query_aware_assign, keys, codebook, None,
                   self.beta, lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
-                  count=self.count, codes=self.codes, workspace=sws)
+                  count=self.count, codes=self.codes_retrieval, workspace=sws)
         self._side_done.record(side)
+        # caller's stream: the bulk rule over every row (it needs no split),
+        # then the retrieval rows' codes over it
         stage("assign_bulk", st, a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
-              rope=self.rope, rows="bulk", perm=self.perm, count=self.count, codes=self.codes,
-              workspace=ws, reuse=reuse_codebook)
+              rope=self.rope, rows="all", codes=self.codes, workspace=ws, reuse=reuse_codebook)
         st.wait_event(self._side_done)
+        stage("route", st, a2ats_copy_retrieval_rows, self.codes_retrieval, self.codes,
+              self.perm, self.count, lengths=lengths)
         return self
 
 

@@ -114,3 +114,12 @@ def test_rotated_split_validation(lib):
              FAKE, FAKE, ws, None) == -4
     assert r(FAKE, 1, 1, 2, 64, 128, None, None, 0.2, ctypes.byref(rope), FAKE + 4096, 1, FAKE,
              FAKE, None, 0, None) == -6
+
+
+def test_copy_retrieval_rows_validation(lib):
+    f = lib.a2ats_copy_retrieval_rows
+    assert f(FAKE, FAKE, -1, 2, 10, None, FAKE, FAKE, None) == -2
+    assert f(FAKE, FAKE, 1, 70000, 10, None, FAKE, FAKE, None) == -2
+    assert f(None, FAKE, 1, 2, 10, None, FAKE, FAKE, None) == -1
+    assert f(FAKE, FAKE, 1, 2, 10, None, None, FAKE, None) == -1
+    assert f(None, None, 0, 2, 10, None, None, None, None) == 0

@@ -105,3 +105,19 @@ def test_rotated_split_equals_the_two_calls(case):
     for b in range(B):
         n = int(lens[b])
         assert torch.equal(perm[b, :, :n], want_perm[b, :, :n])
+
+
+def test_copy_retrieval_rows_touches_only_the_retrieval_rows():
+    B, H, N = 2, 3, 500
+    k = dev(synth.gaussian((B, H, N, 64), seed=3, dtype="bf16"))
+    lens = dev(torch.tensor([N, 321], dtype=torch.int32))
+    perm, count = q.a2ats_select_retrieval_set(k, None, 0.1, lengths=lens)
+    src = torch.arange(B * H * N, dtype=torch.int32, device="cuda").reshape(B, H, N)
+    dst = torch.full((B, H, N), -1, dtype=torch.int32, device="cuda")
+    q.a2ats_copy_retrieval_rows(src, dst, perm, count, lengths=lens)
+    want = torch.full_like(dst, -1)
+    for b in range(B):
+        for h in range(H):
+            sel = perm[b, h, :int(count[b, h])].long()
+            want[b, h, sel] = src[b, h, sel]
+    assert torch.equal(dst, want)
