@@ -150,6 +150,7 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.hneg = c.take<float>((size_t)(H * kpad));
     w.tc.head_bits = c.take<uint32_t>((size_t)(2 * H * 4));
     w.tc.head = c.take<float>((size_t)(2 * H * 4));
+    w.tc.gstat = c.take<float2>((size_t)(2 * H * (kpad / 32)));
     w.tc.scale = c.take<float>((size_t)(2 * H));
     w.tc.planes = c.take<uint16_t>((size_t)(2 * H * 3 * K * d));
     w.tc.compact = c.take<uint16_t>(2 * rows * (size_t)d);

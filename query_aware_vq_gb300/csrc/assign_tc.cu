@@ -69,6 +69,9 @@ struct Params {
     int32_t* status;           // 0, or the code of a timed-out wait
     uint32_t shr5_mul, shl5_mul;  // 2^27 and 32 (see embed_pos)
     const int32_t* max_rows;   // compact list: longest list over (b, h), or null
+    // per 32-centroid group: (max |chat_j|, max h_j) over the group, [H, ngroups]
+    const float2* gstat;
+    int32_t ngroups;
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -215,24 +218,28 @@ __device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
     t2 = lo[0];
 }
 
-// The decision for one row of a pass, from its top two (m1 with the column
-// bits, m2), the group index c1 of m1 and |x|^2 of its row operand: the code
-// when the gap clears the error bound, else the row joins the exact list.
+// The decision for one row of a pass.  Every value the contraction yields is
+// off from the exact x . chat_j - h_j by at most err_coef (|x| |chat_j| + h_j)
+// (plus the absolute fp16 term), which is bounded group by group with the
+// group maxima of |chat_j| and h_j: s_g = alpha max|chat| + beta max h over
+// 32-centroid group g.  The row carries m1 (its best key, column position in
+// the low bits) from group c1; U, an upper bound of the exact value of every
+// other centroid (the largest t1_g + s_g over the other groups, and t2 + s of
+// c1's own group); the code is certified when m1 - s_c1 still exceeds U, with
+// room for the position bits and the absolute term, else the row joins the
+// exact list.
 __device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int h,
-                                           float m1, float m2, int32_t c1, float nrm) {
+                                           float m1, float U, int32_t c1, float xn) {
     const int32_t j = p.row_map ? p.row_map[(int64_t)bh * p.seg + ri] : ri;
     const int32_t Lb = seq_len(p.len, bh / p.H, p.out_ncap);
     if (j < 0 || j >= Lb) return;
     const int64_t out = (int64_t)bh * p.out_ncap + j;
     if (p.skip && p.skip[out]) return;
-    // bound on |v_hat - v| for every centroid, plus the perturbation of the
-    // column bits in both keys
-    const float xn = sqrtf(nrm) * p.norm_slack;
-    const float cmax = p.head[h * 4 + 0], hmax = p.head[h * 4 + 1];
-    const float e = p.err_coef * (xn * cmax + hmax) + p.head[h * 4 + 3] * xn;
-    const float mag = fmaxf(fabsf(m1), fabsf(m2));
-    const float tau = 2.f * e + 64.f * mag * 1.1920929e-07f;
-    if (!(m1 - m2 > tau)) {
+    const float2 g1 = p.gstat[(int64_t)h * p.ngroups + c1];
+    const float e1 = p.err_coef * fmaf(xn, g1.x, g1.y);
+    const float mag = fmaxf(fabsf(m1), fabsf(U));
+    const float tau = e1 + 2.f * p.head[h * 4 + 3] * xn + 64.f * mag * 1.1920929e-07f;
+    if (!(m1 - U > tau)) {
         const int32_t slot = atomicAdd(p.exact_count, 1);
         p.exact_list[slot] = out;
     } else {
@@ -268,9 +275,10 @@ struct Smem {
     static constexpr int kBBytes = BST * kB;
     static constexpr int kHOff = kABytes + kBBytes;          // 2 x 256 floats of -h
     static constexpr int kBarOff = kHOff + 2 * BN * 4;
-    static constexpr int kBars = 2 * AST + 2 * BST + 10;
+    static constexpr int kBars = 2 * AST + 2 * BST + 14;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
-    static constexpr int kTotal = kMergeOff + (kParts - 1) * 4 * 32 * 16 + 1024;  // + slack
+    static constexpr int kNrmOff = kMergeOff + (kParts - 1) * 2 * 4 * 32 * 16;
+    static constexpr int kTotal = kNrmOff + 2 * kParts * BM * 4 + 1024;  // + alignment slack
 };
 
 template <bool BF16, int DK, int PA, int AST, int BST>
@@ -295,8 +303,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* h_empty = acc_full + 6;
     uint64_t* merge_full = acc_full + 8;   // column-part handoff, after the h ring
     uint64_t* merge_empty = acc_full + 9;
+    uint64_t* nrm_full = acc_full + 10;    // [4] one per TMEM lane quarter: row-norm partials
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
+    float* nrm_part = reinterpret_cast<float*>(sm + S::kNrmOff);  // [2][kParts][BM]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiles per (b, h): the host's bound, cut to the longest compact list
@@ -322,6 +332,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         mbar_init(merge_full, kEpiWarps - 4);  // every warp of parts 1.. hands over
         mbar_init(merge_empty, 4);             // the part-0 warps take the handoff
+        for (int i = 0; i < 4; i++) mbar_init(&nrm_full[i], kParts);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -455,7 +466,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int part = ew >> 2;        // which BN / kParts accumulator columns
         const int row_in_tile = 32 * q + lane;
-        uint32_t a_it = 0, acc_it = 0, m_it = 0;
+        uint32_t a_it = 0, acc_it = 0, m_it = 0, t_it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info(p, t, tpb);
@@ -464,14 +475,17 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int sa = a_it % AST;
             ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 7);
             if (!ok) break;
-            // |x|^2 of this row from the swizzled tile of plane 0 (order does not matter)
+            // |x|^2 of this row from the swizzled tile of plane 0: each of the
+            // four parts sums a quarter of the row's 16-byte chunks, the
+            // partials meet in shared memory (named barrier of the quarter's
+            // four warps) and every part adds them in the same order
             float nrm = 0.f;
-            if (part == 0) {
+            {
 #pragma unroll
-                for (int kb = 0; kb < DK; kb++) {
+                for (int ci = part * 2 * DK; ci < (part + 1) * 2 * DK; ci++) {
+                    const int kb = ci >> 3, c = ci & 7;
                     const uint8_t* rowp = smA + (sa * PA * DK + kb) * S::kA + row_in_tile * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; c++) {
+                    {
                         const uint4 raw = *reinterpret_cast<const uint4*>(
                             rowp + 16 * (c ^ (row_in_tile & 7)));
                         const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -492,13 +506,28 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         }
                     }
                 }
+                float* np = nrm_part + (t_it & 1) * kParts * BM;
+                np[part * BM + row_in_tile] = nrm;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&nrm_full[q]);
+                ok = mbar_wait(&nrm_full[q], t_it & 1, p.status, 13);
+                nrm = 0.f;
+#pragma unroll
+                for (int pp = 0; pp < kParts; pp++) nrm += np[pp * BM + row_in_tile];
+                t_it++;
             }
+            if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_empty[sa]);
             a_it++;
 
-            float m1 = -FLT_MAX, m2 = -FLT_MAX;
-            int32_t c1 = 0;
+            // m1 / c1: the best key and its group; w2: t2 + s of that group;
+            // ub1 / gb1 / ub2: the two largest t1_g + s_g and the first's group
+            float m1 = -FLT_MAX, w2 = -FLT_MAX, ub1 = -FLT_MAX, ub2 = -FLT_MAX;
+            int32_t c1 = 0, gb1 = -1;
+            const float xn = sqrtf(nrm) * p.norm_slack;
+            const float alpha = p.err_coef * xn, beta = p.err_coef;
+            const float2* gst = p.gstat + (int64_t)h * p.ngroups;
             const float inv_scale = p.head[h * 4 + 2];
             const float2 inv2 = make_float2(inv_scale, inv_scale);
             const uint32_t m27 = p.shr5_mul, m5 = p.shl5_mul;
@@ -534,10 +563,22 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                     float t1, t2;
                     top2_32(key, t1, t2);
-                    const int j0 = c * BN + col;
-                    if (t1 > m1) c1 = j0 >> 5;
-                    m2 = max3f(fminf(m1, t1), m2, t2);
-                    m1 = fmaxf(m1, t1);
+                    const int g = (c * BN + col) >> 5;
+                    const float2 gs = __ldg(gst + g);
+                    const float sg = fmaf(alpha, gs.x, beta * gs.y);
+                    const float b1 = t1 + sg;
+                    if (b1 > ub1) {
+                        ub2 = ub1;
+                        ub1 = b1;
+                        gb1 = g;
+                    } else {
+                        ub2 = fmaxf(ub2, b1);
+                    }
+                    if (t1 > m1) {
+                        m1 = t1;
+                        c1 = g;
+                        w2 = t2 + sg;
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -552,30 +593,42 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (part != 0) {
                 ok = mbar_wait(merge_empty, (m_it & 1) ^ 1, p.status, 9);
                 if (!ok) break;
-                merge[(part - 1) * 128 + q * 32 + lane] = make_float4(m1, m2, __int_as_float(c1), 0.f);
+                float4* mg = merge + ((part - 1) * 128 + q * 32 + lane) * 2;
+                mg[0] = make_float4(m1, w2, __int_as_float(c1), 0.f);
+                mg[1] = make_float4(ub1, ub2, __int_as_float(gb1), 0.f);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_full);
             } else {
                 ok = mbar_wait(merge_full, m_it & 1, p.status, 10);
                 if (!ok) break;
-                float4 o[kParts - 1];
-#pragma unroll
-                for (int pp = 0; pp < kParts - 1; pp++) o[pp] = merge[pp * 128 + q * 32 + lane];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(merge_empty);
+                float4 o[kParts - 1][2];
 #pragma unroll
                 for (int pp = 0; pp < kParts - 1; pp++) {
-                    const int32_t oc = __float_as_int(o[pp].z);
-                    if (o[pp].x > m1) {
-                        m2 = fmaxf(m1, o[pp].y);
-                        m1 = o[pp].x;
-                        c1 = oc;
+                    const float4* mg = merge + (pp * 128 + q * 32 + lane) * 2;
+                    o[pp][0] = mg[0];
+                    o[pp][1] = mg[1];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(merge_empty);
+                // parts in column order, so equal keys keep the earlier columns
+#pragma unroll
+                for (int pp = 0; pp < kParts - 1; pp++) {
+                    if (o[pp][0].x > m1) {
+                        m1 = o[pp][0].x;
+                        w2 = o[pp][0].y;
+                        c1 = __float_as_int(o[pp][0].z);
+                    }
+                    if (o[pp][1].x > ub1) {
+                        ub2 = fmaxf(ub1, o[pp][1].y);
+                        ub1 = o[pp][1].x;
+                        gb1 = __float_as_int(o[pp][1].z);
                     } else {
-                        m2 = fmaxf(m2, o[pp].x);
+                        ub2 = fmaxf(ub2, o[pp][1].x);
                     }
                 }
+                const float U = fmaxf(gb1 == c1 ? ub2 : ub1, w2);
                 const int32_t ri = ti.r0 + row_in_tile;
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, m2, c1, nrm);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, c1, xn);
             }
             m_it++;
         }
@@ -614,7 +667,8 @@ __global__ void rotate_rows_kernel(const float* __restrict__ in, int64_t rows, i
 // zeroed by the caller): max |chat_j|, max h_j, max |element|.
 __global__ void __launch_bounds__(256)
 codebook_stats_kernel(const float* __restrict__ chat, int64_t K, int32_t d,
-                      const float* __restrict__ half_norm, uint32_t* __restrict__ head_bits) {
+                      const float* __restrict__ half_norm, uint32_t* __restrict__ head_bits,
+                      uint32_t* __restrict__ group_bits, int32_t ngroups) {
     // one warp per centroid, one head per block row; the block's maxima are
     // combined in shared memory first, so a head takes one atomic per block
     __shared__ float red[3][8];
@@ -636,6 +690,12 @@ codebook_stats_kernel(const float* __restrict__ chat, int64_t K, int32_t d,
         }
         cm = sqrtf(n.value()) * 1.000001f;
         hm = fmaxf(half_norm[h * K + j], 0.f);
+        // the same maxima per 32-centroid group (bits of non-negative floats)
+        if (lane == 0) {
+            uint32_t* gb = group_bits + 2 * (h * ngroups + (j >> 5));
+            atomicMax(gb, __float_as_uint(cm));
+            atomicMax(gb + 1, __float_as_uint(hm));
+        }
     }
     if (lane == 0) {
         red[0][w] = cm;
@@ -1082,6 +1142,7 @@ struct BSide {
     int P;
     bool exact;           // products exact without planes (raw 16-bit codebook)
     const float* head;
+    const float2* gstat;  // [H, ngroups] group maxima of |chat_j| and h_j
 };
 
 // The codebook operand (variant v: 0 as is, 1 rotated by -far_offset) and,
@@ -1092,9 +1153,12 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
                       cudaStream_t st, bool launch = true) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d;
+    const int64_t ngroups = (K + BN - 1) / BN * BN / 32;
+    out.gstat = c.gstat + v * H * ngroups;
     if (launch) {
         codebook_stats_kernel<<<dim3((unsigned)((K + 7) / 8), (unsigned)H), 256, 0, st>>>(
-            chat, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4);
+            chat, K, (int32_t)d, c.half_norm, c.head_bits + v * H * 4,
+            reinterpret_cast<uint32_t*>(c.gstat + v * H * ngroups), (int32_t)ngroups);
         note_launches(1);
         head_finish_kernel<<<(unsigned)((H + 63) / 64), 64, 0, st>>>(
             c.head_bits + v * H * 4, (int32_t)H, (int32_t)d, (bf16 || raw) ? 1 : 0,
@@ -1161,6 +1225,8 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.skip_near = skip_near;
     p.hneg = c.hneg;
     p.head = b.head;
+    p.gstat = b.gstat;
+    p.ngroups = p.kpad / 32;
     // The products are exact; the tensor core adds (d/16 per operand pair)
     // partial sums into fp32, each addition off by at most 2^-23 of the
     // running magnitude, which |x| max|chat| + max h bounds; plus the rounding
@@ -1216,6 +1282,8 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     const bool build = !c.prepared;
     if (build) {
         e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(c.gstat, 0, sizeof(float2) * 2 * H * (kpad / 32), st);
         if (e != cudaSuccess) return e;
         pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K,
                                                                              kpad, c.hneg);

@@ -121,6 +121,7 @@ struct TcCall {
     float* hneg;          // [H, Kpad]  -|c L|^2 / 2, padded to 256 columns
     uint32_t* head_bits;  // [2, H, 4]
     float* head;          // [2, H, 4]
+    float2* gstat;        // [2, H, Kpad / 32] group maxima of |chat_j| and h_j
     float* scale;         // [2, H]
     uint16_t* planes;     // [2, H, 3, K, d]
     uint16_t* compact;    // [2, B*H*Ncap, d] two 16-bit planes of rotated rows
