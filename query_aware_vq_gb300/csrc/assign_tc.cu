@@ -1115,11 +1115,9 @@ cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const 
         }
     }
     else {
-        // two-plane row operands: a second A stage (the next item's key
-        // tile loads while this one is in use) is worth more than B stages
         switch (p.d) {
             case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 2, 2>(ta, tb, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, p, st);
             case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, p, st);
             default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, p, st);
         }
