@@ -398,6 +398,110 @@ def run_ours(a):
         dist.destroy_process_group()
 
 
+def run_decode(a):
+    """The decode-streaming workload: each step appends one key per (sequence,
+    head), re-rotates and re-splits every cached key, and assigns the new keys
+    (cosine blend, proxy query = the new key).  The cache (several GB) is far
+    larger than L2, so nothing is flushed between steps.  `value` counts the
+    cached keys each step processes (re-rotated and ranked); the new keys per
+    second are reported beside it."""
+    import query_aware_vq_gb300 as q
+    from query_aware_vq_gb300.pipeline import A2ATSDecodeStep
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    total = min(a.warmup + a.steps, w.decode_steps)
+    warm = min(a.warmup, max(total - 1, 0))
+    steps = total - warm
+    lens0 = synth.decode_lengths(w)
+    keys = synth.keys(synth.scaled(w, N=int(lens0.max())))
+    cache = torch.zeros((w.B, w.H, w.N, w.d), dtype=synth.DTYPES[w.dtype], device="cuda")
+    cache[:, :, :keys.shape[2]] = keys.cuda()
+    del keys
+    lengths = torch.from_numpy(lens0).cuda()
+    cb = synth.codebook(w).cuda()
+    new = [synth.decode_new_keys(w, s) for s in range(total)]
+    new_d = [t.cuda() for t in new]
+    step = A2ATSDecodeStep(w.B, w.H, w.N, w.d, w.K, synth.DTYPES[w.dtype], window=w.W,
+                           fraction=w.fraction, rope_base=w.rope_base, beta=w.betas[0])
+    stream = torch.cuda.current_stream()
+    for s in range(warm):
+        step(cache, lengths, new_d[s], cb)
+    torch.cuda.synchronize()
+    cached = [int(lengths.sum()) + w.B * (i + 1) for i in range(steps)]  # after each append
+    events, step_ev = {}, []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    for i in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(cache, lengths, new_d[warm + i], cb, events=events)
+        e1.record(stream)
+        step_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    _barrier(world)
+    launches = q.kernel_launches() - launches0
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in step_ev) / steps, world)
+    keys_per_step = w.H * sum(cached) / steps
+    value = world * keys_per_step / (ms * 1e-3)
+    stage_ms = {k: sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in events.items()}
+    hbm, _, src = _peaks()
+    s_el = {"f32": 4, "bf16": 2, "f16": 2}[w.dtype]
+    amount = keys_per_step * (2.0 * w.d * s_el + 12.0)
+    achieved = amount / (stage_ms["rope_and_split"] * 1e-3) / 1e9
+    roof = {"kernel": "cosine_score_kernel + select_kernel (re-rotation and split of the cache)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 5), "traffic": None,
+            "bytes_per_step": amount, "peak_source": f"{src} (hbm_gbs)"}
+    # end to end: the new keys from pinned host memory, their codes back
+    e2e = None
+    if not a.no_e2e:
+        hnew = [t.pin_memory() for t in new[warm:]]
+        out = torch.empty((w.B, w.H), dtype=torch.int32).pin_memory()
+        staged = torch.empty_like(new_d[0])
+        e2e_ms = []
+        room = w.N - int(lengths.max())
+        for i in range(min(steps, room)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            staged.copy_(hnew[i], non_blocking=True)
+            step(cache, lengths, staged, cb)
+            idx = (lengths.long() - 1).view(w.B, 1, 1).expand(w.B, w.H, 1)
+            out.copy_(step.codes.gather(2, idx).squeeze(2), non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+        if e2e_ms:
+            em = _max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+            e2e = {"value": world * keys_per_step / (em * 1e-3), "unit": "keys/s",
+                   "ms_per_step": round(em, 4),
+                   "h2d_bytes_per_step": staged.numel() * staged.element_size(),
+                   "d2h_bytes_per_step": out.numel() * out.element_size()}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; correlated-Gaussian keys with outlier channels; no model "
+                    "weights)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Ncap": w.N, "d": w.d, "K": w.K,
+                       "window": w.W, "fraction": w.fraction, "beta": w.betas[0],
+                       "storage": w.dtype, "l2": "inputs larger than L2 (no flush)",
+                       "value_counts": "cached keys re-rotated and ranked per second",
+                       "new_keys_per_s": world * w.B * w.H / (ms * 1e-3),
+                       "parallelism": f"replicas x{world} (independent batches)"},
+            "roofline": roof,
+            "stages": {k: {"ms": round(v, 4)} for k, v in stage_ms.items()},
+            "cpu_baseline": None, "clocks": clk, "e2e": e2e, "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def _oracle_sample(w, keys, cb, queries, hg, rows: int, h: int):
     """One bounded sample of the workload on the oracle: the first `rows`
     keys of head h (as a sequence of that length) through the whole step."""
@@ -466,5 +570,7 @@ if __name__ == "__main__":
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif synth.WORKLOADS[args.workload].decode_steps:
+        run_decode(args)
     else:
         run_ours(args)

@@ -153,6 +153,7 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
     float* xs = sm;                 // [kRB][d+1]
     float* cs = xs + kRB * ld;      // [kCT][d+1]
     float* qs = cs + kCT * ld;      // [d] shared query
+    float* cosc = qs + d;           // [kCT] cos(query, c_j) of the tile's centroids
     __shared__ int32_t rows[kRB];
     const int64_t bh = blockIdx.y;
     const int64_t h = bh % H;
@@ -170,7 +171,6 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
     const float* xr = xs + r * ld;
     const float qn = qnorm[bh];
     __syncthreads();
-    const float* qv = qs;
     float emax = 0.f;
     float best = -INFINITY;
     int32_t bj = 0;
@@ -186,7 +186,22 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
                 cs[c * ld + a] = c < nc ? cf[((h * K) + j0 + c) * d + a] : 0.f;
             }
             __syncthreads();
-            for (int c = slot; c < nc; c += kSlots) {
+            if (pass == 1) {
+                // the cosine term depends on the centroid only (one query per
+                // (b, h)): kSlots threads per centroid, compensated sums
+                const int cc_i = threadIdx.x / kSlots, part = threadIdx.x % kSlots;
+                Dot2 dq;
+                if (cc_i < nc)
+                    for (int aa = part; aa < d; aa += kSlots) dq.add_prod(qs[aa], cs[cc_i * ld + aa]);
+                for (int m = kSlots / 2; m; m >>= 1) dq.merge(shfl_xor(dq, m));
+                if (part == 0 && cc_i < nc) {
+                    const float cn = cnorm[h * K + j0 + cc_i];
+                    cosc[cc_i] = (qn > 0.f && cn > 0.f) ? dq.value() / (qn * cn) : 0.f;
+                }
+                __syncthreads();
+            }
+            // rows of the list that are empty do no work
+            for (int c = slot; c < nc && rows[r] >= 0; c += kSlots) {
                 const float* cc = cs + c * ld;
                 float e4[4] = {0.f, 0.f, 0.f, 0.f}, dq = 0.f;
                 int a = 0;
@@ -206,11 +221,8 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
                     emax = fmaxf(emax, e);
                     continue;
                 }
-                Dot2 dot;
-                for (int aa = 0; aa < d; aa++) dot.add_prod(qv[aa], cc[aa]);
                 const int32_t j = (int32_t)(j0 + c);
-                const float cn = cnorm[h * K + j];
-                const float cosv = (qn > 0.f && cn > 0.f) ? dot.value() / (qn * cn) : 0.f;
+                const float cosv = cosc[c];
                 const float err = emax > 0.f ? e / emax : 0.f;
                 const float s = fmaf(-beta, err, (1.f - beta) * cosv);
                 if (s > best || (s == best && j < bj)) { best = s; bj = j; }
@@ -227,7 +239,116 @@ assign_blend_kernel(const void* __restrict__ x, const float* __restrict__ cf, in
 }
 
 size_t exact_smem(int d) { return sizeof(float) * (size_t)((2 * kRB + kCT) * (d + 1)); }
-size_t blend_smem(int d) { return sizeof(float) * (size_t)((kRB + kCT) * (d + 1) + d); }
+// The cosine blend of the decode row alone (rows = LAST): one block per
+// (b, h) and one row, so the block's lanes spread over the centroids instead
+// of over rows.  8 lanes share a centroid (each 1/8 of its elements, 16-byte
+// loads); pass 1 finds e_max = max_j |x - c_j|^2, pass 2 scores every
+// centroid.  The arithmetic is the general kernel's: e_j as a plain fp32 sum
+// of squares, q . c_j compensated.
+template <int DT>
+__global__ void __launch_bounds__(256)
+assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ cf, int32_t H,
+                         int32_t ncap, int32_t d, const int32_t* __restrict__ len,
+                         const RopeArgs ra, const float* __restrict__ q,
+                         const float* __restrict__ qnorm, float beta, int64_t K,
+                         const float* __restrict__ cnorm, int32_t* __restrict__ codes) {
+    __shared__ __align__(16) float xs[kMaxD];
+    __shared__ __align__(16) float qs[kMaxD];
+    __shared__ float wmax[8];
+    __shared__ float wbest[8];
+    __shared__ int32_t wj[8];
+    const int64_t bh = blockIdx.x;
+    const int64_t h = bh % H;
+    const int32_t Ls = seq_len(len, (int32_t)(bh / H), ncap);
+    if (Ls <= 0) return;
+    // the row with its windowed RoPE, and the query
+    for (int a = threadIdx.x; a < d; a += blockDim.x) xs[a] = load1<DT>(x, (bh * ncap + Ls - 1) * d + a);
+    for (int a = threadIdx.x; a < d; a += blockDim.x) qs[a] = q[bh * d + a];
+    __syncthreads();
+    if (ra.enabled) {
+        const int half = d / 2;
+        const int32_t pos = rope_position(Ls - 1, Ls - 1, ra);
+        if (pos != 0)
+            for (int i = threadIdx.x; i < half; i += blockDim.x) {
+                float sn, cs;
+                rope_angle(pos, ra.omega_hi[i], ra.omega_lo[i], ra, sn, cs);
+                const int a = ra.interleaved ? 2 * i : i;
+                const int b = ra.interleaved ? 2 * i + 1 : i + half;
+                const float xa = xs[a], xb = xs[b];
+                xs[a] = fmaf(xa, cs, -__fmul_rn(xb, sn));
+                xs[b] = fmaf(xa, sn, __fmul_rn(xb, cs));
+            }
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int grp = threadIdx.x >> 3, seg = threadIdx.x & 7;  // 32 centroids at a time
+    const float qn = qnorm[bh];
+    const float* ch = cf + h * K * d;
+    float emax = 0.f, best = -INFINITY;
+    int32_t bj = 0;
+    for (int pass = 0; pass < 2; pass++) {
+        // uniform trip count: the shuffles below need every lane
+        for (int64_t j0 = 0; j0 < K; j0 += 32) {
+            const int64_t j = j0 + grp;
+            const bool ok = j < K;
+            const float* c = ch + (ok ? j : 0) * d;
+            float e0 = 0.f, e1 = 0.f;
+            Dot2 dq;
+            for (int a = seg * 4; a < d; a += 32) {
+                const float4 cv = *reinterpret_cast<const float4*>(c + a);
+                const float4 xv = *reinterpret_cast<const float4*>(xs + a);
+                const float t0 = xv.x - cv.x, t1 = xv.y - cv.y, t2 = xv.z - cv.z, t3 = xv.w - cv.w;
+                e0 = fmaf(t0, t0, e0);
+                e1 = fmaf(t1, t1, e1);
+                e0 = fmaf(t2, t2, e0);
+                e1 = fmaf(t3, t3, e1);
+                if (pass == 1) {
+                    const float4 qv = *reinterpret_cast<const float4*>(qs + a);
+                    dq.add_prod(qv.x, cv.x);
+                    dq.add_prod(qv.y, cv.y);
+                    dq.add_prod(qv.z, cv.z);
+                    dq.add_prod(qv.w, cv.w);
+                }
+            }
+            float e = e0 + e1;
+            for (int m = 4; m; m >>= 1) e += __shfl_xor_sync(0xffffffffu, e, m);
+            if (pass == 0) {
+                if (ok) emax = fmaxf(emax, e);
+                continue;
+            }
+            for (int m = 4; m; m >>= 1) dq.merge(shfl_xor(dq, m));
+            if (ok) {
+                const float cn = cnorm[h * K + j];
+                const float cosv = (qn > 0.f && cn > 0.f) ? dq.value() / (qn * cn) : 0.f;
+                const float err = emax > 0.f ? e / emax : 0.f;
+                const float sc = fmaf(-beta, err, (1.f - beta) * cosv);
+                if (sc > best || (sc == best && j < bj)) { best = sc; bj = (int32_t)j; }
+            }
+        }
+        if (pass == 0) {
+            // e_max over the block
+            for (int m = 16; m; m >>= 1) emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, m));
+            if (lane == 0) wmax[w] = emax;
+            __syncthreads();
+            emax = wmax[0];
+            for (int ww = 1; ww < 8; ww++) emax = fmaxf(emax, wmax[ww]);
+        }
+    }
+    for (int m = 16; m; m >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, m);
+        const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
+        if (ov > best || (ov == best && oj < bj)) { best = ov; bj = oj; }
+    }
+    if (lane == 0) { wbest[w] = best; wj[w] = bj; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int ww = 1; ww < 8; ww++)
+            if (wbest[ww] > best || (wbest[ww] == best && wj[ww] < bj)) { best = wbest[ww]; bj = wj[ww]; }
+        codes[bh * ncap + Ls - 1] = bj;
+    }
+}
+
+size_t blend_smem(int d) { return sizeof(float) * (size_t)((kRB + kCT) * (d + 1) + d + kCT); }
 
 }  // namespace
 
@@ -262,6 +383,29 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
                                 const float* q, const float* qnorm, float beta, int64_t K,
                                 const float* cnorm, int32_t* codes, cudaStream_t st) {
     if (s.B * s.H * s.Ncap == 0) return cudaSuccess;
+    if (sel.mode == 3) {
+        // one row per (b, h): the lanes go to the centroids
+        const float* cf = reinterpret_cast<const float*>(c);
+        const unsigned nbh = (unsigned)(s.B * s.H);
+        switch (dt) {
+            case kF32:
+                assign_blend_last_kernel<kF32><<<nbh, 256, 0, st>>>(
+                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
+                    K, cnorm, codes);
+                break;
+            case kBF16:
+                assign_blend_last_kernel<kBF16><<<nbh, 256, 0, st>>>(
+                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
+                    K, cnorm, codes);
+                break;
+            default:
+                assign_blend_last_kernel<kF16><<<nbh, 256, 0, st>>>(
+                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
+                    K, cnorm, codes);
+        }
+        note_launches(1);
+        return cudaGetLastError();
+    }
     dim3 grid(sel.mode == 3 ? 1u : (unsigned)((s.Ncap + kRB - 1) / kRB), (unsigned)(s.B * s.H));
     const size_t smem = blend_smem((int)s.d);
     const float* cf = reinterpret_cast<const float*>(c);  // fp32 copy of the codebook
