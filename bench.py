@@ -22,9 +22,11 @@ H from 8192 calibration queries per head; window 512; retrieval fraction
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is keys assigned per second over all
-ranks with the inputs resident on the GPU; `e2e` repeats the measurement with
-the inputs copied from pinned host memory and the codes / split copied back
-inside the timed region.  The reference arm (`--impl reference`) times the
+ranks with the inputs resident on the GPU, the step replayed as one captured
+CUDA graph (A2ATSStep.capture; the stage table and the contraction's roofline
+come from a pass of eager calls before it); `e2e` repeats the measurement
+through eager calls of the public API with the inputs copied from pinned host
+memory and the codes / split copied back inside the timed region.  The reference arm (`--impl reference`) times the
 fp64 CPU oracle on this machine's host cores on a bounded sample of the same
 workload.  Under torchrun each rank runs an independent replica of the
 workload (weak scaling, no data-path collective).
@@ -263,37 +265,61 @@ def run_ours(a):
         flush.zero_()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps on resident inputs, L2 flushed between steps
+    # ---- a profiling pass (eager calls): per-stage CUDA events, the
+    # library's own timing of the stored-order contraction, and the number of
+    # kernel launches per step
     events = {}
+    launches0 = q.kernel_launches()
+    q.set_kernel_timing(True)
+    q.timed_kernels_ms()
+    for _ in range(a.steps):
+        step(kd, cd, events=events, **kw)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches_per_step = (q.kernel_launches() - launches0) / a.steps
+    tc_ms, tc_launches = q.timed_kernels_ms()
+    q.set_kernel_timing(False)
+    stage_ms = {k: sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in events.items()}
+
+    # ---- the step as one CUDA graph (both streams), replayed K times; eager
+    # calls if the capture is refused
+    try:
+        graph = step.capture(kd, cd, **kw)
+        run_step = graph.replay
+        launch_mode = "CUDA graph of one step, replayed"
+    except Exception as ex:  # noqa: BLE001
+        torch.cuda.synchronize()
+        run_step = lambda: step(kd, cd, **kw)  # noqa: E731
+        launch_mode = f"eager calls (graph capture refused: {type(ex).__name__})"
+    for _ in range(a.warmup):
+        run_step()
+        flush.zero_()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps on resident inputs, L2 flushed between steps
     step_ev = []
     clocks = Clocks(local)
     clocks.start()
     _barrier(world)
     torch.cuda.synchronize()
-    launches0 = q.kernel_launches()
-    q.set_kernel_timing(True)
-    q.timed_kernels_ms()
     t_wall = time.perf_counter()
     for _ in range(a.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step(kd, cd, events=events, **kw)
+        run_step()
         e1.record(stream)
         step_ev.append((e0, e1))
         flush.zero_()
     torch.cuda.synchronize()
     _barrier(world)
     t_wall = time.perf_counter() - t_wall
-    launches = q.kernel_launches() - launches0
-    tc_ms, tc_launches = q.timed_kernels_ms()
-    q.set_kernel_timing(False)
+    launches = int(round(launches_per_step * a.steps))
     clk = clocks.stop()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in step_ev]
     ms = sum(step_ms) / len(step_ms)
     ms = _max_over_ranks(ms, world)
     keys_per_step = w.B * w.H * w.N
     value = world * keys_per_step / (ms * 1e-3)
-    stage_ms = {k: sum(e0.elapsed_time(e1) for e0, e1 in v) / len(v) for k, v in events.items()}
 
     # ---- roofline of the dominant kernel: the tensor-core contraction over
     # the keys in stored order (every key outside the RoPE window), timed by
@@ -387,6 +413,7 @@ def run_ours(a):
                        "calibration": calib_mode,
                        "calibration_ms": None if calib_ms is None else round(calib_ms, 4),
                        "codebook_side": "built once, reused by every timed step",
+                       "launch": launch_mode,
                        "ms_per_step_rebuilding_codebook_side": round(rebuild_ms, 4),
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": roof, "stages": stages, "cpu_baseline": cpu, "clocks": clk,

@@ -165,6 +165,22 @@ class A2ATSStep:
               self.perm, self.count, lengths=lengths)
         return self
 
+    def capture(self, keys, codebook, **kw):
+        """One step, with the same arguments as a call, captured into a CUDA
+        graph (both streams: the second forks from and joins the capturing
+        stream through events).  Every replay runs that step again on the same
+        buffers; the inputs may be refilled in place between replays.  The
+        call warms the step up once on a side stream before capturing."""
+        s = torch.cuda.Stream(device=keys.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self(keys, codebook, **kw)
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self(keys, codebook, **kw)
+        return graph
+
 
 class A2ATSDecodeStep:
     """One decode step over a batch of growing caches (v0.39.0 page, "How it
