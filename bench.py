@@ -71,6 +71,9 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--separate-split", action="store_true",
+                   help="run RoPE and the split on the second stream beside a separate "
+                        "plain-VQ call, instead of the fused call (same outputs)")
     return p.parse_args()
 
 
@@ -205,6 +208,9 @@ def _work(w, count):
         # copied over it afterwards
         "assign_bulk": ("tensor", keys * 2.0 * w.d * w.K),
         "route": ("hbm", n_ret * 12.0),
+        # the fused call: RoPE, split and the bulk rule over every row; its
+        # work is dominated by the contraction
+        "rope_split_bulk": ("tensor", keys * 2.0 * w.d * w.K),
     }
 
 
@@ -219,7 +225,7 @@ def run_ours(a):
     dt = synth.DTYPES[w.dtype]
     step = A2ATSStep(w.B, w.H, w.N, w.d, w.K, dt, window=w.W, fraction=w.fraction,
                      rope_base=w.rope_base, far_offset=w.far_offset, M=w.M, ridge=w.ridge,
-                     beta=w.betas[-1])
+                     beta=w.betas[-1], fused=not a.separate_split)
     kd, cd = keys.cuda(), cb.cuda()
     qd = queries.cuda() if queries is not None else None
     hd = hg.cuda() if hg is not None else None
@@ -414,6 +420,10 @@ def run_ours(a):
                        "calibration_ms": None if calib_ms is None else round(calib_ms, 4),
                        "codebook_side": "built once, reused by every timed step",
                        "launch": launch_mode,
+                       "composition": ("RoPE and split on the second stream, plain VQ apart"
+                                       if a.separate_split else
+                                       "one call for RoPE, split and plain VQ; the retrieval "
+                                       "rule on the second stream"),
                        "ms_per_step_rebuilding_codebook_side": round(rebuild_ms, 4),
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": roof, "stages": stages, "cpu_baseline": cpu, "clocks": clk,

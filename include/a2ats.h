@@ -251,6 +251,48 @@ int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t 
                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_rope_split_plain_assign -- a2ats_select_retrieval_set_rotated
+ * (out_dtype = dtype) and plain VQ over every row,
+ * a2ats_h_weighted_assign(keys, codebook, L = NULL, fused_rope = rope,
+ * rows = A2ATS_ROWS_ALL), in one call (no counterpart on the pages: it joins
+ * the per-step re-rotation of [ALG] "Per-step re-rotation", the split of
+ * [API] a2ats_select_retrieval_set and the bulk rule of [V039] step 2, the
+ * nearest centroid, so that with far_offset = 0 one pass over the stored
+ * keys outside the RoPE window copies them to k_out, scores them and
+ * assigns them).
+ *   keys, dtype, B, H, Ncap, d, len, query, fraction, rope: as
+ *          a2ats_select_retrieval_set_rotated (rope required)
+ *   codebook [H, K, d] in dtype; K in [1, 2^24]
+ *   k_out  [B, H, Ncap, d] in dtype: the windowed-RoPE keys (rows j < len[b],
+ *          exactly what a2ats_windowed_rope writes); must not be keys
+ *   perm, count: the split, as a2ats_select_retrieval_set writes it
+ *   codes  [B, H, Ncap] int32: the nearest centroid of every row j < len[b]
+ *          (the exactness of a2ats_h_weighted_assign)
+ *   reuse  nonzero: the codebook side (decoded centroids, norms, planes,
+ *          tables) is taken from the workspace as the previous call of this
+ *          function on it, with the same codebook, shapes and rope, left it
+ *   split_done  a cudaEvent_t, or NULL: recorded on the stream as soon as
+ *          k_out, perm and count are complete (before the codes are), so a
+ *          second stream can start on the split while this call finishes
+ *   workspace  a2ats_rope_split_plain_assign_workspace_size(B, H, Ncap, d, K)
+ *          bytes of device memory, owned by the caller
+ * The scores of this call may differ from those of
+ * a2ats_select_retrieval_set in the last bits (another order of fp32
+ * additions), so the split is exact except on the near-ties that call
+ * exempts too.
+ * Errors: those of both calls; WORKSPACE when workspace is NULL or short.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_rope_split_plain_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap,
+                                                    int64_t d, int64_t K);
+int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                                  int64_t Ncap, int64_t d, const int32_t* len, const void* query,
+                                  double fraction, const a2ats_rope_params* rope,
+                                  const void* codebook, int64_t K, void* k_out, int32_t* perm,
+                                  int32_t* count, int32_t* codes, int32_t reuse,
+                                  void* split_done, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

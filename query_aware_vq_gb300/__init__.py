@@ -67,6 +67,9 @@ _SIGS = {
     "a2ats_select_retrieval_set_rotated": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
                                            _I32, _P, _P, _P, _SZ, _P],
     "a2ats_copy_retrieval_rows": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "a2ats_rope_split_plain_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
+                                      _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
@@ -96,7 +99,8 @@ def _load():
         for name in ("a2ats_query_second_moment_workspace_size",
                      "a2ats_h_weighted_assign_workspace_size",
                      "a2ats_query_aware_assign_workspace_size",
-                     "a2ats_select_retrieval_set_workspace_size"):
+                     "a2ats_select_retrieval_set_workspace_size",
+                     "a2ats_rope_split_plain_assign_workspace_size"):
             getattr(lib, name).restype = ctypes.c_size_t
         lib.a2ats_kernel_launches.restype = ctypes.c_uint64
         lib.a2ats_timed_kernels_ms.restype = ctypes.c_double
@@ -353,6 +357,47 @@ def a2ats_select_retrieval_set_rotated(keys, query=None, fraction: float = 0.2, 
         ctypes.byref(rp), _ptr(o4), _dt(o4), _ptr(perm), _ptr(count), _ptr(ws), nb,
         _stream(stream)))
     return out, perm, count
+
+
+def a2ats_rope_split_plain_assign(keys, codebook, query=None, fraction: float = 0.2, *, rope,
+                                  lengths=None, out=None, perm=None, count=None, codes=None,
+                                  reuse=False, split_done=None, workspace=None, stream=None):
+    """Windowed RoPE, the retrieval split and plain VQ of every row in one
+    call over the pre-RoPE keys; returns (out, perm, count, codes).
+    split_done: a torch.cuda.Event, recorded on the stream once out, perm and
+    count are written (the codes follow).  reuse=True takes the codebook side
+    from `workspace` as the previous call on it left it."""
+    _dev(keys, codebook, query, lengths, out, perm, count, codes)
+    k4, cb, K, codes = _assign_common(keys, codebook, codes)
+    B, H, N, d = k4.shape
+    if query is not None and query.dtype != k4.dtype:
+        raise TypeError("query and keys must share a dtype")
+    if out is None:
+        out = torch.empty(keys.shape, dtype=keys.dtype, device=keys.device)
+    if out.dtype != keys.dtype:
+        raise TypeError("out must have the keys' dtype")
+    o4 = _as4(out)
+    if perm is None:
+        perm = torch.empty((B, H, N), dtype=torch.int32, device=keys.device)
+    if count is None:
+        count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
+    lib = _load()
+    if reuse and workspace is None:
+        raise ValueError("reuse needs the workspace of the preparing call")
+    ws, nb = _workspace(lib.a2ats_rope_split_plain_assign_workspace_size(B, H, N, d, K),
+                        keys.device, workspace)
+    ev = None
+    if split_done is not None:
+        ev = split_done.cuda_event
+        if not ev:
+            raise ValueError("split_done must have been recorded once (its handle is made "
+                             "lazily)")
+    rp = _rope(rope)
+    _check("a2ats_rope_split_plain_assign", lib.a2ats_rope_split_plain_assign(
+        _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
+        ctypes.byref(rp), _ptr(cb), K, _ptr(o4), _ptr(perm), _ptr(count), _ptr(codes),
+        int(bool(reuse)), ev, _ptr(ws), nb, _stream(stream)))
+    return out, perm, count, codes
 
 
 def a2ats_copy_retrieval_rows(src, dst, perm, count, *, lengths=None, stream=None):

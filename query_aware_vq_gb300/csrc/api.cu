@@ -537,6 +537,119 @@ int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t 
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+size_t a2ats_rope_split_plain_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap,
+                                                    int64_t d, int64_t K) {
+    Carve c(nullptr);
+    carve_assign(c, B, H, Ncap, d, K);
+    carve_select(c, B, H, Ncap, d);
+    return c.used + 256;
+}
+
+namespace {
+// The split, launched between the pass over the stored keys (the last
+// scores it needs) and the rest of the assignment; then the caller's event.
+struct SplitAfter {
+    const float* scores;
+    Shape sh;
+    const int32_t* len;
+    double fraction;
+    int32_t* perm;
+    int32_t* count;
+    cudaEvent_t done;
+};
+
+cudaError_t split_after_natural(void* ctx, cudaStream_t st) {
+    const SplitAfter* a = static_cast<const SplitAfter*>(ctx);
+    cudaError_t e = launch_select(a->scores, a->sh, a->len, a->fraction, a->perm, a->count, st);
+    if (e == cudaSuccess && a->done) e = cudaEventRecord(a->done, st);
+    return e;
+}
+}  // namespace
+
+int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, int64_t H,
+                                  int64_t Ncap, int64_t d, const int32_t* len, const void* query,
+                                  double fraction, const a2ats_rope_params* rope,
+                                  const void* codebook, int64_t K, void* k_out, int32_t* perm,
+                                  int32_t* count, int32_t* codes, int32_t reuse,
+                                  void* split_done, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
+    if (!rope) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(rope, d, ra))) return st;
+    if (B * H == 0) return A2ATS_OK;
+    if (!count || (Ncap > 0 && (!keys || !perm || !k_out || !codebook || !codes)))
+        return A2ATS_ERR_INVALID_ARG;
+    if ((keys && !aligned16(keys)) || (query && !aligned16(query)) || (perm && !aligned16(perm)) ||
+        (k_out && !aligned16(k_out)) || (codebook && !aligned16(codebook)) ||
+        (codes && !aligned16(codes)))
+        return A2ATS_ERR_ALIGN;
+    // the keys are read again after k_out is written, so they may not share memory
+    if (Ncap > 0 && k_out == keys) return A2ATS_ERR_INVALID_ARG;
+    if (!workspace ||
+        workspace_bytes < a2ats_rope_split_plain_assign_workspace_size(B, H, Ncap, d, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    AssignWs w = carve_assign(c, B, H, Ncap, d, K);
+    SelectWs sw = carve_select(c, B, H, Ncap, d);
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    SplitAfter after{sw.scores, sh, len, fraction, perm, count, (cudaEvent_t)split_done};
+    cudaError_t e;
+    if (Ncap == 0) {
+        e = split_after_natural(&after, s);
+        return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+    }
+    e = launch_prepare_query(keys, query, dtype, sh, len, ra, sw.q, sw.qnorm, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const bool tc = tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30);
+    // one pass over the stored keys serves all three when the far rows are
+    // the keys themselves (far_offset = 0)
+    const bool fused = tc && ra.far_offset == 0;
+    if (!fused) {
+        // the separate passes: RoPE and scores, the split, then plain VQ
+        e = launch_cosine_scores(keys, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, s, k_out,
+                                 dtype);
+        if (e == cudaErrorNotSupported) {
+            e = launch_cosine_scores(keys, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, s);
+            if (e == cudaSuccess) e = launch_windowed_rope(keys, dtype, k_out, dtype, sh, len, ra, s);
+        }
+        if (e == cudaSuccess) e = split_after_natural(&after, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else {
+        // the RoPE window: rotated rows and their scores
+        e = launch_window_scores(keys, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, k_out, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!reuse) {
+        e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, w.tc.Lt, w.cp,
+                                      w.half_norm, tc ? w.tc.chat : nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const RowSel all{A2ATS_ROWS_ALL, nullptr, nullptr};
+    if (tc) {
+        w.tc.prepared = reuse != 0;
+        if (fused) {
+            w.tc.score_q = sw.q;
+            w.tc.score_qn = sw.qnorm;
+            w.tc.scores = sw.scores;
+            w.tc.kcopy = k_out;
+            w.tc.after_natural = split_after_natural;
+            w.tc.after_ctx = &after;
+        }
+        e = assign_on_tensor_cores(w, dtype, sh, len, keys, codebook, K, nullptr, ra, all, codes,
+                                   s);
+    } else {
+        e = launch_assign_exact(keys, dtype, sh, len, ra, all, nullptr, w.cp, w.half_norm, K,
+                                codes, s);
+    }
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
 int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64_t H,
                               int64_t Ncap, const int32_t* len, const int32_t* perm,
                               const int32_t* count, void* stream) {

@@ -72,6 +72,14 @@ struct Params {
     // per 32-centroid group: (max |chat_j|, max h_j) over the group, [H, ngroups]
     const float2* gstat;
     int32_t ngroups;
+    // natural order over stored keys only (else null): the cosine of every
+    // row of the pass with the query of its (b, h), and a copy of the row
+    const float* sq;           // [num_bh, d] fp32 query
+    const float* sqn;          // [num_bh] |query|
+    float* scores;             // [num_bh * out_ncap], or null
+    void* kcopy;               // [num_bh * out_ncap, d] 16-bit, or null
+    int32_t kcopy_tma;         // tiles whose rows are all valid are copied by TMA
+                               // stores through the third tensor map
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -132,6 +140,25 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, uint64_t
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+// Tensor store of one box from shared memory, tracked by the issuing
+// thread's bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y,
+                                             int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(su32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// every committed store has read its shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed store is complete
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -278,13 +305,14 @@ struct Smem {
     static constexpr int kBars = 2 * AST + 2 * BST + 14;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
     static constexpr int kNrmOff = kMergeOff + (kParts - 1) * 2 * 4 * 32 * 16;
-    static constexpr int kTotal = kNrmOff + 2 * kParts * BM * 4 + 1024;  // + alignment slack
+    static constexpr int kQOff = kNrmOff + 2 * kParts * BM * 8;  // [AST][kMaxD] fp32 queries
+    static constexpr int kTotal = kQOff + AST * kMaxD * 4 + 1024;  // + alignment slack
 };
 
 template <bool BF16, int DK, int PA, int AST, int BST>
 __global__ void __launch_bounds__(kThreads, 1)
 assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const Params p) {
+                 const __grid_constant__ CUtensorMap tmK, const Params p) {
     using S = Smem<DK, PA, AST, BST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -306,7 +334,9 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* nrm_full = acc_full + 10;    // [4] one per TMEM lane quarter: row-norm partials
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
-    float* nrm_part = reinterpret_cast<float*>(sm + S::kNrmOff);  // [2][kParts][BM]
+    // [2][kParts][BM] partial (|x|^2, x . q) of each row
+    float2* nrm_part = reinterpret_cast<float2*>(sm + S::kNrmOff);
+    float* smQ = reinterpret_cast<float*>(sm + S::kQOff);  // the tile's query, per A stage
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiles per (b, h): the host's bound, cut to the longest compact list
@@ -358,7 +388,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_empty[sa], ((a_it / AST) & 1) ^ 1, p.status, 1);
                 if (!ok) break;
-                mbar_expect_tx(&a_full[sa], PA * DK * S::kA);
+                mbar_expect_tx(&a_full[sa], PA * DK * S::kA + (p.sq ? p.d * 4 : 0));
                 const int row0 = ti.bh * p.seg + ti.r0;
 #pragma unroll
                 for (int pa = 0; pa < PA; pa++)
@@ -366,6 +396,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     for (int kb = 0; kb < DK; kb++)
                         tma_2d(smA + ((sa * PA + pa) * DK + kb) * S::kA, &tmA, &a_full[sa], kb * BK,
                                (int)(pa * p.plane_rows) + row0);
+                if (p.sq)
+                    asm volatile(
+                        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], "
+                        "[%1], %2, [%3];" ::"r"(su32(smQ + sa * kMaxD)),
+                        "l"(p.sq + (int64_t)ti.bh * p.d), "r"(p.d * 4), "r"(su32(&a_full[sa]))
+                        : "memory");
                 a_it++;
                 const int h = ti.bh % p.H;
                 for (int c = 0; c < p.nchunks && ok; c++) {
@@ -423,6 +459,18 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 4);
                 if (!ok) break;
                 tc_fence_after();
+                // a tile of valid rows only is copied out whole by TMA stores
+                // (rows ti.r0 .. + BM of (b, h) ti.bh; the coordinates are
+                // non-negative and x is a multiple of 64 elements)
+                const bool store = p.kcopy_tma && ti.r0 + BM <= ti.nvalid;
+                if (store) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+                    for (int kb = 0; kb < DK; kb++)
+                        tma_store_3d(&tmK, smA + (sa * PA * DK + kb) * S::kA, kb * BK, ti.r0,
+                                     ti.bh);
+                    bulk_commit();
+                }
                 for (int c = 0; c < p.nchunks && ok; c++) {
                     const int acc = acc_it & 1;
                     ok = mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, p.status, 5);
@@ -456,9 +504,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tc_commit(&acc_full[acc]);
                     acc_it++;
                 }
+                // the stores have read the tile before the stage is released
+                if (store) bulk_wait_read();
                 tc_commit(&a_empty[sa]);
                 a_it++;
             }
+            bulk_wait_all();
         }
     } else {
         // ------------------------------------------------------ epilogue --
@@ -477,10 +528,20 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!ok) break;
             // |x|^2 of this row from the swizzled tile of plane 0: each of the
             // four parts sums a quarter of the row's 16-byte chunks, the
-            // partials meet in shared memory (named barrier of the quarter's
-            // four warps) and every part adds them in the same order
-            float nrm = 0.f;
+            // partials meet in shared memory (an mbarrier per lane quarter)
+            // and every part adds them in the same order.  With scores on,
+            // the same pass takes x . q and copies the row's chunks out.
+            const int32_t ri = ti.r0 + row_in_tile;
+            const bool sc = p.scores != nullptr;
+            float nrm = 0.f, dot = 0.f;
             {
+                // rows of a tile that the TMA stores do not copy
+                const bool by_tma = p.kcopy_tma && ti.r0 + BM <= ti.nvalid;
+                uint8_t* kc = (p.kcopy && !by_tma && ri < ti.nvalid)
+                                  ? reinterpret_cast<uint8_t*>(p.kcopy) +
+                                        ((int64_t)ti.bh * p.out_ncap + ri) * p.d * 2
+                                  : nullptr;
+                const float* qrow = smQ + sa * kMaxD;
 #pragma unroll
                 for (int ci = part * 2 * DK; ci < (part + 1) * 2 * DK; ci++) {
                     const int kb = ci >> 3, c = ci & 7;
@@ -488,6 +549,15 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     {
                         const uint4 raw = *reinterpret_cast<const uint4*>(
                             rowp + 16 * (c ^ (row_in_tile & 7)));
+                        if (kc) __stcs(reinterpret_cast<uint4*>(kc + (kb * 64 + c * 8) * 2), raw);
+                        float qv[8];
+                        if (sc) {
+                            const float4* q4 =
+                                reinterpret_cast<const float4*>(qrow + kb * 64 + c * 8);
+                            const float4 qa = q4[0], qb = q4[1];
+                            qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
+                            qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
+                        }
                         const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
@@ -503,18 +573,34 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             }
                             nrm = fmaf(lo, lo, nrm);
                             nrm = fmaf(hi, hi, nrm);
+                            if (sc) {
+                                dot = fmaf(lo, qv[2 * u], dot);
+                                dot = fmaf(hi, qv[2 * u + 1], dot);
+                            }
                         }
                     }
                 }
-                float* np = nrm_part + (t_it & 1) * kParts * BM;
-                np[part * BM + row_in_tile] = nrm;
+                float2* np = nrm_part + (t_it & 1) * kParts * BM;
+                np[part * BM + row_in_tile] = make_float2(nrm, dot);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&nrm_full[q]);
                 ok = mbar_wait(&nrm_full[q], t_it & 1, p.status, 13);
                 nrm = 0.f;
+                dot = 0.f;
 #pragma unroll
-                for (int pp = 0; pp < kParts; pp++) nrm += np[pp * BM + row_in_tile];
+                for (int pp = 0; pp < kParts; pp++) {
+                    const float2 v = np[pp * BM + row_in_tile];
+                    nrm += v.x;
+                    dot += v.y;
+                }
                 t_it++;
+            }
+            // cosine of the row with its query; 0 when either norm is 0
+            if (ok && sc && part == 1 && ri < ti.nvalid) {
+                const float qn = p.sqn[ti.bh];
+                const float kn = sqrtf(nrm);
+                p.scores[(int64_t)ti.bh * p.out_ncap + ri] =
+                    (kn > 0.f && qn > 0.f) ? dot / (kn * qn) : 0.f;
             }
             if (!ok) break;
             __syncwarp();
@@ -627,7 +713,6 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                 }
                 const float U = fmaxf(gb1 == c1 ? ub2 : ub1, w2);
-                const int32_t ri = ti.r0 + row_in_tile;
                 if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, c1, xn);
             }
             m_it++;
@@ -1089,8 +1174,8 @@ unsigned blocks_for(int64_t n, int per, unsigned cap) {
 }
 
 template <bool BF16, int DK, int PA, int AST, int BST>
-cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                          cudaStream_t st) {
+cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tk,
+                          const Params& p, cudaStream_t st) {
     using S = Smem<DK, PA, AST, BST>;
     static_assert(S::kTotal <= 232448, "shared memory budget");
     auto k = assign_tc_kernel<BF16, DK, PA, AST, BST>;
@@ -1098,28 +1183,28 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const Pa
     if (e != cudaSuccess) return e;
     const int tiles = p.num_bh * p.tiles_per_bh;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    k<<<grid, kThreads, S::kTotal, st>>>(ta, tb, p);
+    k<<<grid, kThreads, S::kTotal, st>>>(ta, tb, tk, p);
     note_launches(1);
     return cudaGetLastError();
 }
 
 template <bool BF16, int PA>
-cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                            cudaStream_t st) {
+cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tk,
+                            const Params& p, cudaStream_t st) {
     if constexpr (PA == 1) {
         switch (p.d) {
-            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 2, 4>(ta, tb, p, st);
-            case 192: return launch_kernel<BF16, 3, PA, 1, 4>(ta, tb, p, st);
-            default: return launch_kernel<BF16, 4, PA, 1, 4>(ta, tb, p, st);
+            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, tk, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 2, 4>(ta, tb, tk, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 4>(ta, tb, tk, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 4>(ta, tb, tk, p, st);
         }
     }
     else {
         switch (p.d) {
-            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, p, st);
-            case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, p, st);
-            default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, p, st);
+            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, tk, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, tk, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, tk, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, tk, p, st);
         }
     }
 }
@@ -1188,7 +1273,8 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
 // are not visited).
 cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, int64_t plane_rows,
                      const int32_t* count, const int32_t* row_map, const uint8_t* skip,
-                     int32_t skip_near, int64_t max_rows, cudaStream_t st) {
+                     int32_t skip_near, int64_t max_rows, cudaStream_t st,
+                     bool with_scores = false) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
     CUtensorMap ta, tb;
@@ -1246,10 +1332,30 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.shr5_mul = 1u << 27;
     p.shl5_mul = 32u;
     p.max_rows = count ? c.exact_count + 2 : nullptr;
+    // scores and the row copy: the stored keys in natural order only
+    const bool sc = with_scores && PA == 1 && !count && !row_map && c.scores;
+    p.sq = sc ? c.score_q : nullptr;
+    p.sqn = sc ? c.score_qn : nullptr;
+    p.scores = sc ? c.scores : nullptr;
+    p.kcopy = sc ? c.kcopy : nullptr;
+    // the copy's tensor map: [nbh][ncap][d] with the A tile's box and
+    // swizzle, so the staged tile is stored as it landed (a 3-d map keeps
+    // every box inside its (b, h))
+    CUtensorMap tk = ta;
+    p.kcopy_tma = 0;
+    if (p.kcopy) {
+        const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)ncap, (cuuint64_t)nbh};
+        const cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(ncap * d * 2)};
+        const cuuint32_t box[3] = {BK, BM, 1};
+        if (encode(&tk, bf16, 3, p.kcopy, dims, strides, box)) p.kcopy_tma = 1;
+        else tk = ta;
+    }
     if (p.num_bh * p.tiles_per_bh == 0) return cudaSuccess;
     if (PA == 1)
-        return bf16 ? launch_by_width<true, 1>(ta, tb, p, st) : launch_by_width<false, 1>(ta, tb, p, st);
-    return bf16 ? launch_by_width<true, 2>(ta, tb, p, st) : launch_by_width<false, 2>(ta, tb, p, st);
+        return bf16 ? launch_by_width<true, 1>(ta, tb, tk, p, st)
+                    : launch_by_width<false, 1>(ta, tb, tk, p, st);
+    return bf16 ? launch_by_width<true, 2>(ta, tb, tk, p, st)
+                : launch_by_width<false, 2>(ta, tb, tk, p, st);
 }
 
 }  // namespace tc
@@ -1313,10 +1419,12 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     if (natural) {
         const int32_t skip_near = (c.ra.enabled && c.ra.window > 0) ? c.ra.window : 0;
         timing_begin(st);
-        e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, ncap, st);
+        e = run_pass(c, rot ? br : bu, 1, c.x, 0, nullptr, nullptr, skip, skip_near, ncap, st,
+                     !rot && !skip);
         timing_end(st);
         if (e != cudaSuccess) return e;
     }
+    if (c.after_natural && (e = c.after_natural(c.after_ctx, st)) != cudaSuccess) return e;
     // rotated rows (the RoPE window, or every routed row) as two 16-bit planes
     if (compact) {
         // rows per (b, h): at most the window (natural order), one (decode),

@@ -42,6 +42,12 @@ cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const
                                  float* scores, cudaStream_t st, void* kout = nullptr,
                                  int out_dt = -1);
 
+// The RoPE window only (rows j in [len - W, len) of each (b, h)): kout
+// <- the rotated rows in the keys' dtype, scores <- their cosine with q.
+cudaError_t launch_window_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
+                                 const RopeArgs& ra, const float* q, const float* qnorm,
+                                 float* scores, void* kout, cudaStream_t st);
+
 // row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)
 cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
                                cudaStream_t st);
@@ -132,6 +138,18 @@ struct TcCall {
     unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
     int32_t* exact_count; // [3]: count, status, longest compact list
     int32_t* head_count;  // [H] listed rows per head (the exact path)
+    // optional, for the pass over the stored keys in natural order (rows
+    // outside the RoPE window, far_offset = 0): the cosine of each row with
+    // score_q of its (b, h) into scores, and a copy of the row into kcopy
+    // (null: not taken)
+    const float* score_q;   // [B*H, d]
+    const float* score_qn;  // [B*H]
+    float* scores;          // [B*H*Ncap]
+    void* kcopy;            // [B*H*Ncap, d], the keys' dtype
+    // optional: launched on the stream right after that pass, before the
+    // rotated rows and the exact path
+    cudaError_t (*after_natural)(void* ctx, cudaStream_t st);
+    void* after_ctx;
 };
 bool tc_supported(int dt, int64_t d);
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st);

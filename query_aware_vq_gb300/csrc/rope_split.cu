@@ -687,6 +687,64 @@ cudaError_t score_dispatch_out(const void* keys, const Shape& s, const int32_t* 
     }
 }
 
+// The RoPE window only: rows j in [len - W, len) of every (b, h), one warp
+// per row.  Each row is rotated at its own position and stored in the
+// keys' dtype (the values windowed_rope_kernel writes), and its cosine with
+// the query goes to scores.  The rows outside the window are left to the
+// pass over the stored keys, which copies them and scores them.
+template <int DT>
+__global__ void __launch_bounds__(kRopeThreads)
+window_score_kernel(const void* __restrict__ keys, int64_t nbh, int32_t H, int32_t ncap,
+                    int32_t d, int32_t win, const int32_t* __restrict__ len, const RopeArgs ra,
+                    const float* __restrict__ q, const float* __restrict__ qnorm,
+                    float* __restrict__ scores, void* __restrict__ kout) {
+    __shared__ float buf[kRopeThreads / 32][kMaxD];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rows = nbh * win;
+    for (int64_t r = (int64_t)blockIdx.x * (kRopeThreads / 32) + w; r < rows;
+         r += (int64_t)gridDim.x * (kRopeThreads / 32)) {
+        const int64_t bh = r / win;
+        const int32_t L = seq_len(len, (int32_t)(bh / H), ncap);
+        const int32_t j = L - win + (int32_t)(r - bh * win);
+        if (j < 0 || j >= L) continue;
+        const int64_t row = bh * ncap + j;
+        float* v = buf[w];
+        for (int i = lane; i < d; i += 32) v[i] = load1<DT>(keys, row * d + i);
+        __syncwarp();
+        const int32_t pos = rope_position(j, L - 1, ra);
+        if (ra.enabled && pos != 0) {
+            const int half = d / 2;
+            for (int i = lane; i < half; i += 32) {
+                const int a = ra.interleaved ? 2 * i : i;
+                const int bb = ra.interleaved ? 2 * i + 1 : i + half;
+                float sn, cs;
+                rope_angle(pos, ra.omega_hi[i], ra.omega_lo[i], ra, sn, cs);
+                const float xa = v[a], xb = v[bb];
+                v[a] = fmaf(xa, cs, -__fmul_rn(xb, sn));
+                v[bb] = fmaf(xa, sn, __fmul_rn(xb, cs));
+            }
+        }
+        __syncwarp();
+        using T = typename Elem<DT>::T;
+        float dot = 0.f, nn = 0.f;
+        for (int i = lane; i < d; i += 32) {
+            reinterpret_cast<T*>(kout)[row * d + i] = from_f32<DT>(v[i]);
+            dot = fmaf(v[i], q[bh * d + i], dot);
+            nn = fmaf(v[i], v[i], nn);
+        }
+        for (int m = 16; m; m >>= 1) {
+            dot += __shfl_xor_sync(0xffffffffu, dot, m);
+            nn += __shfl_xor_sync(0xffffffffu, nn, m);
+        }
+        if (lane == 0) {
+            const float qn = qnorm[bh];
+            const float kn = sqrtf(nn);
+            scores[row] = (kn > 0.f && qn > 0.f) ? dot / (kn * qn) : 0.f;
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_windowed_rope(const void* k_in, int in_dt, void* k_out, int out_dt,
@@ -723,6 +781,29 @@ cudaError_t launch_prepare_query(const void* keys, const void* query, int dt, co
                                                             ra, q_out, qnorm);
                                                             note_launches(1);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_window_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
+                                 const RopeArgs& ra, const float* q, const float* qnorm,
+                                 float* scores, void* kout, cudaStream_t st) {
+    const int64_t nbh = s.B * s.H;
+    const int64_t win = ra.enabled ? (ra.window < s.Ncap ? ra.window : s.Ncap) : 0;
+    if (nbh == 0 || win <= 0) return cudaSuccess;
+    const int grid = grid_for(nbh * win, kRopeThreads / 32);
+    if (dt == kBF16)
+        window_score_kernel<kBF16><<<grid, kRopeThreads, 0, st>>>(
+            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
+            qnorm, scores, kout);
+    else if (dt == kF16)
+        window_score_kernel<kF16><<<grid, kRopeThreads, 0, st>>>(
+            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
+            qnorm, scores, kout);
+    else
+        window_score_kernel<kF32><<<grid, kRopeThreads, 0, st>>>(
+            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
+            qnorm, scores, kout);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -20,11 +20,19 @@ pre-RoPE cache once.
 
 The routing is computed as two halves at the same time.  The caller's
 stream assigns every row by the bulk rule (plain VQ needs neither the split
-nor L); a second stream runs the calibration when it is part of the step,
-steps 3-4, and the retrieval rule on the retrieval rows into a buffer of its
-own.  The caller's stream then waits for the second and copies the
-retrieval rows' codes over the bulk ones (a2ats_copy_retrieval_rows), which
-gives exactly step 5 on the retrieval rows and step 6 on the others.
+nor L) and a second stream the retrieval rows by the retrieval rule into a
+buffer of its own; the caller's stream then waits for the second and copies
+the retrieval rows' codes over the bulk ones (a2ats_copy_retrieval_rows),
+which gives exactly step 5 on the retrieval rows and step 6 on the others.
+
+By default (fused=True) steps 3, 4 and 6 are one call on the caller's
+stream, a2ats_rope_split_plain_assign: with far_offset = 0 the keys outside
+the RoPE window are their own k~, so the pass of the tensor-core assignment
+over them also copies them out and scores them for the split.  The call
+records an event once the split is written, and the second stream (after
+the calibration, when it is part of the step) starts the retrieval rule
+there, while the caller's stream finishes the window rows of step 6.  With
+fused=False the second stream runs steps 3-4 itself, beside step 6.
 
 Steps 1-2 may also run once, ahead of the steps that reuse their L
 (A2ATSStep.calibrate), as the pages do when H is calibrated offline.
@@ -37,7 +45,8 @@ import torch
 
 from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_copy_retrieval_rows,
                a2ats_h_weighted_assign,
-               a2ats_query_aware_assign, a2ats_query_second_moment, a2ats_select_retrieval_set,
+               a2ats_query_aware_assign, a2ats_query_second_moment,
+               a2ats_rope_split_plain_assign, a2ats_select_retrieval_set,
                a2ats_select_retrieval_set_rotated, a2ats_windowed_rope, library)
 
 
@@ -45,8 +54,9 @@ class A2ATSStep:
     def __init__(self, B: int, H: int, N: int, d: int, K: int, dtype: torch.dtype, *,
                  window: int, fraction: float, rope_base: float, far_offset: int = 0,
                  M: int = 0, ridge: float = 1e-4, beta: float = 0.5, interleaved: bool = False,
-                 device="cuda"):
+                 fused: bool = True, device="cuda"):
         self.B, self.H, self.N, self.d, self.K, self.M = B, H, N, d, K, M
+        self.fused = fused
         self.dtype, self.fraction, self.ridge, self.beta = dtype, fraction, ridge, beta
         self.rope = dict(window=window, far_offset=far_offset, rope_base=rope_base,
                          interleaved=interleaved)
@@ -61,7 +71,8 @@ class A2ATSStep:
         self.L = torch.empty((H, d, d), dtype=torch.float32, device=dev)
         self.info = torch.empty((H,), dtype=torch.int32, device=dev)
         ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
-                 lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K))
+                 lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
+                 lib.a2ats_rope_split_plain_assign_workspace_size(B, H, N, d, K))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
         # the split has its own workspace, so the bulk call's codebook side
         # survives from one step to the next
@@ -78,6 +89,10 @@ class A2ATSStep:
         self.calibrated = False
         self._inputs_ready = torch.cuda.Event()
         self._side_done = torch.cuda.Event()
+        # recorded by the library through its handle, which the first record
+        # creates
+        self._split_done = torch.cuda.Event()
+        self._split_done.record(torch.cuda.current_stream(dev))
 
     @staticmethod
     def _stage(events, name, on, fn, *a, **kw):
@@ -139,11 +154,20 @@ class A2ATSStep:
                 raise ValueError("calibrated=True before any calibrate()")
             L = self.L
         in_step = queries is not None or h_given is not None
-        # second stream: steps 3-4 in one pass over the pre-RoPE cache, then
-        # the retrieval rows into a buffer of their own
-        stage("rope_and_split", side, a2ats_select_retrieval_set_rotated, keys, None,
-              self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde, perm=self.perm,
-              count=self.count, workspace=self.split_workspace)
+        if self.fused:
+            # caller's stream: steps 3, 4 and 6 in one call; the second
+            # stream waits for the split only
+            stage("rope_split_bulk", st, a2ats_rope_split_plain_assign, keys, codebook, None,
+                  self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde,
+                  perm=self.perm, count=self.count, codes=self.codes, reuse=reuse_codebook,
+                  split_done=self._split_done, workspace=ws)
+            side.wait_event(self._split_done)
+        else:
+            # second stream: steps 3-4 in one pass over the pre-RoPE cache
+            stage("rope_and_split", side, a2ats_select_retrieval_set_rotated, keys, None,
+                  self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde,
+                  perm=self.perm, count=self.count, workspace=self.split_workspace)
+        # second stream: the retrieval rows into a buffer of their own
         if L is not None:
             stage("assign_retrieval", side, a2ats_h_weighted_assign, keys, codebook, L,
                   lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
@@ -156,10 +180,13 @@ class A2ATSStep:
                   self.beta, lengths=lengths, rope=self.rope, rows="retrieval", perm=self.perm,
                   count=self.count, codes=self.codes_retrieval, workspace=sws)
         self._side_done.record(side)
-        # caller's stream: the bulk rule over every row (it needs no split),
-        # then the retrieval rows' codes over it
-        stage("assign_bulk", st, a2ats_h_weighted_assign, keys, codebook, None, lengths=lengths,
-              rope=self.rope, rows="all", codes=self.codes, workspace=ws, reuse=reuse_codebook)
+        if not self.fused:
+            # caller's stream: the bulk rule over every row (it needs no
+            # split)
+            stage("assign_bulk", st, a2ats_h_weighted_assign, keys, codebook, None,
+                  lengths=lengths, rope=self.rope, rows="all", codes=self.codes, workspace=ws,
+                  reuse=reuse_codebook)
+        # the retrieval rows' codes over the bulk ones
         st.wait_event(self._side_done)
         stage("route", st, a2ats_copy_retrieval_rows, self.codes_retrieval, self.codes,
               self.perm, self.count, lengths=lengths)

@@ -116,6 +116,32 @@ def test_rotated_split_validation(lib):
              FAKE, None, 0, None) == -6
 
 
+def test_rope_split_plain_assign_validation(lib):
+    f = lib.a2ats_rope_split_plain_assign
+    rope = q.RopeParams(64, 0, 500000.0, 0)
+    ws = 1 << 30
+
+    def call(keys=FAKE, dt=1, K=256, k_out=FAKE + 4096, codes=FAKE + 8192, rp=rope, frac=0.2,
+             ws_ptr=FAKE, nb=ws, codebook=FAKE + 12288):
+        return f(keys, dt, 1, 2, 64, 128, None, None, frac,
+                 ctypes.byref(rp) if rp is not None else None, codebook, K, k_out, FAKE, FAKE,
+                 codes, 0, None, ws_ptr, nb, None)
+
+    assert call(rp=None) == -1                 # rope is required
+    assert call(k_out=FAKE) == -1              # k_out may not alias keys
+    assert call(dt=7) == -3
+    assert call(K=0) == -2
+    assert call(frac=-0.1) == -1
+    assert call(codes=None) == -1
+    assert call(codebook=FAKE + 12290) == -4   # misaligned codebook
+    assert call(ws_ptr=None, nb=0) == -6
+    # the workspace holds both the assignment's and the split's
+    need = lib.a2ats_rope_split_plain_assign_workspace_size(1, 2, 64, 128, 256)
+    assert need > lib.a2ats_h_weighted_assign_workspace_size(1, 2, 64, 128, 256)
+    assert need > lib.a2ats_select_retrieval_set_workspace_size(1, 2, 64, 128)
+    assert call(nb=need - 1) == -6
+
+
 def test_copy_retrieval_rows_validation(lib):
     f = lib.a2ats_copy_retrieval_rows
     assert f(FAKE, FAKE, -1, 2, 10, None, FAKE, FAKE, None) == -2

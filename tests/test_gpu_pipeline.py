@@ -22,12 +22,12 @@ def _oracle_L(Q, ridge):
     return l.astype(np.float32).astype(np.float64)
 
 
-def _run(w, rows_sample=None, beta_path=False, seed=0):
+def _run(w, rows_sample=None, beta_path=False, seed=0, fused=True):
     k, c = synth.keys(w), synth.codebook(w)
     Q = None if beta_path else synth.queries(w)
     step = A2ATSStep(w.B, w.H, w.N, w.d, w.K, synth.DTYPES[w.dtype], window=w.W,
                      fraction=w.fraction, rope_base=w.rope_base, far_offset=w.far_offset,
-                     M=w.M, ridge=w.ridge, beta=w.betas[-1])
+                     M=w.M, ridge=w.ridge, beta=w.betas[-1], fused=fused)
     kd, cd = dev(k), dev(c)
     step(kd, cd, queries=dev(Q) if Q is not None else None)
     torch.cuda.synchronize()
@@ -62,13 +62,40 @@ def _run(w, rows_sample=None, beta_path=False, seed=0):
     return step
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("beta_path", [False, True])
-def test_step_tiny(beta_path):
-    _run(synth.WORKLOADS["tiny"], beta_path=beta_path)
+def test_step_tiny(beta_path, fused):
+    _run(synth.WORKLOADS["tiny"], beta_path=beta_path, fused=fused)
 
 
-def test_step_llama32_3b_layer_sampled():
-    _run(synth.WORKLOADS["llama32_3b_layer"], rows_sample=1024)
+@pytest.mark.parametrize("fused", [True, False])
+def test_step_llama32_3b_layer_sampled(fused):
+    _run(synth.WORKLOADS["llama32_3b_layer"], rows_sample=1024, fused=fused)
+
+
+@pytest.mark.parametrize("beta_path", [False, True])
+def test_step_bf16_small(beta_path):
+    """A bf16 step small enough to check every row: the one-call RoPE, split
+    and plain VQ on the tensor cores, ragged tiles, the window rows."""
+    w = synth.scaled(synth.WORKLOADS["llama32_3b_layer"], H=2, N=3001, K=300, W=200, M=512)
+    _run(w, beta_path=beta_path)
+
+
+def test_fused_and_separate_compositions_agree():
+    """The fused composition (RoPE, split and plain VQ in one call, the
+    retrieval rule after the split) and the separate one (RoPE and split on
+    the second stream beside plain VQ) write the same step."""
+    w = synth.scaled(synth.WORKLOADS["llama32_3b_layer"], H=4, N=8192, M=1024)
+    k, c, Q = dev(synth.keys(w)), dev(synth.codebook(w)), dev(synth.queries(w))
+    outs = []
+    for fused in (True, False):
+        step = A2ATSStep(w.B, w.H, w.N, w.d, w.K, torch.bfloat16, window=w.W,
+                         fraction=w.fraction, rope_base=w.rope_base, M=w.M, fused=fused)
+        step(k, c, queries=Q)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (step.k_tilde, step.count, step.perm, step.codes)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_step_is_deterministic():
