@@ -604,13 +604,13 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
         e = split_after_natural(&after, s);
         return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
     }
-    e = launch_prepare_query(keys, query, dtype, sh, len, ra, sw.q, sw.qnorm, s);
-    if (e != cudaSuccess) return cuda_fail(e);
     const bool tc = tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30);
     // one pass over the stored keys serves all three when the far rows are
     // the keys themselves (far_offset = 0)
     const bool fused = tc && ra.far_offset == 0;
     if (!fused) {
+        e = launch_prepare_query(keys, query, dtype, sh, len, ra, sw.q, sw.qnorm, s);
+        if (e != cudaSuccess) return cuda_fail(e);
         // the separate passes: RoPE and scores, the split, then plain VQ
         e = launch_cosine_scores(keys, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, s, k_out,
                                  dtype);
@@ -621,8 +621,9 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
         if (e == cudaSuccess) e = split_after_natural(&after, s);
         if (e != cudaSuccess) return cuda_fail(e);
     } else {
-        // the RoPE window: rotated rows and their scores
-        e = launch_window_scores(keys, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, k_out, s);
+        // the query, and the RoPE window: rotated rows and their scores
+        e = launch_window_scores(keys, query, dtype, sh, len, ra, sw.q, sw.qnorm, sw.scores, k_out,
+                                 s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (!reuse) {

@@ -42,10 +42,12 @@ cudaError_t launch_cosine_scores(const void* keys, int dt, const Shape& s, const
                                  float* scores, cudaStream_t st, void* kout = nullptr,
                                  int out_dt = -1);
 
-// The RoPE window only (rows j in [len - W, len) of each (b, h)): kout
-// <- the rotated rows in the keys' dtype, scores <- their cosine with q.
-cudaError_t launch_window_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
-                                 const RopeArgs& ra, const float* q, const float* qnorm,
+// The query of each (b, h) into q / qnorm (exactly what launch_prepare_query
+// writes) and the RoPE window only (rows j in [len - W, len) of each
+// (b, h)): kout <- the rotated rows in the keys' dtype, scores <- their
+// cosine with the query.  cudaErrorNotSupported when d % 16 != 0.
+cudaError_t launch_window_scores(const void* keys, const void* query, int dt, const Shape& s,
+                                 const int32_t* len, const RopeArgs& ra, float* q, float* qnorm,
                                  float* scores, void* kout, cudaStream_t st);
 
 // row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)

@@ -687,61 +687,133 @@ cudaError_t score_dispatch_out(const void* keys, const Shape& s, const int32_t* 
     }
 }
 
-// The RoPE window only: rows j in [len - W, len) of every (b, h), one warp
-// per row.  Each row is rotated at its own position and stored in the
-// keys' dtype (the values windowed_rope_kernel writes), and its cosine with
-// the query goes to scores.  The rows outside the window are left to the
-// pass over the stored keys, which copies them and scores them.
-template <int DT>
+// The RoPE window only, with the query: blocks (x, bh) of a (b, h) first
+// form its query as prepare_query_kernel does (the first 128 threads, the
+// same order of operations, so the values are the same) and block x = 0
+// stores it; then each block takes window rows j in [len - W, len), lpr
+// lanes per row as in cosine_score_kernel: the row rotated at its own
+// position is stored in the keys' dtype (the values windowed_rope_kernel
+// writes) and its cosine with the query goes to scores.  The rows outside
+// the window are left to the pass over the stored keys, which copies them
+// and scores them.
+template <int DT, bool INTERLEAVED>
 __global__ void __launch_bounds__(kRopeThreads)
-window_score_kernel(const void* __restrict__ keys, int64_t nbh, int32_t H, int32_t ncap,
-                    int32_t d, int32_t win, const int32_t* __restrict__ len, const RopeArgs ra,
-                    const float* __restrict__ q, const float* __restrict__ qnorm,
+window_score_kernel(const void* __restrict__ keys, const void* __restrict__ query, int32_t H,
+                    int32_t ncap, int32_t d, int32_t win, const int32_t* __restrict__ len,
+                    const RopeArgs ra, float* __restrict__ q_out, float* __restrict__ qnorm_out,
                     float* __restrict__ scores, void* __restrict__ kout) {
-    __shared__ float buf[kRopeThreads / 32][kMaxD];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t rows = nbh * win;
-    for (int64_t r = (int64_t)blockIdx.x * (kRopeThreads / 32) + w; r < rows;
-         r += (int64_t)gridDim.x * (kRopeThreads / 32)) {
-        const int64_t bh = r / win;
-        const int32_t L = seq_len(len, (int32_t)(bh / H), ncap);
-        const int32_t j = L - win + (int32_t)(r - bh * win);
-        if (j < 0 || j >= L) continue;
-        const int64_t row = bh * ncap + j;
-        float* v = buf[w];
-        for (int i = lane; i < d; i += 32) v[i] = load1<DT>(keys, row * d + i);
-        __syncwarp();
-        const int32_t pos = rope_position(j, L - 1, ra);
-        if (ra.enabled && pos != 0) {
-            const int half = d / 2;
-            for (int i = lane; i < half; i += 32) {
-                const int a = ra.interleaved ? 2 * i : i;
-                const int bb = ra.interleaved ? 2 * i + 1 : i + half;
-                float sn, cs;
-                rope_angle(pos, ra.omega_hi[i], ra.omega_lo[i], ra, sn, cs);
-                const float xa = v[a], xb = v[bb];
-                v[a] = fmaf(xa, cs, -__fmul_rn(xb, sn));
-                v[bb] = fmaf(xa, sn, __fmul_rn(xb, cs));
+    __shared__ __align__(16) float qv[kMaxD];
+    __shared__ Dot2 red[4];
+    __shared__ float qn_s;
+    __shared__ float2 part[kRopeThreads];
+    const int bh = blockIdx.y;
+    const int32_t L = seq_len(len, bh / H, ncap);
+    const int tid = threadIdx.x;
+    // ---- the query (threads 0..127)
+    if (tid < 128) {
+        if (query) {
+            for (int i = tid; i < d; i += 128) qv[i] = load1<DT>(query, (int64_t)bh * d + i);
+        } else if (L == 0) {
+            for (int i = tid; i < d; i += 128) qv[i] = 0.f;
+        } else {
+            const int64_t row = ((int64_t)bh * ncap + (L - 1)) * d;
+            for (int i = tid; i < d; i += 128) qv[i] = load1<DT>(keys, row + i);
+        }
+    }
+    __syncthreads();
+    if (!query && L > 0 && ra.enabled) {
+        const int32_t pos = rope_position(L - 1, L - 1, ra);
+        const int half = d / 2;
+        float a = 0.f, bv = 0.f;
+        int ia = 0, ib = 0;
+        if (tid < half) {
+            ia = ra.interleaved ? 2 * tid : tid;
+            ib = ra.interleaved ? 2 * tid + 1 : tid + half;
+            a = qv[ia];
+            bv = qv[ib];
+        }
+        __syncthreads();
+        if (tid < half && pos != 0) {
+            float sn, cs;
+            rope_angle(pos, ra.omega_hi[tid], ra.omega_lo[tid], ra, sn, cs);
+            qv[ia] = fmaf(a, cs, -__fmul_rn(bv, sn));
+            qv[ib] = fmaf(a, sn, __fmul_rn(bv, cs));
+        }
+        __syncthreads();
+    }
+    if (tid < 128) {
+        Dot2 acc;
+        for (int i = tid; i < d; i += 128) {
+            if (blockIdx.x == 0) q_out[(int64_t)bh * d + i] = qv[i];
+            acc.add_prod(qv[i], qv[i]);
+        }
+        for (int m = 16; m; m >>= 1) acc.merge(shfl_xor(acc, m));
+        if ((tid & 31) == 0) red[tid >> 5] = acc;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        Dot2 t = red[0];
+        for (int w = 1; w < 4; w++) t.merge(red[w]);
+        qn_s = sqrtf(t.value());
+        if (blockIdx.x == 0) qnorm_out[bh] = qn_s;
+    }
+    __syncthreads();
+    const float qn = qn_s;
+
+    // ---- the window rows of this block
+    const int lpr = INTERLEAVED ? d / 8 : d / 16;
+    const int rpb = kRopeThreads / lpr;
+    const int lane = tid % lpr, rl = tid / lpr;
+    const bool active = tid < rpb * lpr;
+    const int e0 = lane * 8, e1 = e0 + d / 2;
+    const int pair0 = INTERLEAVED ? e0 / 2 : e0;
+    const int32_t j0 = L - win;  // window rows are j0 + i, i in [0, win), kept if j >= 0
+    for (int base = blockIdx.x * rpb; base < win; base += gridDim.x * rpb) {
+        const int32_t j = j0 + base + rl;
+        const bool valid = active && base + rl < win && j >= 0 && j < L;
+        const int64_t row = (int64_t)bh * ncap + j;
+        float dot = 0.f, nn = 0.f;
+        if (valid) {
+            float v0[8], v1[8];
+            load8<DT>(keys, row * d + e0, v0);
+            if (!INTERLEAVED) load8<DT>(keys, row * d + e1, v1);
+            const int32_t pos = rope_position(j, L - 1, ra);
+            if (ra.enabled && pos != 0) {
+                float c[8], sn[8];
+                angles8<INTERLEAVED>(pos, pair0, ra, c, sn);
+                rotate8<INTERLEAVED>(v0, v1, c, sn);
+            }
+            store8<DT>(kout, row * d + e0, v0);
+            if (!INTERLEAVED) store8<DT>(kout, row * d + e1, v1);
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                dot = fmaf(v0[k], qv[e0 + k], dot);
+                nn = fmaf(v0[k], v0[k], nn);
+            }
+            if (!INTERLEAVED) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    dot = fmaf(v1[k], qv[e1 + k], dot);
+                    nn = fmaf(v1[k], v1[k], nn);
+                }
             }
         }
-        __syncwarp();
-        using T = typename Elem<DT>::T;
-        float dot = 0.f, nn = 0.f;
-        for (int i = lane; i < d; i += 32) {
-            reinterpret_cast<T*>(kout)[row * d + i] = from_f32<DT>(v[i]);
-            dot = fmaf(v[i], q[bh * d + i], dot);
-            nn = fmaf(v[i], v[i], nn);
+        part[tid] = make_float2(dot, nn);
+        __syncthreads();
+        if (tid < rpb) {
+            const int32_t jj = j0 + base + tid;
+            if (base + tid < win && jj >= 0 && jj < L) {
+                float dd = 0.f, n2 = 0.f;
+                for (int i = 0; i < lpr; i++) {
+                    const float2 pp = part[tid * lpr + i];
+                    dd += pp.x;
+                    n2 += pp.y;
+                }
+                const float kn = sqrtf(n2);
+                scores[(int64_t)bh * ncap + jj] = (kn > 0.f && qn > 0.f) ? dd / (kn * qn) : 0.f;
+            }
         }
-        for (int m = 16; m; m >>= 1) {
-            dot += __shfl_xor_sync(0xffffffffu, dot, m);
-            nn += __shfl_xor_sync(0xffffffffu, nn, m);
-        }
-        if (lane == 0) {
-            const float qn = qnorm[bh];
-            const float kn = sqrtf(nn);
-            scores[row] = (kn > 0.f && qn > 0.f) ? dot / (kn * qn) : 0.f;
-        }
-        __syncwarp();
+        __syncthreads();
     }
 }
 
@@ -784,25 +856,36 @@ cudaError_t launch_prepare_query(const void* keys, const void* query, int dt, co
     return cudaGetLastError();
 }
 
-cudaError_t launch_window_scores(const void* keys, int dt, const Shape& s, const int32_t* len,
-                                 const RopeArgs& ra, const float* q, const float* qnorm,
+cudaError_t launch_window_scores(const void* keys, const void* query, int dt, const Shape& s,
+                                 const int32_t* len, const RopeArgs& ra, float* q, float* qnorm,
                                  float* scores, void* kout, cudaStream_t st) {
     const int64_t nbh = s.B * s.H;
     const int64_t win = ra.enabled ? (ra.window < s.Ncap ? ra.window : s.Ncap) : 0;
-    if (nbh == 0 || win <= 0) return cudaSuccess;
-    const int grid = grid_for(nbh * win, kRopeThreads / 32);
-    if (dt == kBF16)
-        window_score_kernel<kBF16><<<grid, kRopeThreads, 0, st>>>(
-            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
-            qnorm, scores, kout);
-    else if (dt == kF16)
-        window_score_kernel<kF16><<<grid, kRopeThreads, 0, st>>>(
-            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
-            qnorm, scores, kout);
-    else
-        window_score_kernel<kF32><<<grid, kRopeThreads, 0, st>>>(
-            keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, (int32_t)win, len, ra, q,
-            qnorm, scores, kout);
+    const int d = (int)s.d;
+    if (nbh == 0) return cudaSuccess;
+    if (d % 16 != 0 || d > kMaxD) return cudaErrorNotSupported;
+    const bool il = ra.enabled && ra.interleaved;
+    const int rpb = kRopeThreads / (il ? d / 8 : d / 16);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t per = (win + rpb - 1) / rpb;
+    const int64_t cap = (4 * (int64_t)sms + nbh - 1) / nbh;
+    if (per > cap) per = cap;
+    if (per < 1) per = 1;
+    const dim3 g((unsigned)per, (unsigned)nbh);
+#define A2ATS_WIN(DT, IL)                                                                      \
+    window_score_kernel<DT, IL><<<g, kRopeThreads, 0, st>>>(keys, query, (int32_t)s.H,         \
+                                                            (int32_t)s.Ncap, d, (int32_t)win,  \
+                                                            len, ra, q, qnorm, scores, kout)
+    if (dt == kBF16) {
+        if (il) A2ATS_WIN(kBF16, true); else A2ATS_WIN(kBF16, false);
+    } else if (dt == kF16) {
+        if (il) A2ATS_WIN(kF16, true); else A2ATS_WIN(kF16, false);
+    } else {
+        if (il) A2ATS_WIN(kF32, true); else A2ATS_WIN(kF32, false);
+    }
+#undef A2ATS_WIN
     note_launches(1);
     return cudaGetLastError();
 }
