@@ -159,6 +159,7 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.skip = c.take<uint8_t>(rows);
     w.tc.exact_list = c.take<int64_t>(rows);
     w.tc.exact_best = c.take<unsigned long long>(rows);
+    w.tc.exact_done = c.take<int32_t>(rows);
     w.tc.exact_count = c.take<int32_t>(4);
     w.tc.head_count = c.take<int32_t>((size_t)H);
     return w;

@@ -966,7 +966,7 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
 }
 
 // ------------------------------------------------------ exact list kernels --
-// Rows the contraction could not decide, in three short launches so that a
+// Rows the contraction could not decide, in two short launches so that a
 // handful of rows still spreads over the whole GPU:
 //   exact_rows_kernel   one block per listed row: windowed RoPE in fp32 and
 //                       z = x L (compensated) into zbuf; best <- +inf; the
@@ -976,8 +976,8 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
 //                       once and every row of the chunk takes the direct
 //                       distance sum_b (z_b - cp_jb)^2 to each cp_j = c_j L;
 //                       a 64-bit atomicMin on (distance bits, j) merges the
-//                       slices, so ties go to the lowest index
-//   exact_write_kernel  codes <- the index half of best
+//                       slices, so ties go to the lowest index, and the
+//                       slice that finishes a row last writes its code
 constexpr int kExactThreads = 256;
 constexpr int kScanCents = 128;  // centroids per scan block (8 warps x 16)
 
@@ -987,8 +987,8 @@ exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
                   const int32_t* __restrict__ len, const RopeArgs ra, const float* __restrict__ L,
                   const int64_t* __restrict__ list, const int32_t* __restrict__ list_count,
                   float* __restrict__ zbuf, unsigned long long* __restrict__ best,
-                  int32_t* __restrict__ head_count, int32_t* __restrict__ head_rows,
-                  int64_t head_cap) {
+                  int32_t* __restrict__ done, int32_t* __restrict__ head_count,
+                  int32_t* __restrict__ head_rows, int64_t head_cap) {
     __shared__ __align__(16) float xv[kMaxD];
     __shared__ Dot2 part[kExactThreads];
     const int tid = threadIdx.x;
@@ -1046,25 +1046,35 @@ exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
         }
         if (tid == 0) {
             best[e] = ~0ull;
+            done[e] = 0;
             head_rows[h * head_cap + atomicAdd(head_count + h, 1)] = e;
         }
         __syncthreads();
     }
 }
 
-constexpr int kScanRows = 8;   // rows of a head per chunk: one per warp
+constexpr int kScanRows = 16;  // rows of a head per chunk: two per warp
 
 // The slice [j0, j0 + S) of head h's cp is staged transposed, cT[a][c] with a
-// padded stride S + 1 (conflict-free both when it is written along a and when
-// lanes read along c).  Each warp takes rows of the chunk; lane l owns
-// centroids l, l + 32, ... of the slice.
+// padded stride S + 1 (few bank conflicts when it is written along a, none
+// when lanes read along c).  Each warp takes two rows of the chunk at a time
+// (rows w and w + 8), so every centroid value read from shared memory serves
+// both; lane l owns centroids l, l + 32, ... of the slice, in pairs
+// (l + 64 m, l + 64 m + 32) whose differences and squares run as packed
+// two-float instructions (each rounded as the scalar one).  The row's code is
+// written by the slice block that adds the last of the gridDim.x partial
+// minima (a counter per row).
 template <int S>
 __global__ void __launch_bounds__(kExactThreads)
 exact_scan_kernel(int32_t d, const float* __restrict__ cp, int64_t K,
                   const int32_t* __restrict__ head_count, const int32_t* __restrict__ head_rows,
                   int64_t head_cap, const float* __restrict__ zbuf,
-                  unsigned long long* __restrict__ best) {
-    extern __shared__ float cT[];  // [d][S + 1], then [warps][d] for the rows' z
+                  unsigned long long* __restrict__ best, int32_t* __restrict__ done,
+                  const int64_t* __restrict__ list, int32_t* __restrict__ codes) {
+    static_assert(S % 64 == 0, "centroids come in pairs of lanes' columns");
+    constexpr int kWarps = kExactThreads / 32;
+    static_assert(kScanRows == 2 * kWarps, "two rows per warp");
+    extern __shared__ float cT[];  // [d][S + 1], then [warps][2][d] for the rows' z
     const int h = blockIdx.y;
     const int64_t j0 = (int64_t)blockIdx.x * S;
     const int n = head_count[h];
@@ -1098,53 +1108,71 @@ exact_scan_kernel(int32_t d, const float* __restrict__ cp, int64_t K,
     }
     __syncthreads();
     const int32_t* rows = head_rows + (int64_t)h * head_cap;
-    float* zs = cT + d * (S + 1) + w * d;  // this warp's row, staged once
+    float* zs0 = cT + d * (S + 1) + 2 * w * d;  // this warp's two rows, staged once
+    float* zs1 = zs0 + d;
+    const float2 neg1 = make_float2(-1.f, -1.f);
     for (int chunk = blockIdx.z; chunk < nchunks; chunk += gridDim.z) {
         const int r_end = min(n, (chunk + 1) * kScanRows);
-        for (int r = chunk * kScanRows + w; r < r_end; r += kExactThreads / 32) {
-            const int64_t e = rows[r];
-            for (int a = lane; a < d; a += 32) zs[a] = __ldg(zbuf + e * d + a);
-            __syncwarp();
-            float acc[S / 32];
+        const int r0 = chunk * kScanRows + w, r1 = r0 + kWarps;
+        if (r0 >= r_end) continue;
+        const bool two = r1 < r_end;
+        const int64_t e0 = rows[r0];
+        const int64_t e1 = two ? rows[r1] : e0;
+        for (int a = lane; a < d; a += 32) {
+            zs0[a] = __ldg(zbuf + e0 * d + a);
+            zs1[a] = __ldg(zbuf + e1 * d + a);
+        }
+        __syncwarp();
+        // acc[r][m] = distances of row r to l + 64 m and l + 64 m + 32
+        float2 acc0[S / 64], acc1[S / 64];
 #pragma unroll
-            for (int k = 0; k < S / 32; k++) acc[k] = 0.f;
+        for (int m = 0; m < S / 64; m++) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
 #pragma unroll 4
-            for (int a = 0; a < d; a++) {
-                const float za = zs[a];
-                const float* col = cT + a * (S + 1) + lane;
+        for (int a = 0; a < d; a++) {
+            const float2 za0 = make_float2(zs0[a], zs0[a]);
+            const float2 za1 = make_float2(zs1[a], zs1[a]);
+            const float* col = cT + a * (S + 1) + lane;
 #pragma unroll
-                for (int k = 0; k < S / 32; k++) {
-                    const float t = za - col[32 * k];
-                    acc[k] = fmaf(t, t, acc[k]);
-                }
+            for (int m = 0; m < S / 64; m++) {
+                const float2 cv = make_float2(col[64 * m], col[64 * m + 32]);
+                const float2 t0 = __ffma2_rn(cv, neg1, za0);  // za - c, exact negation
+                const float2 t1 = __ffma2_rn(cv, neg1, za1);
+                acc0[m] = __ffma2_rn(t0, t0, acc0[m]);
+                acc1[m] = __ffma2_rn(t1, t1, acc1[m]);
             }
-            __syncwarp();  // zs is rewritten by the warp's next row
+        }
+        __syncwarp();  // zs is rewritten by the warp's next rows
+#pragma unroll
+        for (int rr = 0; rr < 2; rr++) {
+            if (rr == 1 && !two) break;
+            const float2* acc = rr == 0 ? acc0 : acc1;
+            const int64_t e = rr == 0 ? e0 : e1;
             float bv = INFINITY;
             int32_t bj = 0;
 #pragma unroll
-            for (int k = 0; k < S / 32; k++)
-                if (lane + 32 * k < nc && acc[k] < bv) {  // ascending j: strict < keeps the lowest
-                    bv = acc[k];
-                    bj = (int32_t)(j0 + lane + 32 * k);
+            for (int k = 0; k < S / 32; k++) {  // ascending j: strict < keeps the lowest
+                const float v = (k & 1) ? acc[k >> 1].y : acc[k >> 1].x;
+                const int c = lane + 32 * k;
+                if (c < nc && v < bv) {
+                    bv = v;
+                    bj = (int32_t)(j0 + c);
                 }
+            }
             for (int m = 16; m; m >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
                 const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
                 if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
             }
-            if (lane == 0 && bv < INFINITY)
-                atomicMin(best + e, ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
+            if (lane == 0) {
+                if (bv < INFINITY)
+                    atomicMin(best + e,
+                              ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
+                __threadfence();
+                if (atomicAdd(done + e, 1) == (int)gridDim.x - 1)
+                    codes[list[e]] = (int32_t)(uint32_t)(atomicOr(best + e, 0ull) & 0xffffffffull);
+            }
         }
     }
-}
-
-__global__ void exact_write_kernel(const int64_t* __restrict__ list,
-                                   const int32_t* __restrict__ list_count,
-                                   const unsigned long long* __restrict__ best,
-                                   int32_t* __restrict__ codes) {
-    const int n = *list_count;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n; e += gridDim.x * blockDim.x)
-        codes[list[e]] = (int32_t)(uint32_t)(best[e] & 0xffffffffull);
 }
 
 // ------------------------------------------------------------ host side --
@@ -1432,7 +1460,9 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         const int cmode = c.sel.mode == 2 ? 0 : c.sel.mode;
         const int64_t most = cmode == 0 ? (c.ra.window < ncap ? c.ra.window : ncap)
                                         : (cmode == 3 ? 1 : ncap);
-        const int64_t per_bh = 4 * (int64_t)sm_count() / (nbh > 0 ? nbh : 1);
+        // one warp per row when the grid allows (each warp's rows run one
+        // after another, each a chain of a load, the rotation and stores)
+        const int64_t per_bh = 16 * (int64_t)sm_count() / (nbh > 0 ? nbh : 1);
         dim3 g(blocks_for(most, 8, (unsigned)(per_bh > 1 ? per_bh : 1)), (unsigned)nbh);
         if (c.dt == kBF16)
             compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
@@ -1456,24 +1486,30 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     if (c.dt == kBF16)
         exact_rows_kernel<kBF16><<<sms * 4, kExactThreads, 0, st>>>(
             c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
-            c.exact_count, zbuf, c.exact_best, c.head_count, head_rows, head_cap);
+            c.exact_count, zbuf, c.exact_best, c.exact_done, c.head_count, head_rows, head_cap);
     else
         exact_rows_kernel<kF16><<<sms * 4, kExactThreads, 0, st>>>(
             c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.L, c.exact_list,
-            c.exact_count, zbuf, c.exact_best, c.head_count, head_rows, head_cap);
+            c.exact_count, zbuf, c.exact_best, c.exact_done, c.head_count, head_rows, head_cap);
     {
         // slices of 128 centroids (64 at d > 128) keep the staged slice near 66 KB
         const int S = d <= 128 ? 128 : 64;
-        const size_t smem = sizeof(float) * (size_t)d * (S + 1 + kExactThreads / 32);
+        const size_t smem = sizeof(float) * (size_t)d * (S + 1 + 2 * (kExactThreads / 32));
         auto scan = S == 128 ? exact_scan_kernel<128> : exact_scan_kernel<64>;
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        dim3 g((unsigned)((K + S - 1) / S), (unsigned)H, 8);
+        // chunks of a head's rows run side by side in z: up to 32 (8 at the
+        // least), within about 8192 blocks in all (the blocks past a head's
+        // last chunk leave at once)
+        const int64_t slices = (K + S - 1) / S;
+        int64_t zc = 8192 / (slices * H);
+        zc = zc < 8 ? 8 : (zc > 32 ? 32 : zc);
+        dim3 g((unsigned)slices, (unsigned)H, (unsigned)zc);
         scan<<<g, kExactThreads, smem, st>>>((int32_t)d, c.cp, K, c.head_count, head_rows, head_cap,
-                                             zbuf, c.exact_best);
+                                             zbuf, c.exact_best, c.exact_done, c.exact_list,
+                                             c.codes);
     }
-    exact_write_kernel<<<sms, 256, 0, st>>>(c.exact_list, c.exact_count, c.exact_best, c.codes);
-    note_launches(3);
+    note_launches(2);
     return cudaGetLastError();
 }
 

@@ -138,6 +138,7 @@ struct TcCall {
     uint8_t* skip;        // [B*H*Ncap]
     int64_t* exact_list;  // [B*H*Ncap]
     unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
+    int32_t* exact_done;  // [B*H*Ncap] centroid slices finished per listed row
     int32_t* exact_count; // [3]: count, status, longest compact list
     int32_t* head_count;  // [H] listed rows per head (the exact path)
     // optional, for the pass over the stored keys in natural order (rows

@@ -466,11 +466,17 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint32_t ks[];  // [kSelCache] ordered keys of the segment
-    __shared__ uint32_t hist[256];
+    // per-pass histogram the cluster reads, alternating between two buffers:
+    // the one a pass fills was last read by the other CTAs two passes
+    // earlier, before the cluster barrier of the previous pass
+    __shared__ uint32_t hist[2][256];
+    // per-warp histograms: a pass's keys crowd into few digits, so each warp
+    // counts on its own copy
+    __shared__ uint32_t hist_w[kSelThreads / 32][256];
     __shared__ uint32_t tot[256];
     __shared__ int seg_counts[2];     // this CTA's rows above the threshold, equal to it
     __shared__ int warp_tot[65];
-    __shared__ uint32_t sel_prefix, sel_need;
+    __shared__ uint32_t sel_prefix, sel_need, sel_all;
     const int rank = (int)cluster.block_rank();
     const int bh = blockIdx.x / kSelCluster;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -496,25 +502,35 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
 
     uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
     if (partial) {
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+        int pass = 0;
+        for (int shift = 24; shift >= 0; shift -= 8, pass++) {
+            uint32_t* hb = hist[pass & 1];
+            uint32_t* hw = &hist_w[0][0];
+            for (int i = tid; i < (kSelThreads / 32) * 256; i += blockDim.x) hw[i] = 0;
             __syncthreads();
             for (int i = tid; i < m; i += blockDim.x) {
                 const uint32_t u = key(i);
-                if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+                if ((u & mask) == prefix) atomicAdd(&hist_w[w][(u >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid < 256) {
+                uint32_t t = 0;
+#pragma unroll
+                for (int ww = 0; ww < kSelThreads / 32; ww++) t += hist_w[ww][tid];
+                hb[tid] = t;
             }
             cluster.sync();
             // every CTA sums the cluster's histograms and takes the same digit
             if (tid < 256) {
                 uint32_t part[kSelCluster];
 #pragma unroll
-                for (int r = 0; r < kSelCluster; r++) part[r] = cluster.map_shared_rank(hist, r)[tid];
+                for (int r = 0; r < kSelCluster; r++) part[r] = cluster.map_shared_rank(hb, r)[tid];
                 uint32_t t = 0;
 #pragma unroll
                 for (int r = 0; r < kSelCluster; r++) t += part[r];
                 tot[tid] = t;
             }
-            cluster.sync();  // no CTA resets its histogram while another reads it
+            __syncthreads();
             if (w == 0) {
                 // lane l holds digits 255 - 8l ... 248 - 8l (descending);
                 // suffix sums from the top digit find the one holding the
@@ -539,6 +555,9 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
                         if (cum + c[e] >= need) {
                             sel_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
                             sel_need = need - cum;
+                            // every key of the digit is taken: the later
+                            // digits cannot change the set
+                            sel_all = c[e] == need - cum;
                             break;
                         }
                         cum += c[e];
@@ -549,15 +568,20 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
             prefix = sel_prefix;
             need = sel_need;
             mask |= 255u << shift;
+            // the same on every CTA of the cluster (the same totals), so they
+            // leave after the same number of cluster barriers
+            if (sel_all) break;
         }
     }
     // each thread owns the contiguous run [r0, r1) of the segment
     const int per = (m + (int)blockDim.x - 1) / (int)blockDim.x;
     const int r0 = min(m, tid * per), r1 = min(m, r0 + per);
     int gt_local = 0, eq_local = 0;
+    // keys compare on the digits chosen so far (all of them unless the
+    // selection ended early, when every key equal on them is taken)
     if (partial)
         for (int i = r0; i < r1; i++) {
-            const uint32_t u = key(i);
+            const uint32_t u = key(i) & mask;
             gt_local += u > prefix;
             eq_local += u == prefix;
         }
@@ -602,7 +626,7 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     for (int i = r0; i < r1; i++) {
         bool take = k == n;
         if (partial) {
-            const uint32_t u = key(i);
+            const uint32_t u = key(i) & mask;
             const bool eq = u == prefix;
             take = u > prefix || (eq && eq_seen < (int)need);
             eq_seen += eq;
