@@ -49,7 +49,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
 
 struct Params {
-    int32_t H, d, K, P;
+    int32_t H, d, K, P;        // P: codebook planes the pass multiplies
+    int32_t pstride;           // planes stored per head in the B tensor map
+    int32_t max_order;         // plane products of order pa + pl above this are dropped
     int32_t num_bh, seg, tiles_per_bh, nchunks, kpad;
     int32_t out_ncap;          // rows per (b, h) of the keys and of codes
     int64_t plane_rows;        // rows of one A plane in the A tensor map
@@ -423,7 +425,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             if (!ok) break;
                             mbar_expect_tx(&b_full[sb], S::kB);
                             tma_3d(smB + sb * S::kB, &tmB, &b_full[sb], kb * BK, c * BN,
-                                   h * p.P + pl);
+                                   h * p.pstride + pl);
                             b_it++;
                         }
                 }
@@ -487,8 +489,9 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             const uint32_t b_base = su32(smB + sb * S::kB);
 #pragma unroll
                             for (int pa = 0; pa < PA; pa++) {
-                                // products of order pa + pl > 2 are below 2^-24
-                                if (pa + pl > 2) continue;
+                                // products of a higher order are dropped (the
+                                // bound counts them)
+                                if (pa + pl > p.max_order) continue;
                                 const uint32_t a_base =
                                     su32(smA + ((sa * PA + pa) * DK + kb) * S::kA);
 #pragma unroll
@@ -1322,7 +1325,12 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.H = (int32_t)H;
     p.d = (int32_t)d;
     p.K = (int32_t)K;
-    p.P = b.P;
+    // two row planes against the codebook planes keep the products of order
+    // 0 and 1 only: planes 0 and 1 of chat (of 3 stored for bf16)
+    const bool cut = PA == 2 && !b.exact;
+    p.P = cut ? 2 : b.P;
+    p.pstride = b.P;
+    p.max_order = cut ? 1 : 2;
     p.num_bh = (int32_t)nbh;
     p.seg = (int32_t)ncap;
     p.tiles_per_bh = (int32_t)(((max_rows < ncap ? max_rows : ncap) + BM - 1) / BM);
@@ -1345,12 +1353,17 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     // of chat and of the planes that are dropped, of the two-plane row
     // operand, and of h and of acc - h.
     int pairs = 0;
-    for (int pb = 0; pb < b.P; pb++)
+    for (int pb = 0; pb < p.P; pb++)
         for (int pa = 0; pa < PA; pa++)
-            if (pa + pb <= 2) pairs++;
+            if (pa + pb <= p.max_order) pairs++;
     double coef = ((double)pairs * (double)(d / 16) + 8.0) * 0x1p-22;
     if (!b.exact) coef += bf16 ? 0x1p-21 : 0x1p-20;
     if (PA == 2) coef += bf16 ? 0x1p-15 : 0x1p-20;
+    // the dropped products, each elementwise within a relative 2^-16 (bf16;
+    // 2^-22 fp16) of |x| |chat|: the row's second plane against chat's second
+    // (|lo| <= 2^-8 |x|, |c1| <= 2^-8 |chat|), and for bf16 chat's third plane
+    // against the row (|c2| <= 2^-16 |chat|)
+    if (cut) coef += bf16 ? 0x1.1p-15 : 0x1p-20;
     p.err_coef = (float)coef;
     p.norm_slack = PA == 2 ? 1.01f : 1.0001f;
     p.codes = c.codes;
