@@ -57,7 +57,7 @@ METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of rooflin
 # profiles/assign_tc_kernel_llama32_3b_layer.md.  It holds only for the
 # contraction source it was taken on (the first 16 hex digits of the sha256 of
 # csrc/assign_tc.cu); for any other source the bench reports null.
-TC_TRAFFIC = {"llama32_3b_layer": ("b971019781beaa10", 68889600)}
+TC_TRAFFIC = {"llama32_3b_layer": ("71a0dc64edb07245", 93701120)}
 DEFAULT_WORKLOAD = "llama32_3b_layer"
 L2_FLUSH_BYTES = 256 << 20
 
