@@ -243,8 +243,11 @@ size_t exact_smem(int d) { return sizeof(float) * (size_t)((2 * kRB + kCT) * (d 
 // (b, h) and one row, so the block's lanes spread over the centroids instead
 // of over rows.  8 lanes share a centroid (each 1/8 of its elements, 16-byte
 // loads); pass 1 finds e_max = max_j |x - c_j|^2, pass 2 scores every
-// centroid.  The arithmetic is the general kernel's: e_j as a plain fp32 sum
-// of squares, q . c_j compensated.
+// centroid.  With K <= kLastCache pass 1 also keeps e_j and q . c_j in
+// shared memory and pass 2 reads them back instead of the codebook.  The
+// arithmetic is the general kernel's: e_j as a plain fp32 sum of squares,
+// q . c_j compensated.
+constexpr int64_t kLastCache = 8192;
 template <int DT>
 __global__ void __launch_bounds__(256)
 assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ cf, int32_t H,
@@ -257,6 +260,8 @@ assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ c
     __shared__ float wmax[8];
     __shared__ float wbest[8];
     __shared__ int32_t wj[8];
+    extern __shared__ float ecache[];  // [2][K]: e_j, then q . c_j (K <= kLastCache)
+    const bool cached = K <= kLastCache;
     const int64_t bh = blockIdx.x;
     const int64_t h = bh % H;
     const int32_t Ls = seq_len(len, (int32_t)(bh / H), ncap);
@@ -287,6 +292,19 @@ assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ c
     float emax = 0.f, best = -INFINITY;
     int32_t bj = 0;
     for (int pass = 0; pass < 2; pass++) {
+        if (pass == 1 && cached) {
+            // scores from the values pass 1 kept; each thread takes j = t,
+            // t + 256, ... in ascending order
+            for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
+                const float e = ecache[j], dqv = ecache[K + j];
+                const float cn = cnorm[h * K + j];
+                const float cosv = (qn > 0.f && cn > 0.f) ? dqv / (qn * cn) : 0.f;
+                const float err = emax > 0.f ? e / emax : 0.f;
+                const float sc = fmaf(-beta, err, (1.f - beta) * cosv);
+                if (sc > best || (sc == best && j < bj)) { best = sc; bj = (int32_t)j; }
+            }
+            break;
+        }
         // uniform trip count: the shuffles below need every lane
         for (int64_t j0 = 0; j0 < K; j0 += 32) {
             const int64_t j = j0 + grp;
@@ -302,7 +320,7 @@ assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ c
                 e1 = fmaf(t1, t1, e1);
                 e0 = fmaf(t2, t2, e0);
                 e1 = fmaf(t3, t3, e1);
-                if (pass == 1) {
+                if (pass == 1 || cached) {
                     const float4 qv = *reinterpret_cast<const float4*>(qs + a);
                     dq.add_prod(qv.x, cv.x);
                     dq.add_prod(qv.y, cv.y);
@@ -313,6 +331,13 @@ assign_blend_last_kernel(const void* __restrict__ x, const float* __restrict__ c
             float e = e0 + e1;
             for (int m = 4; m; m >>= 1) e += __shfl_xor_sync(0xffffffffu, e, m);
             if (pass == 0) {
+                if (cached) {
+                    for (int m = 4; m; m >>= 1) dq.merge(shfl_xor(dq, m));
+                    if (ok && seg == 0) {
+                        ecache[j] = e;
+                        ecache[K + j] = dq.value();
+                    }
+                }
                 if (ok) emax = fmaxf(emax, e);
                 continue;
             }
@@ -387,22 +412,15 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
         // one row per (b, h): the lanes go to the centroids
         const float* cf = reinterpret_cast<const float*>(c);
         const unsigned nbh = (unsigned)(s.B * s.H);
-        switch (dt) {
-            case kF32:
-                assign_blend_last_kernel<kF32><<<nbh, 256, 0, st>>>(
-                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
-                    K, cnorm, codes);
-                break;
-            case kBF16:
-                assign_blend_last_kernel<kBF16><<<nbh, 256, 0, st>>>(
-                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
-                    K, cnorm, codes);
-                break;
-            default:
-                assign_blend_last_kernel<kF16><<<nbh, 256, 0, st>>>(
-                    x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q, qnorm, beta,
-                    K, cnorm, codes);
-        }
+        const size_t smem = K <= kLastCache ? sizeof(float) * 2 * (size_t)K : 0;
+        auto k = dt == kF32 ? assign_blend_last_kernel<kF32>
+                            : (dt == kBF16 ? assign_blend_last_kernel<kBF16>
+                                           : assign_blend_last_kernel<kF16>);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(float) * 2 * kLastCache));
+        if (e != cudaSuccess) return e;
+        k<<<nbh, 256, smem, st>>>(x, cf, (int32_t)s.H, (int32_t)s.Ncap, (int32_t)s.d, len, ra, q,
+                                  qnorm, beta, K, cnorm, codes);
         note_launches(1);
         return cudaGetLastError();
     }
