@@ -411,7 +411,6 @@ cosine_score_warp_kernel(const void* __restrict__ keys, int64_t rows, int32_t H,
     }
 }
 
-constexpr int kSelThreads = 512;
 constexpr int kSelCluster = 8;
 constexpr int kSelCache = 16384;  // keys of a CTA's segment kept in shared memory (66 KB)
 
@@ -451,6 +450,7 @@ __device__ __forceinline__ int block_scan(int v, int& excl, int* warp_tot) {
 // per-pass histograms and the compaction offsets are combined through
 // distributed shared memory.  In the compaction each thread owns a contiguous
 // run of the segment, so two block scans place every row.
+template <int kSelThreads>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
               const int32_t* __restrict__ len, double fraction, int32_t* __restrict__ perm,
@@ -947,13 +947,28 @@ cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* le
     if (nbh == 0) return cudaSuccess;
     const int64_t seg = (s.Ncap + kSelCluster - 1) / kSelCluster;
     const size_t smem = seg <= kSelCache ? sizeof(uint32_t) * (size_t)(seg + seg / 32 + 1) : 0;
-    cudaError_t e = cudaFuncSetAttribute(select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(uint32_t) * (kSelCache + kSelCache / 32 + 1)));
+    const int cache_bytes = (int)(sizeof(uint32_t) * (kSelCache + kSelCache / 32 + 1));
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<512>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, cache_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(select_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 cache_bytes);
     if (e != cudaSuccess) return e;
-    select_kernel<<<nbh * kSelCluster, kSelThreads, smem, st>>>(scores, (int32_t)s.H,
-                                                             (int32_t)s.Ncap, len, fraction, perm,
-                                                             count);
+    // 512 threads per CTA for a few (b, h); with many (a decode batch, more
+    // clusters than about four CTAs per SM), 256, so more CTAs are resident
+    // and the chain of barriers of each runs in fewer waves
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool few = (int64_t)nbh * kSelCluster <= 4 * (int64_t)sms;
+    if (few)
+        select_kernel<512><<<nbh * kSelCluster, 512, smem, st>>>(scores, (int32_t)s.H,
+                                                                 (int32_t)s.Ncap, len, fraction,
+                                                                 perm, count);
+    else
+        select_kernel<256><<<nbh * kSelCluster, 256, smem, st>>>(scores, (int32_t)s.H,
+                                                                 (int32_t)s.Ncap, len, fraction,
+                                                                 perm, count);
                                                note_launches(1);
     return cudaGetLastError();
 }

@@ -25,6 +25,8 @@ CASES = [
     (1, 1, 70000, 128, "bf16", 0.02, "proxy", dict(window=100, rope_base=500000.0)),
     # segments too long for the select kernel's shared-memory cache
     (1, 1, 140000, 16, "bf16", 0.03, "proxy", None),
+    # many (b, h): the select's smaller CTAs
+    (16, 8, 300, 64, "bf16", 0.1, "proxy", dict(window=32, rope_base=500000.0)),
 ]
 
 
