@@ -183,7 +183,9 @@ def _tc_traffic(workload: str):
 
 
 def _inputs(w, rank):
-    keys = synth.keys(w)
+    # each rank its own batch of sequences; the codebook and the calibration
+    # inputs are the layer's, shared by every rank
+    keys = synth.keys(w, batch_offset=rank * w.B)
     cb = synth.codebook(w)
     queries = synth.queries(w) if (w.M and not w.h_given) else None
     hg = synth.given_h(w) if w.h_given else None

@@ -132,14 +132,17 @@ def _to_storage(x: np.ndarray, dtype: str) -> torch.Tensor:
     return t.to(DTYPES[dtype])
 
 
-def keys(w: Workload, rows: int | None = None, threads: int = 8) -> torch.Tensor:
-    """Keys [B, H, rows, d] in the storage dtype (rows defaults to N)."""
+def keys(w: Workload, rows: int | None = None, threads: int = 8,
+         batch_offset: int = 0) -> torch.Tensor:
+    """Keys [B, H, rows, d] in the storage dtype (rows defaults to N).
+    batch_offset: the batch holds sequences batch_offset .. batch_offset + B - 1
+    of the stream (another batch of the same workload)."""
     n = w.N if rows is None else rows
     out = torch.empty((w.B, w.H, n, w.d), dtype=DTYPES[w.dtype])
 
     def one(bh):
         b, h = divmod(bh, w.H)
-        out[b, h] = _to_storage(_keys_for(w, b, h, n), w.dtype)
+        out[b, h] = _to_storage(_keys_for(w, b + batch_offset, h, n), w.dtype)
 
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(one, range(w.B * w.H)))
