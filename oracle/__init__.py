@@ -71,6 +71,12 @@ def _load():
         lib.orc_select_retrieval_set.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, _f64p,
                                                  ctypes.c_double, _i32p, _f64p, _f64p]
         lib.orc_select_retrieval_set.restype = ctypes.c_int64
+        lib.orc_code_attention_topk.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_int64, _i32p, _f64p, ctypes.c_int64,
+                                                _f64p, ctypes.c_int64, ctypes.c_double,
+                                                ctypes.c_double, ctypes.c_int, ctypes.c_double,
+                                                _i32p, _f64p, _f64p]
+        lib.orc_code_attention_topk.restype = ctypes.c_int64
         _lib = lib
     return _lib
 
@@ -185,6 +191,25 @@ def select_retrieval_set(keys, q, fraction: float):
     count = _load().orc_select_retrieval_set(_p(keys, _f64p), n, d, _p(q, _f64p),
                                              float(fraction), _p(perm, _i32p),
                                              _p(scores, _f64p), _p(kth, _f64p))
+    return perm, int(count), scores, float(kth[0])
+
+
+def code_attention_topk(keys, t: int, codes, codebook, q, window: int, far_b: float,
+                        base: float, fraction: float, interleaved: bool = False):
+    """Code-based attention scores of one (b, h) and its top tokens; keys
+    [n, d] pre-RoPE, codes [n], codebook [K, d], q [d] pre-RoPE at position t.
+    Returns (perm, count, scores, kth_score)."""
+    keys, codebook, q = _f64(keys), _f64(codebook), _f64(q)
+    n, d = keys.shape
+    K = codebook.shape[0]
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    perm = np.empty(n, np.int32)
+    scores = np.empty(n)
+    kth = np.empty(1)
+    count = _load().orc_code_attention_topk(
+        _p(keys, _f64p), n, d, int(t), _p(codes, _i32p), _p(codebook, _f64p), K, _p(q, _f64p),
+        int(window), float(far_b), float(base), int(bool(interleaved)), float(fraction),
+        _p(perm, _i32p), _p(scores, _f64p), _p(kth, _f64p))
     return perm, int(count), scores, float(kth[0])
 
 

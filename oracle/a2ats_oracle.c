@@ -327,3 +327,59 @@ int64_t orc_select_retrieval_set(const double* keys, int64_t n, int64_t d,
     free(s);
     return count;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Code-based attention-score estimation and top-K token retrieval.         */
+/* "A2ATS-adapted" page, paper-fidelity section, "Windowed RoPE (Eq.         */
+/* 11-12)": far keys stay in the unrotated frame and the constant far        */
+/* relative position b rides on the query, u_ij = q_i R_b k_j^T; keys inside */
+/* the window keep exact RoPE.  The paper's abstract: the attention score    */
+/* is approximated through the vector-quantised keys so that the top-K       */
+/* tokens are retrieved.  Reading: with q the decode query before RoPE and   */
+/* t its position,                                                           */
+/*   near row j (0 <= t - j < window):  u_j = RoPE(q, t) . RoPE(k_j, j)       */
+/*   far row j:                         u_j = RoPE(q, b) . c_{code_j}         */
+/* (a code outside [0, K) scores 0), and the retrieved set is the top        */
+/* ceil(fraction n) rows by (u desc, index asc), both halves of perm in      */
+/* ascending order as the split writes them.                                 */
+/* ------------------------------------------------------------------------ */
+int64_t orc_code_attention_topk(const double* keys, int64_t n, int64_t d, int64_t t,
+                                const int32_t* codes, const double* codebook, int64_t K,
+                                const double* q, int64_t window, double far_b, double base,
+                                int interleaved, double fraction, int32_t* perm,
+                                double* scores, double* kth) {
+    double* qn = (double*)malloc(sizeof(double) * (size_t)d);
+    double* qf = (double*)malloc(sizeof(double) * (size_t)d);
+    double* kr = (double*)malloc(sizeof(double) * (size_t)d);
+    orc_rope_row(q, qn, d, (double)t, base, interleaved);
+    orc_rope_row(q, qf, d, far_b, base, interleaved);
+    scored* s = (scored*)malloc(sizeof(scored) * (size_t)(n > 0 ? n : 1));
+    for (int64_t j = 0; j < n; j++) {
+        int64_t dist = t - j;
+        int near = window > 0 && dist >= 0 && dist < window;
+        double u = 0.0;
+        if (near) {
+            orc_rope_row(keys + j * d, kr, d, (double)j, base, interleaved);
+            for (int64_t a = 0; a < d; a++) u += qn[a] * kr[a];
+        } else if (codes[j] >= 0 && codes[j] < K) {
+            const double* c = codebook + (int64_t)codes[j] * d;
+            for (int64_t a = 0; a < d; a++) u += qf[a] * c[a];
+        }
+        s[j].s = u;
+        s[j].i = (int32_t)j;
+        if (scores) scores[j] = u;
+    }
+    int64_t count = (int64_t)ceil(fraction * (double)n);
+    if (count > n) count = n;
+    if (count < 0) count = 0;
+    qsort(s, (size_t)n, sizeof(scored), by_score_then_index);
+    for (int64_t i = 0; i < n; i++) perm[i] = s[i].i;
+    if (kth) *kth = count > 0 ? s[count - 1].s : INFINITY;
+    qsort(perm, (size_t)count, sizeof(int32_t), by_value);
+    qsort(perm + count, (size_t)(n - count), sizeof(int32_t), by_value);
+    free(s);
+    free(kr);
+    free(qf);
+    free(qn);
+    return count;
+}

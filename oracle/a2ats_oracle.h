@@ -79,6 +79,17 @@ int64_t orc_select_retrieval_set(const double* keys, int64_t n, int64_t d,
                                  const double* q, double fraction, int32_t* perm,
                                  double* scores, double* kth);
 
+/* Code-based attention scores and the top ceil(fraction n) tokens of one
+ * (b, h): near rows (0 <= t - j < window) score RoPE(q, t) . RoPE(k_j, j),
+ * far rows RoPE(q, far_b) . codebook[codes[j]] (0 for a code outside
+ * [0, K)).  keys [n, d] pre-RoPE, codebook [K, d], q [d] pre-RoPE.  perm,
+ * scores and kth as orc_select_retrieval_set.  Returns the count. */
+int64_t orc_code_attention_topk(const double* keys, int64_t n, int64_t d, int64_t t,
+                                const int32_t* codes, const double* codebook, int64_t K,
+                                const double* q, int64_t window, double far_b, double base,
+                                int interleaved, double fraction, int32_t* perm,
+                                double* scores, double* kth);
+
 #ifdef __cplusplus
 }
 #endif
