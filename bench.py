@@ -71,6 +71,9 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--path", choices=["step", "attention"], default="step",
+                   help="attention: time the code-based attention scores and top tokens "
+                        "(the step after the path) instead of the step")
     p.add_argument("--separate-split", action="store_true",
                    help="run RoPE and the split on the second stream beside a separate "
                         "plain-VQ call, instead of the fused call (same outputs)")
@@ -678,10 +681,88 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def run_attention(a):
+    """The code-based attention scores of the decode query with every cached
+    key (far keys through the codes the one-call step wrote, window keys
+    exactly) and the top tokens by them, on the workload's keys; the newest
+    key of each (b, h) is the query.  The codes are computed once, before
+    the timed calls; L2 is flushed between calls."""
+    import query_aware_vq_gb300 as q
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    keys, cb, _, _ = _inputs(w, rank)
+    kd, cd = keys.cuda(), cb.cuda()
+    rope = dict(window=w.W, rope_base=w.rope_base)
+    _, _, _, codes = q.a2ats_rope_split_plain_assign(kd, cd, None, w.fraction, rope=rope)
+    qd = kd[:, :, -1, :].contiguous()
+    lib = q.library()
+    ws = torch.empty(lib.a2ats_code_attention_topk_workspace_size(w.B, w.H, w.N, w.d, w.K),
+                     dtype=torch.uint8, device="cuda")
+    scores = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    perm = torch.empty((w.B, w.H, w.N), dtype=torch.int32, device="cuda")
+    count = torch.empty((w.B, w.H), dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        q.a2ats_code_attention_topk(kd, codes, cd, qd, w.fraction, rope=rope, far_b=2048,
+                                    scores=scores, perm=perm, count=count, workspace=ws)
+
+    for _ in range(max(a.warmup, 3)):
+        call()
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    evs = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        evs.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / a.steps, world)
+    keys_per_call = w.B * w.H * w.N
+    hbm, _, src = _peaks()
+    # per key: its code read, its score written, read by the select, its
+    # slot of perm written (the window keys' extra reads are left out)
+    bytes_per_call = keys_per_call * 16.0
+    achieved = bytes_per_call / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "keys scored/sec (code-based attention scores + top tokens)",
+            "value": world * keys_per_call / (ms * 1e-3), "unit": "keys/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; the workload's keys and codebook; no model weights)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
+                       "window": w.W, "far_b": 2048, "fraction": w.fraction,
+                       "l2": "flushed between calls (256 MB write)"},
+            "roofline": {"kernel": "query table + far-row gather + window rows + select",
+                         "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                         "bytes_per_call": bytes_per_call,
+                         "peak_source": f"{src} (hbm_gbs)"},
+            "clocks": clk,
+            "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,
+        }), flush=True)
+
+
 if __name__ == "__main__":
     args = _args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "attention":
+        run_attention(args)
     elif synth.WORKLOADS[args.workload].decode_steps:
         run_decode(args)
     else:

@@ -293,6 +293,45 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
                                   void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_code_attention_topk -- the attention score of the decode query with
+ * every cached key, far keys through their codes, and the top tokens by it:
+ * deploy-preview "A2ATS-adapted" page, paper-fidelity section, "Windowed
+ * RoPE (Eq. 11-12)" (far keys unrotated, the far relative position b on the
+ * query, u_ij = q_i R_b k_j^T, the page's a2ats_apply_far_query_rope half;
+ * keys inside the window with exact RoPE), and the paper's abstract (top-K
+ * tokens retrieved by the approximate attention score).  The pages give no
+ * function for it.  With t = len[b] - 1:
+ *   near row j (0 <= t - j < window):  u_j = RoPE(q, t) . RoPE(keys_j, j)
+ *   far row j:                         u_j = RoPE(q, far_b) . codebook[codes_j]
+ * (0 for a code outside [0, K)).
+ *   keys     [B, H, Ncap, d] pre-RoPE, in dtype (only the window rows are read)
+ *   codes    [B, H, Ncap] int32 (e.g. from the assignment of k~)
+ *   codebook [H, K, d] in dtype; K in [1, 2^24]
+ *   query    [B, H, d] in dtype, the decode query before RoPE
+ *   rope     required: window and RoPE base / pairing (far_offset unused)
+ *   far_b    the far relative position, |far_b| < 2^24 (the page's default 2048)
+ *   fraction in [0, 1]: the top ceil(fraction len) rows are retrieved
+ *   scores   [B, H, Ncap] fp32: u_j for rows j < len[b]
+ *   perm, count: as a2ats_select_retrieval_set writes them, ranked by u
+ *   workspace  a2ats_code_attention_topk_workspace_size(B, H, Ncap, d, K)
+ *            bytes of device memory, owned by the caller
+ * Scores are fp32 (table entries and near dots summed in fp32); the set is
+ * exact except possibly for rows whose score is within 1e-5 of the largest
+ * score's magnitude from the threshold.
+ * Errors: SHAPE, DTYPE, ALIGN as the other calls; INVALID_ARG for a NULL
+ * rope, fraction outside [0, 1], |far_b| >= 2^24 or a NULL array when
+ * Ncap > 0; WORKSPACE when workspace is NULL or short.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_code_attention_topk_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                                int64_t K);
+int a2ats_code_attention_topk(const void* keys, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                              int64_t d, const int32_t* len, const int32_t* codes,
+                              const void* codebook, int64_t K, const void* query,
+                              const a2ats_rope_params* rope, int32_t far_b, double fraction,
+                              float* scores, int32_t* perm, int32_t* count, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

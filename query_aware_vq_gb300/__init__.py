@@ -68,6 +68,9 @@ _SIGS = {
                                            _I32, _P, _P, _P, _SZ, _P],
     "a2ats_copy_retrieval_rows": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "a2ats_rope_split_plain_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_code_attention_topk_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_code_attention_topk": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P,
+                                  _I32, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
                                       _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
     "a2ats_status_string": [_I32],
@@ -100,7 +103,8 @@ def _load():
                      "a2ats_h_weighted_assign_workspace_size",
                      "a2ats_query_aware_assign_workspace_size",
                      "a2ats_select_retrieval_set_workspace_size",
-                     "a2ats_rope_split_plain_assign_workspace_size"):
+                     "a2ats_rope_split_plain_assign_workspace_size",
+                     "a2ats_code_attention_topk_workspace_size"):
             getattr(lib, name).restype = ctypes.c_size_t
         lib.a2ats_kernel_launches.restype = ctypes.c_uint64
         lib.a2ats_timed_kernels_ms.restype = ctypes.c_double
@@ -398,6 +402,38 @@ def a2ats_rope_split_plain_assign(keys, codebook, query=None, fraction: float = 
         ctypes.byref(rp), _ptr(cb), K, _ptr(o4), _ptr(perm), _ptr(count), _ptr(codes),
         int(bool(reuse)), ev, _ptr(ws), nb, _stream(stream)))
     return out, perm, count, codes
+
+
+def a2ats_code_attention_topk(keys, codes, codebook, query, fraction: float = 0.2, *, rope,
+                              far_b: int = 2048, lengths=None, scores=None, perm=None,
+                              count=None, workspace=None, stream=None):
+    """Attention scores of the decode query with every cached key (far keys
+    through their codes, window keys exactly) and the top tokens by them;
+    returns (scores [B, H, N] fp32, perm, count)."""
+    _dev(keys, codes, codebook, query, lengths, scores, perm, count)
+    k4 = _as4(keys)
+    B, H, N, d = k4.shape
+    cb = codebook if codebook.dim() == 3 else codebook.unsqueeze(0)
+    if cb.dtype != k4.dtype or query.dtype != k4.dtype:
+        raise TypeError("keys, codebook and query must share a dtype")
+    if codes.dtype != torch.int32:
+        raise TypeError("codes must be int32")
+    K = cb.shape[1]
+    if scores is None:
+        scores = torch.empty((B, H, N), dtype=torch.float32, device=keys.device)
+    if perm is None:
+        perm = torch.empty((B, H, N), dtype=torch.int32, device=keys.device)
+    if count is None:
+        count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_code_attention_topk_workspace_size(B, H, N, d, K),
+                        keys.device, workspace)
+    rp = _rope(rope)
+    _check("a2ats_code_attention_topk", lib.a2ats_code_attention_topk(
+        _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(codes), _ptr(cb), K,
+        _ptr(query), ctypes.byref(rp), int(far_b), float(fraction), _ptr(scores), _ptr(perm),
+        _ptr(count), _ptr(ws), nb, _stream(stream)))
+    return scores, perm, count
 
 
 def a2ats_copy_retrieval_rows(src, dst, perm, count, *, lengths=None, stream=None):

@@ -652,6 +652,52 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+size_t a2ats_code_attention_topk_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                                int64_t K) {
+    (void)Ncap;
+    if (B < 0 || H < 0 || d < 0 || K < 0) return 0;
+    Carve c(nullptr);
+    c.take<float>((size_t)(B * H * d));  // RoPE(q, t)
+    c.take<float>((size_t)(B * H * K));  // the per-(b, h) table
+    return c.used + 256;
+}
+
+int a2ats_code_attention_topk(const void* keys, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                              int64_t d, const int32_t* len, const int32_t* codes,
+                              const void* codebook, int64_t K, const void* query,
+                              const a2ats_rope_params* rope, int32_t far_b, double fraction,
+                              float* scores, int32_t* perm, int32_t* count, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
+    if (!rope) return A2ATS_ERR_INVALID_ARG;
+    if (far_b <= -(1 << 24) || far_b >= (1 << 24)) return A2ATS_ERR_INVALID_ARG;
+    RopeArgs ra;
+    if ((st = make_rope(rope, d, ra))) return st;
+    if (B * H == 0) return A2ATS_OK;
+    if (!count || (Ncap > 0 && (!keys || !codes || !codebook || !query || !scores || !perm)))
+        return A2ATS_ERR_INVALID_ARG;
+    if ((keys && !aligned16(keys)) || (codes && !aligned16(codes)) ||
+        (codebook && !aligned16(codebook)) || (query && !aligned16(query)) ||
+        (scores && !aligned16(scores)) || (perm && !aligned16(perm)))
+        return A2ATS_ERR_ALIGN;
+    if (!workspace ||
+        workspace_bytes < a2ats_code_attention_topk_workspace_size(B, H, Ncap, d, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    float* q_near = c.take<float>((size_t)(B * H * d));
+    float* lut = c.take<float>((size_t)(B * H * K));
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    cudaError_t e = launch_code_attention(keys, dtype, sh, len, codes, codebook, K, query, ra,
+                                          far_b, q_near, lut, scores, s);
+    if (e == cudaSuccess) e = launch_select(scores, sh, len, fraction, perm, count, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
 int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64_t H,
                               int64_t Ncap, const int32_t* len, const int32_t* perm,
                               const int32_t* count, void* stream) {

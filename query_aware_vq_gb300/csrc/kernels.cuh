@@ -50,6 +50,16 @@ cudaError_t launch_window_scores(const void* keys, const void* query, int dt, co
                                  const int32_t* len, const RopeArgs& ra, float* q, float* qnorm,
                                  float* scores, void* kout, cudaStream_t st);
 
+// code_attention.cu ------------------------------------------------------
+// Code-based attention scores of every row j < len[b]: near rows (t - j <
+// window, t = len - 1) RoPE(q, t) . RoPE(k_j, j), far rows
+// RoPE(q, far_b) . c[code_j] through the per-(b, h) table lut [B*H, K];
+// q_near [B*H, d] receives RoPE(q, t).
+cudaError_t launch_code_attention(const void* keys, int dt, const Shape& s, const int32_t* len,
+                                  const int32_t* codes, const void* codebook, int64_t K,
+                                  const void* query, const RopeArgs& ra, int32_t far_b,
+                                  float* q_near, float* lut, float* scores, cudaStream_t st);
+
 // row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)
 cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
                                cudaStream_t st);

@@ -142,6 +142,30 @@ def test_rope_split_plain_assign_validation(lib):
     assert call(nb=need - 1) == -6
 
 
+def test_code_attention_topk_validation(lib):
+    f = lib.a2ats_code_attention_topk
+    rope = q.RopeParams(64, 0, 500000.0, 0)
+    ws = 1 << 30
+
+    def call(dt=1, K=256, rp=rope, far_b=2048, frac=0.1, codes=FAKE + 4096, query=FAKE + 8192,
+             ws_ptr=FAKE, nb=ws):
+        return f(FAKE, dt, 1, 2, 64, 128, None, codes, FAKE + 12288, K, query,
+                 ctypes.byref(rp) if rp is not None else None, far_b, frac, FAKE + 16384,
+                 FAKE + 20480, FAKE, ws_ptr, nb, None)
+
+    assert call(rp=None) == -1
+    assert call(dt=5) == -3
+    assert call(K=0) == -2
+    assert call(frac=1.5) == -1
+    assert call(far_b=1 << 24) == -1
+    assert call(codes=None) == -1
+    assert call(query=FAKE + 8196) == -4
+    assert call(ws_ptr=None, nb=0) == -6
+    need = lib.a2ats_code_attention_topk_workspace_size(1, 2, 64, 128, 256)
+    assert need >= 4 * (2 * 128 + 2 * 256)
+    assert call(nb=need - 1) == -6
+
+
 def test_copy_retrieval_rows_validation(lib):
     f = lib.a2ats_copy_retrieval_rows
     assert f(FAKE, FAKE, -1, 2, 10, None, FAKE, FAKE, None) == -2
