@@ -77,6 +77,8 @@ def _load():
                                                 ctypes.c_double, ctypes.c_int, ctypes.c_double,
                                                 _i32p, _f64p, _f64p]
         lib.orc_code_attention_topk.restype = ctypes.c_int64
+        lib.orc_dequantize.argtypes = [_i32p, ctypes.c_int64, _f64p, ctypes.c_int64,
+                                       ctypes.c_int64, _f64p]
         _lib = lib
     return _lib
 
@@ -211,6 +213,32 @@ def code_attention_topk(keys, t: int, codes, codebook, q, window: int, far_b: fl
         int(window), float(far_b), float(base), int(bool(interleaved)), float(fraction),
         _p(perm, _i32p), _p(scores, _f64p), _p(kth, _f64p))
     return perm, int(count), scores, float(kth[0])
+
+
+def dequantize(codes, codebook) -> np.ndarray:
+    """codes [n] int32, codebook [K, d]: [n, d] of the codes' centroids
+    (zeros for a code outside [0, K))."""
+    codebook = _f64(codebook)
+    K, d = codebook.shape
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    n = codes.shape[0]
+    out = np.empty((n, d))
+    _load().orc_dequantize(_p(codes, _i32p), n, _p(codebook, _f64p), K, d, _p(out, _f64p))
+    return out
+
+
+def byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:
+    """The v0.39.0 page's byte accounting of one head's keys ("Byte
+    accounting"; "What you get with the defaults"): each token stores
+    d / sub_dim codes of codebook_bits bits; fp16 stores 16 bits per number;
+    the codebook holds 2^bits entries of sub_dim fp16 numbers."""
+    groups = d // sub_dim
+    compressed = tokens * groups * codebook_bits / 8.0
+    fp16 = tokens * d * 2.0
+    return {"compressed_key_bytes": compressed, "fp16_key_bytes": fp16,
+            "compression_ratio": fp16 / compressed if compressed else math.inf,
+            "codebook_bytes": float((1 << codebook_bits) * sub_dim * 2),
+            "assigned_avg_bits": codebook_bits / sub_dim}
 
 
 def retrieval_count(fraction: float, n: int) -> int:

@@ -383,3 +383,17 @@ int64_t orc_code_attention_topk(const double* keys, int64_t n, int64_t d, int64_
     free(qn);
     return count;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Dequantisation.  v0.39.0 page, "How it works", step 3: a key is          */
+/* reconstructed from its assigned centroid, k ~ c_{code}.  Row j of out is */
+/* codebook row codes[j] (zeros for a code outside [0, K)).                 */
+/* ------------------------------------------------------------------------ */
+void orc_dequantize(const int32_t* codes, int64_t n, const double* codebook, int64_t K,
+                    int64_t d, double* out) {
+    for (int64_t j = 0; j < n; j++) {
+        int32_t c = codes[j];
+        for (int64_t a = 0; a < d; a++)
+            out[j * d + a] = (c >= 0 && c < K) ? codebook[(int64_t)c * d + a] : 0.0;
+    }
+}

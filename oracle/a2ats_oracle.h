@@ -90,6 +90,11 @@ int64_t orc_code_attention_topk(const double* keys, int64_t n, int64_t d, int64_
                                 int interleaved, double fraction, int32_t* perm,
                                 double* scores, double* kth);
 
+/* Row j of out [n, d] = codebook [K, d] row codes[j]; zeros for a code
+ * outside [0, K). */
+void orc_dequantize(const int32_t* codes, int64_t n, const double* codebook, int64_t K,
+                    int64_t d, double* out);
+
 #ifdef __cplusplus
 }
 #endif
