@@ -71,9 +71,10 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--path", choices=["step", "attention"], default="step",
-                   help="attention: time the code-based attention scores and top tokens "
-                        "(the step after the path) instead of the step")
+    p.add_argument("--path", choices=["step", "attention", "dequantize"], default="step",
+                   help="attention: time the code-based attention scores and top tokens; "
+                        "dequantize: time the reconstruction of the keys from their codes "
+                        "(both steps after the path) instead of the step")
     p.add_argument("--separate-split", action="store_true",
                    help="run RoPE and the split on the second stream beside a separate "
                         "plain-VQ call, instead of the fused call (same outputs)")
@@ -757,12 +758,75 @@ def run_attention(a):
         }), flush=True)
 
 
+def run_dequantize(a):
+    """The keys reconstructed from the codes the one-call step writes
+    (codebook[h, code] per row), on the workload's cache; L2 flushed between
+    calls.  HBM-bound: a 4-byte code read and a d-element row written per
+    key (the codebook stays in L2)."""
+    import query_aware_vq_gb300 as q
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    keys, cb, _, _ = _inputs(w, rank)
+    kd, cd = keys.cuda(), cb.cuda()
+    rope = dict(window=w.W, rope_base=w.rope_base)
+    _, _, _, codes = q.a2ats_rope_split_plain_assign(kd, cd, None, w.fraction, rope=rope)
+    out = torch.empty_like(kd)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(a.warmup, 3)):
+        q.a2ats_dequantize(codes, cd, out=out)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    evs = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q.a2ats_dequantize(codes, cd, out=out)
+        e1.record(stream)
+        evs.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / a.steps, world)
+    keys_per_call = w.B * w.H * w.N
+    esize = out.element_size()
+    bytes_per_call = keys_per_call * (4.0 + w.d * esize)
+    hbm, _, src = _peaks()
+    achieved = bytes_per_call / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "keys reconstructed/sec (dequantisation from codes)",
+            "value": world * keys_per_call / (ms * 1e-3), "unit": "keys/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; the workload's keys and codebook)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "K": w.K,
+                       "l2": "flushed between calls (256 MB write)"},
+            "roofline": {"kernel": "dequantize_kernel", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": None,
+                         "bytes_per_call": bytes_per_call, "peak_source": f"{src} (hbm_gbs)"},
+            "clocks": clk,
+            "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,
+        }), flush=True)
+
+
 if __name__ == "__main__":
     args = _args()
     if args.impl == "reference":
         run_reference(args)
     elif args.path == "attention":
         run_attention(args)
+    elif args.path == "dequantize":
+        run_dequantize(args)
     elif synth.WORKLOADS[args.workload].decode_steps:
         run_decode(args)
     else:

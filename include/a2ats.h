@@ -332,6 +332,45 @@ int a2ats_code_attention_topk(const void* keys, int32_t dtype, int64_t B, int64_
                               size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_dequantize -- v0.39.0 page, "How it works", step 3: each key is
+ * reconstructed from its assigned centroid.  out[b, h, j] = codebook[h,
+ * codes[b, h, j]] for rows j < len[b] (zeros for a code outside [0, K));
+ * rows past len[b] are not written.
+ *   codes    [B, H, Ncap] int32 device
+ *   codebook [H, K, d] device, in dtype; K in [1, 2^24]
+ *   len      [B] int32 device, or NULL for Ncap everywhere
+ *   out      [B, H, Ncap, d] device, in dtype; must not be the codebook
+ * Errors: DTYPE, SHAPE (d a multiple of 8 in [8, 256]), ALIGN, INVALID_ARG
+ * for a NULL array when B*H*Ncap > 0 or out == codebook.
+ * ------------------------------------------------------------------------ */
+int a2ats_dequantize(const int32_t* codes, const void* codebook, int32_t dtype, int64_t B,
+                     int64_t H, int64_t Ncap, int64_t d, int64_t K, const int32_t* len, void* out,
+                     void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_key_byte_accounting -- v0.39.0 page, "Byte accounting" and "What you
+ * get with the defaults": the storage of `tokens` keys of width d as codes
+ * of codebook_bits bits, one per sub_dim numbers (the full-width VQ here has
+ * sub_dim = d and codebook_bits = log2 K).  Host only; no device memory.
+ *   compressed_key_bytes = tokens (d / sub_dim) codebook_bits / 8
+ *   fp16_key_bytes       = tokens d 2
+ *   compression_ratio    = fp16 / compressed = 16 sub_dim / codebook_bits
+ *   codebook_bytes       = 2^codebook_bits sub_dim 2 (fp16 entries)
+ *   assigned_avg_bits    = codebook_bits / sub_dim
+ * Errors: INVALID_ARG for a NULL out, sub_dim < 1 or codebook_bits outside
+ * [1, 24]; SHAPE for tokens < 0, d < 1 or d not a multiple of sub_dim.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    double compressed_key_bytes;
+    double fp16_key_bytes;
+    double compression_ratio;
+    double codebook_bytes;
+    double assigned_avg_bits;
+} a2ats_key_bytes;
+int a2ats_key_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
+                              a2ats_key_bytes* out);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

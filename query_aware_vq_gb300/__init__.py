@@ -69,6 +69,8 @@ _SIGS = {
     "a2ats_copy_retrieval_rows": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "a2ats_rope_split_plain_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_code_attention_topk_workspace_size": [_I64, _I64, _I64, _I64, _I64],
+    "a2ats_dequantize": [_P, _P, _I32, _I64, _I64, _I64, _I64, _I64, _P, _P, _P],
+    "a2ats_key_byte_accounting": [_I64, _I64, _I64, _I32, _P],
     "a2ats_code_attention_topk": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P,
                                   _I32, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
@@ -434,6 +436,40 @@ def a2ats_code_attention_topk(keys, codes, codebook, query, fraction: float = 0.
         _ptr(query), ctypes.byref(rp), int(far_b), float(fraction), _ptr(scores), _ptr(perm),
         _ptr(count), _ptr(ws), nb, _stream(stream)))
     return scores, perm, count
+
+
+class KeyBytes(ctypes.Structure):
+    """a2ats_key_bytes: the byte accounting of a key cache as codes."""
+
+    _fields_ = [("compressed_key_bytes", ctypes.c_double), ("fp16_key_bytes", ctypes.c_double),
+                ("compression_ratio", ctypes.c_double), ("codebook_bytes", ctypes.c_double),
+                ("assigned_avg_bits", ctypes.c_double)]
+
+
+def a2ats_key_byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:
+    """Bytes of `tokens` keys of width d stored as codebook_bits-bit codes,
+    one per sub_dim numbers, against fp16 (host arithmetic only)."""
+    out = KeyBytes()
+    _check("a2ats_key_byte_accounting", _load().a2ats_key_byte_accounting(
+        int(tokens), int(d), int(sub_dim), int(codebook_bits), ctypes.byref(out)))
+    return {name: getattr(out, name) for name, _ in KeyBytes._fields_}
+
+
+def a2ats_dequantize(codes, codebook, *, lengths=None, out=None, stream=None):
+    """Keys reconstructed from their codes: out[b, h, j] = codebook[h,
+    codes[b, h, j]] for rows j < len[b]; returns out [B, H, N, d]."""
+    _dev(codes, codebook, lengths, out)
+    if codes.dtype != torch.int32 or codes.dim() != 3:
+        raise TypeError("codes must be int32 [B, H, N]")
+    cb = codebook if codebook.dim() == 3 else codebook.unsqueeze(0)
+    B, H, N = codes.shape
+    K, d = cb.shape[1], cb.shape[2]
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=cb.dtype, device=codes.device)
+    _check("a2ats_dequantize", _load().a2ats_dequantize(
+        _ptr(codes), _ptr(cb), _dt(cb), B, H, N, d, K, _ptr(_lens(lengths)), _ptr(out),
+        _stream(stream)))
+    return out
 
 
 def a2ats_copy_retrieval_rows(src, dst, perm, count, *, lengths=None, stream=None):

@@ -698,6 +698,37 @@ int a2ats_code_attention_topk(const void* keys, int32_t dtype, int64_t B, int64_
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+int a2ats_dequantize(const int32_t* codes, const void* codebook, int32_t dtype, int64_t B,
+                     int64_t H, int64_t Ncap, int64_t d, int64_t K, const int32_t* len, void* out,
+                     void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (!codes || !codebook || !out) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(codes) || !aligned16(codebook) || !aligned16(out)) return A2ATS_ERR_ALIGN;
+    if (out == codebook) return A2ATS_ERR_INVALID_ARG;
+    cudaError_t e = launch_dequantize(codes, codebook, dtype, Shape{B, H, Ncap, d}, K, len, out,
+                                      (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+int a2ats_key_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
+                              a2ats_key_bytes* out) {
+    if (!out) return A2ATS_ERR_INVALID_ARG;
+    if (tokens < 0 || d < 1) return A2ATS_ERR_SHAPE;
+    if (sub_dim < 1 || codebook_bits < 1 || codebook_bits > 24) return A2ATS_ERR_INVALID_ARG;
+    if (d % sub_dim != 0) return A2ATS_ERR_SHAPE;
+    const double groups = (double)(d / sub_dim);
+    out->compressed_key_bytes = (double)tokens * groups * (double)codebook_bits / 8.0;
+    out->fp16_key_bytes = (double)tokens * (double)d * 2.0;
+    out->compression_ratio = 16.0 * (double)sub_dim / (double)codebook_bits;
+    out->codebook_bytes = (double)(int64_t(1) << codebook_bits) * (double)sub_dim * 2.0;
+    out->assigned_avg_bits = (double)codebook_bits / (double)sub_dim;
+    return A2ATS_OK;
+}
+
 int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64_t H,
                               int64_t Ncap, const int32_t* len, const int32_t* perm,
                               const int32_t* count, void* stream) {

@@ -151,6 +151,40 @@ near_score_kernel(const void* __restrict__ keys, int64_t nbh, int32_t H, int32_t
     }
 }
 
+// Dequantisation (v0.39.0 page, "How it works", step 3: a key is
+// reconstructed from its assigned centroid): row j of out = codebook row
+// codes[j] of its head, zeros for a code outside [0, K).  vec lanes per row,
+// one 16-byte chunk each; grid-stride over rows with (bh, j) advanced by the
+// stride without divisions; rows past len are left alone.
+__global__ void __launch_bounds__(kRowThreads)
+dequantize_kernel(const int32_t* __restrict__ codes, const uint4* __restrict__ cb,
+                  uint4* __restrict__ out, int64_t rows, int32_t H, int32_t ncap, int32_t vec,
+                  int64_t K, const int32_t* __restrict__ len) {
+    const int rpb = kRowThreads / vec;
+    const int lane = threadIdx.x % vec, rl = threadIdx.x / vec;
+    if (rl >= rpb) return;  // vec need not divide the block
+    const int64_t stride = (int64_t)gridDim.x * rpb;
+    const int64_t qs = stride / ncap;
+    const int32_t rs = (int32_t)(stride - qs * ncap);
+    int64_t row = (int64_t)blockIdx.x * rpb + rl;
+    int32_t bh = (int32_t)(row / ncap);  // B H <= 65535
+    int32_t j = (int32_t)(row - (int64_t)bh * ncap);
+    for (; row < rows; row += stride) {
+        if (j < seq_len(len, bh / H, ncap)) {
+            const int32_t c = codes[row];
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (c >= 0 && c < K) v = cb[((int64_t)(bh % H) * K + c) * vec + lane];
+            out[row * vec + lane] = v;
+        }
+        j += rs;
+        bh += (int32_t)qs;
+        if (j >= ncap) {
+            j -= ncap;
+            bh++;
+        }
+    }
+}
+
 int device_sms() {
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
@@ -208,6 +242,22 @@ cudaError_t launch_code_attention(const void* keys, int dt, const Shape& s, cons
                 keys, nbh, (int32_t)s.H, (int32_t)s.Ncap, d, (int32_t)win, len, ra, q_near, scores);
         note_launches(1);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const int32_t* codes, const void* codebook, int dt, const Shape& s,
+                              int64_t K, const int32_t* len, void* out, cudaStream_t st) {
+    const int64_t rows = s.B * s.H * s.Ncap;
+    if (rows == 0) return cudaSuccess;
+    const int32_t vec = (int32_t)(s.d * (dt == kF32 ? 4 : 2) / 16);
+    const int64_t rpb = kRowThreads / vec;
+    int64_t blocks = (rows + rpb - 1) / rpb;
+    const int64_t cap = 16 * (int64_t)device_sms();
+    if (blocks > cap) blocks = cap;
+    dequantize_kernel<<<(unsigned)blocks, kRowThreads, 0, st>>>(
+        codes, reinterpret_cast<const uint4*>(codebook), reinterpret_cast<uint4*>(out), rows,
+        (int32_t)s.H, (int32_t)s.Ncap, vec, K, len);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,11 @@ cudaError_t launch_code_attention(const void* keys, int dt, const Shape& s, cons
                                   const void* query, const RopeArgs& ra, int32_t far_b,
                                   float* q_near, float* lut, float* scores, cudaStream_t st);
 
+// out [B, H, Ncap, d] (the codebook's dtype) <- codebook[h, codes[b, h, j]]
+// for rows j < len[b]; zeros for a code outside [0, K).
+cudaError_t launch_dequantize(const int32_t* codes, const void* codebook, int dt, const Shape& s,
+                              int64_t K, const int32_t* len, void* out, cudaStream_t st);
+
 // row len[b] of each (b, h) <- rows[b, h]; then len[b] += 1 (capped at Ncap)
 cudaError_t launch_append_rows(void* cache, int dt, const Shape& s, int32_t* len, const void* rows,
                                cudaStream_t st);

@@ -166,6 +166,33 @@ def test_code_attention_topk_validation(lib):
     assert call(nb=need - 1) == -6
 
 
+def test_dequantize_validation(lib):
+    f = lib.a2ats_dequantize
+    assert f(FAKE, FAKE + 4096, 9, 1, 2, 64, 128, 256, None, FAKE + 8192, None) == -3
+    assert f(FAKE, FAKE + 4096, 1, 1, 2, 64, 12, 256, None, FAKE + 8192, None) == -2
+    assert f(FAKE, FAKE + 4096, 1, 1, 2, 64, 128, 0, None, FAKE + 8192, None) == -2
+    assert f(None, FAKE + 4096, 1, 1, 2, 64, 128, 256, None, FAKE + 8192, None) == -1
+    assert f(FAKE, FAKE + 4096, 1, 1, 2, 64, 128, 256, None, FAKE + 4096, None) == -1
+    assert f(FAKE, FAKE + 4100, 1, 1, 2, 64, 128, 256, None, FAKE + 8192, None) == -4
+    assert f(None, None, 1, 0, 2, 64, 128, 256, None, None, None) == 0
+
+
+def test_key_byte_accounting_matches_the_page_table():
+    """v0.39.0 page, "What you get with the defaults", through the C ABI."""
+    from _golden import lines
+    for row in lines("compression_defaults.txt"):
+        acc = q.a2ats_key_byte_accounting(1000, 128, int(row[0]), int(row[1]))
+        assert acc["assigned_avg_bits"] == float(row[2])
+        assert acc["compression_ratio"] == float(row[3])
+        assert acc["codebook_bytes"] / 1024 == float(row[4])
+    # the full-width codes of the Llama-3.2-3B layer: 10 bits per 128-number key
+    acc = q.a2ats_key_byte_accounting(32768, 128, 128, 10)
+    assert acc["compressed_key_bytes"] == 32768 * 10 / 8
+    assert acc["compression_ratio"] == 16 * 128 / 10
+    with pytest.raises(q.A2ATSError):
+        q.a2ats_key_byte_accounting(10, 128, 5, 8)
+
+
 def test_copy_retrieval_rows_validation(lib):
     f = lib.a2ats_copy_retrieval_rows
     assert f(FAKE, FAKE, -1, 2, 10, None, FAKE, FAKE, None) == -2
