@@ -71,7 +71,8 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--path", choices=["step", "attention", "dequantize"], default="step",
+    p.add_argument("--path", choices=["step", "attention", "dequantize", "subvector"],
+                   default="step",
                    help="attention: time the code-based attention scores and top tokens; "
                         "dequantize: time the reconstruction of the keys from their codes "
                         "(both steps after the path) instead of the step")
@@ -819,6 +820,65 @@ def run_dequantize(a):
         }), flush=True)
 
 
+def run_subvector(a):
+    """The pages' wrapper defaults on the workload's cache: sub-vector VQ at
+    sub_dim = 8 with 2^8 centroids for keys (H-weighted retrieval tokens,
+    8 x 8 factor) and values (plain); L2 flushed between steps."""
+    import query_aware_vq_gb300 as q
+    from query_aware_vq_gb300.pipeline import A2ATSSubvectorStep
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    s, K = 8, 256
+    keys, _, _, _ = _inputs(w, rank)
+    kd = keys.cuda()
+    vd = synth.gaussian((w.B, w.H, w.N, w.d), seed=7000 + rank, dtype="f32").cuda()
+    ck = synth.gaussian((w.H, K, s), seed=7100, dtype="f32").cuda()
+    cv = synth.gaussian((w.H, K, s), seed=7200, dtype="f32").cuda()
+    Qd = synth.gaussian((w.H, 8192, s), seed=7300, dtype="f32").cuda()
+    L, _ = q.a2ats_cholesky_factor(q.a2ats_query_second_moment(Qd, 1e-4))
+    step = A2ATSSubvectorStep(w.B, w.H, w.N, w.d, s, K, synth.DTYPES[w.dtype], window=w.W,
+                              fraction=w.fraction, rope_base=w.rope_base)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(a.warmup, 3)):
+        step(kd, vd, ck, cv, L)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    evs = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(kd, vd, ck, cv, L)
+        e1.record(stream)
+        evs.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / a.steps, world)
+    keys_per_step = w.B * w.H * w.N
+    if rank == 0:
+        print(json.dumps({
+            "metric": "tokens quantised/sec (sub-vector VQ of keys and values)",
+            "value": world * keys_per_step / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; the workload's keys, Gaussian values and tables)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "sub_dim": s, "K": K, "window": w.W, "fraction": w.fraction,
+                       "l2": "flushed between steps (256 MB write)"},
+            "clocks": clk,
+            "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,
+        }), flush=True)
+
+
 if __name__ == "__main__":
     args = _args()
     if args.impl == "reference":
@@ -827,6 +887,8 @@ if __name__ == "__main__":
         run_attention(args)
     elif args.path == "dequantize":
         run_dequantize(args)
+    elif args.path == "subvector":
+        run_subvector(args)
     elif synth.WORKLOADS[args.workload].decode_steps:
         run_decode(args)
     else:

@@ -269,3 +269,93 @@ class A2ATSDecodeStep:
                   lengths=lengths, rope=self.rope, rows="last", codes=self.codes, workspace=ws,
                   stream=st)
         return self
+
+
+class A2ATSSubvectorStep:
+    """The pages' wrapper defaults: sub-vector (product) VQ of keys and
+    values (v0.39.0 page, configuration a2ats_sub_dim = 8 and
+    a2ats_codebook_bits = 8, "How it works" steps 1-5; the API page's
+    functions take [N, d] sub-vectors), composed from the C-ABI calls:
+
+      1. k~ = windowed RoPE of the cache, fp32 (the rotation
+         pairs elements across sub-vectors, so it runs on
+         the whole head first)                                 a2ats_windowed_rope
+      2. the retrieval split over tokens (full-width cosine
+         with the proxy query k~_t)                            a2ats_select_retrieval_set
+      3. every token's sub-vectors: plain nearest centroid     a2ats_h_weighted_assign, L = I
+      4. the retrieval tokens' sub-vectors: the H-weighted
+         rule with the sub_dim x sub_dim factor L               a2ats_h_weighted_assign
+      5. routed by copy over the sub-vector rows               a2ats_copy_retrieval_rows
+      6. values' sub-vectors: plain nearest centroid, no RoPE
+         and no retrieval preference ("How it works" step 5)   a2ats_h_weighted_assign, L = I
+
+    A token of width d is d / sub_dim sub-vector rows; sub-vector row
+    j * G + g of a (b, h) is elements g * sub_dim .. of token j (G = d /
+    sub_dim).  Codebooks are [H, K, sub_dim] (a table shared by the heads is
+    passed once per head).  codes_k and codes_v are [B, H, N, G] int32.
+    Buffers are allocated once in the constructor."""
+
+    def __init__(self, B: int, H: int, N: int, d: int, sub_dim: int, K: int, dtype, *,
+                 window: int, fraction: float, rope_base: float, interleaved: bool = False,
+                 device="cuda"):
+        if sub_dim < 8 or d % sub_dim:
+            raise ValueError("sub_dim must divide d and be at least 8")
+        self.B, self.H, self.N, self.d, self.s, self.K = B, H, N, d, sub_dim, K
+        self.G = d // sub_dim
+        self.fraction = fraction
+        self.rope = dict(window=window, far_offset=0, rope_base=rope_base,
+                         interleaved=interleaved)
+        dev = torch.device(device)
+        lib = library()
+        G, NG = self.G, N * self.G
+        self.k_tilde = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.perm = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+        self.count = torch.empty((B, H), dtype=torch.int32, device=dev)
+        self.sub_perm = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
+        self.sub_count = torch.empty((B, H), dtype=torch.int32, device=dev)
+        self.sub_len = torch.empty((B,), dtype=torch.int32, device=dev)
+        self._g = torch.arange(G, dtype=torch.int32, device=dev)
+        self.codes_k = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
+        self.codes_ret = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
+        self.codes_v = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
+        ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, NG, sub_dim, K),
+                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def __call__(self, keys, values, codebook_k, codebook_v, L, lengths=None, stream=None):
+        """keys, values [B, H, N, d] (keys pre-RoPE); codebook_k [H, K, sub_dim]
+        fp32 (the rotated keys are fp32), codebook_v [H, K, sub_dim] in the
+        values' dtype; L [H, sub_dim, sub_dim] the factor of the sub-vector
+        H; lengths [B] int32 or None."""
+        st = stream if stream is not None else torch.cuda.current_stream()
+        B, H, N, G, s = self.B, self.H, self.N, self.G, self.s
+        ws = self.workspace
+        with torch.cuda.stream(st):
+            if lengths is None:
+                self.sub_len.fill_(N * G)
+            else:
+                torch.mul(lengths, G, out=self.sub_len)
+            a2ats_windowed_rope(keys, lengths=lengths, out=self.k_tilde, stream=st, **self.rope)
+            a2ats_select_retrieval_set(self.k_tilde, None, self.fraction, lengths=lengths,
+                                       perm=self.perm, count=self.count, workspace=ws, stream=st)
+            # sub-vector rows of the retrieval tokens: j * G + g for the
+            # token-level split (both halves stay ascending)
+            self.sub_perm.copy_(self.perm.unsqueeze(-1).expand(B, H, N, G))
+            self.sub_perm.mul_(G).add_(self._g)
+            torch.mul(self.count, G, out=self.sub_count)
+            ksub = self.k_tilde.view(B, H, N * G, s)
+            kc = self.codes_k.view(B, H, N * G)
+            a2ats_h_weighted_assign(ksub, codebook_k, None, lengths=self.sub_len, rows="all",
+                                    codes=kc, workspace=ws, stream=st)
+            a2ats_h_weighted_assign(ksub, codebook_k, L, lengths=self.sub_len, rows="retrieval",
+                                    perm=self.sub_perm.view(B, H, N * G), count=self.sub_count,
+                                    codes=self.codes_ret.view(B, H, N * G), workspace=ws,
+                                    stream=st)
+            a2ats_copy_retrieval_rows(self.codes_ret.view(B, H, N * G), kc,
+                                      self.sub_perm.view(B, H, N * G), self.sub_count,
+                                      lengths=self.sub_len, stream=st)
+            vsub = values.reshape(B, H, N * G, s)
+            a2ats_h_weighted_assign(vsub, codebook_v, None, lengths=self.sub_len, rows="all",
+                                    codes=self.codes_v.view(B, H, N * G), workspace=ws,
+                                    stream=st)
+        return self
