@@ -79,6 +79,8 @@ def _load():
         lib.orc_code_attention_topk.restype = ctypes.c_int64
         lib.orc_dequantize.argtypes = [_i32p, ctypes.c_int64, _f64p, ctypes.c_int64,
                                        ctypes.c_int64, _f64p]
+        lib.orc_kmeanspp.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     _f64p, ctypes.c_int64, _f64p, _i32p, _f64p]
         _lib = lib
     return _lib
 
@@ -225,6 +227,22 @@ def dequantize(codes, codebook) -> np.ndarray:
     out = np.empty((n, d))
     _load().orc_dequantize(_p(codes, _i32p), n, _p(codebook, _f64p), K, d, _p(out, _f64p))
     return out
+
+
+def kmeanspp(z, K: int, u, iters: int):
+    """k-means++ seeding with uniform draws u [K], then `iters` Lloyd rounds,
+    on points z [n, d].  Returns (centroids [K, d], codes [n], objective
+    [iters + 1])."""
+    z = _f64(z)
+    n, d = z.shape
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    assert u.shape == (K,)
+    cent = np.empty((K, d))
+    codes = np.empty(n, np.int32)
+    obj = np.empty(iters + 1)
+    _load().orc_kmeanspp(_p(z, _f64p), n, d, K, _p(u, _f64p), int(iters), _p(cent, _f64p),
+                         _p(codes, _i32p), _p(obj, _f64p))
+    return cent, codes, obj
 
 
 def byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:

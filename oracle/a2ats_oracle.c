@@ -397,3 +397,100 @@ void orc_dequantize(const int32_t* codes, int64_t n, const double* codebook, int
             out[j * d + a] = (c >= 0 && c < K) ? codebook[(int64_t)c * d + a] : 0.0;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Codebook calibration in z space.  API page, a2ats_cholesky_factor: L     */
+/* maps the H-weighted objective to a plain Euclidean one on z = k L, which */
+/* lets conventional k-means++ build the codebook (the codebook in key      */
+/* space is then c = c_z L^-1).  Reading: k-means++ seeding, each centre    */
+/* drawn with probability proportional to the squared distance D^2 to the    */
+/* nearest centre chosen so far (the first uniformly), with the uniform      */
+/* draws u[0..K) given as input: centre k is the first point whose running   */
+/* sum of D^2 exceeds u[k] * (sum of D^2), or point floor(u[k] n) when every */
+/* D^2 is 0 (the first centre: point floor(u[0] n)); then `iters` Lloyd      */
+/* rounds: assign each point to its nearest centre (ties to the lower       */
+/* index), move each centre to the mean of its points (a centre without     */
+/* points stays).  objective[r] is the sum of squared distances after the   */
+/* assignment of round r (r = iters: the final assignment, whose codes are   */
+/* returned).                                                               */
+/* ------------------------------------------------------------------------ */
+static double sq_dist(const double* a, const double* b, int64_t d) {
+    double s = 0.0;
+    for (int64_t i = 0; i < d; i++) {
+        double t = a[i] - b[i];
+        s += t * t;
+    }
+    return s;
+}
+
+static double assign_all(const double* z, int64_t n, int64_t d, const double* c, int64_t K,
+                         int32_t* codes) {
+    double total = 0.0;
+    for (int64_t i = 0; i < n; i++) {
+        double best = INFINITY;
+        int32_t bj = 0;
+        for (int64_t j = 0; j < K; j++) {
+            double v = sq_dist(z + i * d, c + j * d, d);
+            if (v < best) {
+                best = v;
+                bj = (int32_t)j;
+            }
+        }
+        codes[i] = bj;
+        total += best;
+    }
+    return total;
+}
+
+void orc_kmeanspp(const double* z, int64_t n, int64_t d, int64_t K, const double* u,
+                  int64_t iters, double* centroids, int32_t* codes, double* objective) {
+    double* d2 = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    int64_t first = (int64_t)floor(u[0] * (double)n);
+    if (first >= n) first = n - 1;
+    if (first < 0) first = 0;
+    memcpy(centroids, z + first * d, sizeof(double) * (size_t)d);
+    for (int64_t i = 0; i < n; i++) d2[i] = sq_dist(z + i * d, centroids, d);
+    for (int64_t k = 1; k < K; k++) {
+        double total = 0.0;
+        for (int64_t i = 0; i < n; i++) total += d2[i];
+        int64_t pick;
+        if (total > 0.0) {
+            double target = u[k] * total, run = 0.0;
+            pick = n - 1;
+            for (int64_t i = 0; i < n; i++) {
+                run += d2[i];
+                if (run > target) {
+                    pick = i;
+                    break;
+                }
+            }
+        } else {
+            pick = (int64_t)floor(u[k] * (double)n);
+            if (pick >= n) pick = n - 1;
+            if (pick < 0) pick = 0;
+        }
+        memcpy(centroids + k * d, z + pick * d, sizeof(double) * (size_t)d);
+        for (int64_t i = 0; i < n; i++) {
+            double v = sq_dist(z + i * d, centroids + k * d, d);
+            if (v < d2[i]) d2[i] = v;
+        }
+    }
+    double* sum = (double*)malloc(sizeof(double) * (size_t)(K * d));
+    int64_t* cnt = (int64_t*)malloc(sizeof(int64_t) * (size_t)K);
+    for (int64_t r = 0; r < iters; r++) {
+        objective[r] = assign_all(z, n, d, centroids, K, codes);
+        memset(sum, 0, sizeof(double) * (size_t)(K * d));
+        memset(cnt, 0, sizeof(int64_t) * (size_t)K);
+        for (int64_t i = 0; i < n; i++) {
+            cnt[codes[i]]++;
+            for (int64_t a = 0; a < d; a++) sum[codes[i] * d + a] += z[i * d + a];
+        }
+        for (int64_t j = 0; j < K; j++)
+            if (cnt[j] > 0)
+                for (int64_t a = 0; a < d; a++) centroids[j * d + a] = sum[j * d + a] / (double)cnt[j];
+    }
+    objective[iters] = assign_all(z, n, d, centroids, K, codes);
+    free(cnt);
+    free(sum);
+    free(d2);
+}
