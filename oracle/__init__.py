@@ -77,6 +77,8 @@ def _load():
                                                 ctypes.c_double, ctypes.c_int, ctypes.c_double,
                                                 _i32p, _f64p, _f64p]
         lib.orc_code_attention_topk.restype = ctypes.c_int64
+        for fn in (lib.orc_cholesky_rows, lib.orc_cholesky_solve_rows):
+            fn.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p]
         lib.orc_dequantize.argtypes = [_i32p, ctypes.c_int64, _f64p, ctypes.c_int64,
                                        ctypes.c_int64, _f64p]
         lib.orc_kmeanspp.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -227,6 +229,30 @@ def dequantize(codes, codebook) -> np.ndarray:
     out = np.empty((n, d))
     _load().orc_dequantize(_p(codes, _i32p), n, _p(codebook, _f64p), K, d, _p(out, _f64p))
     return out
+
+
+def cholesky_rows(x, l) -> np.ndarray:
+    """z = x L for rows x [n, d] (the change of variables of the Cholesky
+    route, API page, a2ats_cholesky_factor)."""
+    x = _f64(x)
+    l = _f64(l)
+    n, d = x.shape
+    assert l.shape == (d, d)
+    z = np.empty((n, d))
+    _load().orc_cholesky_rows(_p(x, _f64p), n, d, _p(l, _f64p), _p(z, _f64p))
+    return z
+
+
+def cholesky_solve_rows(z, l) -> np.ndarray:
+    """c [n, d] with c L = z, L lower triangular (z-space centroids mapped
+    back to key space)."""
+    z = _f64(z)
+    l = _f64(l)
+    n, d = z.shape
+    assert l.shape == (d, d)
+    c = np.empty((n, d))
+    _load().orc_cholesky_solve_rows(_p(z, _f64p), n, d, _p(l, _f64p), _p(c, _f64p))
+    return c
 
 
 def kmeanspp(z, K: int, u, iters: int):

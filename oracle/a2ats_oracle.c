@@ -399,6 +399,32 @@ void orc_dequantize(const int32_t* codes, int64_t n, const double* codebook, int
 }
 
 /* ------------------------------------------------------------------------ */
+/* The change of variables of the Cholesky route.  API page,                */
+/* a2ats_cholesky_factor: with H = L L^T, (k - c) H (k - c)^T equals         */
+/* |z_k - z_c|^2 for z = k L, so k-means in z is the H-weighted objective.  */
+/* orc_cholesky_rows maps rows to z; orc_cholesky_solve_rows maps z-space   */
+/* rows (the centroids k-means finds there) back: c with c L = z, by back   */
+/* substitution from the last column (L lower triangular, so column b of    */
+/* c L only involves c_a for a >= b).                                       */
+/* ------------------------------------------------------------------------ */
+void orc_cholesky_rows(const double* x, int64_t n, int64_t d, const double* l, double* z) {
+    for (int64_t i = 0; i < n; i++) times_l(x + i * d, l, d, z + i * d);
+}
+
+void orc_cholesky_solve_rows(const double* z, int64_t n, int64_t d, const double* l,
+                             double* c) {
+    for (int64_t i = 0; i < n; i++) {
+        const double* zi = z + i * d;
+        double* ci = c + i * d;
+        for (int64_t b = d - 1; b >= 0; b--) {
+            double s = zi[b];
+            for (int64_t a = b + 1; a < d; a++) s -= ci[a] * l[a * d + b];
+            ci[b] = s / l[b * d + b];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Codebook calibration in z space.  API page, a2ats_cholesky_factor: L     */
 /* maps the H-weighted objective to a plain Euclidean one on z = k L, which */
 /* lets conventional k-means++ build the codebook (the codebook in key      */

@@ -95,6 +95,12 @@ int64_t orc_code_attention_topk(const double* keys, int64_t n, int64_t d, int64_
 void orc_dequantize(const int32_t* codes, int64_t n, const double* codebook, int64_t K,
                     int64_t d, double* out);
 
+/* z [n, d] = x L (row vectors times L [d, d]); c [n, d] with c L = z for a
+ * lower-triangular L with nonzero diagonal. */
+void orc_cholesky_rows(const double* x, int64_t n, int64_t d, const double* l, double* z);
+void orc_cholesky_solve_rows(const double* z, int64_t n, int64_t d, const double* l,
+                             double* c);
+
 /* k-means++ seeding with the given uniform draws u [K], then `iters` Lloyd
  * rounds, on points z [n, d]; centroids [K, d], the final codes [n] and
  * objective [iters + 1] (sum of squared distances after each assignment). */

@@ -70,3 +70,36 @@ def test_codebook_in_key_space_reaches_the_h_weighted_rule():
     c = np.linalg.solve(L.T, cz.T).T  # c L = c_z
     want, _, _ = oracle.assign_cholesky(k, c, L)
     assert want.tolist() == codes.tolist()
+
+
+def test_cholesky_rows_hand_worked():
+    # x = (1, 2), L = [[2, 0], [3, 4]]: z_0 = 1*2 + 2*3 = 8, z_1 = 2*4 = 8
+    l = np.array([[2.0, 0.0], [3.0, 4.0]])
+    z = oracle.cholesky_rows(np.array([[1.0, 2.0]]), l)
+    np.testing.assert_array_equal(z, [[8.0, 8.0]])
+    # back: c_1 = 8 / 4 = 2, c_0 = (8 - 2 * 3) / 2 = 1
+    np.testing.assert_array_equal(oracle.cholesky_solve_rows(z, l), [[1.0, 2.0]])
+
+
+def test_cholesky_rows_give_the_h_weighted_norm():
+    """|x L|^2 = x H x^T with H = L L^T (the identity behind the route)."""
+    rng = np.random.default_rng(5)
+    d = 12
+    A = rng.standard_normal((d, d))
+    hm = A @ A.T / d + 0.2 * np.eye(d)
+    L = np.linalg.cholesky(hm)
+    x = rng.standard_normal((40, d))
+    z = oracle.cholesky_rows(x, L)
+    np.testing.assert_allclose((z * z).sum(1), np.einsum("na,ab,nb->n", x, hm, x), rtol=1e-12)
+    np.testing.assert_array_equal(oracle.cholesky_rows(x, np.eye(d)), x)
+
+
+def test_cholesky_solve_rows_is_the_triangular_solve():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(6)
+    d = 16
+    A = rng.standard_normal((d, d))
+    L = np.linalg.cholesky(A @ A.T / d + 0.1 * np.eye(d))
+    z = rng.standard_normal((25, d))
+    want = scipy_linalg.solve_triangular(L.T, z.T, lower=False).T
+    np.testing.assert_allclose(oracle.cholesky_solve_rows(z, L), want, rtol=1e-10, atol=1e-12)
