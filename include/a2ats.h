@@ -371,6 +371,76 @@ int a2ats_key_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_
                               a2ats_key_bytes* out);
 
 /* --------------------------------------------------------------------------
+ * a2ats_cholesky_rows -- the change of variables of [API]
+ * a2ats_cholesky_factor: z = x L for every row, so that the H-weighted
+ * distance (x - c) H (x - c)^T with H = L L^T is |z_x - z_c|^2 and
+ * conventional k-means on z calibrates an H-weighted codebook.
+ *   x  [H, n, d] device, in dtype (e.g. calibration keys of one layer, head
+ *      by head)
+ *   L  [H, d, d] fp32 device; only the lower triangle (with the diagonal) is
+ *      read
+ *   z  [H, n, d] fp32 device output; must not be x
+ * Each element is a compensated fp32 dot product (twice-fp32 accumulation)
+ * rounded once.  n < 2^24; d a multiple of 8 in [8, 256].
+ * Errors: DTYPE, SHAPE, ALIGN, INVALID_ARG for a NULL array when H*n > 0 or
+ * z == x, WORKSPACE.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_cholesky_rows_workspace_size(int64_t H, int64_t n, int64_t d);
+int a2ats_cholesky_rows(const void* x, int32_t dtype, int64_t H, int64_t n, int64_t d,
+                        const float* L, float* z, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_cholesky_solve_rows -- back from z space ([API]
+ * a2ats_cholesky_factor): c with c L = zc for every row, so that centroids
+ * found by k-means on z = x L become a key-space codebook for
+ * a2ats_h_weighted_assign with the same L.
+ *   zc [H, rows, d] fp32 device; c [H, rows, d] fp32 device output (may be
+ *   zc itself)
+ *   L  [H, d, d] fp32 device, lower triangular with a nonzero diagonal (a
+ *      Cholesky factor); only the lower triangle is read
+ * Back substitution from the last column in fp64, rounded to fp32.
+ * rows <= 2^24, H*rows <= 2^30; d a multiple of 8 in [8, 256].
+ * Errors: SHAPE, ALIGN, INVALID_ARG for a NULL array when H*rows > 0.
+ * ------------------------------------------------------------------------ */
+int a2ats_cholesky_solve_rows(const float* zc, int64_t H, int64_t rows, int64_t d, const float* L,
+                              float* c, void* stream);
+
+/* --------------------------------------------------------------------------
+ * a2ats_kmeanspp -- codebook calibration by k-means++ in z space ([API]
+ * a2ats_cholesky_factor: k-means++ on z = k L builds the H-weighted
+ * codebook), head by head.
+ *   Seeding: centre 0 is row floor(u[h, 0] n); centre k is the first row
+ *   whose running sum of D^2 (the squared distance to the nearest centre
+ *   chosen so far) exceeds u[h, k] times the sum of D^2 over all rows, or
+ *   row floor(u[h, k] n) when every D^2 is 0 (row indices clamped to
+ *   [0, n)).  D^2 and its running sums are fp64.
+ *   Then `iters` Lloyd rounds: each row takes its nearest centroid (ties to
+ *   the lower index; the exact assignment of a2ats_h_weighted_assign with
+ *   L = NULL), each centroid moves to the fp64 mean of its rows (rounded to
+ *   fp32) and a centroid without rows stays; a last assignment follows.
+ *   z          [H, n, d] fp32 device (e.g. from a2ats_cholesky_rows); 1 <= n
+ *              < 2^24; d a multiple of 8 in [8, 256]
+ *   u          [H, K] fp64 device: the uniform draws, in [0, 1)
+ *   iters      Lloyd rounds, in [0, 2^20]
+ *   centroids  [H, K, d] fp32 device output: the z-space codebook after the
+ *              last mean step (the seeds when iters = 0); K in [1, 2^24]
+ *   codes      [H, n] int32 device output: the last assignment
+ *   objective  [H, iters + 1] fp64 device output: the sum over rows of the
+ *              squared distance to the assigned centroid, after each
+ *              assignment (entry iters belongs to the returned codes)
+ * z, centroids and codes must not overlap.  The rows must be finite with
+ * squares that do not overflow fp32.
+ * Errors: SHAPE (also n = 0 with H > 0), INVALID_ARG for a NULL array,
+ * iters out of range or overlapping arrays, ALIGN (z, centroids, codes
+ * 16-byte; u, objective 8-byte), WORKSPACE.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_kmeanspp_workspace_size(int64_t H, int64_t n, int64_t d, int64_t K);
+int a2ats_kmeanspp(const float* z, int64_t H, int64_t n, int64_t d, int64_t K, const double* u,
+                   int32_t iters, float* centroids, int32_t* codes, double* objective,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

@@ -75,6 +75,11 @@ _SIGS = {
                                   _I32, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
                                       _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
+    "a2ats_cholesky_rows_workspace_size": [_I64, _I64, _I64],
+    "a2ats_cholesky_rows": [_P, _I32, _I64, _I64, _I64, _P, _P, _P, _SZ, _P],
+    "a2ats_cholesky_solve_rows": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "a2ats_kmeanspp_workspace_size": [_I64, _I64, _I64, _I64],
+    "a2ats_kmeanspp": [_P, _I64, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _P, _SZ, _P],
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
@@ -106,7 +111,9 @@ def _load():
                      "a2ats_query_aware_assign_workspace_size",
                      "a2ats_select_retrieval_set_workspace_size",
                      "a2ats_rope_split_plain_assign_workspace_size",
-                     "a2ats_code_attention_topk_workspace_size"):
+                     "a2ats_code_attention_topk_workspace_size",
+                     "a2ats_cholesky_rows_workspace_size",
+                     "a2ats_kmeanspp_workspace_size"):
             getattr(lib, name).restype = ctypes.c_size_t
         lib.a2ats_kernel_launches.restype = ctypes.c_uint64
         lib.a2ats_timed_kernels_ms.restype = ctypes.c_double
@@ -483,6 +490,77 @@ def a2ats_copy_retrieval_rows(src, dst, perm, count, *, lengths=None, stream=Non
         _ptr(src), _ptr(dst), B, H, N, _ptr(_lens(lengths)), _ptr(perm), _ptr(count),
         _stream(stream)))
     return dst
+
+
+def _as3(t: torch.Tensor, what: str) -> torch.Tensor:
+    if t.dim() == 2:
+        return t.unsqueeze(0)
+    if t.dim() != 3:
+        raise ValueError(f"{what} must be [n, d] or [H, n, d]")
+    return t
+
+
+def a2ats_cholesky_rows(x, L, *, out=None, workspace=None, stream=None):
+    """z = x L per head: x [H, n, d] (or [n, d]) in any supported dtype, L
+    [H, d, d] fp32 (lower triangle read); returns fp32 z of x's shape."""
+    _dev(x, L, out)
+    x3 = _as3(x, "x")
+    L3 = L if L.dim() == 3 else L.unsqueeze(0)
+    Hh, n, d = x3.shape
+    if L3.dtype != torch.float32 or L3.shape != (Hh, d, d):
+        raise TypeError("L must be fp32 [H, d, d]")
+    if out is None:
+        out = torch.empty((Hh, n, d), dtype=torch.float32, device=x.device)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_cholesky_rows_workspace_size(Hh, n, d), x.device, workspace)
+    _check("a2ats_cholesky_rows", lib.a2ats_cholesky_rows(
+        _ptr(x3), _dt(x3), Hh, n, d, _ptr(L3), _ptr(out), _ptr(ws), nb, _stream(stream)))
+    return out if x.dim() == 3 else out[0]
+
+
+def a2ats_cholesky_solve_rows(zc, L, *, out=None, stream=None):
+    """c with c L = zc per head (z-space rows back to key space): zc [H, rows,
+    d] fp32 (or [rows, d]), L [H, d, d] fp32 lower triangular."""
+    _dev(zc, L, out)
+    z3 = _as3(zc, "zc")
+    L3 = L if L.dim() == 3 else L.unsqueeze(0)
+    Hh, rows, d = z3.shape
+    if z3.dtype != torch.float32 or L3.dtype != torch.float32 or L3.shape != (Hh, d, d):
+        raise TypeError("zc must be fp32 [H, rows, d] and L fp32 [H, d, d]")
+    if out is None:
+        out = torch.empty((Hh, rows, d), dtype=torch.float32, device=zc.device)
+    _check("a2ats_cholesky_solve_rows", _load().a2ats_cholesky_solve_rows(
+        _ptr(z3), Hh, rows, d, _ptr(L3), _ptr(out), _stream(stream)))
+    return out if zc.dim() == 3 else out[0]
+
+
+def a2ats_kmeanspp(z, K: int, u, iters: int, *, centroids=None, codes=None, objective=None,
+                   workspace=None, stream=None):
+    """k-means++ seeding with the uniform draws u [H, K] (fp64), then `iters`
+    Lloyd rounds, on fp32 rows z [H, n, d] (or [n, d] with u [K]).  Returns
+    (centroids [H, K, d] fp32, codes [H, n] int32, objective [H, iters + 1]
+    fp64), without the head axis for 2-d z."""
+    _dev(z, u, centroids, codes, objective)
+    z3 = _as3(z, "z")
+    Hh, n, d = z3.shape
+    u2 = (u if u.dim() == 2 else u.unsqueeze(0)).contiguous()
+    if z3.dtype != torch.float32 or u2.dtype != torch.float64 or u2.shape != (Hh, K):
+        raise TypeError("z must be fp32 [H, n, d] and u fp64 [H, K]")
+    dev = z.device
+    if centroids is None:
+        centroids = torch.empty((Hh, K, d), dtype=torch.float32, device=dev)
+    if codes is None:
+        codes = torch.empty((Hh, n), dtype=torch.int32, device=dev)
+    if objective is None:
+        objective = torch.empty((Hh, iters + 1), dtype=torch.float64, device=dev)
+    lib = _load()
+    ws, nb = _workspace(lib.a2ats_kmeanspp_workspace_size(Hh, n, d, K), dev, workspace)
+    _check("a2ats_kmeanspp", lib.a2ats_kmeanspp(
+        _ptr(z3), Hh, n, d, int(K), _ptr(u2), int(iters), _ptr(centroids),
+        _ptr(codes), _ptr(objective), _ptr(ws), nb, _stream(stream)))
+    if z.dim() == 3:
+        return centroids, codes, objective
+    return centroids[0], codes[0], objective[0]
 
 
 def split_views(perm, count, b: int = 0, h: int = 0, n: int | None = None):

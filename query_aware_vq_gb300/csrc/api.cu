@@ -67,6 +67,12 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Do the byte ranges [p, p + pb) and [q, q + qb) share a byte?
+bool overlap(const void* p, size_t pb, const void* q, size_t qb) {
+    const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+    return a < b + qb && b < a + pb;
+}
+
 bool dtype_ok(int32_t dt) { return dt == A2ATS_F32 || dt == A2ATS_BF16 || dt == A2ATS_F16; }
 
 size_t dtype_bytes(int32_t dt) { return dt == A2ATS_F32 ? 4 : 2; }
@@ -739,6 +745,100 @@ int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64
     cudaError_t e = launch_copy_retrieval_rows(src, dst, Shape{B, H, Ncap, 8}, len, perm, count,
                                                (cudaStream_t)stream);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_cholesky_rows_workspace_size(int64_t H, int64_t n, int64_t d) {
+    if (H < 0 || n < 0 || d < 0) return 0;
+    Carve c(nullptr);
+    c.take<float>((size_t)(H * d * d));  // lower triangle of L
+    c.take<float>((size_t)(H * d * d));  // its transpose
+    c.take<float>((size_t)(H * n));      // |z|^2 / 2 (written, not returned)
+    return c.used + 256;
+}
+
+int a2ats_cholesky_rows(const void* x, int32_t dtype, int64_t H, int64_t n, int64_t d,
+                        const float* L, float* z, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    if (H < 0 || H > 4096 || n < 0 || n >= (int64_t(1) << 24) || d < 8 || d > kMaxD || d % 8)
+        return A2ATS_ERR_SHAPE;
+    if (H * n == 0) return A2ATS_OK;
+    if (!x || !L || !z) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(L) || !aligned16(z)) return A2ATS_ERR_ALIGN;
+    if ((const void*)z == x) return A2ATS_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < a2ats_cholesky_rows_workspace_size(H, n, d))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    float* Lc = c.take<float>((size_t)(H * d * d));
+    float* Lt = c.take<float>((size_t)(H * d * d));
+    float* half_norm = c.take<float>((size_t)(H * n));
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_factor_prep(L, H, d, Lc, Lt, s);
+    if (e == cudaSuccess)
+        e = launch_codebook_transform(x, dtype, H, n, d, Lc, nullptr, z, half_norm, nullptr, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+int a2ats_cholesky_solve_rows(const float* zc, int64_t H, int64_t rows, int64_t d, const float* L,
+                              float* c, void* stream) {
+    if (H < 0 || H > 4096 || rows < 0 || rows > (int64_t(1) << 24) || d < 8 || d > kMaxD ||
+        d % 8 || H * rows > (int64_t(1) << 30))
+        return A2ATS_ERR_SHAPE;
+    if (H * rows == 0) return A2ATS_OK;
+    if (!zc || !L || !c) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(zc) || !aligned16(L) || !aligned16(c)) return A2ATS_ERR_ALIGN;
+    cudaError_t e = launch_cholesky_solve(zc, H, rows, d, L, c, (cudaStream_t)stream);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
+size_t a2ats_kmeanspp_workspace_size(int64_t H, int64_t n, int64_t d, int64_t K) {
+    if (H < 0 || n < 0 || d < 0 || K < 0) return 0;
+    Carve c(nullptr);
+    c.take<double>((size_t)(H * n));  // D^2 of the seeding
+    c.take<double>((size_t)(H * K));  // per-centroid objectives
+    c.take<char>(a2ats_h_weighted_assign_workspace_size(1, H, n, d, K));
+    return c.used + 256;
+}
+
+int a2ats_kmeanspp(const float* z, int64_t H, int64_t n, int64_t d, int64_t K, const double* u,
+                   int32_t iters, float* centroids, int32_t* codes, double* objective,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (H < 0 || H > 4096 || n < 0 || n >= (int64_t(1) << 24) || d < 8 || d > kMaxD || d % 8)
+        return A2ATS_ERR_SHAPE;
+    if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
+    if (iters < 0 || iters > (1 << 20)) return A2ATS_ERR_INVALID_ARG;
+    if (H == 0) return A2ATS_OK;
+    if (n == 0) return A2ATS_ERR_SHAPE;
+    if (!z || !u || !centroids || !codes || !objective) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(centroids) || !aligned16(codes) || ((uintptr_t)u & 7u) ||
+        ((uintptr_t)objective & 7u))
+        return A2ATS_ERR_ALIGN;
+    const size_t zb = sizeof(float) * (size_t)(H * n * d), cb = sizeof(float) * (size_t)(H * K * d),
+                 kb = sizeof(int32_t) * (size_t)(H * n);
+    if (overlap(z, zb, centroids, cb) || overlap(z, zb, codes, kb) ||
+        overlap(centroids, cb, codes, kb))
+        return A2ATS_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < a2ats_kmeanspp_workspace_size(H, n, d, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    double* d2 = c.take<double>((size_t)(H * n));
+    double* obj_part = c.take<double>((size_t)(H * K));
+    const size_t assign_bytes = a2ats_h_weighted_assign_workspace_size(1, H, n, d, K);
+    void* assign_ws = c.take<char>(assign_bytes);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_kmeans_seed(z, H, n, d, K, u, centroids, d2, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (int32_t r = 0; r <= iters; r++) {
+        // nearest centroid of every row (L = identity), then the mean step
+        const int st = h_weighted(z, A2ATS_F32, 1, H, n, d, nullptr, centroids, K, nullptr,
+                                  nullptr, A2ATS_ROWS_ALL, nullptr, nullptr, codes, assign_ws,
+                                  assign_bytes, stream, false);
+        if (st) return st;
+        e = launch_kmeans_update(z, H, n, d, K, codes, centroids, obj_part, r < iters,
+                                 objective + r, (int64_t)iters + 1, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return A2ATS_OK;
 }
 
 }  // extern "C"

@@ -172,6 +172,25 @@ struct TcCall {
 bool tc_supported(int dt, int64_t d);
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st);
 
+// kmeans.cu --------------------------------------------------------------
+// k-means++ seeds of z [H, n, d] fp32 with the draws u [H, K] into cent
+// [H, K, d]; d2 [H, n] fp64 scratch.
+cudaError_t launch_kmeans_seed(const float* z, int64_t H, int64_t n, int64_t d, int64_t K,
+                               const double* u, float* cent, double* d2, cudaStream_t st);
+
+// The objective of the assignment codes [H, n] against cent (sum over rows
+// of |z_i - cent[code_i]|^2, fp64) into objective[h * obj_stride]; with
+// update, each centroid then moves to the mean of its rows (kept when it has
+// none).  obj_part [H, K] fp64 scratch.
+cudaError_t launch_kmeans_update(const float* z, int64_t H, int64_t n, int64_t d, int64_t K,
+                                 const int32_t* codes, float* cent, double* obj_part,
+                                 bool update, double* objective, int64_t obj_stride,
+                                 cudaStream_t st);
+
+// c [H, rows, d] with c L = zc (back substitution on the lower triangle of L).
+cudaError_t launch_cholesky_solve(const float* zc, int64_t H, int64_t rows, int64_t d,
+                                  const float* L, float* c, cudaStream_t st);
+
 cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
                                   float* cnorm, cudaStream_t st);
 

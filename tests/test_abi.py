@@ -200,3 +200,50 @@ def test_copy_retrieval_rows_validation(lib):
     assert f(None, FAKE, 1, 2, 10, None, FAKE, FAKE, None) == -1
     assert f(FAKE, FAKE, 1, 2, 10, None, None, FAKE, None) == -1
     assert f(None, None, 0, 2, 10, None, None, None, None) == 0
+
+
+def test_cholesky_rows_validation(lib):
+    f = lib.a2ats_cholesky_rows
+    ws = lib.a2ats_cholesky_rows_workspace_size(2, 100, 64)
+    assert ws >= 2 * (2 * 64 * 64 + 100) * 4
+    W = FAKE + (1 << 24)
+    assert f(FAKE, 9, 2, 100, 64, FAKE + 65536, FAKE + 131072, W, ws, None) == -3
+    assert f(FAKE, 1, 2, 100, 12, FAKE + 65536, FAKE + 131072, W, ws, None) == -2
+    assert f(FAKE, 1, 2, 1 << 24, 64, FAKE + 65536, FAKE + 131072, W, ws, None) == -2
+    assert f(None, 1, 2, 100, 64, FAKE + 65536, FAKE + 131072, W, ws, None) == -1
+    assert f(FAKE, 0, 2, 100, 64, FAKE + 65536, FAKE, W, ws, None) == -1
+    assert f(FAKE + 8, 1, 2, 100, 64, FAKE + 65536, FAKE + 131072, W, ws, None) == -4
+    assert f(FAKE, 1, 2, 100, 64, FAKE + 65536, FAKE + 131072, W, ws - 1, None) == -6
+    assert f(FAKE, 1, 2, 100, 64, FAKE + 65536, FAKE + 131072, None, ws, None) == -6
+    assert f(None, 1, 0, 100, 64, None, None, None, 0, None) == 0
+
+
+def test_cholesky_solve_rows_validation(lib):
+    f = lib.a2ats_cholesky_solve_rows
+    assert f(FAKE, 2, 100, 12, FAKE + 65536, FAKE, None) == -2
+    assert f(FAKE, 4096, 1 << 24, 64, FAKE + 65536, FAKE, None) == -2
+    assert f(None, 2, 100, 64, FAKE + 65536, FAKE, None) == -1
+    assert f(FAKE, 2, 100, 64, None, FAKE, None) == -1
+    assert f(FAKE, 2, 100, 64, FAKE + 65540, FAKE, None) == -4
+    assert f(None, 2, 0, 64, None, None, None) == 0
+
+
+def test_kmeanspp_validation(lib):
+    f = lib.a2ats_kmeanspp
+    H, n, d, K = 2, 100, 8, 4
+    ws = lib.a2ats_kmeanspp_workspace_size(H, n, d, K)
+    assert ws >= (H * n + H * K) * 8 + lib.a2ats_h_weighted_assign_workspace_size(1, H, n, d, K)
+    z, u, c, k, o, W = (FAKE, FAKE + 65536, FAKE + 131072, FAKE + 196608, FAKE + 262144,
+                        FAKE + (1 << 24))
+    assert f(z, H, n, 12, K, u, 3, c, k, o, W, ws, None) == -2
+    assert f(z, H, n, d, 0, u, 3, c, k, o, W, ws, None) == -2
+    assert f(z, H, 0, d, K, u, 3, c, k, o, W, ws, None) == -2
+    assert f(z, H, n, d, K, u, -1, c, k, o, W, ws, None) == -1
+    assert f(z, H, n, d, K, None, 3, c, k, o, W, ws, None) == -1
+    assert f(z, H, n, d, K, u + 4, 3, c, k, o, W, ws, None) == -4
+    assert f(z, H, n, d, K, u, 3, c + 8, k, o, W, ws, None) == -4
+    # z [H, n, d] fp32 spans 6400 bytes: centroids 1 KB in overlap it
+    assert f(z, H, n, d, K, u, 3, z + 1024, k, o, W, ws, None) == -1
+    assert f(z, H, n, d, K, u, 3, c, c + 128, o, W, ws, None) == -1
+    assert f(z, H, n, d, K, u, 3, c, k, o, W, ws - 1, None) == -6
+    assert f(None, 0, n, d, K, None, 3, None, None, None, None, 0, None) == 0
