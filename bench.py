@@ -71,11 +71,18 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--path", choices=["step", "attention", "dequantize", "subvector"],
+    p.add_argument("--path", choices=["step", "attention", "dequantize", "subvector",
+                                       "calibrate"],
                    default="step",
                    help="attention: time the code-based attention scores and top tokens; "
                         "dequantize: time the reconstruction of the keys from their codes "
-                        "(both steps after the path) instead of the step")
+                        "(both steps after the path); calibrate: time one layer's codebook "
+                        "calibration (H, L, z = k L, k-means++, back to key space) instead "
+                        "of the step")
+    p.add_argument("--calib-tokens", type=int, default=4096,
+                   help="calibration keys per head for --path calibrate")
+    p.add_argument("--lloyd", type=int, default=10,
+                   help="Lloyd rounds after the k-means++ seeding for --path calibrate")
     p.add_argument("--separate-split", action="store_true",
                    help="run RoPE and the split on the second stream beside a separate "
                         "plain-VQ call, instead of the fused call (same outputs)")
@@ -879,6 +886,74 @@ def run_subvector(a):
         }), flush=True)
 
 
+def run_calibrate(a):
+    """One layer's codebook calibration in Cholesky space: H from the
+    workload's calibration queries, L = chol(H), z = k L for the calibration
+    keys, k-means++ seeding and Lloyd rounds on z, and the codebook back in
+    key space.  Inputs resident; L2 flushed between calibrations."""
+    import query_aware_vq_gb300 as q
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.scaled(synth.WORKLOADS[a.workload], N=a.calib_tokens)
+    keys = synth.keys(w, batch_offset=rank * w.B)[0].cuda()  # [H, n, d]
+    Qd = synth.queries(w).cuda()
+    u = torch.from_numpy(np.random.default_rng(5000 + rank).random((w.H, w.K))).cuda()
+    H_, n, d = keys.shape
+    z = torch.empty((H_, n, d), dtype=torch.float32, device="cuda")
+    cz = torch.empty((H_, w.K, d), dtype=torch.float32, device="cuda")
+    c = torch.empty_like(cz)
+    codes = torch.empty((H_, n), dtype=torch.int32, device="cuda")
+    obj = torch.empty((H_, a.lloyd + 1), dtype=torch.float64, device="cuda")
+
+    def calibrate():
+        hm = q.a2ats_query_second_moment(Qd, w.ridge)
+        L, _ = q.a2ats_cholesky_factor(hm)
+        q.a2ats_cholesky_rows(keys, L, out=z)
+        q.a2ats_kmeanspp(z, w.K, u, a.lloyd, centroids=cz, codes=codes, objective=obj)
+        q.a2ats_cholesky_solve_rows(cz, L, out=c)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(a.warmup, 3)):
+        calibrate()
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    evs = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        calibrate()
+        e1.record(stream)
+        evs.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / a.steps, world)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "codebook calibrations/sec (one layer: H, L, z = k L, k-means++, "
+                      "Lloyd rounds, key-space codebook)",
+            "value": world / (ms * 1e-3), "unit": "layers/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32+f64",
+            "data": "synthetic (seeded; the workload's keys and queries, uniform draws)",
+            "config": {"workload": w.name, "H": w.H, "tokens": n, "d": d, "K": w.K,
+                       "M": w.M, "lloyd_rounds": a.lloyd,
+                       "l2": "flushed between calibrations (256 MB write)"},
+            "objective_last": float(obj[:, -1].sum().item()),
+            "clocks": clk,
+            "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,
+        }), flush=True)
+
+
 if __name__ == "__main__":
     args = _args()
     if args.impl == "reference":
@@ -889,6 +964,8 @@ if __name__ == "__main__":
         run_dequantize(args)
     elif args.path == "subvector":
         run_subvector(args)
+    elif args.path == "calibrate":
+        run_calibrate(args)
     elif synth.WORKLOADS[args.workload].decode_steps:
         run_decode(args)
     else:
