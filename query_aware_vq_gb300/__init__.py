@@ -188,10 +188,16 @@ def _rope(rope):
                       float(rope.get("rope_base", 10000.0)), int(bool(rope.get("interleaved", 0))))
 
 
-def _workspace(nbytes: int, device, ws):
+def _workspace(nbytes: int, device, ws, stream=None):
+    """The caller's workspace, or a fresh one.  A fresh one is freed when the
+    binding returns, while the call may still run on `stream`: recording the
+    stream keeps the allocator from handing the memory out before then."""
     if ws is not None:
         return ws, ws.numel() * ws.element_size()
-    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device), int(nbytes)
+    ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+    if stream is not None:
+        ws.record_stream(stream)
+    return ws, int(nbytes)
 
 
 def _lens(lengths):
@@ -242,7 +248,7 @@ def a2ats_query_second_moment(queries, ridge: float = 1e-4, *, out=None, workspa
         out = torch.empty((Hh, d, d), dtype=torch.float32, device=q.device)
     lib = _load()
     ws, nb = _workspace(lib.a2ats_query_second_moment_workspace_size(Hh, M, d), q.device,
-                        workspace)
+                        workspace, stream)
     _check("a2ats_query_second_moment", lib.a2ats_query_second_moment(
         _ptr(q), _dt(q), Hh, M, d, float(ridge), _ptr(out), _ptr(ws), nb, _stream(stream)))
     return out if queries.dim() == 3 else out[0]
@@ -288,7 +294,7 @@ def a2ats_h_weighted_assign(x, codebook, L=None, *, lengths=None, rope=None, row
     if reuse and workspace is None:
         raise ValueError("reuse needs the workspace of the preparing call")
     ws, nb = _workspace(lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K), x.device,
-                        workspace)
+                        workspace, stream)
     rp = _rope(rope)
     name = "a2ats_h_weighted_assign_reuse" if reuse else "a2ats_h_weighted_assign"
     _check(name, getattr(lib, name)(
@@ -310,7 +316,7 @@ def a2ats_query_aware_assign(x, codebook, query=None, beta: float = 0.5, *, leng
         raise TypeError("query and keys must share a dtype")
     lib = _load()
     ws, nb = _workspace(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K), x.device,
-                        workspace)
+                        workspace, stream)
     rp = _rope(rope)
     _check("a2ats_query_aware_assign", lib.a2ats_query_aware_assign(
         _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), _ptr(cb), K, _ptr(query),
@@ -334,7 +340,7 @@ def a2ats_select_retrieval_set(keys, query=None, fraction: float = 0.2, *, lengt
         count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
     lib = _load()
     ws, nb = _workspace(lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d), keys.device,
-                        workspace)
+                        workspace, stream)
     rp = _rope(rope)
     _check("a2ats_select_retrieval_set", lib.a2ats_select_retrieval_set(
         _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
@@ -363,7 +369,7 @@ def a2ats_select_retrieval_set_rotated(keys, query=None, fraction: float = 0.2, 
         count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
     lib = _load()
     ws, nb = _workspace(lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d), keys.device,
-                        workspace)
+                        workspace, stream)
     rp = _rope(rope)
     _check("a2ats_select_retrieval_set_rotated", lib.a2ats_select_retrieval_set_rotated(
         _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
@@ -398,7 +404,7 @@ def a2ats_rope_split_plain_assign(keys, codebook, query=None, fraction: float = 
     if reuse and workspace is None:
         raise ValueError("reuse needs the workspace of the preparing call")
     ws, nb = _workspace(lib.a2ats_rope_split_plain_assign_workspace_size(B, H, N, d, K),
-                        keys.device, workspace)
+                        keys.device, workspace, stream)
     ev = None
     if split_done is not None:
         ev = split_done.cuda_event
@@ -436,7 +442,7 @@ def a2ats_code_attention_topk(keys, codes, codebook, query, fraction: float = 0.
         count = torch.empty((B, H), dtype=torch.int32, device=keys.device)
     lib = _load()
     ws, nb = _workspace(lib.a2ats_code_attention_topk_workspace_size(B, H, N, d, K),
-                        keys.device, workspace)
+                        keys.device, workspace, stream)
     rp = _rope(rope)
     _check("a2ats_code_attention_topk", lib.a2ats_code_attention_topk(
         _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(codes), _ptr(cb), K,
@@ -512,7 +518,8 @@ def a2ats_cholesky_rows(x, L, *, out=None, workspace=None, stream=None):
     if out is None:
         out = torch.empty((Hh, n, d), dtype=torch.float32, device=x.device)
     lib = _load()
-    ws, nb = _workspace(lib.a2ats_cholesky_rows_workspace_size(Hh, n, d), x.device, workspace)
+    ws, nb = _workspace(lib.a2ats_cholesky_rows_workspace_size(Hh, n, d), x.device, workspace,
+                        stream)
     _check("a2ats_cholesky_rows", lib.a2ats_cholesky_rows(
         _ptr(x3), _dt(x3), Hh, n, d, _ptr(L3), _ptr(out), _ptr(ws), nb, _stream(stream)))
     return out if x.dim() == 3 else out[0]
@@ -554,7 +561,7 @@ def a2ats_kmeanspp(z, K: int, u, iters: int, *, centroids=None, codes=None, obje
     if objective is None:
         objective = torch.empty((Hh, iters + 1), dtype=torch.float64, device=dev)
     lib = _load()
-    ws, nb = _workspace(lib.a2ats_kmeanspp_workspace_size(Hh, n, d, K), dev, workspace)
+    ws, nb = _workspace(lib.a2ats_kmeanspp_workspace_size(Hh, n, d, K), dev, workspace, stream)
     _check("a2ats_kmeanspp", lib.a2ats_kmeanspp(
         _ptr(z3), Hh, n, d, int(K), _ptr(u2), int(iters), _ptr(centroids),
         _ptr(codes), _ptr(objective), _ptr(ws), nb, _stream(stream)))
