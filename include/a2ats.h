@@ -441,6 +441,41 @@ int a2ats_kmeanspp(const float* z, int64_t H, int64_t n, int64_t d, int64_t K, c
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_subvector_assign -- sub-vector (product) VQ, the v0.39.0 page's
+ * configuration (a2ats_sub_dim, a2ats_codebook_bits) with "How it works"
+ * steps 2 and 5: every token row j < len[b] of width d is G = d / sub_dim
+ * sub-vectors x_g = x[j, g sub_dim .. (g + 1) sub_dim), each coded by
+ *   code[b, h, j, g] = argmin_k |x_g L - c_k L|^2   (H-weighted rule, [API]
+ *                      a2ats_h_weighted_assignment, Eq. 14-18)
+ * on the retrieval tokens (perm[b, h, :count[b, h]]) when L is given, and by
+ *   code[b, h, j, g] = argmin_k |x_g - c_k|^2       (plain VQ)
+ * on every other token; ties go to the lowest k.
+ *   x        [B, H, Ncap, d] device, in dtype (for keys: k~ after windowed
+ *            RoPE, which pairs elements of different sub-vectors and so runs
+ *            on the whole row first; for values: the values)
+ *   codebook [H, K, sub_dim] device, in dtype: one table per head
+ *   L        [H, sub_dim, sub_dim] fp32 device (lower triangle read), or
+ *            NULL: plain VQ for every token
+ *   perm, count  the token split as a2ats_select_retrieval_set writes it, or
+ *            both NULL: with L given, every token takes the H-weighted rule
+ *   codes    [B, H, Ncap, G] int32 device output; rows past len[b] are not
+ *            written
+ * sub_dim is 8 or 16 and divides d; K * sub_dim <= 8192.  The distance of a
+ * sub_dim-wide difference is a direct fp32 sum (relative error below
+ * (sub_dim + 2) 2^-24), so a code can differ from the exact argmin only
+ * where the two best distances are that close.
+ * Errors: DTYPE, SHAPE, INVALID_ARG for a NULL array when B*H*Ncap > 0 or
+ * only one of perm / count, ALIGN, WORKSPACE.
+ * ------------------------------------------------------------------------ */
+size_t a2ats_subvector_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                                             int64_t sub_dim, int64_t K);
+int a2ats_subvector_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                           int64_t d, const int32_t* len, int64_t sub_dim, const void* codebook,
+                           int64_t K, const float* L, const int32_t* perm, const int32_t* count,
+                           int32_t* codes, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

@@ -191,6 +191,26 @@ cudaError_t launch_kmeans_update(const float* z, int64_t H, int64_t n, int64_t d
 cudaError_t launch_cholesky_solve(const float* zc, int64_t H, int64_t rows, int64_t d,
                                   const float* L, float* c, cudaStream_t st);
 
+// subvector.cu -----------------------------------------------------------
+// Largest K * sub_dim a sub-vector table may have (both tables sit in
+// shared memory).
+int64_t subvector_table_limit();
+
+// mark [B*H*Ncap] <- 1 for the tokens perm[:count] of each (b, h), 0 for the
+// rest of the split (rows below len only).
+cudaError_t launch_mark_retrieval(const int32_t* perm, const int32_t* count, const int32_t* len,
+                                  const Shape& s, uint8_t* mark, cudaStream_t st);
+
+// codes [B, H, Ncap, d / sub_dim] of the sub-vectors of x (rows below len):
+// nearest entry of tab_plain [H, K, sub_dim], or, where Lc is given and the
+// token is marked (every token when mark is null), nearest entry of
+// tab_weighted = c Lc after z = x Lc.  sub_dim is 8 or 16.
+cudaError_t launch_subvector_assign(const void* x, int dt, const Shape& s, const int32_t* len,
+                                    int64_t sub_dim, const float* tab_plain,
+                                    const float* tab_weighted, const float* Lc,
+                                    const uint8_t* mark, int64_t K, int32_t* codes,
+                                    cudaStream_t st);
+
 cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
                                   float* cnorm, cudaStream_t st);
 

@@ -47,7 +47,8 @@ from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_copy_retrieval_ro
                a2ats_h_weighted_assign,
                a2ats_query_aware_assign, a2ats_query_second_moment,
                a2ats_rope_split_plain_assign, a2ats_select_retrieval_set,
-               a2ats_select_retrieval_set_rotated, a2ats_windowed_rope, library)
+               a2ats_select_retrieval_set_rotated, a2ats_subvector_assign,
+               a2ats_windowed_rope, library)
 
 
 class A2ATSStep:
@@ -289,6 +290,10 @@ class A2ATSSubvectorStep:
       6. values' sub-vectors: plain nearest centroid, no RoPE
          and no retrieval preference ("How it works" step 5)   a2ats_h_weighted_assign, L = I
 
+    With dedicated=True, steps 3-6 are two calls of a2ats_subvector_assign
+    (one pass over the rotated keys applying each token's rule from the
+    split, then the values), with the same results up to near-ties.
+
     A token of width d is d / sub_dim sub-vector rows; sub-vector row
     j * G + g of a (b, h) is elements g * sub_dim .. of token j (G = d /
     sub_dim).  Codebooks are [H, K, sub_dim] (a table shared by the heads is
@@ -297,9 +302,12 @@ class A2ATSSubvectorStep:
 
     def __init__(self, B: int, H: int, N: int, d: int, sub_dim: int, K: int, dtype, *,
                  window: int, fraction: float, rope_base: float, interleaved: bool = False,
-                 device="cuda"):
+                 dedicated: bool = False, device="cuda"):
         if sub_dim < 8 or d % sub_dim:
             raise ValueError("sub_dim must divide d and be at least 8")
+        if dedicated and sub_dim not in (8, 16):
+            raise ValueError("the sub-vector kernel takes sub_dim 8 or 16")
+        self.dedicated = dedicated
         self.B, self.H, self.N, self.d, self.s, self.K = B, H, N, d, sub_dim, K
         self.G = d // sub_dim
         self.fraction = fraction
@@ -319,7 +327,8 @@ class A2ATSSubvectorStep:
         self.codes_ret = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
         self.codes_v = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
         ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, NG, sub_dim, K),
-                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
+                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d),
+                 lib.a2ats_subvector_assign_workspace_size(B, H, N, d, sub_dim, K))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, keys, values, codebook_k, codebook_v, L, lengths=None, stream=None):
@@ -330,6 +339,19 @@ class A2ATSSubvectorStep:
         st = stream if stream is not None else torch.cuda.current_stream()
         B, H, N, G, s = self.B, self.H, self.N, self.G, self.s
         ws = self.workspace
+        if self.dedicated:
+            # steps 3-6 in the sub-vector kernel: both rules in one pass over
+            # the rotated keys (the split read from perm / count), then the
+            # values
+            a2ats_windowed_rope(keys, lengths=lengths, out=self.k_tilde, stream=st, **self.rope)
+            a2ats_select_retrieval_set(self.k_tilde, None, self.fraction, lengths=lengths,
+                                       perm=self.perm, count=self.count, workspace=ws, stream=st)
+            a2ats_subvector_assign(self.k_tilde, codebook_k, s, L, lengths=lengths,
+                                   perm=self.perm, count=self.count, codes=self.codes_k,
+                                   workspace=ws, stream=st)
+            a2ats_subvector_assign(values, codebook_v, s, None, lengths=lengths,
+                                   codes=self.codes_v, workspace=ws, stream=st)
+            return self
         with torch.cuda.stream(st):
             if lengths is None:
                 self.sub_len.fill_(N * G)

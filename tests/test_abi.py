@@ -247,3 +247,22 @@ def test_kmeanspp_validation(lib):
     assert f(z, H, n, d, K, u, 3, c, c + 128, o, W, ws, None) == -1
     assert f(z, H, n, d, K, u, 3, c, k, o, W, ws - 1, None) == -6
     assert f(None, 0, n, d, K, None, 3, None, None, None, None, 0, None) == 0
+
+
+def test_subvector_assign_validation(lib):
+    f = lib.a2ats_subvector_assign
+    B, H, N, d, s, K = 1, 2, 64, 128, 8, 256
+    ws = lib.a2ats_subvector_assign_workspace_size(B, H, N, d, s, K)
+    assert ws >= (2 * H * K * s + H * K) * 4 + B * H * N
+    x, c, L, p, n, k, W = (FAKE, FAKE + 65536, FAKE + 131072, FAKE + 196608, FAKE + 262144,
+                           FAKE + 327680, FAKE + (1 << 24))
+    assert f(x, 9, B, H, N, d, None, s, c, K, L, p, n, k, W, ws, None) == -3
+    assert f(x, 1, B, H, N, d, None, 12, c, K, L, p, n, k, W, ws, None) == -2
+    assert f(x, 1, B, H, N, 24, None, 16, c, K, L, p, n, k, W, ws, None) == -2
+    assert f(x, 1, B, H, N, d, None, s, c, 1025, L, p, n, k, W, ws, None) == -2
+    assert f(x, 1, B, H, N, d, None, s, c, K, L, p, None, k, W, ws, None) == -1
+    assert f(x, 1, B, H, N, d, None, s, None, K, L, p, n, k, W, ws, None) == -1
+    assert f(x, 1, B, H, N, d, None, s, c + 4, K, L, p, n, k, W, ws, None) == -4
+    assert f(x, 1, B, H, N, d, None, s, c, K, L + 8, p, n, k, W, ws, None) == -4
+    assert f(x, 1, B, H, N, d, None, s, c, K, L, p, n, k, W, ws - 1, None) == -6
+    assert f(None, 1, 0, H, N, d, None, s, None, K, None, None, None, None, None, 0, None) == 0
