@@ -233,11 +233,11 @@ kmeans_update_kernel(const float* __restrict__ z, int64_t n, int32_t d, int64_t 
     for (int o = 16; o; o >>= 1) obj = __dadd_rn(obj, __shfl_xor_sync(0xffffffffu, obj, o));
     if (lane == 0) obj_part[(int64_t)h * K + j] = obj;
     if (update && cnt > 0) {
-        const double inv_n = (double)cnt;
+        const double members = (double)cnt;
 #pragma unroll
         for (int m = 0; m < kCols; m++) {
             const int a = lane + 32 * m;
-            if (a < d) cj[a] = (float)(sum[m] / inv_n);
+            if (a < d) cj[a] = (float)(sum[m] / members);
         }
     }
 }
