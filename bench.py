@@ -79,9 +79,9 @@ def _args():
                         "(both steps after the path); calibrate: time one layer's codebook "
                         "calibration (H, L, z = k L, k-means++, back to key space) instead "
                         "of the step")
-    p.add_argument("--subvector-kernel", action="store_true",
-                   help="--path subvector: code the sub-vectors with the dedicated sub-vector "
-                        "kernel instead of the composed assignment calls")
+    p.add_argument("--subvector-composed", action="store_true",
+                   help="--path subvector: code the sub-vectors with the composed assignment "
+                        "calls instead of the sub-vector kernel")
     p.add_argument("--calib-tokens", type=int, default=4096,
                    help="calibration keys per head for --path calibrate")
     p.add_argument("--lloyd", type=int, default=10,
@@ -850,7 +850,7 @@ def run_subvector(a):
     L, _ = q.a2ats_cholesky_factor(q.a2ats_query_second_moment(Qd, 1e-4))
     step = A2ATSSubvectorStep(w.B, w.H, w.N, w.d, s, K, synth.DTYPES[w.dtype], window=w.W,
                               fraction=w.fraction, rope_base=w.rope_base,
-                              dedicated=a.subvector_kernel)
+                              dedicated=not a.subvector_composed)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     for _ in range(max(a.warmup, 3)):
@@ -884,8 +884,8 @@ def run_subvector(a):
             "data": "synthetic (seeded; the workload's keys, Gaussian values and tables)",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
                        "sub_dim": s, "K": K, "window": w.W, "fraction": w.fraction,
-                       "assignment": "sub-vector kernel" if a.subvector_kernel
-                       else "composed calls",
+                       "assignment": "composed calls" if a.subvector_composed
+                       else "sub-vector kernel",
                        "l2": "flushed between steps (256 MB write)"},
             "clocks": clk,
             "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,

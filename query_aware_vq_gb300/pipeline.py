@@ -290,9 +290,10 @@ class A2ATSSubvectorStep:
       6. values' sub-vectors: plain nearest centroid, no RoPE
          and no retrieval preference ("How it works" step 5)   a2ats_h_weighted_assign, L = I
 
-    With dedicated=True, steps 3-6 are two calls of a2ats_subvector_assign
-    (one pass over the rotated keys applying each token's rule from the
-    split, then the values), with the same results up to near-ties.
+    By default (dedicated=True) steps 3-6 are two calls of
+    a2ats_subvector_assign (one pass over the rotated keys applying each
+    token's rule from the split, then the values); dedicated=False runs the
+    composition listed above, with the same results up to near-ties.
 
     A token of width d is d / sub_dim sub-vector rows; sub-vector row
     j * G + g of a (b, h) is elements g * sub_dim .. of token j (G = d /
@@ -302,7 +303,7 @@ class A2ATSSubvectorStep:
 
     def __init__(self, B: int, H: int, N: int, d: int, sub_dim: int, K: int, dtype, *,
                  window: int, fraction: float, rope_base: float, interleaved: bool = False,
-                 dedicated: bool = False, device="cuda"):
+                 dedicated: bool = True, device="cuda"):
         if sub_dim < 8 or d % sub_dim:
             raise ValueError("sub_dim must divide d and be at least 8")
         if dedicated and sub_dim not in (8, 16):

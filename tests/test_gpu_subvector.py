@@ -1,4 +1,5 @@
-"""GPU parity of the sub-vector (product) VQ step against the oracle's
+"""GPU parity of the sub-vector (product) VQ step, composed from the
+assignment calls (dedicated=False), against the oracle's
 composition of the same steps (v0.39.0 page, configuration a2ats_sub_dim and
 a2ats_codebook_bits, "How it works" steps 1-5; the API page's functions on
 [N, sub_dim] sub-vectors): windowed RoPE of the whole head, the split over
@@ -35,7 +36,7 @@ def test_subvector_step_matches_oracle(case):
     L, info = q.a2ats_cholesky_factor(Hm)
     lens = torch.tensor([max(N - 41 * b, 1) for b in range(B)], dtype=torch.int32)
     step = A2ATSSubvectorStep(B, H, N, d, s, K, torch.bfloat16, window=W, fraction=f,
-                              rope_base=base)
+                              rope_base=base, dedicated=False)
     step(dev(k), dev(v), dev(ck), dev(cv), L, lengths=dev(lens))
     torch.cuda.synchronize()
     codes_k, codes_v = step.codes_k.cpu().numpy(), step.codes_v.cpu().numpy()
