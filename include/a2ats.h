@@ -476,6 +476,35 @@ int a2ats_subvector_assign(const void* x, int32_t dtype, int64_t B, int64_t H, i
                            void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_subvector_query_aware_assign -- sub-vector VQ with the cosine blend
+ * of [API] a2ats_query_aware_assignment on the retrieval tokens: the rule
+ * the v0.39.0 page's wrapper takes when no calibrated H (a2ats_query_h) is
+ * given, with a2ats_beta.  For sub-vector g of a retrieval token j < len[b]
+ * (perm[b, h, :count[b, h]], or every token when perm and count are NULL):
+ *   e_k = |x_g - c_k|^2,  m = max_k e_k,
+ *   score_k = -beta e_k / m + (1 - beta) cos(q_g, c_k),
+ *   code = argmax_k score_k (ties to the lowest k),
+ * with q_g the query's slice g (elements g sub_dim .. (g + 1) sub_dim);
+ * e_k / m is 0 when m = 0 and a cosine with a zero-norm vector is 0.  Every
+ * other token, and every token when beta = 1, takes plain VQ (argmin_k e_k).
+ *   query  [B, H, d] device in dtype, one query per (sequence, head); NULL =
+ *          the row of x at t = len[b] - 1 (for keys: the proxy query k~_t)
+ *   beta in [0, 1]; other arguments as a2ats_subvector_assign.
+ * A code can differ from the exact argmax only where the two best scores
+ * are within about 10^-5 of each other (fp32 distances and cosines).
+ * Errors: as a2ats_subvector_assign, and INVALID_ARG for beta outside
+ * [0, 1].
+ * ------------------------------------------------------------------------ */
+size_t a2ats_subvector_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap,
+                                                         int64_t d, int64_t sub_dim, int64_t K);
+int a2ats_subvector_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                       int64_t Ncap, int64_t d, const int32_t* len,
+                                       int64_t sub_dim, const void* codebook, int64_t K,
+                                       const void* query, double beta, const int32_t* perm,
+                                       const int32_t* count, int32_t* codes, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_copy_retrieval_rows -- dst[b, h, j] = src[b, h, j] for the retrieval
  * rows j = perm[b, h, i], i < count[b, h], j < len[b] (no counterpart on the
  * pages: it joins the two halves of [V039] step 2's routing when they are

@@ -83,6 +83,9 @@ _SIGS = {
     "a2ats_subvector_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64, _I64],
     "a2ats_subvector_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P,
                                _P, _P, _P, _SZ, _P],
+    "a2ats_subvector_query_aware_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64, _I64],
+    "a2ats_subvector_query_aware_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P, _I64,
+                                           _P, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_status_string": [_I32],
     "a2ats_last_error": [],
     "a2ats_kernel_launches": [],
@@ -117,7 +120,8 @@ def _load():
                      "a2ats_code_attention_topk_workspace_size",
                      "a2ats_cholesky_rows_workspace_size",
                      "a2ats_kmeanspp_workspace_size",
-                     "a2ats_subvector_assign_workspace_size"):
+                     "a2ats_subvector_assign_workspace_size",
+                     "a2ats_subvector_query_aware_assign_workspace_size"):
             getattr(lib, name).restype = ctypes.c_size_t
         lib.a2ats_kernel_launches.restype = ctypes.c_uint64
         lib.a2ats_timed_kernels_ms.restype = ctypes.c_double
@@ -524,6 +528,35 @@ def a2ats_subvector_assign(x, codebook, sub_dim: int, L=None, *, lengths=None, p
     _check("a2ats_subvector_assign", lib.a2ats_subvector_assign(
         _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), int(sub_dim), _ptr(cb), K,
         _ptr(L), _ptr(perm), _ptr(count), _ptr(codes), _ptr(ws), nb, _stream(stream)))
+    return codes
+
+
+def a2ats_subvector_query_aware_assign(x, codebook, sub_dim: int, query=None,
+                                       beta: float = 0.5, *, lengths=None, perm=None,
+                                       count=None, codes=None, workspace=None, stream=None):
+    """Sub-vector codes [B, H, N, d // sub_dim] of x [B, H, N, d]: the cosine
+    blend with the query's slice on the retrieval tokens of the split (perm,
+    count; every token when they are None), plain VQ elsewhere.  query [B,
+    H, d] in x's dtype, or None for the row of x at t = len - 1."""
+    _dev(x, codebook, query, lengths, perm, count, codes)
+    x4 = _as4(x)
+    B, H, N, d = x4.shape
+    cb = codebook if codebook.dim() == 3 else codebook.unsqueeze(0)
+    if cb.dtype != x4.dtype or cb.shape[2] != sub_dim:
+        raise TypeError("codebook must be [H, K, sub_dim] in the dtype of x")
+    if query is not None and query.dtype != x4.dtype:
+        raise TypeError("query must share the dtype of x")
+    K = cb.shape[1]
+    if codes is None:
+        codes = torch.empty((B, H, N, d // sub_dim), dtype=torch.int32, device=x.device)
+    lib = _load()
+    ws, nb = _workspace(
+        lib.a2ats_subvector_query_aware_assign_workspace_size(B, H, N, d, sub_dim, K), x.device,
+        workspace, stream)
+    _check("a2ats_subvector_query_aware_assign", lib.a2ats_subvector_query_aware_assign(
+        _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), int(sub_dim), _ptr(cb), K,
+        _ptr(query), float(beta), _ptr(perm), _ptr(count), _ptr(codes), _ptr(ws), nb,
+        _stream(stream)))
     return codes
 
 

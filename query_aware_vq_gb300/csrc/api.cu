@@ -897,4 +897,54 @@ int a2ats_subvector_assign(const void* x, int32_t dtype, int64_t B, int64_t H, i
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
+size_t a2ats_subvector_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Ncap,
+                                                         int64_t d, int64_t sub_dim, int64_t K) {
+    (void)d;
+    if (B < 0 || H < 0 || Ncap < 0 || sub_dim < 0 || K < 0) return 0;
+    Carve c(nullptr);
+    c.take<float>((size_t)(H * K * sub_dim));  // decoded table
+    c.take<float>((size_t)(H * K));            // half norms (written, not read)
+    c.take<float>((size_t)(H * K));            // |c_k|
+    c.take<uint8_t>((size_t)(B * H * Ncap));   // retrieval marks
+    return c.used + 256;
+}
+
+int a2ats_subvector_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                       int64_t Ncap, int64_t d, const int32_t* len,
+                                       int64_t sub_dim, const void* codebook, int64_t K,
+                                       const void* query, double beta, const int32_t* perm,
+                                       const int32_t* count, int32_t* codes, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if ((sub_dim != 8 && sub_dim != 16) || d % sub_dim != 0) return A2ATS_ERR_SHAPE;
+    if (K < 1 || K * sub_dim > subvector_table_limit()) return A2ATS_ERR_SHAPE;
+    if (!unit_interval(beta)) return A2ATS_ERR_INVALID_ARG;
+    if ((perm == nullptr) != (count == nullptr)) return A2ATS_ERR_INVALID_ARG;
+    if (B * H * Ncap == 0) return A2ATS_OK;
+    if (!x || !codebook || !codes) return A2ATS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codebook) || !aligned16(codes) ||
+        (query && !aligned16(query)))
+        return A2ATS_ERR_ALIGN;
+    if (!workspace || workspace_bytes < a2ats_subvector_query_aware_assign_workspace_size(
+                                            B, H, Ncap, d, sub_dim, K))
+        return A2ATS_ERR_WORKSPACE;
+    Carve c(workspace);
+    float* table = c.take<float>((size_t)(H * K * sub_dim));
+    float* half_norm = c.take<float>((size_t)(H * K));
+    float* cnorm = c.take<float>((size_t)(H * K));
+    uint8_t* mark = c.take<uint8_t>((size_t)(B * H * Ncap));
+    cudaStream_t s = (cudaStream_t)stream;
+    const Shape sh{B, H, Ncap, d};
+    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, sub_dim, nullptr, nullptr,
+                                              table, half_norm, nullptr, s);
+    if (e == cudaSuccess) e = launch_centroid_norms(codebook, dtype, H, K, sub_dim, cnorm, s);
+    if (e == cudaSuccess && perm) e = launch_mark_retrieval(perm, count, len, sh, mark, s);
+    if (e == cudaSuccess)
+        e = launch_subvector_blend(x, dtype, sh, len, sub_dim, table, cnorm, query, (float)beta,
+                                   perm ? mark : nullptr, K, codes, s);
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+
 }  // extern "C"

@@ -211,6 +211,15 @@ cudaError_t launch_subvector_assign(const void* x, int dt, const Shape& s, const
                                     const uint8_t* mark, int64_t K, int32_t* codes,
                                     cudaStream_t st);
 
+// codes [B, H, Ncap, d / sub_dim] by the cosine blend on the marked tokens
+// (every token when mark is null; none when beta = 1) with the query's
+// slice g (query [B*H, d], or the row at t = len - 1 of x when null), plain
+// VQ elsewhere; tab [H, K, sub_dim] the decoded table, cnorm [H, K] |c_k|.
+cudaError_t launch_subvector_blend(const void* x, int dt, const Shape& s, const int32_t* len,
+                                   int64_t sub_dim, const float* tab, const float* cnorm,
+                                   const void* query, float beta, const uint8_t* mark, int64_t K,
+                                   int32_t* codes, cudaStream_t st);
+
 cudaError_t launch_centroid_norms(const void* c, int dt, int64_t H, int64_t K, int64_t d,
                                   float* cnorm, cudaStream_t st);
 

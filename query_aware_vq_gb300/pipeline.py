@@ -48,7 +48,7 @@ from . import (a2ats_append_rows, a2ats_cholesky_factor, a2ats_copy_retrieval_ro
                a2ats_query_aware_assign, a2ats_query_second_moment,
                a2ats_rope_split_plain_assign, a2ats_select_retrieval_set,
                a2ats_select_retrieval_set_rotated, a2ats_subvector_assign,
-               a2ats_windowed_rope, library)
+               a2ats_subvector_query_aware_assign, a2ats_windowed_rope, library)
 
 
 class A2ATSStep:
@@ -293,7 +293,11 @@ class A2ATSSubvectorStep:
     By default (dedicated=True) steps 3-6 are two calls of
     a2ats_subvector_assign (one pass over the rotated keys applying each
     token's rule from the split, then the values); dedicated=False runs the
-    composition listed above, with the same results up to near-ties.
+    composition listed above, with the same results up to near-ties.  With
+    L = None the dedicated path gives the retrieval tokens the page's
+    wrapper rule for a cache without a calibrated H: the cosine blend with
+    `beta` against the proxy query k~_t, slice by slice
+    (a2ats_subvector_query_aware_assign).
 
     A token of width d is d / sub_dim sub-vector rows; sub-vector row
     j * G + g of a (b, h) is elements g * sub_dim .. of token j (G = d /
@@ -303,12 +307,13 @@ class A2ATSSubvectorStep:
 
     def __init__(self, B: int, H: int, N: int, d: int, sub_dim: int, K: int, dtype, *,
                  window: int, fraction: float, rope_base: float, interleaved: bool = False,
-                 dedicated: bool = True, device="cuda"):
+                 dedicated: bool = True, beta: float = 0.5, device="cuda"):
         if sub_dim < 8 or d % sub_dim:
             raise ValueError("sub_dim must divide d and be at least 8")
         if dedicated and sub_dim not in (8, 16):
             raise ValueError("the sub-vector kernel takes sub_dim 8 or 16")
         self.dedicated = dedicated
+        self.beta = beta
         self.B, self.H, self.N, self.d, self.s, self.K = B, H, N, d, sub_dim, K
         self.G = d // sub_dim
         self.fraction = fraction
@@ -329,14 +334,16 @@ class A2ATSSubvectorStep:
         self.codes_v = torch.empty((B, H, N, G), dtype=torch.int32, device=dev)
         ws = max(lib.a2ats_h_weighted_assign_workspace_size(B, H, NG, sub_dim, K),
                  lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d),
-                 lib.a2ats_subvector_assign_workspace_size(B, H, N, d, sub_dim, K))
+                 lib.a2ats_subvector_assign_workspace_size(B, H, N, d, sub_dim, K),
+                 lib.a2ats_subvector_query_aware_assign_workspace_size(B, H, N, d, sub_dim, K))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
     def __call__(self, keys, values, codebook_k, codebook_v, L, lengths=None, stream=None):
         """keys, values [B, H, N, d] (keys pre-RoPE); codebook_k [H, K, sub_dim]
         fp32 (the rotated keys are fp32), codebook_v [H, K, sub_dim] in the
         values' dtype; L [H, sub_dim, sub_dim] the factor of the sub-vector
-        H; lengths [B] int32 or None."""
+        H, or None (the dedicated path then takes the cosine blend);
+        lengths [B] int32 or None."""
         st = stream if stream is not None else torch.cuda.current_stream()
         B, H, N, G, s = self.B, self.H, self.N, self.G, self.s
         ws = self.workspace
@@ -347,9 +354,17 @@ class A2ATSSubvectorStep:
             a2ats_windowed_rope(keys, lengths=lengths, out=self.k_tilde, stream=st, **self.rope)
             a2ats_select_retrieval_set(self.k_tilde, None, self.fraction, lengths=lengths,
                                        perm=self.perm, count=self.count, workspace=ws, stream=st)
-            a2ats_subvector_assign(self.k_tilde, codebook_k, s, L, lengths=lengths,
-                                   perm=self.perm, count=self.count, codes=self.codes_k,
-                                   workspace=ws, stream=st)
+            if L is not None:
+                a2ats_subvector_assign(self.k_tilde, codebook_k, s, L, lengths=lengths,
+                                       perm=self.perm, count=self.count, codes=self.codes_k,
+                                       workspace=ws, stream=st)
+            else:
+                # no calibrated H: the wrapper's cosine blend with the proxy
+                # query k~_t, slice by slice
+                a2ats_subvector_query_aware_assign(self.k_tilde, codebook_k, s, None, self.beta,
+                                                   lengths=lengths, perm=self.perm,
+                                                   count=self.count, codes=self.codes_k,
+                                                   workspace=ws, stream=st)
             a2ats_subvector_assign(values, codebook_v, s, None, lengths=lengths,
                                    codes=self.codes_v, workspace=ws, stream=st)
             return self

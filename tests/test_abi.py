@@ -266,3 +266,22 @@ def test_subvector_assign_validation(lib):
     assert f(x, 1, B, H, N, d, None, s, c, K, L + 8, p, n, k, W, ws, None) == -4
     assert f(x, 1, B, H, N, d, None, s, c, K, L, p, n, k, W, ws - 1, None) == -6
     assert f(None, 1, 0, H, N, d, None, s, None, K, None, None, None, None, None, 0, None) == 0
+
+
+def test_subvector_query_aware_assign_validation(lib):
+    f = lib.a2ats_subvector_query_aware_assign
+    B, H, N, d, s, K = 1, 2, 64, 128, 8, 256
+    ws = lib.a2ats_subvector_query_aware_assign_workspace_size(B, H, N, d, s, K)
+    assert ws >= (H * K * s + 2 * H * K) * 4 + B * H * N
+    x, c, q_, p, n, k, W = (FAKE, FAKE + 65536, FAKE + 131072, FAKE + 196608, FAKE + 262144,
+                            FAKE + 327680, FAKE + (1 << 24))
+    assert f(x, 9, B, H, N, d, None, s, c, K, q_, 0.5, p, n, k, W, ws, None) == -3
+    assert f(x, 1, B, H, N, d, None, 12, c, K, q_, 0.5, p, n, k, W, ws, None) == -2
+    assert f(x, 1, B, H, N, d, None, s, c, 2048, q_, 0.5, p, n, k, W, ws, None) == -2
+    assert f(x, 1, B, H, N, d, None, s, c, K, q_, 1.5, p, n, k, W, ws, None) == -1
+    assert f(x, 1, B, H, N, d, None, s, c, K, q_, float("nan"), p, n, k, W, ws, None) == -1
+    assert f(x, 1, B, H, N, d, None, s, c, K, q_, 0.5, None, n, k, W, ws, None) == -1
+    assert f(x, 1, B, H, N, d, None, s, c, K, q_ + 4, 0.5, p, n, k, W, ws, None) == -4
+    assert f(x, 1, B, H, N, d, None, s, c, K, q_, 0.5, p, n, k, W, ws - 1, None) == -6
+    assert f(None, 1, B, 0, N, d, None, s, None, K, None, 0.5, None, None, None, None, 0,
+             None) == 0

@@ -128,3 +128,85 @@ def test_subvector_step_with_the_kernel_matches_oracle(case):
             vc, e1, e2 = oracle.assign_cholesky(f64(v[b, h, :n]).reshape(n * G, s), f64(cv[h]),
                                                 None)
             check_codes(codes_v[b, h, :n].ravel(), vc, (e2 - e1) / e2, "value sub-codes")
+
+
+def _blend_expected(sub, c, qfull, beta, rows, G, s):
+    """Oracle codes and gaps of the sub-vectors: plain VQ everywhere, then
+    the blend with the query's slice g on the sub-vector rows `rows`."""
+    code, d1, d2 = oracle.assign_cholesky(sub, c, None)
+    gap = (d2 - d1) / np.maximum(d2, 1e-300)
+    if beta < 1.0 and len(rows):
+        n = sub.shape[0] // G
+        qrows = np.tile(qfull.reshape(G, s), (n, 1))
+        cb, s1, s2 = oracle.assign_blend(sub[rows], c, qrows[rows], beta)
+        code[rows], gap[rows] = cb, s1 - s2
+    return code, gap
+
+
+@pytest.mark.parametrize("case", [
+    # B, H, N, d, sub_dim, K, dtype, beta, query, split
+    (2, 2, 300, 128, 8, 256, "f32", 0.5, "proxy", True),
+    (1, 3, 200, 64, 16, 64, "bf16", 0.0, "given", True),
+    (1, 1, 129, 32, 8, 1024, "f16", 0.7, "given", False),
+    (2, 1, 77, 128, 8, 5, "f32", 1.0, "proxy", True),
+])
+def test_subvector_blend_matches_oracle(case):
+    B, H, N, d, s, K, dt, beta, qmode, split = case
+    G = d // s
+    x = synth.gaussian((B, H, N, d), seed=N + 2 * d, dtype=dt)
+    c = synth.gaussian((H, K, s), seed=K + 2 * s, dtype=dt)
+    qg = synth.gaussian((B, H, d), seed=N + 9, dtype=dt)
+    lens = np.array([max(N - 29 * b, 1) for b in range(B)], np.int32)
+    rng = np.random.default_rng(N + 1)
+    perm = np.zeros((B, H, N), np.int32)
+    count = np.zeros((B, H), np.int32)
+    for b in range(B):
+        for h in range(H):
+            perm[b, h], count[b, h] = _split(int(lens[b]), N, 0.25, rng)
+    codes = torch.full((B, H, N, G), -5, dtype=torch.int32, device="cuda")
+    q.a2ats_subvector_query_aware_assign(
+        dev(x), dev(c), s, dev(qg) if qmode == "given" else None, beta,
+        lengths=dev(torch.from_numpy(lens)),
+        perm=dev(torch.from_numpy(perm)) if split else None,
+        count=dev(torch.from_numpy(count)) if split else None, codes=codes)
+    torch.cuda.synchronize()
+    got = codes.cpu().numpy()
+    for b in range(B):
+        n = int(lens[b])
+        assert (got[b, :, n:] == -5).all()
+        for h in range(H):
+            sub = f64(x[b, h, :n]).reshape(n * G, s)
+            qfull = f64(qg[b, h]) if qmode == "given" else f64(x[b, h, n - 1])
+            toks = perm[b, h, :count[b, h]] if split else np.arange(n)
+            rows = (np.sort(toks)[:, None] * G + np.arange(G)).ravel()
+            code, gap = _blend_expected(sub, f64(c[h]), qfull, beta, rows, G, s)
+            check_codes(got[b, h, :n].ravel(), code, gap)
+
+
+def test_subvector_step_without_a_factor_takes_the_blend():
+    """No calibrated H: the step gives the retrieval tokens' sub-vectors the
+    cosine blend against the proxy query k~_t, slice by slice."""
+    B, H, N, d, s, K, W, f, beta = 1, 2, 500, 64, 8, 64, 64, 0.15, 0.5
+    G, base = d // s, 500000.0
+    k = synth.gaussian((B, H, N, d), seed=N + 11, dtype="bf16")
+    v = synth.gaussian((B, H, N, d), seed=N + 12, dtype="f32")
+    ck = synth.gaussian((H, K, s), seed=K + 13, dtype="f32")
+    cv = synth.gaussian((H, K, s), seed=K + 14, dtype="f32")
+    step = A2ATSSubvectorStep(B, H, N, d, s, K, torch.bfloat16, window=W, fraction=f,
+                              rope_base=base, beta=beta)
+    step(dev(k), dev(v), dev(ck), dev(cv), None)
+    torch.cuda.synchronize()
+    codes_k, codes_v = step.codes_k.cpu().numpy(), step.codes_v.cpu().numpy()
+    perm, count = step.perm.cpu().numpy(), step.count.cpu().numpy()
+    for h in range(H):
+        n = N
+        kt = oracle.windowed_rope(f64(k[0, h]), np.arange(n), n - 1, W, 0, base)
+        _, cnt, scores, kth = oracle.select_retrieval_set(kt, kt[n - 1], f)
+        check_split(perm[0, h], int(count[0, h]), n, cnt, scores, kth)
+        ret = np.sort(perm[0, h, :int(count[0, h])])
+        rows = (ret[:, None] * G + np.arange(G)).ravel()
+        code, gap = _blend_expected(kt.reshape(n * G, s), f64(ck[h]), kt[n - 1], beta, rows,
+                                    G, s)
+        check_codes(codes_k[0, h].ravel(), code, gap, "key sub-codes")
+        vc, e1, e2 = oracle.assign_cholesky(f64(v[0, h]).reshape(n * G, s), f64(cv[h]), None)
+        check_codes(codes_v[0, h].ravel(), vc, (e2 - e1) / e2, "value sub-codes")
