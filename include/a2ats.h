@@ -348,27 +348,35 @@ int a2ats_dequantize(const int32_t* codes, const void* codebook, int32_t dtype, 
                      void* stream);
 
 /* --------------------------------------------------------------------------
- * a2ats_key_byte_accounting -- v0.39.0 page, "Byte accounting" and "What you
- * get with the defaults": the storage of `tokens` keys of width d as codes
- * of codebook_bits bits, one per sub_dim numbers (the full-width VQ here has
- * sub_dim = d and codebook_bits = log2 K).  Host only; no device memory.
- *   compressed_key_bytes = tokens (d / sub_dim) codebook_bits / 8
- *   fp16_key_bytes       = tokens d 2
- *   compression_ratio    = fp16 / compressed = 16 sub_dim / codebook_bits
- *   codebook_bytes       = 2^codebook_bits sub_dim 2 (fp16 entries)
+ * a2ats_byte_accounting -- v0.39.0 page, "Byte accounting" and "What you
+ * get with the defaults": the storage of `tokens` keys and `tokens` values
+ * of width d as codes of codebook_bits bits, one per sub_dim numbers (both
+ * follow the cache's one a2ats_sub_dim / a2ats_codebook_bits; the
+ * full-width VQ here has sub_dim = d and codebook_bits = log2 K).  Host
+ * only; no device memory.
+ *   compressed_key_bytes = compressed_value_bytes = tokens (d / sub_dim)
+ *                          codebook_bits / 8
+ *   fp16_key_bytes       = fp16_value_bytes = tokens d 2
+ *   compression_ratio    = (fp16 keys + values) / (compressed keys + values)
+ *                        = 16 sub_dim / codebook_bits (also for tokens = 0:
+ *                          the settings alone decide it)
+ *   codebook_bytes       = 2^codebook_bits sub_dim 2: one table of fp16
+ *                          entries, the page's "Table size"
  *   assigned_avg_bits    = codebook_bits / sub_dim
  * Errors: INVALID_ARG for a NULL out, sub_dim < 1 or codebook_bits outside
  * [1, 24]; SHAPE for tokens < 0, d < 1 or d not a multiple of sub_dim.
  * ------------------------------------------------------------------------ */
 typedef struct {
     double compressed_key_bytes;
+    double compressed_value_bytes;
     double fp16_key_bytes;
+    double fp16_value_bytes;
     double compression_ratio;
     double codebook_bytes;
     double assigned_avg_bits;
-} a2ats_key_bytes;
-int a2ats_key_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
-                              a2ats_key_bytes* out);
+} a2ats_cache_bytes;
+int a2ats_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
+                          a2ats_cache_bytes* out);
 
 /* --------------------------------------------------------------------------
  * a2ats_cholesky_rows -- the change of variables of [API]

@@ -272,15 +272,20 @@ def kmeanspp(z, K: int, u, iters: int):
 
 
 def byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:
-    """The v0.39.0 page's byte accounting of one head's keys ("Byte
-    accounting"; "What you get with the defaults"): each token stores
-    d / sub_dim codes of codebook_bits bits; fp16 stores 16 bits per number;
-    the codebook holds 2^bits entries of sub_dim fp16 numbers."""
+    """The v0.39.0 page's byte accounting of a cache's keys and values
+    ("Byte accounting"; "What you get with the defaults"): each key and each
+    value of width d stores d / sub_dim codes of codebook_bits bits; fp16
+    stores 16 bits per number; the ratio is the combined fp16 size over the
+    combined compressed size; the codebook is one table of 2^bits entries of
+    sub_dim fp16 numbers."""
     groups = d // sub_dim
-    compressed = tokens * groups * codebook_bits / 8.0
-    fp16 = tokens * d * 2.0
-    return {"compressed_key_bytes": compressed, "fp16_key_bytes": fp16,
-            "compression_ratio": fp16 / compressed if compressed else math.inf,
+    ck = tokens * groups * codebook_bits / 8.0
+    fk = tokens * d * 2.0
+    cv, fv = ck, fk
+    ratio = (fk + fv) / (ck + cv) if ck + cv else 16.0 * sub_dim / codebook_bits
+    return {"compressed_key_bytes": ck, "compressed_value_bytes": cv,
+            "fp16_key_bytes": fk, "fp16_value_bytes": fv,
+            "compression_ratio": ratio,
             "codebook_bytes": float((1 << codebook_bits) * sub_dim * 2),
             "assigned_avg_bits": codebook_bits / sub_dim}
 

@@ -70,7 +70,7 @@ _SIGS = {
     "a2ats_rope_split_plain_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_code_attention_topk_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_dequantize": [_P, _P, _I32, _I64, _I64, _I64, _I64, _I64, _P, _P, _P],
-    "a2ats_key_byte_accounting": [_I64, _I64, _I64, _I32, _P],
+    "a2ats_byte_accounting": [_I64, _I64, _I64, _I32, _P],
     "a2ats_code_attention_topk": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P,
                                   _I32, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
@@ -459,21 +459,23 @@ def a2ats_code_attention_topk(keys, codes, codebook, query, fraction: float = 0.
     return scores, perm, count
 
 
-class KeyBytes(ctypes.Structure):
-    """a2ats_key_bytes: the byte accounting of a key cache as codes."""
-
-    _fields_ = [("compressed_key_bytes", ctypes.c_double), ("fp16_key_bytes", ctypes.c_double),
+class CacheBytes(ctypes.Structure):
+    """a2ats_cache_bytes: the byte accounting of a cache's keys and values
+    as codes."""
+    _fields_ = [("compressed_key_bytes", ctypes.c_double),
+                ("compressed_value_bytes", ctypes.c_double),
+                ("fp16_key_bytes", ctypes.c_double), ("fp16_value_bytes", ctypes.c_double),
                 ("compression_ratio", ctypes.c_double), ("codebook_bytes", ctypes.c_double),
                 ("assigned_avg_bits", ctypes.c_double)]
 
 
-def a2ats_key_byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:
-    """Bytes of `tokens` keys of width d stored as codebook_bits-bit codes,
-    one per sub_dim numbers, against fp16 (host arithmetic only)."""
-    out = KeyBytes()
-    _check("a2ats_key_byte_accounting", _load().a2ats_key_byte_accounting(
+def a2ats_byte_accounting(tokens: int, d: int, sub_dim: int, codebook_bits: int) -> dict:
+    """The page's byte accounting of `tokens` keys and values of width d
+    (host arithmetic through the C ABI)."""
+    out = CacheBytes()
+    _check("a2ats_byte_accounting", _load().a2ats_byte_accounting(
         int(tokens), int(d), int(sub_dim), int(codebook_bits), ctypes.byref(out)))
-    return {name: getattr(out, name) for name, _ in KeyBytes._fields_}
+    return {name: getattr(out, name) for name, _ in CacheBytes._fields_}
 
 
 def a2ats_dequantize(codes, codebook, *, lengths=None, out=None, stream=None):

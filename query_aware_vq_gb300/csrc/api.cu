@@ -720,15 +720,17 @@ int a2ats_dequantize(const int32_t* codes, const void* codebook, int32_t dtype, 
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 
-int a2ats_key_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
-                              a2ats_key_bytes* out) {
+int a2ats_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t codebook_bits,
+                          a2ats_cache_bytes* out) {
     if (!out) return A2ATS_ERR_INVALID_ARG;
     if (tokens < 0 || d < 1) return A2ATS_ERR_SHAPE;
     if (sub_dim < 1 || codebook_bits < 1 || codebook_bits > 24) return A2ATS_ERR_INVALID_ARG;
     if (d % sub_dim != 0) return A2ATS_ERR_SHAPE;
     const double groups = (double)(d / sub_dim);
     out->compressed_key_bytes = (double)tokens * groups * (double)codebook_bits / 8.0;
+    out->compressed_value_bytes = out->compressed_key_bytes;
     out->fp16_key_bytes = (double)tokens * (double)d * 2.0;
+    out->fp16_value_bytes = out->fp16_key_bytes;
     out->compression_ratio = 16.0 * (double)sub_dim / (double)codebook_bits;
     out->codebook_bytes = (double)(int64_t(1) << codebook_bits) * (double)sub_dim * 2.0;
     out->assigned_avg_bits = (double)codebook_bits / (double)sub_dim;

@@ -177,20 +177,24 @@ def test_dequantize_validation(lib):
     assert f(None, None, 1, 0, 2, 64, 128, 256, None, None, None) == 0
 
 
-def test_key_byte_accounting_matches_the_page_table():
-    """v0.39.0 page, "What you get with the defaults", through the C ABI."""
+def test_byte_accounting_matches_the_page_table():
+    """v0.39.0 page, "What you get with the defaults", through the C ABI, and
+    the same figures as the oracle's accounting."""
+    import oracle
     from _golden import lines
     for row in lines("compression_defaults.txt"):
-        acc = q.a2ats_key_byte_accounting(1000, 128, int(row[0]), int(row[1]))
+        acc = q.a2ats_byte_accounting(1000, 128, int(row[0]), int(row[1]))
         assert acc["assigned_avg_bits"] == float(row[2])
         assert acc["compression_ratio"] == float(row[3])
         assert acc["codebook_bytes"] / 1024 == float(row[4])
+        assert acc == oracle.byte_accounting(1000, 128, int(row[0]), int(row[1]))
     # the full-width codes of the Llama-3.2-3B layer: 10 bits per 128-number key
-    acc = q.a2ats_key_byte_accounting(32768, 128, 128, 10)
-    assert acc["compressed_key_bytes"] == 32768 * 10 / 8
+    acc = q.a2ats_byte_accounting(32768, 128, 128, 10)
+    assert acc["compressed_key_bytes"] == acc["compressed_value_bytes"] == 32768 * 10 / 8
     assert acc["compression_ratio"] == 16 * 128 / 10
+    assert q.a2ats_byte_accounting(0, 128, 8, 8)["compression_ratio"] == 16.0
     with pytest.raises(q.A2ATSError):
-        q.a2ats_key_byte_accounting(10, 128, 5, 8)
+        q.a2ats_byte_accounting(10, 128, 5, 8)
 
 
 def test_copy_retrieval_rows_validation(lib):

@@ -37,4 +37,13 @@ def test_byte_accounting_matches_the_page_table(row):
     assert acc["assigned_avg_bits"] == per_number
     assert acc["compression_ratio"] == smaller
     assert acc["codebook_bytes"] / 1024 == table_kb
-    assert acc["fp16_key_bytes"] == 1000 * 128 * 2
+    assert acc["fp16_key_bytes"] == acc["fp16_value_bytes"] == 1000 * 128 * 2
+    assert acc["compressed_key_bytes"] == acc["compressed_value_bytes"]
+    # the stated bits per number times the numbers stored, in bytes
+    assert acc["compressed_key_bytes"] == 1000 * 128 * per_number / 8
+
+
+def test_byte_accounting_with_no_tokens_keeps_the_settings_ratio():
+    acc = oracle.byte_accounting(tokens=0, d=128, sub_dim=8, codebook_bits=8)
+    assert acc["compressed_key_bytes"] == acc["fp16_value_bytes"] == 0
+    assert acc["compression_ratio"] == 16.0
