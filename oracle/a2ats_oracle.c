@@ -470,7 +470,8 @@ static double assign_all(const double* z, int64_t n, int64_t d, const double* c,
 
 void orc_kmeanspp(const double* z, int64_t n, int64_t d, int64_t K, const double* u,
                   int64_t iters, double* centroids, int32_t* codes, double* objective) {
-    double* d2 = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (n <= 0 || K <= 0) return; /* no points to seed from */
+    double* d2 = (double*)malloc(sizeof(double) * (size_t)n);
     int64_t first = (int64_t)floor(u[0] * (double)n);
     if (first >= n) first = n - 1;
     if (first < 0) first = 0;
