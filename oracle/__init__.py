@@ -33,15 +33,22 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc the C source `src` (which includes a2ats_oracle.h from this
+    directory) into the shared library `out`, with no FMA contraction so
+    results do not depend on the host ISA."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-fno-fast-math", "-I", _HERE, src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (no FMA contraction, so results do not
-    depend on the host ISA)."""
+    """Compile the oracle (compile_source) unless the library is current."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
             os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "a2ats_oracle.h"))):
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_source(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -52,7 +59,9 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        # A2ATS_ORACLE_LIB: a library built from a planted-mistake copy of the
+        # source, for the tests that check the pins catch such mistakes
+        lib = ctypes.CDLL(os.environ.get("A2ATS_ORACLE_LIB") or build())
         lib.orc_rope_row.argtypes = [_f64p, _f64p, ctypes.c_int64, ctypes.c_double,
                                      ctypes.c_double, ctypes.c_int]
         lib.orc_windowed_rope.argtypes = [_f64p, _f64p, ctypes.c_int64, ctypes.c_int64, _i64p,

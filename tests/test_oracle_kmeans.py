@@ -9,10 +9,13 @@ import oracle
 from _golden import table
 
 
-def test_hand_worked_fixture():
-    g = table("kmeanspp_1d.txt")
+@pytest.mark.parametrize("name", ["kmeanspp_1d.txt", "kmeanspp_1d_offset.txt",
+                                  "kmeanspp_1d_empty.txt"])
+def test_hand_worked_fixture(name):
+    g = table(name)
     f = lambda k: [float(v) for v in g[k][0]]
-    cent, codes, obj = oracle.kmeanspp(np.array(f("points"))[:, None], 2, np.array(f("u")),
+    u = np.array(f("u"))
+    cent, codes, obj = oracle.kmeanspp(np.array(f("points"))[:, None], len(u), u,
                                        int(f("iters")[0]))
     np.testing.assert_array_equal(cent[:, 0], f("centroids"))
     assert codes.tolist() == [int(v) for v in f("codes")]

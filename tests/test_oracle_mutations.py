@@ -1,0 +1,78 @@
+"""The oracle's pins catch plausible mistakes in the oracle itself.
+
+Each case plants one mistake in a copy of oracle/a2ats_oracle.c (a dropped
+term, a wrong sign, a transposed index, an off-by-one, a wrong tie rule),
+builds it with the oracle's own compile step, and runs the pin tests of the
+routine it touches against that library (A2ATS_ORACLE_LIB, in a child
+pytest): at least one pin must fail.  CPU only; nothing here touches the
+CUDA library.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+# name, text in the oracle source, planted text, pin files that must catch it
+MUTATIONS = [
+    ("rope sign", "y[a] = xa * c - xb * s;", "y[a] = xa * c + xb * s;", ["rope"]),
+    ("rope frequency", "pow(base, -2.0 * (double)i / (double)d)",
+     "pow(base, -(double)i / (double)d)", ["rope"]),
+    ("window boundary off by one", "dist < window;\n        double pos",
+     "dist <= window;\n        double pos", ["rope"]),
+    ("second moment not averaged", "(M > 0 ? s / (double)M : 0.0)", "(M > 0 ? s : 0.0)",
+     ["calib"]),
+    ("ridge off the diagonal too", "(a == b ? ridge : 0.0)", "ridge", ["calib"]),
+    ("cholesky index transposed", "s -= l[i * d + k] * l[j * d + k];",
+     "s -= l[i * d + k] * l[k * d + j];", ["calib"]),
+    ("quadratic form drops a factor", "v += diff[a] * row;", "v += row;", ["assign"]),
+    ("row times L transposed", "s += v[a] * l[a * d + b];", "s += v[a] * l[b * d + a];",
+     ["assign", "kmeans"]),
+    ("ties to the highest index", "if (v < *b1) { *b2 = *b1;", "if (v <= *b1) { *b2 = *b1;",
+     ["assign"]),
+    ("blend weights swapped", "double s = -p->beta * err + (1.0 - p->beta) * cosv;",
+     "double s = -(1.0 - p->beta) * err + p->beta * cosv;", ["assign"]),
+    ("blend error not normalised", "double err = m > 0.0 ? e[j] / m : 0.0;",
+     "double err = e[j];", ["assign"]),
+    ("split cosine without the query norm",
+     "double v = (kn > 0.0 && qn > 0.0) ? dot / (kn * qn) : 0.0;",
+     "double v = (kn > 0.0 && qn > 0.0) ? dot / kn : 0.0;", ["split"]),
+    ("split ties to the higher index", "return (x->i > y->i) - (x->i < y->i);",
+     "return (x->i < y->i) - (x->i > y->i);", ["split", "attention"]),
+    ("far query rotated the wrong way", "orc_rope_row(q, qf, d, far_b, base, interleaved);",
+     "orc_rope_row(q, qf, d, -far_b, base, interleaved);", ["attention"]),
+    ("near key rotated at the distance",
+     "orc_rope_row(keys + j * d, kr, d, (double)j, base, interleaved);",
+     "orc_rope_row(keys + j * d, kr, d, (double)(t - j), base, interleaved);", ["attention"]),
+    ("out-of-range code reads centroid 0", "? codebook[(int64_t)c * d + a] : 0.0;",
+     "? codebook[(int64_t)c * d + a] : codebook[a];", ["dequant"]),
+    ("back substitution sign", "s -= ci[a] * l[a * d + b];", "s += ci[a] * l[a * d + b];",
+     ["kmeans"]),
+    ("first centre ignores its draw", "int64_t first = (int64_t)floor(u[0] * (double)n);",
+     "int64_t first = 0;", ["kmeans"]),
+    ("draw not scaled by the D^2 sum", "double target = u[k] * total, run = 0.0;",
+     "double target = u[k], run = 0.0;", ["kmeans"]),
+    ("mean over one member too many", "sum[j * d + a] / (double)cnt[j];",
+     "sum[j * d + a] / (double)(cnt[j] + 1);", ["kmeans"]),
+    ("empty centre moved", "if (cnt[j] > 0)\n", "if (1)\n", ["kmeans"]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new, pins, tmp_path):
+    with open(os.path.join(ROOT, "oracle", "a2ats_oracle.c")) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"the text to change must occur once: {old!r}"
+    planted = tmp_path / "planted.c"
+    planted.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(planted), str(tmp_path / "planted.so"))
+    files = [os.path.join(HERE, f"test_oracle_{p}.py") for p in pins]
+    env = dict(os.environ, A2ATS_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *files], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert r.returncode == 1, f"{name}: no pin failed\n{r.stdout[-2000:]}"
