@@ -60,6 +60,44 @@ MUTATIONS = [
     ("mean over one member too many", "sum[j * d + a] / (double)cnt[j];",
      "sum[j * d + a] / (double)(cnt[j] + 1);", ["kmeans"]),
     ("empty centre moved", "if (cnt[j] > 0)\n", "if (1)\n", ["kmeans"]),
+    ("second best kept wrong", "else if (v < *b2) { *b2 = v; }",
+     "else if (v > *b2) { *b2 = v; }", ["assign"]),
+    ("threshold score of the split off by rank",
+     "if (kth) *kth = count > 0 ? s[count - 1].s : INFINITY;\n    qsort(perm, (size_t)count, "
+     "sizeof(int32_t), by_value);\n    qsort(perm + count, (size_t)(n - count), "
+     "sizeof(int32_t), by_value);\n    free(s);\n    return count;\n}\n\n/* ----",
+     "if (kth) *kth = count > 0 ? s[0].s : INFINITY;\n    qsort(perm, (size_t)count, "
+     "sizeof(int32_t), by_value);\n    qsort(perm + count, (size_t)(n - count), "
+     "sizeof(int32_t), by_value);\n    free(s);\n    return count;\n}\n\n/* ----", ["split"]),
+    ("split size rounded down",
+     "if (scores) scores[i] = v;\n    }\n    int64_t count = (int64_t)ceil(",
+     "if (scores) scores[i] = v;\n    }\n    int64_t count = (int64_t)floor(", ["split"]),
+    ("retrieved count rounded down",
+     "if (scores) scores[j] = u;\n    }\n    int64_t count = (int64_t)ceil(",
+     "if (scores) scores[j] = u;\n    }\n    int64_t count = (int64_t)floor(", ["attention"]),
+    ("blend cosine unnormalised", "cosv = dot / (qn * p->cnorm[j]);", "cosv = dot;",
+     ["assign"]),
+    ("far offset ignored", "double pos = near ? (double)p[r] : far_offset;",
+     "double pos = near ? (double)p[r] : 0.0;", ["rope"]),
+    ("attention window edge off by one",
+     "int near = window > 0 && dist >= 0 && dist < window;\n        double u = 0.0;",
+     "int near = window > 0 && dist >= 0 && dist <= window;\n        double u = 0.0;",
+     ["attention"]),
+    ("cholesky square root dropped", "l[i * d + i] = sqrt(s);", "l[i * d + i] = s;",
+     ["calib"]),
+    ("cholesky failing minor off by one", "if (!(s > 0.0)) return (int)(i + 1);",
+     "if (!(s > 0.0)) return (int)i;", ["calib"]),
+    ("blend beta = 1 not reduced exactly", "if (p->beta == 1.0) {", "if (p->beta == 2.0) {",
+     ["assign"]),
+    ("final objective dropped",
+     "objective[iters] = assign_all(z, n, d, centroids, K, codes);",
+     "objective[iters] = 0.0;", ["kmeans"]),
+    ("k-means distance not squared", "double t = a[i] - b[i];\n        s += t * t;",
+     "double t = a[i] - b[i];\n        s += fabs(t);", ["kmeans"]),
+    ("z-space distance not squared",
+     "for (int64_t b = 0; b < d; b++) { double e = z[b] - cj[b]; v += e * e; }",
+     "for (int64_t b = 0; b < d; b++) { double e = z[b] - cj[b]; v += fabs(e); }",
+     ["assign"]),
 ]
 
 
