@@ -4,10 +4,13 @@ Each case plants one mistake in a copy of oracle/a2ats_oracle.c (a dropped
 term, a wrong sign, a transposed index, an off-by-one, a wrong tie rule),
 builds it with the oracle's own compile step, and runs the pin tests of the
 routine it touches against that library (A2ATS_ORACLE_LIB, in a child
-pytest): at least one pin must fail.  CPU only; nothing here touches the
-CUDA library.
+pytest): at least one pin must fail.  The Python-level routines (the step's
+composition, the split size, the byte accounting) get the same treatment
+through a planted copy of the oracle package placed first on the child's
+path.  CPU only; nothing here touches the CUDA library.
 """
 import os
+import shutil
 import subprocess
 import sys
 
@@ -113,4 +116,44 @@ def test_planted_mistake_is_caught(name, old, new, pins, tmp_path):
     env = dict(os.environ, A2ATS_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         *files], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert r.returncode == 1, f"{name}: no pin failed\n{r.stdout[-2000:]}"
+
+
+# planted mistakes in the Python composition of oracle/__init__.py
+PY_MUTATIONS = [
+    ("retrieval rows take the plain rule",
+     "cr, a, b = assign_cholesky(kt[ret], c, l, nthreads)",
+     "cr, a, b = assign_cholesky(kt[ret], c, None, nthreads)", ["pipeline"]),
+    ("bulk rows take the H rule", "cb, a, b = assign_cholesky(kt[bulk], c, None, nthreads)",
+     "cb, a, b = assign_cholesky(kt[bulk], c, l, nthreads)", ["pipeline"]),
+    ("proxy query from the first row", "    q = kt[t]\n", "    q = kt[0]\n", ["pipeline"]),
+    ("blend with each row as its own query",
+     "cr, a, b = assign_blend(kt[ret], c, q, beta, nthreads)",
+     "cr, a, b = assign_blend(kt[ret], c, kt[ret], beta, nthreads)", ["pipeline"]),
+    ("far offset dropped in the step",
+     "kt = windowed_rope(k, pos, t, window, far_offset, base, interleaved)",
+     "kt = windowed_rope(k, pos, t, window, 0, base, interleaved)", ["pipeline"]),
+    ("split size rounded down", "return min(n, max(0, math.ceil(float(fraction) * n)))",
+     "return min(n, max(0, math.floor(float(fraction) * n)))", ["split"]),
+    ("value bytes dropped", "    cv, fv = ck, fk\n", "    cv, fv = 0.0, fk\n", ["dequant"]),
+    ("codebook bytes per bit", '"codebook_bytes": float((1 << codebook_bits) * sub_dim * 2)',
+     '"codebook_bytes": float(codebook_bits * sub_dim * 2)', ["dequant"]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,pins", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_planted_python_mistake_is_caught(name, old, new, pins, tmp_path):
+    pkg = os.path.join(ROOT, "oracle")
+    with open(os.path.join(pkg, "__init__.py")) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"the text to change must occur once: {old!r}"
+    shutil.copytree(pkg, tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    (tmp_path / "oracle" / "__init__.py").write_text(src.replace(old, new))
+    env = dict(os.environ, A2ATS_ORACLE_LIB=oracle.build(),
+               PYTHONPATH=str(tmp_path) + os.pathsep + ROOT)
+    files = [os.path.join(HERE, f"test_oracle_{p}.py") for p in pins]
+    # run from the planted copy's directory, so that it is the oracle imported
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *files], cwd=str(tmp_path), env=env, capture_output=True, text=True)
     assert r.returncode == 1, f"{name}: no pin failed\n{r.stdout[-2000:]}"

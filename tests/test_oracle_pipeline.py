@@ -52,3 +52,27 @@ def test_token_leaves_window_as_decode_position_advances():
     b = oracle.pipeline_step(k[:60], 59, c, window=8, far_offset=0, base=10000.0, fraction=0.1)
     assert not np.array_equal(a.k_tilde[45], k[45])
     assert np.array_equal(b.k_tilde[45], k[45])
+
+
+def _rotate(x, pos, base):
+    """RoPE of the rows of x at positions pos as complex multiplication
+    (half-split pairs (i, i + d/2), frequency base^(-2i/d))."""
+    d = x.shape[1]
+    h = d // 2
+    w = base ** (-2.0 * np.arange(h) / d)
+    z = (x[:, :h] + 1j * x[:, h:]) * np.exp(1j * np.asarray(pos, float)[:, None] * w)
+    return np.concatenate([z.real, z.imag], axis=1)
+
+
+def test_far_rows_of_the_step_take_the_shared_far_rotation():
+    """With far_offset = b the step's far rows are every key rotated at b,
+    the window rows at their own positions, and the bulk codes are the plain
+    nearest centroid of those rows (deploy-preview page, Eq. 11-12)."""
+    k, c = _case(n=120, seed=4)
+    t, W, b = 119, 10, 37
+    res = oracle.pipeline_step(k, t, c, window=W, far_offset=b, base=10000.0, fraction=0.1)
+    pos = np.where(t - np.arange(120) < W, np.arange(120), b)
+    np.testing.assert_allclose(res.k_tilde, _rotate(k, pos, 10000.0), rtol=0, atol=1e-12)
+    bulk = res.perm[res.count:]
+    np.testing.assert_array_equal(res.codes[bulk],
+                                  cdist(res.k_tilde[bulk], c, "sqeuclidean").argmin(1))
