@@ -289,3 +289,20 @@ def test_subvector_query_aware_assign_validation(lib):
     assert f(x, 1, B, H, N, d, None, s, c, K, q_, 0.5, p, n, k, W, ws - 1, None) == -6
     assert f(None, 1, B, 0, N, d, None, s, None, K, None, 0.5, None, None, None, None, 0,
              None) == 0
+
+
+def test_binding_signatures_match_the_header():
+    """Every call the binding declares has as many arguments as its
+    prototype in include/a2ats.h (the binding passes plain ctypes values, so
+    a drift would go unnoticed until a call misbehaves)."""
+    import re
+    with open(q.HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(?:int|size_t|uint64_t|double|const char\*)\s+(a2ats_\w+)\s*"
+                         r"\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        protos[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    assert set(protos) == set(q.declared_symbols())
+    for name, args in q._SIGS.items():
+        assert protos[name] == len(args), name
