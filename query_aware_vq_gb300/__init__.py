@@ -167,7 +167,12 @@ def _dt(t: torch.Tensor) -> int:
 
 def _dev(*ts):
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (the library reads and writes them "
+                             "through their data pointers in row-major order)")
+        if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device (the library has no CPU path)")
 
 

@@ -306,3 +306,16 @@ def test_binding_signatures_match_the_header():
     assert set(protos) == set(q.declared_symbols())
     for name, args in q._SIGS.items():
         assert protos[name] == len(args), name
+
+
+def test_binding_refuses_strided_and_host_tensors():
+    """The binding hands data pointers to the library: a tensor that is not
+    row-major contiguous, or not on a CUDA device, is refused before any
+    call."""
+    import torch
+    codes = torch.zeros((1, 2, 8), dtype=torch.int32)
+    cb = torch.zeros((2, 4, 16), dtype=torch.float32)
+    with pytest.raises(ValueError, match="contiguous"):
+        q.a2ats_dequantize(codes.transpose(1, 2), cb)
+    with pytest.raises(ValueError, match="CUDA"):
+        q.a2ats_dequantize(codes, cb)
