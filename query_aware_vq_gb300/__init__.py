@@ -5,8 +5,8 @@ Every function here has the name of the C entry point it wraps (see
 include/a2ats.h) and only marshals arguments: tensor pointers, sizes, the
 current CUDA stream, and a scratch workspace tensor when the caller gives none.
 All arithmetic runs in the library's CUDA kernels.  There is no CPU path: the
-functions raise when the library is missing or a tensor is not on a CUDA
-device.
+functions raise when the library is missing or a tensor is not a contiguous
+tensor on a CUDA device.
 
 Layouts: keys [B, H, N, d] (a 2-D [N, d] array is taken as B = H = 1),
 codebooks [H, K, d], H / L matrices [H, d, d] fp32, per-(b, h) queries
