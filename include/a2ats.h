@@ -2,7 +2,10 @@
  * a2ats.h -- C ABI of the GB300 (sm_103a) library for the data-parallel hot path
  * of A2ATS-style retrieval-based KV-cache compression: windowed RoPE, query
  * second moment and its Cholesky factor, H-weighted and cosine-blend codebook
- * assignment, and the retrieval-set split.
+ * assignment, and the retrieval-set split; and the steps around it:
+ * code-based attention scores with top-token retrieval, dequantisation and
+ * byte accounting, sub-vector (product) VQ of keys and values, and codebook
+ * calibration by k-means++ in Cholesky space.
  *
  * Sources.  The operations follow the veloxquant-mlx documentation of its
  * "A2ATS-adapted" method (after He et al., "A2ATS: Retrieval-Based KV Cache
@@ -15,7 +18,10 @@
  *   [ALG]  "A2ATS-adapted" algorithm page (deploy-preview build), section
  *          "For contributors -- paper fidelity": windowed RoPE (Eq. 11-12),
  *          query-aware VQ (Eq. 13-18), per-step re-rotation;
- *   [V039] the v0.39.0 algorithm page, "How it works" (steps 1-5).
+ *   [V039] the v0.39.0 algorithm page, "How it works" (steps 1-5),
+ *          configuration and "Byte accounting";
+ *   [ABS]  the paper's abstract (attention scores approximated through the
+ *          quantised keys to retrieve the top tokens).
  *
  * Conventions shared by every call
  * --------------------------------
