@@ -629,9 +629,10 @@ def run_decode(a):
         print(json.dumps(line), flush=True)
 
 
-def _oracle_sample(w, keys, cb, queries, hg, rows: int, h: int):
+def _oracle_sample(w, keys, cb, queries, hg, rows: int, h: int, nthreads=None):
     """One bounded sample of the workload on the oracle: the first `rows`
-    keys of head h (as a sequence of that length) through the whole step."""
+    keys of head h (as a sequence of that length) through the whole step,
+    on nthreads host threads (None: the oracle's default)."""
     import oracle
     n = min(rows, w.N)
     k = keys[0, h, :n]
@@ -643,7 +644,7 @@ def _oracle_sample(w, keys, cb, queries, hg, rows: int, h: int):
         L, _ = oracle.cholesky(hg[h].double().numpy())
     t0 = time.perf_counter()
     oracle.pipeline_step(k, n - 1, cb[h], w.W, w.far_offset, w.rope_base, w.fraction, l=L,
-                         beta=w.betas[-1])
+                         beta=w.betas[-1], nthreads=nthreads)
     return n, time.perf_counter() - t0
 
 
@@ -654,10 +655,13 @@ def cpu_baseline(w, keys, cb, queries, hg, rows: int = 8192, reps: int = 2):
         n_done += n
         t += dt
     import oracle
+    n1, t1 = _oracle_sample(w, keys, cb, queries, hg, rows // 4, 0, nthreads=1)
     return {"value": n_done / t, "unit": "keys/s", "cores": oracle.default_threads(),
             "kind": "oracle",
             "sample": f"{reps} x the first {rows} keys of one head as a whole sequence "
-                      f"(all stages; calibration of L excluded from the time), fp64 C"}
+                      f"(all stages; calibration of L excluded from the time), fp64 C",
+            "single_thread": {"value": n1 / t1, "unit": "keys/s", "cores": 1,
+                              "sample": f"the first {rows // 4} keys of head 0, one thread"}}
 
 
 def run_reference(a):
