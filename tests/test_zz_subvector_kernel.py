@@ -210,3 +210,28 @@ def test_subvector_step_without_a_factor_takes_the_blend():
         check_codes(codes_k[0, h].ravel(), code, gap, "key sub-codes")
         vc, e1, e2 = oracle.assign_cholesky(f64(v[0, h]).reshape(n * G, s), f64(cv[h]), None)
         check_codes(codes_v[0, h].ravel(), vc, (e2 - e1) / e2, "value sub-codes")
+
+
+def test_config_without_query_awareness_codes_every_token_plainly():
+    """A2ATSConfig(use_query_aware=False): the split is empty and every key
+    and value sub-vector takes plain VQ."""
+    from query_aware_vq_gb300.config import A2ATSConfig
+
+    cfg = A2ATSConfig(head_dim=64, window=32, use_query_aware=False, rope_base=500000.0)
+    B, H, N = 1, 2, 300
+    s, G, K = cfg.sub_dim, 64 // cfg.sub_dim, cfg.n_centroids
+    k = synth.gaussian((B, H, N, 64), seed=61, dtype="bf16")
+    v = synth.gaussian((B, H, N, 64), seed=62, dtype="f32")
+    ck = synth.gaussian((H, K, s), seed=63, dtype="f32")
+    cv = synth.gaussian((H, K, s), seed=64, dtype="f32")
+    step = cfg.subvector_step(B, H, N, torch.bfloat16)
+    step(dev(k), dev(v), dev(ck), dev(cv), None)
+    torch.cuda.synchronize()
+    assert step.count.cpu().numpy().tolist() == [[0] * H]
+    for h in range(H):
+        kt = oracle.windowed_rope(f64(k[0, h]), np.arange(N), N - 1, cfg.window, 0,
+                                  cfg.rope_base)
+        code, d1, d2 = oracle.assign_cholesky(kt.reshape(N * G, s), f64(ck[h]), None)
+        check_codes(step.codes_k[0, h].cpu().numpy().ravel(), code, (d2 - d1) / d2)
+        vc, e1, e2 = oracle.assign_cholesky(f64(v[0, h]).reshape(N * G, s), f64(cv[h]), None)
+        check_codes(step.codes_v[0, h].cpu().numpy().ravel(), vc, (e2 - e1) / e2)
