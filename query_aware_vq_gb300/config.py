@@ -5,7 +5,8 @@ in [0, 1], query_h sub_dim x sub_dim, a codebook of 2^bits entries of
 sub_dim numbers.  `validate()` raises ValueError on the first violated
 rule; the same ranges are enforced again by the C ABI calls the settings
 reach.  `subvector_step()` builds the sub-vector step these settings
-describe; `byte_accounting()` is the page's storage arithmetic for them.
+describe, `factor()` the Cholesky factor of query_h it takes, and
+`byte_accounting()` is the page's storage arithmetic for them.
 """
 from __future__ import annotations
 
@@ -75,6 +76,31 @@ class A2ATSConfig:
         return A2ATSSubvectorStep(B, H, N, self.head_dim, self.sub_dim, self.n_centroids,
                                   dtype, window=self.window, fraction=frac,
                                   rope_base=self.rope_base, beta=self.beta, **kw)
+
+    def factor(self, H: int, device="cuda"):
+        """L with query_h = L L^T for each of the H heads (a2ats_cholesky_factor
+        on the device; a shared [sub_dim, sub_dim] query_h serves every head),
+        or None without query_h.  Raises ValueError when query_h is not
+        positive definite."""
+        import torch
+
+        from . import a2ats_cholesky_factor
+
+        self.validate()
+        if self.query_h is None:
+            return None
+        h = torch.as_tensor(self.query_h, dtype=torch.float32).to(device)
+        if h.dim() == 2:
+            h = h.expand(H, self.sub_dim, self.sub_dim)
+        h = h.contiguous()
+        if h.shape[0] != H:
+            raise ValueError(f"query_h holds {h.shape[0]} heads, not {H}")
+        L, info = a2ats_cholesky_factor(h)
+        bad = info.cpu()
+        if bool((bad != 0).any()):
+            raise ValueError(f"query_h is not positive definite (failing minor per head: "
+                             f"{bad.tolist()})")
+        return L
 
     def byte_accounting(self, tokens: int) -> dict:
         """The page's byte accounting of `tokens` keys and values under

@@ -235,3 +235,40 @@ def test_config_without_query_awareness_codes_every_token_plainly():
         check_codes(step.codes_k[0, h].cpu().numpy().ravel(), code, (d2 - d1) / d2)
         vc, e1, e2 = oracle.assign_cholesky(f64(v[0, h]).reshape(N * G, s), f64(cv[h]), None)
         check_codes(step.codes_v[0, h].cpu().numpy().ravel(), vc, (e2 - e1) / e2)
+
+
+def test_config_factor_drives_the_h_weighted_rule():
+    """A2ATSConfig.factor: L of a shared query_h for every head; the step
+    with it gives the retrieval tokens' sub-vectors the H-weighted rule."""
+    from query_aware_vq_gb300.config import A2ATSConfig
+
+    rng = np.random.default_rng(71)
+    A = rng.standard_normal((8, 8))
+    hq = A @ A.T / 8 + 0.1 * np.eye(8)
+    cfg = A2ATSConfig(head_dim=64, window=32, query_h=hq, retrieval_fraction=0.2,
+                      rope_base=500000.0)
+    B, H, N = 1, 2, 300
+    s, G, K = cfg.sub_dim, 64 // cfg.sub_dim, cfg.n_centroids
+    L = cfg.factor(H)
+    lo, _ = oracle.cholesky(hq.astype(np.float32).astype(np.float64))
+    for h in range(H):
+        np.testing.assert_allclose(f64(L[h]), lo, rtol=0, atol=1e-5)
+    k = synth.gaussian((B, H, N, 64), seed=72, dtype="bf16")
+    v = synth.gaussian((B, H, N, 64), seed=73, dtype="f32")
+    ck = synth.gaussian((H, K, s), seed=74, dtype="f32")
+    cv = synth.gaussian((H, K, s), seed=75, dtype="f32")
+    step = cfg.subvector_step(B, H, N, torch.bfloat16)
+    step(dev(k), dev(v), dev(ck), dev(cv), L)
+    torch.cuda.synchronize()
+    perm, count = step.perm.cpu().numpy(), step.count.cpu().numpy()
+    for h in range(H):
+        lh = f64(L[h])
+        kt = oracle.windowed_rope(f64(k[0, h]), np.arange(N), N - 1, cfg.window, 0,
+                                  cfg.rope_base)
+        ret = np.sort(perm[0, h, :int(count[0, h])])
+        sub = kt.reshape(N * G, s)
+        code, d1, d2 = oracle.assign_cholesky(sub, f64(ck[h]), None)
+        rsub = (ret[:, None] * G + np.arange(G)).ravel()
+        cr, r1, r2 = oracle.assign_cholesky(sub[rsub], f64(ck[h]), lh)
+        code[rsub], d1[rsub], d2[rsub] = cr, r1, r2
+        check_codes(step.codes_k[0, h].cpu().numpy().ravel(), code, (d2 - d1) / d2)
