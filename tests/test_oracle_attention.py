@@ -73,6 +73,25 @@ def test_window_splits_rows_by_distance_to_t():
     np.testing.assert_allclose(s, np.where(near, near_want, far_want), rtol=1e-12, atol=1e-12)
 
 
+def test_far_query_rotation_does_not_depend_on_the_window():
+    """The far relative position b rides on the query whatever the window
+    (deploy-preview page, Eq. 11): rows that are far under two windows score
+    the same under both, and equal the score at relative position b."""
+    rng = np.random.default_rng(5)
+    n, d, K, base, b = 80, 8, 6, 1e4, 2048.0
+    k, q, c = rng.standard_normal((n, d)), rng.standard_normal(d), rng.standard_normal((K, d))
+    codes = rng.integers(0, K, n).astype(np.int32)
+    t = n - 1
+    _, _, s4, _ = oracle.code_attention_topk(k, t, codes, c, q, window=4, far_b=b, base=base,
+                                             fraction=0.2)
+    _, _, s40, _ = oracle.code_attention_topk(k, t, codes, c, q, window=40, far_b=b,
+                                              base=base, fraction=0.2)
+    far_both = t - np.arange(n) >= 40
+    np.testing.assert_array_equal(s4[far_both], s40[far_both])
+    np.testing.assert_allclose(s4[far_both], _rel_score(q, c[codes[far_both]], b, base),
+                               rtol=1e-12, atol=1e-12)
+
+
 def test_out_of_range_codes_score_zero():
     rng = np.random.default_rng(4)
     n, d = 6, 4
