@@ -388,7 +388,7 @@ int a2ats_byte_accounting(int64_t tokens, int64_t d, int64_t sub_dim, int32_t co
  * a2ats_cholesky_rows -- the change of variables of [API]
  * a2ats_cholesky_factor: z = x L for every row, so that the H-weighted
  * distance (x - c) H (x - c)^T with H = L L^T is |z_x - z_c|^2 and
- * conventional k-means on z calibrates an H-weighted codebook.
+ * ordinary k-means on the z rows trains an H-weighted codebook.
  *   x  [H, n, d] device, in dtype (e.g. calibration keys of one layer, head
  *      by head)
  *   L  [H, d, d] fp32 device; only the lower triangle (with the diagonal) is

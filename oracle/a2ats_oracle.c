@@ -425,10 +425,11 @@ void orc_cholesky_solve_rows(const double* z, int64_t n, int64_t d, const double
 }
 
 /* ------------------------------------------------------------------------ */
-/* Codebook calibration in z space.  API page, a2ats_cholesky_factor: L     */
-/* maps the H-weighted objective to a plain Euclidean one on z = k L, which */
-/* lets conventional k-means++ build the codebook (the codebook in key      */
-/* space is then c = c_z L^-1).  Reading: k-means++ seeding, each centre    */
+/* Codebook calibration in z space.  API page, a2ats_cholesky_factor: once */
+/* every row is multiplied by the factor (z = k L, H = L L^T), ordinary     */
+/* squared distances between the z rows are the H-weighted ones, so the    */
+/* codebook is trained by ordinary k-means++ on the z rows and taken back  */
+/* by c = c_z L^-1.  Reading: k-means++ seeding, each centre               */
 /* drawn with probability proportional to the squared distance D^2 to the    */
 /* nearest centre chosen so far (the first uniformly), with the uniform      */
 /* draws u[0..K) given as input: centre k is the first point whose running   */

@@ -2,8 +2,8 @@
 //
 // API page "veloxquant_mlx.quantizers.a2ats module", a2ats_cholesky_factor:
 // with H = L L^T the H-weighted distance (k - c) H (k - c)^T is the plain
-// squared distance between z = k L and c L, so conventional k-means++ on the
-// rows z builds the codebook, and c = c_z L^-1 takes it back to key space.
+// squared distance between z = k L and c L, so ordinary k-means++ on the
+// rows z trains the codebook, and c = c_z L^-1 takes it back to key space.
 //
 //   kmeans_seed_kernel     k-means++ seeding with caller-given uniform draws:
 //                          one CTA per head, persistent over the K picks.

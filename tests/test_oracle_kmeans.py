@@ -1,7 +1,8 @@
 """Pins of the oracle's codebook calibration in z space (API page,
-a2ats_cholesky_factor: L maps the H-weighted objective to a plain Euclidean
-one on z = k L, so conventional k-means++ builds the codebook): k-means++
-seeding with given uniform draws, then Lloyd rounds."""
+a2ats_cholesky_factor: after z = k L with H = L L^T, ordinary squared
+distances between z rows are the H-weighted ones, so ordinary k-means++ on
+the z rows trains the codebook): k-means++ seeding with given uniform draws,
+then Lloyd rounds."""
 import numpy as np
 import pytest
 

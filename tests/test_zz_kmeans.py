@@ -1,6 +1,6 @@
 """GPU parity of the codebook calibration in Cholesky space (API page,
-a2ats_cholesky_factor: with H = L L^T, conventional k-means++ on z = k L
-builds the H-weighted codebook, and c = c_z L^-1 brings it back).
+a2ats_cholesky_factor: with H = L L^T, ordinary k-means++ on the rows
+z = k L trains the H-weighted codebook, and c = c_z L^-1 brings it back).
 
 * a2ats_kmeanspp against the oracle's kmeanspp on the same fp32 rows z: the
   seeds are copies of rows of z, so they must be the oracle's bit for bit;
