@@ -14,8 +14,8 @@
 
 /* ------------------------------------------------------------------------ */
 /* Windowed RoPE.  "A2ATS-adapted" page, paper-fidelity section, "Windowed   */
-/* RoPE (Eq. 11-12)": keys inside the trailing window get exact RoPE at their */
-/* own position; far keys get one shared rotation (the paper's Eq. 12 leaves  */
+/* RoPE (Eq. 11-12)": a key within the trailing window is rotated at its     */
+/* own position p; every other key takes one common rotation (Eq. 12 leaves  */
 /* them unrotated, i.e. far_offset = 0).  The v0.39.0 page, "How it works"    */
 /* step 4: window <= 0 -> every key far; window >= length -> every key exact. */
 /* ------------------------------------------------------------------------ */
@@ -46,8 +46,8 @@ void orc_windowed_rope(const double* x, double* y, int64_t rows, int64_t d,
 
 /* ------------------------------------------------------------------------ */
 /* Query second moment.  API page, a2ats_query_second_moment: H = E[q^T q]   */
-/* over the M calibration queries (paper Eq. 10), plus `ridge` on the        */
-/* diagonal so H is positive definite.  Not mean-centred.                    */
+/* over the M calibration queries (paper Eq. 10), with `ridge` added to     */
+/* each diagonal entry to keep H positive definite.  Not mean-centred.      */
 /* ------------------------------------------------------------------------ */
 void orc_query_second_moment(const double* q, int64_t M, int64_t d, double ridge,
                              double* h) {
@@ -278,9 +278,9 @@ void orc_assign_blend(const double* x, int64_t n, int64_t d, const double* c, in
 }
 
 /* ------------------------------------------------------------------------ */
-/* Retrieval split.  API page, a2ats_select_retrieval_set: the top          */
-/* ceil(retrieval_fraction * N) tokens by key-query cosine similarity form   */
-/* the retrieval set; the two index sets are disjoint and cover 0..N-1.      */
+/* Retrieval split.  API page, a2ats_select_retrieval_set: the retrieval    */
+/* set holds the ceil(retrieval_fraction * N) keys whose cosine with the    */
+/* query is largest; with the bulk it partitions 0..N-1.                    */
 /* Here: a full sort by (score descending, index ascending).                 */
 /* ------------------------------------------------------------------------ */
 typedef struct { double s; int32_t i; } scored;
