@@ -547,7 +547,11 @@ int a2ats_copy_retrieval_rows(const int32_t* src, int32_t* dst, int64_t B, int64
  *   (before anything is enqueued).  Arguments and results are otherwise those
  *   of a2ats_select_retrieval_set, and the results are identical.
  *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ *   that device current, and so does the first call after the device's
+ *   context was replaced (cudaDeviceReset); make such a call before any
+ *   stream capture.  Arguments are validated exactly as
+ *   a2ats_select_retrieval_set validates them, and a CUDA failure leaves its
+ *   message for a2ats_last_error.
  *   All calls share the one array and it keeps the last call's contents
  *   (every word a call reads is written earlier in the same call): calls
  *   that may overlap on the GPU -- on different streams, or from different

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "../../include/a2ats.h"
+#include "entry.cuh"
 #include "kernels.cuh"
 
 using namespace a2ats;
@@ -56,29 +57,20 @@ void a2ats::timing_end(cudaStream_t st) {
 }
 
 namespace {
-
 thread_local char g_last_error[256] = "";
+}  // namespace
 
-int cuda_fail(cudaError_t e) {
+int a2ats::cuda_fail(cudaError_t e) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
              cudaGetErrorString(e));
     return A2ATS_ERR_CUDA;
 }
 
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-// Do the byte ranges [p, p + pb) and [q, q + qb) share a byte?
-bool overlap(const void* p, size_t pb, const void* q, size_t qb) {
-    const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
-    return a < b + qb && b < a + pb;
+bool a2ats::dtype_ok(int32_t dt) {
+    return dt == A2ATS_F32 || dt == A2ATS_BF16 || dt == A2ATS_F16;
 }
 
-bool dtype_ok(int32_t dt) { return dt == A2ATS_F32 || dt == A2ATS_BF16 || dt == A2ATS_F16; }
-
-size_t dtype_bytes(int32_t dt) { return dt == A2ATS_F32 ? 4 : 2; }
-
-// d multiple of 8 in [8, 256]; positions below 2^24 (exact in fp32).
-int check_shape(int64_t B, int64_t H, int64_t Ncap, int64_t d) {
+int a2ats::check_shape(int64_t B, int64_t H, int64_t Ncap, int64_t d) {
     if (B < 0 || H < 0 || Ncap < 0) return A2ATS_ERR_SHAPE;
     if (d < 8 || d > kMaxD || d % 8 != 0) return A2ATS_ERR_SHAPE;
     if (Ncap >= (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
@@ -86,10 +78,9 @@ int check_shape(int64_t B, int64_t H, int64_t Ncap, int64_t d) {
     return A2ATS_OK;
 }
 
-bool unit_interval(double v) { return v >= 0.0 && v <= 1.0; }  // false for NaN
+bool a2ats::unit_interval(double v) { return v >= 0.0 && v <= 1.0; }
 
-// Fill the device-side RoPE constants.  enabled = 0 when p is null.
-int make_rope(const a2ats_rope_params* p, int64_t d, RopeArgs& ra) {
+int a2ats::make_rope(const a2ats_rope_params* p, int64_t d, RopeArgs& ra) {
     memset(&ra, 0, sizeof(ra));
     if (!p) return A2ATS_OK;
     if (!(p->rope_base > 0.0) || !isfinite(p->rope_base)) return A2ATS_ERR_INVALID_ARG;
@@ -114,6 +105,17 @@ int make_rope(const a2ats_rope_params* p, int64_t d, RopeArgs& ra) {
     }
     return A2ATS_OK;
 }
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Do the byte ranges [p, p + pb) and [q, q + qb) share a byte?
+bool overlap(const void* p, size_t pb, const void* q, size_t qb) {
+    const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+    return a < b + qb && b < a + pb;
+}
+
 
 // Bump allocator over the caller's workspace (256-byte aligned pieces).
 struct Carve {
@@ -156,7 +158,7 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.hneg = c.take<float>((size_t)(H * kpad));
     w.tc.head_bits = c.take<uint32_t>((size_t)(2 * H * 4));
     w.tc.head = c.take<float>((size_t)(2 * H * 4));
-    w.tc.gstat = c.take<float2>((size_t)(2 * H * (kpad / 32)));
+    w.tc.gstat = c.take<float2>((size_t)(2 * H * (kpad / kTcGroup)));
     w.tc.scale = c.take<float>((size_t)(2 * H));
     w.tc.planes = c.take<uint16_t>((size_t)(2 * H * 3 * K * d));
     w.tc.compact = c.take<uint16_t>(2 * rows * (size_t)d);

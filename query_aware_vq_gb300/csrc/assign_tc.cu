@@ -14,20 +14,23 @@
 // codebook needs one plane.  Each plane is one more pass of tcgen05.mma into
 // the same TMEM accumulator.
 //
-// Kernel layout (one persistent CTA per SM, 18 warps):
+// Kernel layout (one persistent CTA per SM, 10 warps):
 //   warp 0     TMA producer: the 128-row key tile once per tile (kept for all
 //              centroids), then the codebook in 256 x 64-element stages;
 //   warp 1     TMEM allocation and tcgen05.mma issue (128 x 256 x 16,
 //              bf16/fp16 -> fp32), two accumulators of 256 columns so the
 //              epilogue of one centroid chunk overlaps the MMAs of the next;
-//   warps 2-17 epilogue, one per (TMEM lane quarter, 64-column part):
-//              tcgen05.ld of the accumulator, v = acc - |c'|^2/2, branch-free
-//              top-2 per row with the column index carried in the 5 low
-//              mantissa bits; the parts of a row meet in shared memory, and a
-//              rigorous error bound sends rows whose top two are closer than
-//              the bound (and rows inside the RoPE window) to the exact SIMT
-//              kernels through a list.  Four epilogue warps per scheduler
-//              hide the TMEM and shared-memory latencies of each other.
+//   warps 2-9  epilogue, one per (TMEM lane quarter, 128-column part):
+//              tcgen05.ld of the accumulator, v = acc - |c'|^2/2, and per
+//              32-column group only its largest value (a three-input max
+//              tree); the values of the best group so far are kept in
+//              registers, and the position and second value inside it are
+//              found once per row after the sweep.  The parts of a row meet
+//              in shared memory, and a rigorous error bound sends rows whose
+//              top two are closer than the bound to the exact SIMT kernels
+//              through a list.  Each warp loads the next 32 columns from
+//              TMEM while it reduces the current ones, so two epilogue warps
+//              per scheduler keep it issuing.
 // Every mbarrier wait is bounded; on time-out the kernel records an error
 // code and leaves.
 #include <cuda.h>
@@ -39,12 +42,10 @@
 namespace a2ats {
 namespace tc {
 
-constexpr int BM = 128;   // rows per tile (UMMA M)
-constexpr int BN = 256;   // centroids per accumulator (UMMA N)
+constexpr int BM = 128;   // rows per row block (UMMA M)
 constexpr int BK = 64;    // 16-bit elements per 128-byte swizzle atom
-constexpr int kEpiWarps = 16;                // 4 TMEM lane quarters x 4 column parts
-constexpr int kParts = kEpiWarps / 4;         // column parts of a 256-column chunk
-constexpr int kSubs = BN / 32 / kParts;       // 32-column sub-chunks per part
+constexpr int kPadCols = 256;  // -|c L|^2 / 2 rows are padded to a multiple of this
+constexpr int kEpiWarps = 8;   // 4 TMEM lane quarters x 2 (row blocks or column parts)
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint64_t kWaitNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
 
@@ -69,9 +70,8 @@ struct Params {
     int64_t* exact_list;       // rows for the exact kernel
     int32_t* exact_count;
     int32_t* status;           // 0, or the code of a timed-out wait
-    uint32_t shr5_mul, shl5_mul;  // 2^27 and 32 (see embed_pos)
     const int32_t* max_rows;   // compact list: longest list over (b, h), or null
-    // per 32-centroid group: (max |chat_j|, max h_j) over the group, [H, ngroups]
+    // per group of kTcGroup centroids: (max |chat_j|, max h_j), [H, ngroups]
     const float2* gstat;
     int32_t ngroups;
     // natural order over stored keys only (else null): the cosine of every
@@ -210,32 +210,46 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Ties the 32 registers of an earlier tcgen05.ld to a point after the wait
+// that covers it, so no use of them is scheduled before the load completes.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t* r) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+        asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]),
+                     "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
-// (bits & ~31) | pos: the column position rides in the five low mantissa
-// bits of the key (pos is a compile-time constant at every use).  It is
-// computed as hi(bits * 2^27) * 32 + pos with the two multipliers taken from
-// the kernel parameters, so that it runs as integer multiply-adds on the FMA
-// pipe and leaves the ALU pipe to the min/max network.
-__device__ __forceinline__ float embed_pos(float v, uint32_t pos, uint32_t m27, uint32_t m5) {
-    return __uint_as_float(__umulhi(__float_as_uint(v), m27) * m5 + pos);
+// (bits & ~15) | pos: a column position in the four low mantissa bits, so
+// that the top-2 network below also yields where the largest value sits; the
+// key is within 15 units in the last place of the value.
+__device__ __forceinline__ float embed_pos(float v, uint32_t pos) {
+    return __uint_as_float((__float_as_uint(v) & ~15u) | pos);
 }
 
-// Top two of 32 keys: min/max of pairs, then a merge tree of (max, second)
+// Largest of 16 values: a tree of three-input maxima (8 instructions).
+__device__ __forceinline__ float max_16(const float* v) {
+    const float a0 = max3f(v[0], v[1], v[2]), a1 = max3f(v[3], v[4], v[5]);
+    const float a2 = max3f(v[6], v[7], v[8]), a3 = max3f(v[9], v[10], v[11]);
+    const float a4 = max3f(v[12], v[13], v[14]);
+    return fmaxf(max3f(a0, a1, a2), max3f(a3, a4, v[15]));
+}
+
+// Top two of 16 keys: min/max of pairs, then a merge tree of (max, second)
 // pairs where each merge is max(h1, h2) and max3(min(h1, h2), l1, l2).
-__device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
-    float hi[16], lo[16];
+__device__ __forceinline__ void top2_16(const float* k, float& t1, float& t2) {
+    float hi[8], lo[8];
 #pragma unroll
-    for (int i = 0; i < 16; i++) {
+    for (int i = 0; i < 8; i++) {
         hi[i] = fmaxf(k[2 * i], k[2 * i + 1]);
         lo[i] = fminf(k[2 * i], k[2 * i + 1]);
     }
 #pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
+    for (int w = 4; w >= 1; w >>= 1) {
 #pragma unroll
         for (int i = 0; i < w; i++) {
             const float h = fmaxf(hi[i], hi[i + w]);
@@ -251,28 +265,28 @@ __device__ __forceinline__ void top2_32(const float* k, float& t1, float& t2) {
 // off from the exact x . chat_j - h_j by at most err_coef (|x| |chat_j| + h_j)
 // (plus the absolute fp16 term), which is bounded group by group with the
 // group maxima of |chat_j| and h_j: s_g = alpha max|chat| + beta max h over
-// 32-centroid group g.  The row carries m1 (its best key, column position in
-// the low bits) from group c1; U, an upper bound of the exact value of every
-// other centroid (the largest t1_g + s_g over the other groups, and t2 + s of
-// c1's own group); the code is certified when m1 - s_c1 still exceeds U, with
-// room for the position bits and the absolute term, else the row joins the
-// exact list.
+// group g of kTcGroup centroids.  The row carries m1, its best value, at
+// centroid code (group code / kTcGroup); U, an upper bound of the exact value of every other
+// centroid (the largest t1_g + s_g over the other groups, and the second value
+// of the code's own group plus its s); the code is certified when m1 - s still
+// exceeds U, with room for the rounding of the comparison and the absolute
+// term, else the row joins the exact list.
 __device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int h,
-                                           float m1, float U, int32_t c1, float xn) {
+                                           float m1, float U, int32_t code, float xn) {
     const int32_t j = p.row_map ? p.row_map[(int64_t)bh * p.seg + ri] : ri;
     const int32_t Lb = seq_len(p.len, bh / p.H, p.out_ncap);
     if (j < 0 || j >= Lb) return;
     const int64_t out = (int64_t)bh * p.out_ncap + j;
     if (p.skip && p.skip[out]) return;
-    const float2 g1 = p.gstat[(int64_t)h * p.ngroups + c1];
+    const float2 g1 = p.gstat[(int64_t)h * p.ngroups + code / kTcGroup];
     const float e1 = p.err_coef * fmaf(xn, g1.x, g1.y);
     const float mag = fmaxf(fabsf(m1), fabsf(U));
-    const float tau = e1 + 2.f * p.head[h * 4 + 3] * xn + 64.f * mag * 1.1920929e-07f;
+    const float tau = e1 + 2.f * p.head[h * 4 + 3] * xn + 4.f * mag * 1.1920929e-07f;
     if (!(m1 - U > tau)) {
         const int32_t slot = atomicAdd(p.exact_count, 1);
         p.exact_list[slot] = out;
     } else {
-        p.codes[out] = c1 * 32 + (31 - (int32_t)(__float_as_uint(m1) & 31u));
+        p.codes[out] = code;
     }
 }
 
@@ -281,10 +295,11 @@ struct TileInfo {
     bool skip;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const Params& p, int t, int tpb) {
+// Tile t of a pass covers rows r0 .. r0 + rows - 1 of (b, h) bh.
+__device__ __forceinline__ TileInfo tile_info(const Params& p, int t, int tpb, int rows) {
     TileInfo ti;
     ti.bh = t / tpb;
-    ti.r0 = (t % tpb) * BM;
+    ti.r0 = (t % tpb) * rows;
     if (p.count) {
         ti.nvalid = min(max(p.count[ti.bh], 0), p.seg);
     } else {
@@ -296,26 +311,40 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int t, int tpb) {
     return ti;
 }
 
-template <int DK, int PA, int AST, int BST>
+// RB row blocks of BM rows share each codebook stage: with RB = 2 a tile is
+// 256 rows, and the accumulators are 128 columns wide (RB x 2 buffers x BN
+// columns fill the 512 TMEM columns).
+template <int RB>
+struct Geo {
+    static constexpr int kBN = RB == 2 ? 128 : 256;  // centroids per accumulator (UMMA N)
+    static constexpr int kParts = 2 / RB;             // column parts of a chunk
+    static constexpr int kSubs = kBN / 32 / kParts;   // 32-column loads per part per chunk
+    static constexpr int kRows = BM * RB;             // rows per tile
+};
+
+template <int DK, int PA, int AST, int BST, int RB>
 struct Smem {
+    using G = Geo<RB>;
     static constexpr int kA = BM * 128;        // one 64-element k-block of one A plane
-    static constexpr int kB = BN * 128;        // one B stage
-    static constexpr int kABytes = AST * PA * DK * kA;
+    static constexpr int kB = G::kBN * 128;    // one B stage
+    static constexpr int kABytes = AST * RB * PA * DK * kA;
     static constexpr int kBBytes = BST * kB;
-    static constexpr int kHOff = kABytes + kBBytes;          // 2 x 256 floats of -h
-    static constexpr int kBarOff = kHOff + 2 * BN * 4;
+    static constexpr int kHOff = kABytes + kBBytes;          // 2 x kBN floats of -h
+    static constexpr int kBarOff = kHOff + 2 * G::kBN * 4;
     static constexpr int kBars = 2 * AST + 2 * BST + 14;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
-    static constexpr int kNrmOff = kMergeOff + (kParts - 1) * 2 * 4 * 32 * 16;
-    static constexpr int kQOff = kNrmOff + 2 * kParts * BM * 8;  // [AST][kMaxD] fp32 queries
+    static constexpr int kNrmOff = kMergeOff + (G::kParts - 1) * 2 * 4 * 32 * 16;
+    static constexpr int kQOff = kNrmOff + 2 * G::kParts * BM * 8;  // [AST][kMaxD] fp32 queries
     static constexpr int kTotal = kQOff + AST * kMaxD * 4 + 1024;  // + alignment slack
 };
 
-template <bool BF16, int DK, int PA, int AST, int BST>
+template <bool BF16, int DK, int PA, int AST, int BST, int RB>
 __global__ void __launch_bounds__(kThreads, 1)
 assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmK, const Params p) {
-    using S = Smem<DK, PA, AST, BST>;
+    using S = Smem<DK, PA, AST, BST, RB>;
+    using G = Geo<RB>;
+    constexpr int BN = G::kBN, kParts = G::kParts, kSubs = G::kSubs, kRows = G::kRows;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -336,15 +365,19 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* nrm_full = acc_full + 10;    // [4] one per TMEM lane quarter: row-norm partials
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
-    // [2][kParts][BM] partial (|x|^2, x . q) of each row
+    // [2][kParts][BM] partial (|x|^2, x . q) of each row (column parts only)
     float2* nrm_part = reinterpret_cast<float2*>(sm + S::kNrmOff);
     float* smQ = reinterpret_cast<float*>(sm + S::kQOff);  // the tile's query, per A stage
+    // k-block kb of plane pa of row block rb in A stage sa
+    auto a_block = [&](int sa, int rb, int pa, int kb) {
+        return smA + (((sa * RB + rb) * PA + pa) * DK + kb) * S::kA;
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiles per (b, h): the host's bound, cut to the longest compact list
     // when its length is on the device (the tiles past it hold no row)
     int tpb = p.tiles_per_bh;
-    if (p.max_rows) tpb = min(tpb, (max(*p.max_rows, 0) + BM - 1) / BM);
+    if (p.max_rows) tpb = min(tpb, (max(*p.max_rows, 0) + kRows - 1) / kRows);
     const int total_tiles = p.num_bh * tpb;
 
     if (threadIdx.x == 0) {
@@ -362,15 +395,15 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(&h_full[i], 1);
             mbar_init(&h_empty[i], kEpiWarps);
         }
-        mbar_init(merge_full, kEpiWarps - 4);  // every warp of parts 1.. hands over
-        mbar_init(merge_empty, 4);             // the part-0 warps take the handoff
+        mbar_init(merge_full, 4);   // the part-1 warps hand over (two column parts)
+        mbar_init(merge_empty, 4);  // the part-0 warps take the handoff
         for (int i = 0; i < 4; i++) mbar_init(&nrm_full[i], kParts);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          su32(tmem_holder)),
-                     "r"(2 * BN)
+                     "r"(2 * RB * BN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -385,19 +418,21 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t a_it = 0, b_it = 0, h_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(p, t, tpb);
+                const TileInfo ti = tile_info(p, t, tpb, kRows);
                 if (ti.skip) continue;
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_empty[sa], ((a_it / AST) & 1) ^ 1, p.status, 1);
                 if (!ok) break;
-                mbar_expect_tx(&a_full[sa], PA * DK * S::kA + (p.sq ? p.d * 4 : 0));
+                mbar_expect_tx(&a_full[sa], RB * PA * DK * S::kA + (p.sq ? p.d * 4 : 0));
                 const int row0 = ti.bh * p.seg + ti.r0;
 #pragma unroll
-                for (int pa = 0; pa < PA; pa++)
+                for (int rb = 0; rb < RB; rb++)
 #pragma unroll
-                    for (int kb = 0; kb < DK; kb++)
-                        tma_2d(smA + ((sa * PA + pa) * DK + kb) * S::kA, &tmA, &a_full[sa], kb * BK,
-                               (int)(pa * p.plane_rows) + row0);
+                    for (int pa = 0; pa < PA; pa++)
+#pragma unroll
+                        for (int kb = 0; kb < DK; kb++)
+                            tma_2d(a_block(sa, rb, pa, kb), &tmA, &a_full[sa], kb * BK,
+                                   (int)(pa * p.plane_rows) + row0 + rb * BM);
                 if (p.sq)
                     asm volatile(
                         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], "
@@ -455,31 +490,38 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t a_it = 0, b_it = 0, acc_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(p, t, tpb);
+                const TileInfo ti = tile_info(p, t, tpb, kRows);
                 if (ti.skip) continue;
                 const int sa = a_it % AST;
                 ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 4);
                 if (!ok) break;
                 tc_fence_after();
-                // a tile of valid rows only is copied out whole by TMA stores
-                // (rows ti.r0 .. + BM of (b, h) ti.bh; the coordinates are
-                // non-negative and x is a multiple of 64 elements)
-                const bool store = p.kcopy_tma && ti.r0 + BM <= ti.nvalid;
-                if (store) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                // each row block of valid rows only is copied out whole by
+                // TMA stores (rows ti.r0 + rb BM .. + BM of (b, h) ti.bh; the
+                // coordinates are non-negative and x is a multiple of 64
+                // elements)
+                bool stored = false;
+                if (p.kcopy_tma) {
 #pragma unroll
-                    for (int kb = 0; kb < DK; kb++)
-                        tma_store_3d(&tmK, smA + (sa * PA * DK + kb) * S::kA, kb * BK, ti.r0,
-                                     ti.bh);
-                    bulk_commit();
+                    for (int rb = 0; rb < RB; rb++) {
+                        if (ti.r0 + (rb + 1) * BM > ti.nvalid) continue;
+                        if (!stored) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        stored = true;
+#pragma unroll
+                        for (int kb = 0; kb < DK; kb++)
+                            tma_store_3d(&tmK, a_block(sa, rb, 0, kb), kb * BK, ti.r0 + rb * BM,
+                                         ti.bh);
+                    }
+                    if (stored) bulk_commit();
                 }
                 for (int c = 0; c < p.nchunks && ok; c++) {
                     const int acc = acc_it & 1;
                     ok = mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, p.status, 5);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-                    uint32_t accumulate = 0;
+                    uint32_t accumulate[RB];
+#pragma unroll
+                    for (int rb = 0; rb < RB; rb++) accumulate[rb] = 0;
                     for (int pl = 0; pl < p.P && ok; pl++)
                         for (int kb = 0; kb < DK; kb++) {
                             const int sb = b_it % BST;
@@ -488,17 +530,21 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                             tc_fence_after();
                             const uint32_t b_base = su32(smB + sb * S::kB);
 #pragma unroll
-                            for (int pa = 0; pa < PA; pa++) {
-                                // products of a higher order are dropped (the
-                                // bound counts them)
-                                if (pa + pl > p.max_order) continue;
-                                const uint32_t a_base =
-                                    su32(smA + ((sa * PA + pa) * DK + kb) * S::kA);
+                            for (int rb = 0; rb < RB; rb++) {
+                                const uint32_t d_tmem = tmem + (uint32_t)((acc * RB + rb) * BN);
 #pragma unroll
-                                for (int ks = 0; ks < BK / 16; ks++) {
-                                    tc_mma(d_tmem, sw128_desc(a_base + ks * 32),
-                                           sw128_desc(b_base + ks * 32), idesc, accumulate);
-                                    accumulate = 1;
+                                for (int pa = 0; pa < PA; pa++) {
+                                    // products of a higher order are dropped (the
+                                    // bound counts them)
+                                    if (pa + pl > p.max_order) continue;
+                                    const uint32_t a_base = su32(a_block(sa, rb, pa, kb));
+#pragma unroll
+                                    for (int ks = 0; ks < BK / 16; ks++) {
+                                        tc_mma(d_tmem, sw128_desc(a_base + ks * 32),
+                                               sw128_desc(b_base + ks * 32), idesc,
+                                               accumulate[rb]);
+                                        accumulate[rb] = 1;
+                                    }
                                 }
                             }
                             tc_commit(&b_empty[sb]);
@@ -508,7 +554,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     acc_it++;
                 }
                 // the stores have read the tile before the stage is released
-                if (store) bulk_wait_read();
+                if (stored) bulk_wait_read();
                 tc_commit(&a_empty[sa]);
                 a_it++;
             }
@@ -516,90 +562,90 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------ epilogue --
+        // warp (quarter q, e): with two row blocks, e is the row block and
+        // the warp takes every column; with one, e is the column part
         const int ew = warp - 2;
         const int q = warp & 3;          // TMEM lane quarter this warp may access
-        const int part = ew >> 2;        // which BN / kParts accumulator columns
-        const int row_in_tile = 32 * q + lane;
+        const int rb = RB == 2 ? (ew >> 2) : 0;
+        const int part = RB == 2 ? 0 : (ew >> 2);
+        const int row_in_tile = rb * BM + 32 * q + lane;
         uint32_t a_it = 0, acc_it = 0, m_it = 0, t_it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = tile_info(p, t, tpb);
+            const TileInfo ti = tile_info(p, t, tpb, kRows);
             if (ti.skip) continue;
             const int h = ti.bh % p.H;
             const int sa = a_it % AST;
             ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 7);
             if (!ok) break;
-            // |x|^2 of this row from the swizzled tile of plane 0: each of the
-            // four parts sums a quarter of the row's 16-byte chunks, the
-            // partials meet in shared memory (an mbarrier per lane quarter)
-            // and every part adds them in the same order.  With scores on,
-            // the same pass takes x . q and copies the row's chunks out.
+            // |x|^2 of this row from the swizzled tile of plane 0: each column
+            // part sums its share of the row's 16-byte chunks, the partials
+            // meet in shared memory (an mbarrier per lane quarter) and every
+            // part adds them in the same order.  With scores on, the same pass
+            // takes x . q and copies the row's chunks out.
             const int32_t ri = ti.r0 + row_in_tile;
             const bool sc = p.scores != nullptr;
             float nrm = 0.f, dot = 0.f;
             {
-                // rows of a tile that the TMA stores do not copy
-                const bool by_tma = p.kcopy_tma && ti.r0 + BM <= ti.nvalid;
+                constexpr int kChunks = 8 * DK / kParts;  // 16-byte chunks per part
+                // rows of a block that the TMA stores do not copy
+                const bool by_tma = p.kcopy_tma && ti.r0 + (rb + 1) * BM <= ti.nvalid;
                 uint8_t* kc = (p.kcopy && !by_tma && ri < ti.nvalid)
                                   ? reinterpret_cast<uint8_t*>(p.kcopy) +
                                         ((int64_t)ti.bh * p.out_ncap + ri) * p.d * 2
                                   : nullptr;
                 const float* qrow = smQ + sa * kMaxD;
-#pragma unroll
-                for (int ci = part * 2 * DK; ci < (part + 1) * 2 * DK; ci++) {
+                const int rr_in_block = 32 * q + lane;
+                float2 nrm2 = make_float2(0.f, 0.f), dot2 = make_float2(0.f, 0.f);
+#pragma unroll 4
+                for (int ci = part * kChunks; ci < (part + 1) * kChunks; ci++) {
                     const int kb = ci >> 3, c = ci & 7;
-                    const uint8_t* rowp = smA + (sa * PA * DK + kb) * S::kA + row_in_tile * 128;
-                    {
-                        const uint4 raw = *reinterpret_cast<const uint4*>(
-                            rowp + 16 * (c ^ (row_in_tile & 7)));
-                        if (kc) __stcs(reinterpret_cast<uint4*>(kc + (kb * 64 + c * 8) * 2), raw);
-                        float qv[8];
-                        if (sc) {
-                            const float4* q4 =
-                                reinterpret_cast<const float4*>(qrow + kb * 64 + c * 8);
-                            const float4 qa = q4[0], qb = q4[1];
-                            qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
-                            qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
-                        }
-                        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    const uint8_t* rowp = a_block(sa, rb, 0, kb) + rr_in_block * 128;
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4*>(rowp + 16 * (c ^ (rr_in_block & 7)));
+                    if (kc) __stcs(reinterpret_cast<uint4*>(kc + (kb * 64 + c * 8) * 2), raw);
+                    float qv[8];
+                    if (sc) {
+                        const float4* q4 = reinterpret_cast<const float4*>(qrow + kb * 64 + c * 8);
+                        const float4 qa = q4[0], qb = q4[1];
+                        qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
+                        qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
+                    }
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            float lo, hi;
-                            if (BF16) {
-                                lo = __uint_as_float(w4[u] << 16);
-                                hi = __uint_as_float(w4[u] & 0xFFFF0000u);
-                            } else {
-                                const __half2 hv = *reinterpret_cast<const __half2*>(&w4[u]);
-                                const float2 f = __half22float2(hv);
-                                lo = f.x;
-                                hi = f.y;
-                            }
-                            nrm = fmaf(lo, lo, nrm);
-                            nrm = fmaf(hi, hi, nrm);
-                            if (sc) {
-                                dot = fmaf(lo, qv[2 * u], dot);
-                                dot = fmaf(hi, qv[2 * u + 1], dot);
-                            }
+                    for (int u = 0; u < 4; u++) {
+                        float2 f;
+                        if (BF16) {
+                            f = make_float2(__uint_as_float(w4[u] << 16),
+                                            __uint_as_float(w4[u] & 0xFFFF0000u));
+                        } else {
+                            f = __half22float2(*reinterpret_cast<const __half2*>(&w4[u]));
                         }
+                        nrm2 = __ffma2_rn(f, f, nrm2);
+                        if (sc) dot2 = __ffma2_rn(f, make_float2(qv[2 * u], qv[2 * u + 1]), dot2);
                     }
                 }
-                float2* np = nrm_part + (t_it & 1) * kParts * BM;
-                np[part * BM + row_in_tile] = make_float2(nrm, dot);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&nrm_full[q]);
-                ok = mbar_wait(&nrm_full[q], t_it & 1, p.status, 13);
-                nrm = 0.f;
-                dot = 0.f;
+                nrm = nrm2.x + nrm2.y;
+                dot = dot2.x + dot2.y;
+                if (kParts > 1) {
+                    float2* np = nrm_part + (t_it & 1) * kParts * BM;
+                    np[part * BM + rr_in_block] = make_float2(nrm, dot);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&nrm_full[q]);
+                    ok = mbar_wait(&nrm_full[q], t_it & 1, p.status, 13);
+                    nrm = 0.f;
+                    dot = 0.f;
 #pragma unroll
-                for (int pp = 0; pp < kParts; pp++) {
-                    const float2 v = np[pp * BM + row_in_tile];
-                    nrm += v.x;
-                    dot += v.y;
+                    for (int pp = 0; pp < kParts; pp++) {
+                        const float2 v = np[pp * BM + rr_in_block];
+                        nrm += v.x;
+                        dot += v.y;
+                    }
+                    t_it++;
                 }
-                t_it++;
             }
             // cosine of the row with its query; 0 when either norm is 0
-            if (ok && sc && part == 1 && ri < ti.nvalid) {
+            if (ok && sc && part == kParts - 1 && ri < ti.nvalid) {
                 const float qn = p.sqn[ti.bh];
                 const float kn = sqrtf(nrm);
                 p.scores[(int64_t)ti.bh * p.out_ncap + ri] =
@@ -610,32 +656,53 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (lane == 0) mbar_arrive(&a_empty[sa]);
             a_it++;
 
-            // m1 / c1: the best key and its group; w2: t2 + s of that group;
-            // ub1 / gb1 / ub2: the two largest t1_g + s_g and the first's group
-            float m1 = -FLT_MAX, w2 = -FLT_MAX, ub1 = -FLT_MAX, ub2 = -FLT_MAX;
+            // Per group g of kTcGroup columns this warp takes only t1_g, the
+            // largest value (a three-input max tree), and b_g = t1_g + s_g.  It
+            // keeps m1 / c1, the best t1 so far and its group, with that
+            // group's values (best), and ub1 / gb1 / ub2, the two largest b_g
+            // and the group of the first.  The position of m1 inside its group
+            // and the group's second value are worked out once, after the sweep.
+            constexpr int kG = kTcGroup;
+            constexpr int kGroupsPerPart = kSubs * 32 / kG;
+            float m1 = -INFINITY, ub1 = -FLT_MAX, ub2 = -FLT_MAX;
             int32_t c1 = 0, gb1 = -1;
+            float best[kG];
             const float xn = sqrtf(nrm) * p.norm_slack;
             const float alpha = p.err_coef * xn, beta = p.err_coef;
             const float2* gst = p.gstat + (int64_t)h * p.ngroups;
             const float inv_scale = p.head[h * 4 + 2];
             const float2 inv2 = make_float2(inv_scale, inv_scale);
-            const uint32_t m27 = p.shr5_mul, m5 = p.shl5_mul;
             for (int c = 0; c < p.nchunks && ok; c++) {
                 const int acc = acc_it & 1;
+                // this part's group bounds s_g for the chunk, loaded ahead
+                const int g0 = (c * BN + part * kSubs * 32) / kG;
+                float sg[kGroupsPerPart];
+#pragma unroll
+                for (int i = 0; i < kGroupsPerPart; i++) {
+                    const float2 gs = __ldg(gst + g0 + i);
+                    sg[i] = fmaf(alpha, gs.x, beta * gs.y);
+                }
                 ok = mbar_wait(&h_full[acc], (acc_it >> 1) & 1, p.status, 12) &&
                      mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
                 const float* hrow = smH + acc * BN;
-                const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+                const uint32_t tbase =
+                    tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((acc * RB + rb) * BN);
+                // the next 32 columns are loaded while the current ones are
+                // reduced (the wait covers the load issued before it)
+                uint32_t rr[2][32];
+                A2ATS_TMEM_LD32(tbase + (uint32_t)(part * kSubs * 32), rr[0]);
+                tmem_wait_ld();
+                tmem_regs_ready(rr[0]);
 #pragma unroll
                 for (int sub = 0; sub < kSubs; sub++) {
                     const int col = (part * kSubs + sub) * 32;
-                    uint32_t r[32];
-                    A2ATS_TMEM_LD32(tbase + (uint32_t)col, r);
-                    tmem_wait_ld();
+                    if (sub + 1 < kSubs)
+                        A2ATS_TMEM_LD32(tbase + (uint32_t)(col + 32), rr[(sub + 1) & 1]);
+                    const uint32_t* r = rr[sub & 1];
                     const float4* h4 = reinterpret_cast<const float4*>(hrow + col);
-                    float key[32];
+                    float v[32];
 #pragma unroll
                     for (int u = 0; u < 8; u++) {
                         const float4 hv = h4[u];
@@ -645,28 +712,39 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         const float2 v23 = __ffma2_rn(
                             make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
                             inv2, make_float2(hv.z, hv.w));
-                        key[4 * u + 0] = embed_pos(v01.x, 31u - 4 * u, m27, m5);
-                        key[4 * u + 1] = embed_pos(v01.y, 30u - 4 * u, m27, m5);
-                        key[4 * u + 2] = embed_pos(v23.x, 29u - 4 * u, m27, m5);
-                        key[4 * u + 3] = embed_pos(v23.y, 28u - 4 * u, m27, m5);
+                        v[4 * u + 0] = v01.x;
+                        v[4 * u + 1] = v01.y;
+                        v[4 * u + 2] = v23.x;
+                        v[4 * u + 3] = v23.y;
                     }
-                    float t1, t2;
-                    top2_32(key, t1, t2);
-                    const int g = (c * BN + col) >> 5;
-                    const float2 gs = __ldg(gst + g);
-                    const float sg = fmaf(alpha, gs.x, beta * gs.y);
-                    const float b1 = t1 + sg;
-                    if (b1 > ub1) {
-                        ub2 = ub1;
-                        ub1 = b1;
-                        gb1 = g;
-                    } else {
-                        ub2 = fmaxf(ub2, b1);
+#pragma unroll
+                    for (int half = 0; half < 32 / kG; half++) {
+                        const float* vg = v + half * kG;
+                        const int gi = sub * (32 / kG) + half;
+                        const float t1 = max_16(vg);
+                        const float b1 = t1 + sg[gi];
+                        if (b1 > ub1) {
+                            ub2 = ub1;
+                            ub1 = b1;
+                            gb1 = g0 + gi;
+                        } else {
+                            ub2 = fmaxf(ub2, b1);
+                        }
+                        // a strictly larger group maximum replaces the kept
+                        // group (equal ones keep the earlier columns);
+                        // branch-free, so the work of consecutive groups
+                        // interleaves
+                        const bool upd = t1 > m1;
+#pragma unroll
+                        for (int i = 0; i < kG; i++) best[i] = upd ? vg[i] : best[i];
+                        if (upd) {
+                            m1 = t1;
+                            c1 = g0 + gi;
+                        }
                     }
-                    if (t1 > m1) {
-                        m1 = t1;
-                        c1 = g;
-                        w2 = t2 + sg;
+                    if (sub + 1 < kSubs) {
+                        tmem_wait_ld();
+                        tmem_regs_ready(rr[(sub + 1) & 1]);
                     }
                 }
                 tc_fence_before();
@@ -678,45 +756,56 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 acc_it++;
             }
             if (!ok) break;
-            // merge the column parts of each row, then decide the row
-            if (part != 0) {
+            // the kept group: the position of m1 (lowest index on equal
+            // values) and w2, a bound of its other values plus s of the group
+            int32_t code;
+            float w2;
+            {
+                float key[kG];
+#pragma unroll
+                for (int i = 0; i < kG; i++) key[i] = embed_pos(best[i], kG - 1 - i);
+                float k1, k2;
+                top2_16(key, k1, k2);
+                code = c1 * kG + (kG - 1 - (int32_t)(__float_as_uint(k1) & (kG - 1)));
+                // the second value is within 15 units in the last place of k2
+                const float2 gs = __ldg(gst + c1);
+                w2 = k2 + 16.f * 1.1920929e-07f * fabsf(k2) + fmaf(alpha, gs.x, beta * gs.y);
+            }
+            if (kParts == 1) {
+                const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn);
+            } else if (part != 0) {
+                // merge the column parts of each row, then decide the row
                 ok = mbar_wait(merge_empty, (m_it & 1) ^ 1, p.status, 9);
                 if (!ok) break;
-                float4* mg = merge + ((part - 1) * 128 + q * 32 + lane) * 2;
-                mg[0] = make_float4(m1, w2, __int_as_float(c1), 0.f);
+                float4* mg = merge + (q * 32 + lane) * 2;
+                mg[0] = make_float4(m1, w2, __int_as_float(code), 0.f);
                 mg[1] = make_float4(ub1, ub2, __int_as_float(gb1), 0.f);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_full);
             } else {
                 ok = mbar_wait(merge_full, m_it & 1, p.status, 10);
                 if (!ok) break;
-                float4 o[kParts - 1][2];
-#pragma unroll
-                for (int pp = 0; pp < kParts - 1; pp++) {
-                    const float4* mg = merge + (pp * 128 + q * 32 + lane) * 2;
-                    o[pp][0] = mg[0];
-                    o[pp][1] = mg[1];
-                }
+                const float4* mg = merge + (q * 32 + lane) * 2;
+                const float4 o0 = mg[0], o1 = mg[1];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_empty);
-                // parts in column order, so equal keys keep the earlier columns
-#pragma unroll
-                for (int pp = 0; pp < kParts - 1; pp++) {
-                    if (o[pp][0].x > m1) {
-                        m1 = o[pp][0].x;
-                        w2 = o[pp][0].y;
-                        c1 = __float_as_int(o[pp][0].z);
-                    }
-                    if (o[pp][1].x > ub1) {
-                        ub2 = fmaxf(ub1, o[pp][1].y);
-                        ub1 = o[pp][1].x;
-                        gb1 = __float_as_int(o[pp][1].z);
-                    } else {
-                        ub2 = fmaxf(ub2, o[pp][1].x);
-                    }
+                // part 1 holds the later columns of each chunk: it takes the
+                // row only with a strictly larger value
+                if (o0.x > m1) {
+                    m1 = o0.x;
+                    w2 = o0.y;
+                    code = __float_as_int(o0.z);
                 }
-                const float U = fmaxf(gb1 == c1 ? ub2 : ub1, w2);
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, c1, xn);
+                if (o1.x > ub1) {
+                    ub2 = fmaxf(ub1, o1.y);
+                    ub1 = o1.x;
+                    gb1 = __float_as_int(o1.z);
+                } else {
+                    ub2 = fmaxf(ub2, o1.x);
+                }
+                const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn);
             }
             m_it++;
         }
@@ -726,7 +815,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(2 * BN)
+                     "r"(2 * RB * BN)
                      : "memory");
     }
 }
@@ -778,9 +867,10 @@ codebook_stats_kernel(const float* __restrict__ chat, int64_t K, int32_t d,
         }
         cm = sqrtf(n.value()) * 1.000001f;
         hm = fmaxf(half_norm[h * K + j], 0.f);
-        // the same maxima per 32-centroid group (bits of non-negative floats)
+        // the same maxima per group of kTcGroup centroids (bits of
+        // non-negative floats)
         if (lane == 0) {
-            uint32_t* gb = group_bits + 2 * (h * ngroups + (j >> 5));
+            uint32_t* gb = group_bits + 2 * (h * ngroups + j / kTcGroup);
             atomicMax(gb, __float_as_uint(cm));
             atomicMax(gb + 1, __float_as_uint(hm));
         }
@@ -1204,12 +1294,12 @@ unsigned blocks_for(int64_t n, int per, unsigned cap) {
     return (unsigned)(b < 1 ? 1 : (b > cap ? cap : b));
 }
 
-template <bool BF16, int DK, int PA, int AST, int BST>
+template <bool BF16, int DK, int PA, int AST, int BST, int RB>
 cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tk,
                           const Params& p, cudaStream_t st) {
-    using S = Smem<DK, PA, AST, BST>;
+    using S = Smem<DK, PA, AST, BST, RB>;
     static_assert(S::kTotal <= 232448, "shared memory budget");
-    auto k = assign_tc_kernel<BF16, DK, PA, AST, BST>;
+    auto k = assign_tc_kernel<BF16, DK, PA, AST, BST, RB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
     if (e != cudaSuccess) return e;
     const int tiles = p.num_bh * p.tiles_per_bh;
@@ -1219,23 +1309,28 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     return cudaGetLastError();
 }
 
+// Row blocks per tile: two (256 rows sharing every codebook stage) for the
+// one-plane pass at d <= 128, where two A stages of both blocks fit in
+// shared memory; one otherwise.
+int row_blocks(int PA, int64_t d) { return PA == 1 && d <= 128 ? 2 : 1; }
+
 template <bool BF16, int PA>
 cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tk,
                             const Params& p, cudaStream_t st) {
     if constexpr (PA == 1) {
         switch (p.d) {
-            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, tk, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 2, 4>(ta, tb, tk, p, st);
-            case 192: return launch_kernel<BF16, 3, PA, 1, 4>(ta, tb, tk, p, st);
-            default: return launch_kernel<BF16, 4, PA, 1, 4>(ta, tb, tk, p, st);
+            case 64: return launch_kernel<BF16, 1, PA, 2, 6, 2>(ta, tb, tk, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 2, 4, 2>(ta, tb, tk, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 4, 1>(ta, tb, tk, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 4, 1>(ta, tb, tk, p, st);
         }
     }
     else {
         switch (p.d) {
-            case 64: return launch_kernel<BF16, 1, PA, 2, 4>(ta, tb, tk, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 1, 4>(ta, tb, tk, p, st);
-            case 192: return launch_kernel<BF16, 3, PA, 1, 3>(ta, tb, tk, p, st);
-            default: return launch_kernel<BF16, 4, PA, 1, 2>(ta, tb, tk, p, st);
+            case 64: return launch_kernel<BF16, 1, PA, 2, 4, 1>(ta, tb, tk, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 1, 4, 1>(ta, tb, tk, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, 3, 1>(ta, tb, tk, p, st);
+            default: return launch_kernel<BF16, 4, PA, 1, 2, 1>(ta, tb, tk, p, st);
         }
     }
 }
@@ -1267,7 +1362,7 @@ cudaError_t prepare_b(const TcCall& c, const float* chat, int v, bool raw, BSide
                       cudaStream_t st, bool launch = true) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d;
-    const int64_t ngroups = (K + BN - 1) / BN * BN / 32;
+    const int64_t ngroups = (K + kPadCols - 1) / kPadCols * kPadCols / kTcGroup;
     out.gstat = c.gstat + v * H * ngroups;
     if (launch) {
         codebook_stats_kernel<<<dim3((unsigned)((K + 7) / 8), (unsigned)H), 256, 0, st>>>(
@@ -1308,6 +1403,8 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
                      bool with_scores = false) {
     const bool bf16 = c.dt == kBF16;
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
+    const int rb = row_blocks(PA, d);
+    const int64_t bn = rb == 2 ? 128 : 256, tile_rows = BM * rb;
     CUtensorMap ta, tb;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)(PA * nbh * ncap)};
@@ -1318,7 +1415,7 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     {
         const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)K, (cuuint64_t)(H * b.P)};
         const cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(K * d * 2)};
-        const cuuint32_t box[3] = {BK, BN, 1};
+        const cuuint32_t box[3] = {BK, (cuuint32_t)bn, 1};
         if (!encode(&tb, bf16, 3, b.src, dims, strides, box)) return cudaErrorInvalidValue;
     }
     Params p;
@@ -1333,9 +1430,9 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.max_order = cut ? 1 : 2;
     p.num_bh = (int32_t)nbh;
     p.seg = (int32_t)ncap;
-    p.tiles_per_bh = (int32_t)(((max_rows < ncap ? max_rows : ncap) + BM - 1) / BM);
-    p.nchunks = (int32_t)((K + BN - 1) / BN);
-    p.kpad = p.nchunks * BN;
+    p.tiles_per_bh = (int32_t)(((max_rows < ncap ? max_rows : ncap) + tile_rows - 1) / tile_rows);
+    p.nchunks = (int32_t)((K + bn - 1) / bn);
+    p.kpad = (int32_t)((K + kPadCols - 1) / kPadCols * kPadCols);  // row stride of hneg
     p.out_ncap = (int32_t)ncap;
     p.plane_rows = plane_rows;
     p.len = c.len;
@@ -1346,7 +1443,7 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.hneg = c.hneg;
     p.head = b.head;
     p.gstat = b.gstat;
-    p.ngroups = p.kpad / 32;
+    p.ngroups = p.kpad / kTcGroup;
     // The products are exact; the tensor core adds (d/16 per operand pair)
     // partial sums into fp32, each addition off by at most 2^-23 of the
     // running magnitude, which |x| max|chat| + max h bounds; plus the rounding
@@ -1370,8 +1467,6 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.exact_list = c.exact_list;
     p.exact_count = c.exact_count;
     p.status = c.exact_count + 1;
-    p.shr5_mul = 1u << 27;
-    p.shl5_mul = 32u;
     p.max_rows = count ? c.exact_count + 2 : nullptr;
     // scores and the row copy: the stored keys in natural order only
     const bool sc = with_scores && PA == 1 && !count && !row_map && c.scores;
@@ -1409,7 +1504,7 @@ bool tc_supported(int dt, int64_t d) {
 cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     using namespace tc;
     const int64_t H = c.s.H, K = c.K, d = c.s.d, nbh = c.s.B * c.s.H, ncap = c.s.Ncap;
-    const int64_t kpad = (K + BN - 1) / BN * BN;
+    const int64_t kpad = (K + kPadCols - 1) / kPadCols * kPadCols;
     const bool rot = c.ra.enabled && c.ra.far_offset != 0;
     const bool natural = c.sel.mode == 0 || c.sel.mode == 2;
     const bool compact = !natural || (c.ra.enabled && c.ra.window > 0);
@@ -1428,7 +1523,7 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     if (build) {
         e = cudaMemsetAsync(c.head_bits, 0, sizeof(uint32_t) * 2 * 4 * H, st);
         if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(c.gstat, 0, sizeof(float2) * 2 * H * (kpad / 32), st);
+        e = cudaMemsetAsync(c.gstat, 0, sizeof(float2) * 2 * H * (kpad / kTcGroup), st);
         if (e != cudaSuccess) return e;
         pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K,
                                                                              kpad, c.hneg);

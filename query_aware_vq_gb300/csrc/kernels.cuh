@@ -117,6 +117,10 @@ cudaError_t launch_assign_blend(const void* x, const void* c, int dt, const Shap
                                 const float* cnorm, int32_t* codes, cudaStream_t st);
 
 // assign_tc.cu ----------------------------------------------------------
+// Centroids per group of the tensor-core pass's certification bound (the
+// per-group maxima of |chat_j| and h_j, TcCall::gstat).
+constexpr int kTcGroup = 16;
+
 // Tensor-core assignment (argmin_j |x~ L - c_j L|^2, L null = identity) for
 // bf16 / fp16 keys with d a multiple of 64.  cp / half_norm must already hold
 // c L and |c L|^2 / 2, and with L given chat must hold c L L^T

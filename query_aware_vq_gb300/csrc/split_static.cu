@@ -9,12 +9,13 @@
 // scratch in one fixed array that lives in the library's device image: every
 // GPU that loads the library holds it (a few MB) until the process exits.
 // Shapes beyond the array are refused; nothing is ever allocated.
-#include <math.h>
+#include <cuda.h>
 #include <string.h>
 
 #include <mutex>
 
 #include "../../include/a2ats.h"
+#include "entry.cuh"
 #include "kernels.cuh"
 
 namespace a2ats {
@@ -26,13 +27,50 @@ constexpr int64_t kQOff = 0;
 constexpr int64_t kQNormOff = kStaticHeads * kMaxD;
 constexpr int64_t kScoreOff = kQNormOff + kStaticHeads + 64;  // 256-byte aligned start
 constexpr int64_t kStaticFloats = kScoreOff + kStaticKeys;
+static_assert(kQNormOff >= kQOff + kStaticHeads * kMaxD, "queries overlap their norms");
+static_assert(kScoreOff >= kQNormOff + kStaticHeads, "norms overlap the scores");
+static_assert((kQNormOff * sizeof(float)) % 256 == 0, "norms start 256-byte aligned");
+static_assert((kScoreOff * sizeof(float)) % 256 == 0, "scores start 256-byte aligned");
 
 static __device__ __align__(256) float g_split_scratch[kStaticFloats];
 
-// Device address of g_split_scratch on each device, looked up once per device
-// with that device current (the host-side symbol is not a device address).
+// Device address of g_split_scratch on each device, looked up with that
+// device current (the host-side symbol is not a device address).  It is
+// cached with the id of the context it was taken in and looked up again
+// when the device's current context differs (after cudaDeviceReset the
+// module is loaded anew, possibly at another address).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 std::mutex g_mu;
 float* g_addr[256] = {nullptr};
+unsigned long long g_ctx[256] = {0};
+
+// The current context's unique id, or 0 when it cannot be read.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        looked = true;
+        cudaDriverEntryPointQueryResult qr;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 cudaError_t static_scratch(float** out) {
     int dev = 0;
@@ -40,11 +78,14 @@ cudaError_t static_scratch(float** out) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    unsigned long long id = current_context_id();
+    if (!g_addr[dev] || id == 0 || id != g_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_split_scratch);
         if (e != cudaSuccess) return e;
         g_addr[dev] = static_cast<float*>(p);
+        // the lookup made the device's primary context current if it was not
+        g_ctx[dev] = id ? id : current_context_id();
     }
     *out = g_addr[dev];
     return cudaSuccess;
@@ -61,52 +102,32 @@ extern "C" int a2ats_select_retrieval_set_static(const void* keys, int32_t dtype
                                                  double fraction,
                                                  const a2ats_rope_params* fused_rope,
                                                  int32_t* perm, int32_t* count, void* stream) {
-    if (dtype != A2ATS_F32 && dtype != A2ATS_BF16 && dtype != A2ATS_F16) return A2ATS_ERR_DTYPE;
-    if (B < 0 || H < 0 || Ncap < 0 || d < 8 || d > kMaxD || d % 8 != 0 ||
-        Ncap >= (int64_t(1) << 24) || B * H > 65535)
-        return A2ATS_ERR_SHAPE;
-    if (!(fraction >= 0.0 && fraction <= 1.0)) return A2ATS_ERR_INVALID_ARG;
-    if (B * H > kStaticHeads || B * H * Ncap > kStaticKeys) return A2ATS_ERR_CAPACITY;
+    // the checks of a2ats_select_retrieval_set, then the array's limits
+    if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
+    int st = check_shape(B, H, Ncap, d);
+    if (st) return st;
+    if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
     RopeArgs ra;
-    memset(&ra, 0, sizeof(ra));
-    if (fused_rope) {
-        if (!(fused_rope->rope_base > 0.0) || !isfinite(fused_rope->rope_base))
-            return A2ATS_ERR_INVALID_ARG;
-        if (fused_rope->far_offset <= -(1 << 24) || fused_rope->far_offset >= (1 << 24))
-            return A2ATS_ERR_INVALID_ARG;
-        ra.enabled = 1;
-        ra.window = fused_rope->window;
-        ra.far_offset = fused_rope->far_offset;
-        ra.interleaved = fused_rope->interleaved ? 1 : 0;
-        const double two_pi = 6.283185307179586476925286766559;
-        ra.two_pi_a = (float)two_pi;
-        ra.two_pi_b = (float)(two_pi - (double)ra.two_pi_a);
-        ra.two_pi_c = (float)(two_pi - (double)ra.two_pi_a - (double)ra.two_pi_b);
-        ra.inv_2pi = (float)(1.0 / two_pi);
-        for (int64_t i = 0; i < d / 2; i++) {
-            const double om = pow(fused_rope->rope_base, -2.0 * (double)i / (double)d);
-            ra.omega_hi[i] = (float)om;
-            ra.omega_lo[i] = (float)(om - (double)ra.omega_hi[i]);
-        }
-    }
+    if ((st = make_rope(fused_rope, d, ra))) return st;
+    if (B * H > kStaticHeads || B * H * Ncap > kStaticKeys) return A2ATS_ERR_CAPACITY;
     if (B * H == 0) return A2ATS_OK;
     if (!count || (Ncap > 0 && (!keys || !perm))) return A2ATS_ERR_INVALID_ARG;
     if (((uintptr_t)keys & 15u) || ((uintptr_t)query & 15u) || ((uintptr_t)perm & 15u))
         return A2ATS_ERR_ALIGN;
     float* base = nullptr;
     cudaError_t e = static_scratch(&base);
-    if (e != cudaSuccess) return A2ATS_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail(e);
     cudaStream_t s = (cudaStream_t)stream;
     const Shape sh{B, H, Ncap, d};
     // every scratch word the kernels read is written first in the same call,
     // so nothing has to be cleared between calls
     if (Ncap > 0) {
         e = launch_prepare_query(keys, query, dtype, sh, len, ra, base + kQOff, base + kQNormOff, s);
-        if (e != cudaSuccess) return A2ATS_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_fail(e);
         e = launch_cosine_scores(keys, dtype, sh, len, ra, base + kQOff, base + kQNormOff,
                                  base + kScoreOff, s);
-        if (e != cudaSuccess) return A2ATS_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     e = launch_select(base + kScoreOff, sh, len, fraction, perm, count, s);
-    return e == cudaSuccess ? A2ATS_OK : A2ATS_ERR_CUDA;
+    return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }

@@ -149,6 +149,13 @@ def keys(w: Workload, rows: int | None = None, threads: int = 8,
     return out
 
 
+def head_keys(w: Workload, b: int, h: int, rows: int | None = None) -> torch.Tensor:
+    """Keys [1, 1, rows, d] of sequence b and head h alone, the same values
+    keys(w)[b, h] holds."""
+    n = w.N if rows is None else rows
+    return _to_storage(_keys_for(w, b, h, n), w.dtype).view(1, 1, n, w.d)
+
+
 def queries(w: Workload, M: int | None = None) -> torch.Tensor:
     """Calibration queries [H, M, d] in the storage dtype."""
     M = w.M if M is None else M

@@ -76,6 +76,21 @@ def test_h_weighted_matches_oracle(case):
         check_codes(got[b, h, :len(v)], code, (d2 - d1) / np.maximum(d2, 1e-300))
 
 
+@pytest.mark.parametrize("dt,withL", [("bf16", False), ("bf16", True), ("f16", True),
+                                      ("f32", False)])
+def test_single_centroid_gives_code_zero(dt, withL):
+    """K = 1: the one centroid is every row's nearest (its second distance
+    is infinite, so no row is a near tie)."""
+    B, H, N, d = 2, 2, 333, 128
+    x = synth.gaussian((B, H, N, d), seed=5, dtype=dt, scale=2.0)
+    c = synth.gaussian((H, 1, d), seed=6, dtype=dt, scale=2.0)
+    L = _L(H, d, 30.0, seed=1) if withL else None
+    codes = torch.full((B, H, N), -3, dtype=torch.int32, device="cuda")
+    q.a2ats_h_weighted_assign(dev(x), dev(c), dev(L) if withL else None, codes=codes,
+                              rope=dict(window=40, far_offset=0, rope_base=10000.0))
+    assert (codes.cpu() == 0).all()
+
+
 @pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 48)])
 def test_entries_above_the_diagonal_are_ignored(dt, d):
     """Only the lower triangle of L is read: filling the rest with noise

@@ -10,7 +10,7 @@ import torch
 import oracle
 import query_aware_vq_gb300 as q
 import synth
-from _parity import check_codes, check_split, dev, f64
+from _parity import assert_storage_close, check_codes, check_split, dev, f64
 from query_aware_vq_gb300.pipeline import A2ATSDecodeStep
 
 pytestmark = pytest.mark.gpu
@@ -29,8 +29,7 @@ def _check_step(step, cache, lengths, codebook, W, base, f, beta, pairs, L=None)
         check_split(perm[b, h], int(count[b, h]), n, cnt, scores, kth)
         # the rotated cache at the new position (storage dtype)
         rs = np.arange(max(0, n - W - 2), n)
-        got = f64(kt[b, h, rs])
-        assert np.abs(got - v[rs]).max() <= 1e-2 * np.abs(v[rs]).max()
+        assert_storage_close(f64(kt[b, h, rs]), v[rs], kt.dtype)
         # the new key's code
         if L is None:
             code, s1, s2 = oracle.assign_blend(v[-1:], codebook[h], v[-1], beta)

@@ -12,7 +12,7 @@ import torch
 import oracle
 import query_aware_vq_gb300 as q
 import synth
-from _parity import check_split, dev, f64
+from _parity import assert_storage_close, check_split, dev, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -118,8 +118,11 @@ def test_fused_full_size_sampled():
             check_split(perm[b, h], int(count[b, h]), w.N, cnt, scores, kth)
             rows = np.unique(np.concatenate([rng.choice(w.N, 512, replace=False),
                                              np.arange(w.N - w.W - 2, w.N)]))
-            # far rows are the stored keys themselves
+            # far rows are the stored keys themselves; window rows within one
+            # unit in the last place of the oracle's rotation
             far = rows[rows < w.N - w.W]
             assert torch.equal(kt[b, h, far], k[b, h, far])
+            win = rows[rows >= w.N - w.W]
+            assert_storage_close(f64(kt[b, h, win]), v[win], kt.dtype)
             code, d1, d2 = oracle.assign_cholesky(v[rows], c[h], None)
             check_codes(codes[b, h, rows], code, (d2 - d1) / d2, "codes")

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from _parity import check_codes, check_split, dev, f64, assert_rows_close
+from _parity import assert_storage_close, check_codes, check_split, dev, f64
 from query_aware_vq_gb300.pipeline import A2ATSStep
 
 pytestmark = pytest.mark.gpu
@@ -44,7 +44,7 @@ def _run(w, rows_sample=None, beta_path=False, seed=0, fused=True):
             # the written k~ (storage dtype) against the oracle, sampled rows
             rs = np.unique(np.concatenate([rng.choice(n, min(n, 256), replace=False),
                                            np.arange(max(0, n - w.W - 1), n)]))
-            assert_rows_close(kt[b, h, rs], v[rs], rel=1e-2 if w.dtype != "f32" else 1e-5)
+            assert_storage_close(kt[b, h, rs], v[rs], synth.DTYPES[w.dtype])
             ret = perm[b, h, :cnt]
             bulk = perm[b, h, cnt:]
             if rows_sample is not None and len(bulk) > rows_sample:

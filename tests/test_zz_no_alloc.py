@@ -31,13 +31,17 @@ def _static_fn():
     return fn
 
 
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+
 def _call_static(keys, lengths, fraction, rope):
     B, H, N, d = keys.shape
     perm = torch.full((B, H, N), -1, dtype=torch.int32, device="cuda")
     count = torch.full((B, H), -1, dtype=torch.int32, device="cuda")
-    status = _static_fn()(keys.data_ptr(), 1, B, H, N, d, lengths.data_ptr(), None, fraction,
-                          ctypes.byref(rope), perm.data_ptr(), count.data_ptr(),
-                          torch.cuda.current_stream().cuda_stream)
+    status = _static_fn()(keys.data_ptr(), _DT[keys.dtype], B, H, N, d,
+                          lengths.data_ptr() if lengths is not None else None, None, fraction,
+                          ctypes.byref(rope) if rope is not None else None, perm.data_ptr(),
+                          count.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert status == 0, q.library().a2ats_status_string(status)
     return perm, count
 
@@ -56,6 +60,37 @@ def test_static_split_matches_workspace_split_twice():
         for b in range(w.B):
             n = int(lengths[b])
             assert torch.equal(perm[b, :, :n], want_perm[b, :, :n])
+
+
+@pytest.mark.parametrize("B,H,N,d,dt,with_rope", [
+    # exactly at the key limit (the last slot of the score region), widest rows
+    (1, 8, 131072, 256, "f16", True),
+    # no fused rotation, fp32 keys, ragged lengths
+    (3, 5, 5000, 64, "f32", False),
+])
+def test_static_split_at_the_limits_matches_workspace_split(B, H, N, d, dt, with_rope):
+    keys = synth.gaussian((B, H, N, d), seed=N + d, dtype=dt).cuda()
+    lengths = torch.tensor([N - 999 * b for b in range(B)], dtype=torch.int32, device="cuda")
+    rope = q.RopeParams(300, 0, 10000.0, 0) if with_rope else None
+    want_perm, want_count = q.a2ats_select_retrieval_set(keys, None, 0.1, lengths=lengths,
+                                                         rope=rope)
+    for _ in range(2):
+        perm, count = _call_static(keys, lengths, 0.1, rope)
+        torch.cuda.synchronize()
+        assert torch.equal(count, want_count)
+        for b in range(B):
+            n = int(lengths[b])
+            assert torch.equal(perm[b, :, :n], want_perm[b, :, :n])
+
+
+def test_static_split_refuses_too_many_heads():
+    B, H, N, d = 1, 1025, 4, 64
+    keys = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    perm = torch.empty((B, H, N), dtype=torch.int32, device="cuda")
+    count = torch.empty((B, H), dtype=torch.int32, device="cuda")
+    status = _static_fn()(keys.data_ptr(), 1, B, H, N, d, None, None, 0.1, None,
+                          perm.data_ptr(), count.data_ptr(), None)
+    assert status == -7
 
 
 def test_static_split_refuses_shapes_beyond_its_array():
