@@ -14,23 +14,27 @@
 // codebook needs one plane.  Each plane is one more pass of tcgen05.mma into
 // the same TMEM accumulator.
 //
-// Kernel layout (one persistent CTA per SM, 10 warps):
-//   warp 0     TMA producer: the 128-row key tile once per tile (kept for all
-//              centroids), then the codebook in 256 x 64-element stages;
-//   warp 1     TMEM allocation and tcgen05.mma issue (128 x 256 x 16,
-//              bf16/fp16 -> fp32), two accumulators of 256 columns so the
-//              epilogue of one centroid chunk overlaps the MMAs of the next;
-//   warps 2-9  epilogue, one per (TMEM lane quarter, 128-column part):
-//              tcgen05.ld of the accumulator, v = acc - |c'|^2/2, and per
-//              32-column group only its largest value (a three-input max
+// Kernel layout (one persistent CTA per SM, 11 warps):
+//   warp 10    TMA producer of the key tiles (kept for all centroids), a tile
+//              ahead: 256 rows as two 128-row blocks at d <= 128 with one
+//              operand plane, else 128 rows;
+//   warp 0     TMA producer of the codebook, in stages of 64 elements by the
+//              accumulator width (128 centroids with two row blocks, else
+//              256), and of -|c'|^2/2 per chunk into a ring of kHSlots;
+//   warp 1     TMEM allocation and tcgen05.mma issue (M = 128 per row
+//              block, bf16/fp16 -> fp32) into two accumulators per row block
+//              (the 512 TMEM columns), so the epilogue of one centroid chunk
+//              overlaps the MMAs of the next;
+//   warps 2-9  epilogue, one per (TMEM lane quarter, row block or 128-column
+//              part): tcgen05.ld of the accumulator, v = acc - |c'|^2/2, and
+//              per 16-column group only its largest value (a three-input max
 //              tree); the values of the best group so far are kept in
 //              registers, and the position and second value inside it are
-//              found once per row after the sweep.  The parts of a row meet
-//              in shared memory, and a rigorous error bound sends rows whose
-//              top two are closer than the bound to the exact SIMT kernels
-//              through a list.  Each warp loads the next 32 columns from
-//              TMEM while it reduces the current ones, so two epilogue warps
-//              per scheduler keep it issuing.
+//              found once per row after the sweep.  Column parts of a row
+//              meet in shared memory, and a rigorous error bound sends rows
+//              whose top two are closer than the bound to the exact SIMT
+//              kernels through a list.  Each warp loads the next 32 columns
+//              from TMEM while it reduces the current ones.
 // Every mbarrier wait is bounded; on time-out the kernel records an error
 // code and leaves.
 #include <cuda.h>
@@ -46,7 +50,11 @@ constexpr int BM = 128;   // rows per row block (UMMA M)
 constexpr int BK = 64;    // 16-bit elements per 128-byte swizzle atom
 constexpr int kPadCols = 256;  // -|c L|^2 / 2 rows are padded to a multiple of this
 constexpr int kEpiWarps = 8;   // 4 TMEM lane quarters x 2 (row blocks or column parts)
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// slots of the -|c'|^2/2 ring: its producer is the codebook producer, so the
+// ring lets the codebook stream run this many chunks ahead of the epilogue
+constexpr int kHSlots = 8;
+constexpr int kAWarp = 2 + kEpiWarps;          // the key-tile producer
+constexpr int kThreads = 32 * (kAWarp + 1);
 constexpr uint64_t kWaitNs = 2000000000ull;  // every mbarrier wait gives up after 2 s
 
 struct Params {
@@ -329,9 +337,9 @@ struct Smem {
     static constexpr int kB = G::kBN * 128;    // one B stage
     static constexpr int kABytes = AST * RB * PA * DK * kA;
     static constexpr int kBBytes = BST * kB;
-    static constexpr int kHOff = kABytes + kBBytes;          // 2 x kBN floats of -h
-    static constexpr int kBarOff = kHOff + 2 * G::kBN * 4;
-    static constexpr int kBars = 2 * AST + 2 * BST + 14;
+    static constexpr int kHOff = kABytes + kBBytes;          // kHSlots x kBN floats of -h
+    static constexpr int kBarOff = kHOff + kHSlots * G::kBN * 4;
+    static constexpr int kBars = 2 * AST + 2 * BST + 10 + 2 * kHSlots;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
     static constexpr int kNrmOff = kMergeOff + (G::kParts - 1) * 2 * 4 * 32 * 16;
     static constexpr int kQOff = kNrmOff + 2 * G::kParts * BM * 8;  // [AST][kMaxD] fp32 queries
@@ -359,10 +367,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* acc_full = bars + 2 * AST + 2 * BST;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* h_full = acc_full + 4;
-    uint64_t* h_empty = acc_full + 6;
-    uint64_t* merge_full = acc_full + 8;   // column-part handoff, after the h ring
-    uint64_t* merge_empty = acc_full + 9;
-    uint64_t* nrm_full = acc_full + 10;    // [4] one per TMEM lane quarter: row-norm partials
+    uint64_t* h_empty = h_full + kHSlots;
+    uint64_t* merge_full = h_empty + kHSlots;  // column-part handoff, after the h ring
+    uint64_t* merge_empty = merge_full + 1;
+    uint64_t* nrm_full = merge_full + 2;       // [4] one per TMEM lane quarter: row-norm partials
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
     float4* merge = reinterpret_cast<float4*>(sm + S::kMergeOff);
     // [2][kParts][BM] partial (|x|^2, x . q) of each row (column parts only)
@@ -392,6 +400,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int i = 0; i < 2; i++) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kHSlots; i++) {
             mbar_init(&h_full[i], 1);
             mbar_init(&h_empty[i], kEpiWarps);
         }
@@ -412,10 +422,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ producer --
+    if (warp == kAWarp) {
+        // ---------------------------------------------- key-tile producer --
+        // the rows of each tile (and its query), issued as soon as a stage
+        // is free, a whole tile ahead of the MMAs that read them
         if (lane == 0) {
-            uint32_t a_it = 0, b_it = 0, h_it = 0;
+            uint32_t a_it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info(p, t, tpb, kRows);
@@ -440,10 +452,26 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         "l"(p.sq + (int64_t)ti.bh * p.d), "r"(p.d * 4), "r"(su32(&a_full[sa]))
                         : "memory");
                 a_it++;
+            }
+            // every issued copy has landed before the CTA may leave
+            for (int s = 0; s < AST; s++)
+                if (a_it > (uint32_t)s) {
+                    const uint32_t last = a_it - 1 - ((a_it - 1 - s) % AST);
+                    mbar_wait(&a_full[last % AST], (last / AST) & 1, p.status, 3);
+                }
+        }
+    } else if (warp == 0) {
+        // ---------------------------------------------- codebook producer --
+        if (lane == 0) {
+            uint32_t b_it = 0, h_it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info(p, t, tpb, kRows);
+                if (ti.skip) continue;
                 const int h = ti.bh % p.H;
                 for (int c = 0; c < p.nchunks && ok; c++) {
-                    const int hs = h_it & 1;
-                    ok = mbar_wait(&h_empty[hs], ((h_it >> 1) & 1) ^ 1, p.status, 11);
+                    const int hs = h_it % kHSlots;
+                    ok = mbar_wait(&h_empty[hs], ((h_it / kHSlots) & 1) ^ 1, p.status, 11);
                     if (!ok) break;
                     mbar_expect_tx(&h_full[hs], BN * 4);
                     asm volatile(
@@ -471,15 +499,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t last = b_it - 1 - ((b_it - 1 - s) % BST);
                     mbar_wait(&b_full[last % BST], (last / BST) & 1, p.status, 3);
                 }
-            for (int s = 0; s < AST; s++)
-                if (a_it > (uint32_t)s) {
-                    const uint32_t last = a_it - 1 - ((a_it - 1 - s) % AST);
-                    mbar_wait(&a_full[last % AST], (last / AST) & 1, p.status, 3);
-                }
-            for (int s = 0; s < 2; s++)
+            for (int s = 0; s < kHSlots; s++)
                 if (h_it > (uint32_t)s) {
-                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % 2);
-                    mbar_wait(&h_full[last % 2], (last / 2) & 1, p.status, 3);
+                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % kHSlots);
+                    mbar_wait(&h_full[last % kHSlots], (last / kHSlots) & 1, p.status, 3);
                 }
         }
     } else if (warp == 1) {
@@ -496,6 +519,14 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 ok = mbar_wait(&a_full[sa], (a_it / AST) & 1, p.status, 4);
                 if (!ok) break;
                 tc_fence_after();
+                uint64_t a_desc[RB][PA][DK];
+#pragma unroll
+                for (int rb = 0; rb < RB; rb++)
+#pragma unroll
+                    for (int pa = 0; pa < PA; pa++)
+#pragma unroll
+                        for (int kb = 0; kb < DK; kb++)
+                            a_desc[rb][pa][kb] = sw128_desc(su32(a_block(sa, rb, pa, kb)));
                 // each row block of valid rows only is copied out whole by
                 // TMA stores (rows ti.r0 + rb BM .. + BM of (b, h) ti.bh; the
                 // coordinates are non-negative and x is a multiple of 64
@@ -523,12 +554,16 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                     for (int rb = 0; rb < RB; rb++) accumulate[rb] = 0;
                     for (int pl = 0; pl < p.P && ok; pl++)
+#pragma unroll
                         for (int kb = 0; kb < DK; kb++) {
                             const int sb = b_it % BST;
                             ok = mbar_wait(&b_full[sb], (b_it / BST) & 1, p.status, 6);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t b_base = su32(smB + sb * S::kB);
+                            // descriptors of the stage's start; the k-steps of 16
+                            // elements are 32 bytes apart, i.e. +2 in the address
+                            // field (no carry: shared addresses are below 2^18)
+                            const uint64_t bd = sw128_desc(su32(smB + sb * S::kB));
 #pragma unroll
                             for (int rb = 0; rb < RB; rb++) {
                                 const uint32_t d_tmem = tmem + (uint32_t)((acc * RB + rb) * BN);
@@ -537,11 +572,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                     // products of a higher order are dropped (the
                                     // bound counts them)
                                     if (pa + pl > p.max_order) continue;
-                                    const uint32_t a_base = su32(a_block(sa, rb, pa, kb));
+                                    const uint64_t ad = a_desc[rb][pa][kb];
 #pragma unroll
                                     for (int ks = 0; ks < BK / 16; ks++) {
-                                        tc_mma(d_tmem, sw128_desc(a_base + ks * 32),
-                                               sw128_desc(b_base + ks * 32), idesc,
+                                        tc_mma(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
                                                accumulate[rb]);
                                         accumulate[rb] = 1;
                                     }
@@ -560,7 +594,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             bulk_wait_all();
         }
-    } else {
+    } else if (warp < kAWarp) {
         // ------------------------------------------------------ epilogue --
         // warp (quarter q, e): with two row blocks, e is the row block and
         // the warp takes every column; with one, e is the column part
@@ -682,11 +716,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const float2 gs = __ldg(gst + g0 + i);
                     sg[i] = fmaf(alpha, gs.x, beta * gs.y);
                 }
-                ok = mbar_wait(&h_full[acc], (acc_it >> 1) & 1, p.status, 12) &&
+                const int hs = acc_it % kHSlots;
+                ok = mbar_wait(&h_full[hs], (acc_it / kHSlots) & 1, p.status, 12) &&
                      mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
-                const float* hrow = smH + acc * BN;
+                const float* hrow = smH + hs * BN;
                 const uint32_t tbase =
                     tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((acc * RB + rb) * BN);
                 // the next 32 columns are loaded while the current ones are
@@ -751,7 +786,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&acc_empty[acc]);
-                    mbar_arrive(&h_empty[acc]);
+                    mbar_arrive(&h_empty[hs]);
                 }
                 acc_it++;
             }
