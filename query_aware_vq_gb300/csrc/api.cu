@@ -311,6 +311,7 @@ size_t a2ats_query_second_moment_workspace_size(int64_t H, int64_t M, int64_t d)
     if (H < 0 || M < 1 || d < 1) return 0;
     Carve c(nullptr);
     c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
+    c.take<int32_t>(4);
     return c.used + 256;
 }
 
@@ -328,7 +329,8 @@ int a2ats_query_second_moment(const void* queries, int32_t dtype, int64_t H, int
         return A2ATS_ERR_WORKSPACE;
     Carve c(workspace);
     float* partial = c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
-    cudaError_t e = launch_second_moment(queries, dtype, H, M, d, ridge, partial, h_out,
+    int32_t* status = c.take<int32_t>(4);
+    cudaError_t e = launch_second_moment(queries, dtype, H, M, d, ridge, partial, status, h_out,
                                          (cudaStream_t)stream);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }

@@ -426,34 +426,40 @@ int64_t second_moment_splits(int64_t M) {
 }
 
 cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, int64_t d,
-                                 double ridge, float* partial, float* h_out, cudaStream_t st) {
+                                 double ridge, float* partial, int32_t* status, float* h_out,
+                                 cudaStream_t st) {
     const int64_t splits = second_moment_splits(M);
-    // tiles past the edge of H (d not a multiple of 32) read zeros and write nothing
-    const int Tt = (int)((d + kSmTile - 1) / kSmTile);
-    dim3 grid(Tt * (Tt + 1) / 2, (unsigned)splits, (unsigned)H);
-    switch (dt) {
-        case kF32:
-            second_moment_partial_kernel<kF32><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
-                                                                            splits, partial);
-                                                                            note_launches(1);
-            break;
-        case kBF16:
-            second_moment_partial_kernel<kBF16><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
-                                                                             splits, partial);
-                                                                             note_launches(1);
-            break;
-        default:
-            second_moment_partial_kernel<kF16><<<grid, kSmThreads, 0, st>>>(q, M, (int32_t)d,
-                                                                            splits, partial);
-                                                                            note_launches(1);
+    cudaError_t e = cudaSuccess;
+    if (second_moment_tc_supported(dt, M, d)) {
+        e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        if (e != cudaSuccess) return e;
+        e = launch_second_moment_tc(q, dt, H, M, partial, status, st);
+    } else {
+        // tiles past the edge of H (d not a multiple of 32) read zeros and write nothing
+        const int Tt = (int)((d + kSmTile - 1) / kSmTile);
+        dim3 grid(Tt * (Tt + 1) / 2, (unsigned)splits, (unsigned)H);
+        switch (dt) {
+            case kF32:
+                second_moment_partial_kernel<kF32><<<grid, kSmThreads, 0, st>>>(
+                    q, M, (int32_t)d, splits, partial);
+                break;
+            case kBF16:
+                second_moment_partial_kernel<kBF16><<<grid, kSmThreads, 0, st>>>(
+                    q, M, (int32_t)d, splits, partial);
+                break;
+            default:
+                second_moment_partial_kernel<kF16><<<grid, kSmThreads, 0, st>>>(
+                    q, M, (int32_t)d, splits, partial);
+        }
+        note_launches(1);
+        e = cudaGetLastError();
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t n = H * d * d;
     second_moment_reduce_kernel<<<(unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096),
                                   256, 0, st>>>(partial, H, M, (int32_t)d, splits, (float)ridge,
                                                 h_out);
-                                                note_launches(1);
+    note_launches(1);
     return cudaGetLastError();
 }
 

@@ -17,7 +17,11 @@ def _rel(a, b):
 
 
 @pytest.mark.parametrize("H,M,d,dt", [(2, 1000, 128, "bf16"), (1, 33, 8, "f32"), (3, 517, 24, "f16"),
-                                      (1, 4096, 256, "bf16"), (2, 1, 64, "f32")])
+                                      (1, 4096, 256, "bf16"), (2, 1, 64, "f32"),
+                                      # the tensor-core path: fp16, ragged slices; and the longest
+                                      # slices it takes (512 rows per accumulator)
+                                      (2, 3000, 128, "f16"), (1, 131072, 128, "bf16"),
+                                      (1, 100, 128, "bf16")])
 def test_second_moment_matches_oracle(H, M, d, dt):
     Q = synth.gaussian((H, M, d), seed=M + d, dtype=dt, scale=2.0)
     got = q.a2ats_query_second_moment(dev(Q), 1e-4)
