@@ -96,6 +96,9 @@ def _args():
                    help="calibration keys per head for --path calibrate")
     p.add_argument("--lloyd", type=int, default=10,
                    help="Lloyd rounds after the k-means++ seeding for --path calibrate")
+    p.add_argument("--batch", type=int, default=0,
+                   help="sequences of the decode workload's batch (0: the workload's own); "
+                        "a smaller batch is for profiler captures")
     p.add_argument("--separate-split", action="store_true",
                    help="run RoPE and the split on the second stream beside a separate "
                         "plain-VQ call, instead of the fused call (same outputs)")
@@ -562,6 +565,8 @@ def run_decode(a):
     rank, local, world = _dist()
     torch.cuda.set_device(local)
     w = synth.WORKLOADS[a.workload]
+    if a.batch > 0:
+        w = synth.scaled(w, B=a.batch)
     total = min(a.warmup + a.steps, w.decode_steps)
     warm = min(a.warmup, max(total - 1, 0))
     steps = total - warm

@@ -162,6 +162,99 @@ windowed_rope_scalar_kernel(const void* __restrict__ kin, void* __restrict__ kou
     }
 }
 
+// The same scores (and stored rows) as cosine_score_kernel for the
+// half-split pairing with d % 16 == 0, launched over (chunk of kBhRows rows,
+// (b, h)) so that no thread walks the rows past a sequence's length; the
+// (b, h) query is held in registers, and each lane group takes two rows at
+// a time (four 16-byte loads in flight per lane).  The arithmetic of a row
+// is that of cosine_score_kernel, so both give the same bits.
+constexpr int kBhRows = 1024;
+
+template <int DT, int OUT>
+__global__ void __launch_bounds__(kRopeThreads, 3)
+cosine_score_bh_kernel(const void* __restrict__ keys, int32_t H, int32_t ncap, int32_t d,
+                       const int32_t* __restrict__ len, const RopeArgs ra,
+                       const float* __restrict__ q, const float* __restrict__ qnorm,
+                       float* __restrict__ scores, void* __restrict__ kout) {
+    const int lpr = d / 16;
+    const int rpb = kRopeThreads / lpr;
+    const int lane = threadIdx.x & (lpr - 1);
+    const int rl = threadIdx.x / lpr;
+    const int e0 = lane * 8;
+    const int e1 = e0 + d / 2;
+    const int64_t bh = blockIdx.y;
+    const int32_t L = seq_len(len, (int32_t)(bh / H), ncap);
+    const int32_t jbeg = blockIdx.x * kBhRows;
+    if (jbeg >= L) return;  // uniform over the block
+    const int32_t jend = min(jbeg + kBhRows, L);
+    const bool far_rot = ra.enabled && ra.far_offset != 0;
+    float qv0[8], qv1[8];
+    {
+        const float4* qa = reinterpret_cast<const float4*>(q + bh * d + e0);
+        const float4* qb = reinterpret_cast<const float4*>(q + bh * d + e1);
+        const float4 a0 = __ldg(qa), a1 = __ldg(qa + 1), b0 = __ldg(qb), b1 = __ldg(qb + 1);
+        qv0[0] = a0.x; qv0[1] = a0.y; qv0[2] = a0.z; qv0[3] = a0.w;
+        qv0[4] = a1.x; qv0[5] = a1.y; qv0[6] = a1.z; qv0[7] = a1.w;
+        qv1[0] = b0.x; qv1[1] = b0.y; qv1[2] = b0.z; qv1[3] = b0.w;
+        qv1[4] = b1.x; qv1[5] = b1.y; qv1[6] = b1.z; qv1[7] = b1.w;
+    }
+    const float qn = qnorm[bh];
+    // the loop bounds are uniform over the warp (the shuffles take it whole)
+    for (int32_t jb = jbeg; jb < jend; jb += 2 * rpb) {
+        int32_t jr[2] = {jb + rl, jb + rl + rpb};
+        bool valid[2] = {jr[0] < jend, jr[1] < jend};
+        float v0[2][8], v1[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; u++)
+            if (valid[u]) {
+                const int64_t row = bh * ncap + jr[u];
+                load8<DT>(keys, row * d + e0, v0[u]);
+                load8<DT>(keys, row * d + e1, v1[u]);
+            }
+        float dot[2] = {0.f, 0.f}, nn[2] = {0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            if (!valid[u]) continue;
+            const int64_t row = bh * ncap + jr[u];
+            if (ra.enabled) {
+                const bool near = ra.window > 0 && (L - 1 - jr[u]) < ra.window;
+                if (near || far_rot) {
+                    float c[8], sn[8];
+                    angles8<false>(near ? jr[u] : ra.far_offset, e0, ra, c, sn);
+                    rotate8<false>(v0[u], v1[u], c, sn);
+                }
+            }
+            if constexpr (OUT >= 0) {
+                store8<OUT>(kout, row * d + e0, v0[u]);
+                store8<OUT>(kout, row * d + e1, v1[u]);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                dot[u] = fmaf(v0[u][k], qv0[k], dot[u]);
+                nn[u] = fmaf(v0[u][k], v0[u][k], nn[u]);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                dot[u] = fmaf(v1[u][k], qv1[k], dot[u]);
+                nn[u] = fmaf(v1[u][k], v1[u][k], nn[u]);
+            }
+        }
+        for (int m = lpr >> 1; m; m >>= 1) {
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], m);
+                nn[u] += __shfl_xor_sync(0xffffffffu, nn[u], m);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; u++)
+            if (valid[u] && lane == 0) {
+                const float kn = sqrtf(nn[u]);
+                scores[bh * ncap + jr[u]] = (kn > 0.f && qn > 0.f) ? dot[u] / (kn * qn) : 0.f;
+            }
+    }
+}
+
 int grid_for(int64_t work_items, int per_block) {
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
@@ -678,9 +771,9 @@ cudaError_t score_dispatch(const void* keys, const Shape& s, const int32_t* len,
                                                       d, len, ra, q, qnorm, scores, kout);
         note_launches(1);
     } else if (vec_ok) {
-        cosine_score_kernel<DT, false, OUT><<<grid_for(rows, kRopeThreads / (d / 16)),
-                                              kRopeThreads, 0, st>>>(
-            keys, rows, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra, q, qnorm, scores, kout);
+        dim3 grid((unsigned)((s.Ncap + kBhRows - 1) / kBhRows), (unsigned)(s.B * s.H));
+        cosine_score_bh_kernel<DT, OUT><<<grid, kRopeThreads, 0, st>>>(
+            keys, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra, q, qnorm, scores, kout);
         note_launches(1);
     } else {
         if (OUT >= 0) return cudaErrorNotSupported;  // the caller rotates in a pass of its own
