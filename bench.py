@@ -62,7 +62,7 @@ METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of rooflin
 # profiles/assign_tc_kernel_llama32_3b_layer.md.  It holds only for the
 # contraction source it was taken on (the first 16 hex digits of the sha256 of
 # csrc/assign_tc.cu); for any other source the bench reports null.
-TC_TRAFFIC = {"llama32_3b_layer": ("71a0dc64edb07245", 93701120)}
+TC_TRAFFIC = {"llama32_3b_layer": ("2ef1434f86dd0e01", 87519744)}
 DEFAULT_WORKLOAD = "llama32_3b_layer"
 L2_FLUSH_BYTES = 256 << 20
 # the timed region lasts at least this long (untimed replays between the
