@@ -57,6 +57,10 @@ CASES = [
     (2, 1, 300, 64, 257, "f16", False, dict(window=50, far_offset=3, rope_base=10000.0)),
     (1, 2, 400, 128, 33, "bf16", False, dict(window=128, far_offset=11, rope_base=500000.0)),
     (1, 1, 1000, 256, 513, "f16", True, dict(window=300, far_offset=0, rope_base=10000.0)),
+    # more than 2048 centroids: the pass over the stored keys takes one row
+    # block per tile and 256-column accumulators
+    (2, 1, 700, 128, 2500, "bf16", True, dict(window=64, far_offset=0, rope_base=500000.0)),
+    (1, 2, 400, 64, 3000, "f16", False, None),
 ]
 
 
