@@ -156,6 +156,7 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.chat = c.take<float>((size_t)(H * K * d));
     w.tc.chat_rot = c.take<float>((size_t)(H * K * d));
     w.tc.hneg = c.take<float>((size_t)(H * kpad));
+    w.tc.hplanes = c.take<uint16_t>((size_t)(H * kpad * 16));
     w.tc.head_bits = c.take<uint32_t>((size_t)(2 * H * 4));
     w.tc.head = c.take<float>((size_t)(2 * H * 4));
     w.tc.gstat = c.take<float2>((size_t)(2 * H * (kpad / kTcGroup)));

@@ -20,13 +20,18 @@
 //              operand plane, else 128 rows;
 //   warp 0     TMA producer of the codebook, in stages of 64 elements by the
 //              accumulator width (128 centroids with two row blocks, else
-//              256), and of -|c'|^2/2 per chunk into a ring of kHSlots;
+//              256), and of -|c'|^2/2 per chunk into a small ring;
 //   warp 1     TMEM allocation and tcgen05.mma issue (M = 128 per row
 //              block, bf16/fp16 -> fp32) into two accumulators per row block
 //              (the 512 TMEM columns), so the epilogue of one centroid chunk
-//              overlaps the MMAs of the next;
+//              overlaps the MMAs of the next.  With bf16 operands the first
+//              MMA of a chunk is one more K = 16 step, a constant tile of
+//              ones against three bf16 planes of -|c'|^2/2, which starts the
+//              accumulator at -h_j exactly;
 //   warps 2-9  epilogue, one per (TMEM lane quarter, row block or 128-column
-//              part): tcgen05.ld of the accumulator, v = acc - |c'|^2/2, and
+//              part): tcgen05.ld of the accumulator, v = acc - |c'|^2/2 (the
+//              accumulator itself with bf16 operands; fp16 planes carry a
+//              scale and add -h_j here), and
 //              per 16-column group only its largest value (a three-input max
 //              tree); the values of the best group so far are kept in
 //              registers, and the position and second value inside it are
@@ -51,28 +56,28 @@ constexpr int BM = 128;   // rows per row block (UMMA M)
 constexpr int BK = 64;    // 16-bit elements per 128-byte swizzle atom
 constexpr int kPadCols = 256;  // -|c L|^2 / 2 rows are padded to a multiple of this
 constexpr int kEpiWarps = 8;   // 4 TMEM lane quarters x 2 (row blocks or column parts)
-// slots of the -|c'|^2/2 ring: its producer is the codebook producer, so the
-// ring lets the codebook stream run this many chunks ahead of the epilogue
-constexpr int kHSlots = 8;
 constexpr int kAWarp = 2 + kEpiWarps;          // the key-tile producer
 constexpr int kThreads = 32 * (kAWarp + 1);
 
 struct Params {
     int32_t H, d, K, P;        // P: codebook planes the pass multiplies
     int32_t pstride;           // planes stored per head in the B tensor map
-    int32_t max_order;         // plane products of order pa + pl above this are dropped
     int32_t num_bh, seg, tiles_per_bh, nchunks, kpad;
     int32_t out_ncap;          // rows per (b, h) of the keys and of codes
     int64_t plane_rows;        // rows of one A plane in the A tensor map
     const int32_t* len;        // [B] or null
     const int32_t* count;      // compact list: rows per (b, h); null = natural order
-    const int32_t* row_map;    // compact list: row of the keys each entry stands for
+    const int32_t* row_map;    // compact list: row of the keys each entry stands for,
+                               // | kUnrotated when it was not rotated (its second
+                               // plane is zero: the row operand is exact)
     const uint8_t* skip;       // rows to leave untouched (bulk mode), or null
     int32_t skip_near;         // natural order: rows with t - j < skip_near belong to
                                // the compact pass (0 = none)
-    const float* hneg;         // [H, kpad]: -|c_j L|^2 / 2, -FLT_MAX past K
+    const float* hneg;         // [H, kpad]: -|c_j L|^2 / 2, -FLT_MAX past K (fp16)
+    const uint16_t* hplanes;   // [H, kpad, 16]: the same as bf16 planes of the -h step (bf16)
     const float* head;         // [H, 4]: max |chat_j|, max h_j, 1/scale, abs error
     float err_coef;            // relative error bound of the contraction (host)
+    float err_coef_unrot;      // the same for a compact row stored unrotated
     float norm_slack;          // |x| from plane 0 times this bounds |x|
     int32_t* codes;            // [num_bh * out_ncap]
     int64_t* exact_list;       // rows for the exact kernel
@@ -91,6 +96,9 @@ struct Params {
     int32_t kcopy_tma;         // tiles whose rows are all valid are copied by TMA
                                // stores through the third tensor map
 };
+
+// Flag in a compact row-map entry: the row was stored as it is (no rotation).
+constexpr int32_t kUnrotated = 1 << 30;
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
@@ -145,14 +153,15 @@ __device__ __forceinline__ void top2_16(const float* k, float& t1, float& t2) {
 // exceeds U, with room for the rounding of the comparison and the absolute
 // term, else the row joins the exact list.
 __device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int h,
-                                           float m1, float U, int32_t code, float xn) {
-    const int32_t j = p.row_map ? p.row_map[(int64_t)bh * p.seg + ri] : ri;
+                                           float m1, float U, int32_t code, float xn,
+                                           float coef) {
+    const int32_t j = p.row_map ? (p.row_map[(int64_t)bh * p.seg + ri] & ~kUnrotated) : ri;
     const int32_t Lb = seq_len(p.len, bh / p.H, p.out_ncap);
     if (j < 0 || j >= Lb) return;
     const int64_t out = (int64_t)bh * p.out_ncap + j;
     if (p.skip && p.skip[out]) return;
     const float2 g1 = p.gstat[(int64_t)h * p.ngroups + code / kTcGroup];
-    const float e1 = p.err_coef * fmaf(xn, g1.x, g1.y);
+    const float e1 = coef * fmaf(xn, g1.x, g1.y);
     const float mag = fmaxf(fabsf(m1), fabsf(U));
     const float tau = e1 + 2.f * p.head[h * 4 + 3] * xn + 4.f * mag * 1.1920929e-07f;
     if (!(m1 - U > tau)) {
@@ -195,16 +204,31 @@ struct Geo {
     static constexpr int kRows = BM * RB;             // rows per tile
 };
 
-template <int DK, int PA, int AST, int BST, int RB>
+// The ring of -|c'|^2/2 per chunk, filled by the codebook producer.  Folded
+// (bf16 operands): per chunk the B operand of one more K = 16 step, kBN rows
+// of 32 bytes holding -h_j as three bf16 planes (elements 0-2, zeros after),
+// which the MMA issuer multiplies by a constant tile of ones so that each
+// accumulator starts at -h_j; the ring only has to stay ahead of the MMAs.
+// Else kBN floats per chunk, added by the epilogue, and a deeper ring that
+// lets the codebook stream run ahead of the epilogue.
+template <bool FOLD, int RB>
+struct HRing {
+    static constexpr int kSlots = FOLD ? (RB == 2 ? 4 : 2) : 8;
+    static constexpr int kSlotBytes = Geo<RB>::kBN * (FOLD ? 32 : 4);
+};
+
+template <bool FOLD, int DK, int PA, int AST, int BST, int RB>
 struct Smem {
     using G = Geo<RB>;
+    using R = HRing<FOLD, RB>;
     static constexpr int kA = BM * 128;        // one 64-element k-block of one A plane
     static constexpr int kB = G::kBN * 128;    // one B stage
     static constexpr int kABytes = AST * RB * PA * DK * kA;
     static constexpr int kBBytes = BST * kB;
-    static constexpr int kHOff = kABytes + kBBytes;          // kHSlots x kBN floats of -h
-    static constexpr int kBarOff = kHOff + kHSlots * G::kBN * 4;
-    static constexpr int kBars = 2 * AST + 2 * BST + 10 + 2 * kHSlots;
+    static constexpr int kHOff = kABytes + kBBytes;          // the -h ring
+    static constexpr int kOnesOff = kHOff + R::kSlots * R::kSlotBytes;  // folded: BM x 32 bytes
+    static constexpr int kBarOff = kOnesOff + (FOLD ? BM * 32 : 0);
+    static constexpr int kBars = 2 * AST + 2 * BST + 10 + 2 * R::kSlots;
     static constexpr int kMergeOff = kBarOff + kBars * 8 + 16;
     static constexpr int kNrmOff = kMergeOff + (G::kParts - 1) * 2 * 4 * 32 * 16;
     static constexpr int kQOff = kNrmOff + 2 * G::kParts * BM * 8;  // [AST][kMaxD] fp32 queries
@@ -215,15 +239,19 @@ template <bool BF16, int DK, int PA, int AST, int BST, int RB>
 __global__ void __launch_bounds__(kThreads, 1)
 assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmK, const Params p) {
-    using S = Smem<DK, PA, AST, BST, RB>;
+    // bf16 operands take -h_j into the MMAs (an exact three-plane split);
+    // fp16 planes carry a per-head scale, and their epilogue adds -h_j
+    constexpr bool FOLD = BF16;
+    using S = Smem<FOLD, DK, PA, AST, BST, RB>;
     using G = Geo<RB>;
     constexpr int BN = G::kBN, kParts = G::kParts, kSubs = G::kSubs, kRows = G::kRows;
+    constexpr int kHS = HRing<FOLD, RB>::kSlots, kHBytes = HRing<FOLD, RB>::kSlotBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
     uint8_t* smA = sm;
     uint8_t* smB = sm + S::kABytes;
-    float* smH = reinterpret_cast<float*>(sm + S::kHOff);
+    uint8_t* smH = sm + S::kHOff;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBarOff);
     uint64_t* a_full = bars;
     uint64_t* a_empty = bars + AST;
@@ -232,8 +260,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint64_t* acc_full = bars + 2 * AST + 2 * BST;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* h_full = acc_full + 4;
-    uint64_t* h_empty = h_full + kHSlots;
-    uint64_t* merge_full = h_empty + kHSlots;  // column-part handoff, after the h ring
+    uint64_t* h_empty = h_full + kHS;
+    uint64_t* merge_full = h_empty + kHS;  // column-part handoff, after the h ring
     uint64_t* merge_empty = merge_full + 1;
     uint64_t* nrm_full = merge_full + 2;       // [4] one per TMEM lane quarter: row-norm partials
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kBars);
@@ -266,14 +294,26 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], kEpiWarps);
         }
-        for (int i = 0; i < kHSlots; i++) {
+        for (int i = 0; i < kHS; i++) {
             mbar_init(&h_full[i], 1);
-            mbar_init(&h_empty[i], kEpiWarps);
+            mbar_init(&h_empty[i], FOLD ? 1 : kEpiWarps);  // folded: released by an MMA commit
         }
         mbar_init(merge_full, 4);   // the part-1 warps hand over (two column parts)
         mbar_init(merge_empty, 4);  // the part-0 warps take the handoff
         for (int i = 0; i < 4; i++) mbar_init(&nrm_full[i], kParts);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if constexpr (FOLD) {
+        // the A operand of the -h step: BM rows whose elements 0-2 are 1 (bf16)
+        // and the rest 0, in the 32-byte swizzle
+        uint4* ones = reinterpret_cast<uint4*>(sm + S::kOnesOff);
+        for (int i = threadIdx.x; i < BM * 2; i += kThreads) {
+            const int r = i >> 1, half = i & 1;
+            ones[i] = half == ((r >> 2) & 1) ? make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // the generic-proxy stores are visible to the tensor core's reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -335,15 +375,17 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (ti.skip) continue;
                 const int h = ti.bh % p.H;
                 for (int c = 0; c < p.nchunks && ok; c++) {
-                    const int hs = h_it % kHSlots;
-                    ok = mbar_wait(&h_empty[hs], ((h_it / kHSlots) & 1) ^ 1, p.status, 11);
+                    const int hs = h_it % kHS;
+                    ok = mbar_wait(&h_empty[hs], ((h_it / kHS) & 1) ^ 1, p.status, 11);
                     if (!ok) break;
-                    mbar_expect_tx(&h_full[hs], BN * 4);
+                    mbar_expect_tx(&h_full[hs], kHBytes);
+                    const int64_t hrow = (int64_t)h * p.kpad + c * BN;
+                    const void* hsrc = FOLD ? static_cast<const void*>(p.hplanes + hrow * 16)
+                                            : static_cast<const void*>(p.hneg + hrow);
                     asm volatile(
                         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                        "%2, [%3];" ::"r"(su32(smH + hs * BN)),
-                        "l"(p.hneg + (int64_t)h * p.kpad + c * BN), "r"(BN * 4),
-                        "r"(su32(&h_full[hs]))
+                        "%2, [%3];" ::"r"(su32(smH + hs * kHBytes)),
+                        "l"(hsrc), "r"(kHBytes), "r"(su32(&h_full[hs]))
                         : "memory");
                     h_it++;
                     for (int pl = 0; pl < p.P && ok; pl++)
@@ -364,10 +406,10 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t last = b_it - 1 - ((b_it - 1 - s) % BST);
                     mbar_wait(&b_full[last % BST], (last / BST) & 1, p.status, 3);
                 }
-            for (int s = 0; s < kHSlots; s++)
+            for (int s = 0; s < kHS; s++)
                 if (h_it > (uint32_t)s) {
-                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % kHSlots);
-                    mbar_wait(&h_full[last % kHSlots], (last / kHSlots) & 1, p.status, 3);
+                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % kHS);
+                    mbar_wait(&h_full[last % kHS], (last / kHS) & 1, p.status, 3);
                 }
         }
     } else if (warp == 1) {
@@ -418,6 +460,22 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     uint32_t accumulate[RB];
 #pragma unroll
                     for (int rb = 0; rb < RB; rb++) accumulate[rb] = 0;
+                    if constexpr (FOLD) {
+                        // D = ones x (-h planes)^T starts each accumulator at
+                        // -h_j; the slot is free once these MMAs have read it
+                        const int hs = acc_it % kHS;
+                        ok = mbar_wait(&h_full[hs], (acc_it / kHS) & 1, p.status, 12);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t od = sw32_desc(su32(sm + S::kOnesOff));
+                        const uint64_t hd = sw32_desc(su32(smH + hs * kHBytes));
+#pragma unroll
+                        for (int rb = 0; rb < RB; rb++) {
+                            tc_mma(tmem + (uint32_t)((acc * RB + rb) * BN), od, hd, idesc, 0u);
+                            accumulate[rb] = 1;
+                        }
+                        tc_commit(&h_empty[hs]);
+                    }
                     for (int pl = 0; pl < p.P && ok; pl++)
 #pragma unroll
                         for (int kb = 0; kb < DK; kb++) {
@@ -434,9 +492,9 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                 const uint32_t d_tmem = tmem + (uint32_t)((acc * RB + rb) * BN);
 #pragma unroll
                                 for (int pa = 0; pa < PA; pa++) {
-                                    // products of a higher order are dropped (the
-                                    // bound counts them)
-                                    if (pa + pl > p.max_order) continue;
+                                    // the row's second plane multiplies chat's
+                                    // first only (the bound counts the rest)
+                                    if (pa > 0 && pl > 0) continue;
                                     const uint64_t ad = a_desc[rb][pa][kb];
 #pragma unroll
                                     for (int ks = 0; ks < BK / 16; ks++) {
@@ -567,9 +625,17 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int32_t c1 = 0, gb1 = -1;
             float best[kG];
             const float xn = sqrtf(nrm) * p.norm_slack;
-            const float alpha = p.err_coef * xn, beta = p.err_coef;
+            // a compact row stored without rotation is exact in its first
+            // plane (the second is zero), so only the contraction's own
+            // rounding and chat's count
+            float coef = p.err_coef;
+            if (p.row_map && ri < ti.nvalid) {
+                const int32_t rm = p.row_map[(int64_t)ti.bh * p.seg + ri];
+                if (rm >= 0 && (rm & kUnrotated)) coef = p.err_coef_unrot;
+            }
+            const float alpha = coef * xn, beta = coef;
             const float2* gst = p.gstat + (int64_t)h * p.ngroups;
-            const float inv_scale = p.head[h * 4 + 2];
+            const float inv_scale = FOLD ? 1.f : p.head[h * 4 + 2];
             const float2 inv2 = make_float2(inv_scale, inv_scale);
             for (int c = 0; c < p.nchunks && ok; c++) {
                 const int acc = acc_it & 1;
@@ -581,12 +647,12 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const float2 gs = __ldg(gst + g0 + i);
                     sg[i] = fmaf(alpha, gs.x, beta * gs.y);
                 }
-                const int hs = acc_it % kHSlots;
-                ok = mbar_wait(&h_full[hs], (acc_it / kHSlots) & 1, p.status, 12) &&
+                const int hs = acc_it % kHS;
+                ok = (FOLD || mbar_wait(&h_full[hs], (acc_it / kHS) & 1, p.status, 12)) &&
                      mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
-                const float* hrow = smH + hs * BN;
+                const float* hrow = reinterpret_cast<const float*>(smH + hs * kHBytes);
                 const uint32_t tbase =
                     tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((acc * RB + rb) * BN);
                 // the next 32 columns are loaded while the current ones are
@@ -603,19 +669,25 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const uint32_t* r = rr[sub & 1];
                     const float4* h4 = reinterpret_cast<const float4*>(hrow + col);
                     float v[32];
+                    if constexpr (FOLD) {
+                        // the accumulator already holds x . chat_j - h_j
 #pragma unroll
-                    for (int u = 0; u < 8; u++) {
-                        const float4 hv = h4[u];
-                        const float2 v01 = __ffma2_rn(
-                            make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
-                            inv2, make_float2(hv.x, hv.y));
-                        const float2 v23 = __ffma2_rn(
-                            make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
-                            inv2, make_float2(hv.z, hv.w));
-                        v[4 * u + 0] = v01.x;
-                        v[4 * u + 1] = v01.y;
-                        v[4 * u + 2] = v23.x;
-                        v[4 * u + 3] = v23.y;
+                        for (int u = 0; u < 32; u++) v[u] = __uint_as_float(r[u]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; u++) {
+                            const float4 hv = h4[u];
+                            const float2 v01 = __ffma2_rn(
+                                make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
+                                inv2, make_float2(hv.x, hv.y));
+                            const float2 v23 = __ffma2_rn(
+                                make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                inv2, make_float2(hv.z, hv.w));
+                            v[4 * u + 0] = v01.x;
+                            v[4 * u + 1] = v01.y;
+                            v[4 * u + 2] = v23.x;
+                            v[4 * u + 3] = v23.y;
+                        }
                     }
 #pragma unroll
                     for (int half = 0; half < 32 / kG; half++) {
@@ -651,7 +723,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&acc_empty[acc]);
-                    mbar_arrive(&h_empty[hs]);
+                    if (!FOLD) mbar_arrive(&h_empty[hs]);
                 }
                 acc_it++;
             }
@@ -673,7 +745,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             if (kParts == 1) {
                 const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn, coef);
             } else if (part != 0) {
                 // merge the column parts of each row, then decide the row
                 ok = mbar_wait(merge_empty, (m_it & 1) ^ 1, p.status, 9);
@@ -705,7 +777,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     ub2 = fmaxf(ub2, o1.x);
                 }
                 const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn, coef);
             }
             m_it++;
         }
@@ -819,6 +891,35 @@ __global__ void head_finish_kernel(const uint32_t* __restrict__ head_bits, int32
 }
 
 // hneg [H, kpad] = -half_norm, and -FLT_MAX past K (those columns never win).
+// For bf16 operands the same values go into hplanes [H, kpad, 16] instead, as
+// the B operand of the K = 16 step that starts each accumulator at -h_j:
+// elements 0-2 of row j are three bf16 planes, each the truncation toward
+// zero of what the planes before it leave (8 significant bits each, so their
+// sum is the fp32 value exactly, -FLT_MAX included), elements 3-15 are zero,
+// and the two 16-byte halves of row j are swapped when bit 2 of j is set: the
+// 32-byte swizzle, so that a chunk of rows (a multiple of 8) copies into
+// shared memory as the MMA reads it.
+__global__ void hneg_planes_kernel(const float* __restrict__ half_norm, int64_t H, int64_t K,
+                                   int64_t kpad, uint16_t* __restrict__ hplanes) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < H * kpad;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t h = i / kpad, j = i % kpad;
+        float v = j < K ? -half_norm[h * K + j] : -FLT_MAX;
+        uint32_t pl[3];
+#pragma unroll
+        for (int k = 0; k < 3; k++) {
+            const uint32_t top = __float_as_uint(v) & 0xFFFF0000u;
+            pl[k] = top >> 16;
+            v = v - __uint_as_float(top);  // exact: the low 16 bits of the significand
+        }
+        const uint4 lo = make_uint4(pl[0] | (pl[1] << 16), pl[2], 0u, 0u);
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        uint4* row = reinterpret_cast<uint4*>(hplanes + i * 16);
+        const bool swap = (j >> 2) & 1;
+        row[0] = swap ? zero : lo;
+        row[1] = swap ? lo : zero;
+    }
+}
 __global__ void pad_half_norm_kernel(const float* __restrict__ half_norm, int64_t H, int64_t K,
                                      int64_t kpad, float* __restrict__ hneg) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < H * kpad;
@@ -864,6 +965,45 @@ __global__ void codebook_planes_kernel(const float* __restrict__ chat, int64_t K
 // or the decode row (mode 3).  Each is rotated in fp32 and split into two 16-bit planes
 // hi = rn(k~), lo = rn(k~ - hi); planes [2][nbh * ncap][d].  Rows whose fp16
 // planes would overflow go to the exact list instead.
+//
+// Eight lanes take a row, 16 bytes at a time: with the two-halves layout lane
+// e of the octet holds elements 8 ch .. 8 ch + 7 (ch = e, e + 8, ...) of both
+// halves, i.e. whole rotation pairs; interleaved pairs sit inside one 16-byte
+// chunk.  A block takes 32 rows per sweep, so a few thousand rows per (b, h)
+// are one or two sweeps of a single wave of blocks.
+constexpr int kCompactRows = 32;  // rows per block per sweep (8 warps x 4)
+
+template <int DT>
+__device__ __forceinline__ bool split_store8(const float* v, uint16_t* hi_p, uint16_t* lo_p) {
+    uint32_t hw[4], lw[4];
+    bool over = false;
+#pragma unroll
+    for (int u = 0; u < 8; u += 2) {
+        uint16_t hb[2], lb[2];
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const float x = v[u + k];
+            if (DT == kBF16) {
+                const __nv_bfloat16 hv = __float2bfloat16_rn(x);
+                const __nv_bfloat16 lv = __float2bfloat16_rn(x - __bfloat162float(hv));
+                hb[k] = __bfloat16_as_ushort(hv);
+                lb[k] = __bfloat16_as_ushort(lv);
+            } else {
+                const __half hv = __float2half_rn(x);
+                const __half lv = __float2half_rn(x - __half2float(hv));
+                over |= !(fabsf(x) <= 65504.f);
+                hb[k] = __half_as_ushort(hv);
+                lb[k] = __half_as_ushort(lv);
+            }
+        }
+        hw[u / 2] = (uint32_t)hb[0] | ((uint32_t)hb[1] << 16);
+        lw[u / 2] = (uint32_t)lb[0] | ((uint32_t)lb[1] << 16);
+    }
+    *reinterpret_cast<uint4*>(hi_p) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo_p) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    return over;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(256)
 compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d,
@@ -872,7 +1012,6 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
                     uint16_t* __restrict__ planes, int32_t* __restrict__ row_map,
                     int32_t* __restrict__ ccount, int64_t* __restrict__ exact_list,
                     int32_t* __restrict__ exact_count) {
-    using T = typename Elem<DT>::T;
     const int bh = blockIdx.y;
     const int32_t L = seq_len(len, bh / H, ncap);
     int32_t n;
@@ -887,59 +1026,75 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
         ccount[bh] = n;
         atomicMax(exact_count + 2, n);  // the longest list, for the contraction's tile bound
     }
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, e = lane & 7;
     const int halfd = d / 2;
     const int64_t plane_rows = (int64_t)gridDim.y * ncap;
-    for (int32_t i = blockIdx.x * 8 + w; i < n; i += gridDim.x * 8) {
-        int32_t j = mode == 1 ? perm[(int64_t)bh * ncap + i] : L - n + i;  // mode 3: L - 1
-        if (j < 0 || j >= L) {
-            if (lane == 0) row_map[(int64_t)bh * ncap + i] = -1;
-            continue;
-        }
-        const int64_t src = ((int64_t)bh * ncap + j) * d;
-        const int64_t dst = ((int64_t)bh * ncap + i) * d;
-        const int32_t pos = ra.enabled ? rope_position(j, L - 1, ra) : 0;
+    uint16_t* lo_planes = planes + plane_rows * d;
+    // i0 is the same for the whole block, so every warp runs each sweep whole
+    // (the ballot below takes all its lanes)
+    for (int32_t i0 = blockIdx.x * kCompactRows; i0 < n; i0 += gridDim.x * kCompactRows) {
+        const int32_t i = i0 + (int32_t)(threadIdx.x >> 3);
+        const bool active = i < n;
+        int32_t j = -1;
+        if (active) j = mode == 1 ? perm[(int64_t)bh * ncap + i] : L - n + i;  // mode 3: L - 1
+        const bool valid = active && j >= 0 && j < L;
         bool over = false;
-        for (int pi = lane; pi < halfd; pi += 32) {
-            const int a = ra.interleaved ? 2 * pi : pi;
-            const int b = ra.interleaved ? 2 * pi + 1 : pi + halfd;
-            float xa = load1<DT>(x, src + a), xb = load1<DT>(x, src + b);
-            if (pos != 0) {
-                float s, c;
-                rope_angle(pos, ra.omega_hi[pi], ra.omega_lo[pi], ra, s, c);
-                const float ya = fmaf(xa, c, -__fmul_rn(xb, s));
-                const float yb = fmaf(xa, s, __fmul_rn(xb, c));
-                xa = ya;
-                xb = yb;
-            }
-            const float vals[2] = {xa, xb};
-            const int idx[2] = {a, b};
+        int32_t pos_row = 0;
+        if (valid) {
+            const int64_t src = ((int64_t)bh * ncap + j) * d;
+            const int64_t dst = ((int64_t)bh * ncap + i) * d;
+            const int32_t pos = ra.enabled ? rope_position(j, L - 1, ra) : 0;
+            pos_row = pos;
+            if (!ra.interleaved) {
+                for (int ch = e; ch < halfd / 8; ch += 8) {
+                    float va[8], vb[8];
+                    load_vec<DT>(x, src + 8 * ch, va);
+                    load_vec<DT>(x, src + halfd + 8 * ch, vb);
+                    if (pos != 0) {
 #pragma unroll
-            for (int u = 0; u < 2; u++) {
-                uint16_t hb, lb;
-                if (DT == kBF16) {
-                    const __nv_bfloat16 hv = __float2bfloat16_rn(vals[u]);
-                    const __nv_bfloat16 lv = __float2bfloat16_rn(vals[u] - __bfloat162float(hv));
-                    hb = __bfloat16_as_ushort(hv);
-                    lb = __bfloat16_as_ushort(lv);
-                } else {
-                    const __half hv = __float2half_rn(vals[u]);
-                    const __half lv = __float2half_rn(vals[u] - __half2float(hv));
-                    over |= !(fabsf(vals[u]) <= 65504.f);
-                    hb = __half_as_ushort(hv);
-                    lb = __half_as_ushort(lv);
+                        for (int u = 0; u < 8; u++) {
+                            float s, c;
+                            rope_angle(pos, ra.omega_hi[8 * ch + u], ra.omega_lo[8 * ch + u], ra, s,
+                                       c);
+                            const float ya = fmaf(va[u], c, -__fmul_rn(vb[u], s));
+                            const float yb = fmaf(va[u], s, __fmul_rn(vb[u], c));
+                            va[u] = ya;
+                            vb[u] = yb;
+                        }
+                    }
+                    over |= split_store8<DT>(va, planes + dst + 8 * ch, lo_planes + dst + 8 * ch);
+                    over |= split_store8<DT>(vb, planes + dst + halfd + 8 * ch,
+                                             lo_planes + dst + halfd + 8 * ch);
                 }
-                planes[dst + idx[u]] = hb;
-                planes[plane_rows * d + dst + idx[u]] = lb;
+            } else {
+                for (int ch = e; ch < d / 8; ch += 8) {
+                    float v[8];
+                    load_vec<DT>(x, src + 8 * ch, v);
+                    if (pos != 0) {
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            const int pi = 4 * ch + u;
+                            float s, c;
+                            rope_angle(pos, ra.omega_hi[pi], ra.omega_lo[pi], ra, s, c);
+                            const float xa = v[2 * u], xb = v[2 * u + 1];
+                            v[2 * u] = fmaf(xa, c, -__fmul_rn(xb, s));
+                            v[2 * u + 1] = fmaf(xa, s, __fmul_rn(xb, c));
+                        }
+                    }
+                    over |= split_store8<DT>(v, planes + dst + 8 * ch, lo_planes + dst + 8 * ch);
+                }
             }
         }
-        over = __any_sync(0xffffffffu, over);
-        if (lane == 0) {
-            if (over) {
+        // any lane of the row's octet
+        over = ((__ballot_sync(0xffffffffu, over) >> (lane & ~7)) & 0xFFu) != 0;
+        if (e == 0 && active) {
+            if (!valid) {
+                row_map[(int64_t)bh * ncap + i] = -1;
+            } else if (over) {
                 row_map[(int64_t)bh * ncap + i] = -1;
                 exact_list[atomicAdd(exact_count, 1)] = (int64_t)bh * ncap + j;
             } else {
-                row_map[(int64_t)bh * ncap + i] = j;
+                row_map[(int64_t)bh * ncap + i] = j | (pos_row == 0 ? kUnrotated : 0);
             }
         }
     }
@@ -1197,7 +1352,7 @@ unsigned blocks_for(int64_t n, int per, unsigned cap) {
 template <bool BF16, int DK, int PA, int AST, int BST, int RB>
 cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tk,
                           const Params& p, cudaStream_t st) {
-    using S = Smem<DK, PA, AST, BST, RB>;
+    using S = Smem<BF16, DK, PA, AST, BST, RB>;
     static_assert(S::kTotal <= 232448, "shared memory budget");
     auto k = assign_tc_kernel<BF16, DK, PA, AST, BST, RB>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
@@ -1329,12 +1484,10 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.H = (int32_t)H;
     p.d = (int32_t)d;
     p.K = (int32_t)K;
-    // two row planes against the codebook planes keep the products of order
-    // 0 and 1 only: planes 0 and 1 of chat (of 3 stored for bf16)
-    const bool cut = PA == 2 && !b.exact;
-    p.P = cut ? 2 : b.P;
+    // two row planes: the first against every plane of chat, the second
+    // against chat's first plane only
+    p.P = b.P;
     p.pstride = b.P;
-    p.max_order = cut ? 1 : 2;
     p.num_bh = (int32_t)nbh;
     p.seg = (int32_t)ncap;
     p.tiles_per_bh = (int32_t)(((max_rows < ncap ? max_rows : ncap) + tile_rows - 1) / tile_rows);
@@ -1348,6 +1501,7 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.skip = skip;
     p.skip_near = skip_near;
     p.hneg = c.hneg;
+    p.hplanes = c.hplanes;
     p.head = b.head;
     p.gstat = b.gstat;
     p.ngroups = p.kpad / kTcGroup;
@@ -1355,20 +1509,24 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     // partial sums into fp32, each addition off by at most 2^-23 of the
     // running magnitude, which |x| max|chat| + max h bounds; plus the rounding
     // of chat and of the planes that are dropped, of the two-plane row
-    // operand, and of h and of acc - h.
-    int pairs = 0;
-    for (int pb = 0; pb < p.P; pb++)
-        for (int pa = 0; pa < PA; pa++)
-            if (pa + pb <= p.max_order) pairs++;
-    double coef = ((double)pairs * (double)(d / 16) + 8.0) * 0x1p-22;
-    if (!b.exact) coef += bf16 ? 0x1p-21 : 0x1p-20;
+    // operand, and of h and of acc - h.  A k-step whose products are all
+    // zero (the second plane of a row stored unrotated) adds nothing.
+    const int pairs = p.P + (PA == 2 ? 1 : 0);
+    // bf16: one more k-step, the one that starts the accumulator at -h_j
+    const double fixed = bf16 ? 9.0 : 8.0;
+    double coef = ((double)pairs * (double)(d / 16) + fixed) * 0x1p-22;
+    double coef_unrot = ((double)p.P * (double)(d / 16) + fixed) * 0x1p-22;
+    if (!b.exact) {
+        coef += bf16 ? 0x1p-21 : 0x1p-20;
+        coef_unrot += bf16 ? 0x1p-21 : 0x1p-20;
+    }
     if (PA == 2) coef += bf16 ? 0x1p-15 : 0x1p-20;
-    // the dropped products, each elementwise within a relative 2^-16 (bf16;
-    // 2^-22 fp16) of |x| |chat|: the row's second plane against chat's second
-    // (|lo| <= 2^-8 |x|, |c1| <= 2^-8 |chat|), and for bf16 chat's third plane
-    // against the row (|c2| <= 2^-16 |chat|)
-    if (cut) coef += bf16 ? 0x1.1p-15 : 0x1p-20;
+    // the dropped products, elementwise within a relative 2^-16 (bf16; 2^-22
+    // fp16) of |x| |chat|: the row's second plane (|lo| <= 2^-8 |x|) against
+    // chat's second (|c1| <= 2^-8 |chat|) and, for bf16, third plane
+    if (PA == 2 && !b.exact) coef += bf16 ? 0x1.1p-16 : 0x1p-20;
     p.err_coef = (float)coef;
+    p.err_coef_unrot = (float)coef_unrot;
     p.norm_slack = PA == 2 ? 1.01f : 1.0001f;
     p.codes = c.codes;
     p.exact_list = c.exact_list;
@@ -1432,8 +1590,12 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         e = cudaMemsetAsync(c.gstat, 0, sizeof(float2) * 2 * H * (kpad / kTcGroup), st);
         if (e != cudaSuccess) return e;
-        pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K,
-                                                                             kpad, c.hneg);
+        if (c.dt == kBF16)
+            hneg_planes_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(c.half_norm, H, K,
+                                                                              kpad, c.hplanes);
+        else
+            pad_half_norm_kernel<<<blocks_for(H * kpad, 256, 4096), 256, 0, st>>>(
+                c.half_norm, H, K, kpad, c.hneg);
         note_launches(1);
     }
     const float* chat = c.L ? c.chat : c.cp;
@@ -1475,10 +1637,10 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         const int cmode = c.sel.mode == 2 ? 0 : c.sel.mode;
         const int64_t most = cmode == 0 ? (c.ra.window < ncap ? c.ra.window : ncap)
                                         : (cmode == 3 ? 1 : ncap);
-        // one warp per row when the grid allows (each warp's rows run one
-        // after another, each a chain of a load, the rotation and stores)
-        const int64_t per_bh = 16 * (int64_t)sm_count() / (nbh > 0 ? nbh : 1);
-        dim3 g(blocks_for(most, 8, (unsigned)(per_bh > 1 ? per_bh : 1)), (unsigned)nbh);
+        // one wave of blocks (eight per SM) over all (b, h); each block
+        // sweeps kCompactRows rows at a time
+        const int64_t per_bh = 8 * (int64_t)sm_count() / (nbh > 0 ? nbh : 1);
+        dim3 g(blocks_for(most, kCompactRows, (unsigned)(per_bh > 1 ? per_bh : 1)), (unsigned)nbh);
         if (c.dt == kBF16)
             compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
                 c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,
@@ -1513,12 +1675,12 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         auto scan = S == 128 ? exact_scan_kernel<128> : exact_scan_kernel<64>;
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        // chunks of a head's rows run side by side in z: up to 32 (8 at the
-        // least), within about 8192 blocks in all (the blocks past a head's
-        // last chunk leave at once)
+        // chunks of a head's rows run side by side in z: 4 to 8 (the blocks
+        // past a head's last chunk leave at once, and a block takes the
+        // chunks z, z + zc, ... of its head)
         const int64_t slices = (K + S - 1) / S;
-        int64_t zc = 8192 / (slices * H);
-        zc = zc < 8 ? 8 : (zc > 32 ? 32 : zc);
+        int64_t zc = 2048 / (slices * H);
+        zc = zc < 4 ? 4 : (zc > 8 ? 8 : zc);
         dim3 g((unsigned)slices, (unsigned)H, (unsigned)zc);
         scan<<<g, kExactThreads, smem, st>>>((int32_t)d, c.cp, K, c.head_count, head_rows, head_cap,
                                              zbuf, c.exact_best, c.exact_done, c.exact_list,

@@ -154,7 +154,8 @@ struct TcCall {
     float* Lt;            // [H, d, d]  L^T
     float* chat;          // [H, K, d]  c L L^T
     float* chat_rot;      // [H, K, d]  the same, rotated by -far_offset
-    float* hneg;          // [H, Kpad]  -|c L|^2 / 2, padded to 256 columns
+    float* hneg;          // [H, Kpad]  -|c L|^2 / 2, padded to 256 columns (fp16 keys)
+    uint16_t* hplanes;    // [H, Kpad, 16] the same as the bf16 operand of one MMA step (bf16 keys)
     uint32_t* head_bits;  // [2, H, 4]
     float* head;          // [2, H, 4]
     float2* gstat;        // [2, H, Kpad / 32] group maxima of |chat_j| and h_j

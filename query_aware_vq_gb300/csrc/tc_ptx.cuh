@@ -136,6 +136,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)2u << 61;            // 128-byte swizzle
     return d;
 }
+// The same for a K-major operand of 32-byte rows (one k-step of 16 16-bit
+// elements) in the 32-byte swizzled layout: 8-row groups 256 bytes apart,
+// the two 16-byte halves of a row swapped when bit 2 of the row is set.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;           // leading offset: unused by this layout
+    d |= (uint64_t)(256u >> 4) << 32;  // stride offset between 8-row groups
+    d |= (uint64_t)1u << 46;           // descriptor version
+    d |= (uint64_t)6u << 61;           // 32-byte swizzle
+    return d;
+}
 #define A2ATS_TMEM_LD32(taddr, r)                                                               \
     asm volatile(                                                                               \
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, " \
