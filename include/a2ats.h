@@ -280,6 +280,14 @@ int a2ats_select_retrieval_set_rotated(const void* keys, int32_t dtype, int64_t 
  *   split_done  a cudaEvent_t, or NULL: recorded on the stream as soon as
  *          k_out, perm and count are complete (before the codes are), so a
  *          second stream can start on the split while this call finishes
+ *   split_stream  a cudaStream_t other than stream, or NULL: with split_done
+ *          given, the split itself runs there (split_done is recorded on
+ *          stream once the scores are written, split_stream waits for it,
+ *          and split_done is recorded again on split_stream after the
+ *          split), so the RoPE-window rows' assignment on stream runs beside
+ *          it; stream waits for split_done before the call returns, so every
+ *          output is complete in stream order as without it.  INVALID_ARG
+ *          when given without split_done or equal to stream
  *   workspace  a2ats_rope_split_plain_assign_workspace_size(B, H, Ncap, d, K)
  *          bytes of device memory, owned by the caller
  * The scores of this call may differ from those of
@@ -295,8 +303,8 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
                                   double fraction, const a2ats_rope_params* rope,
                                   const void* codebook, int64_t K, void* k_out, int32_t* perm,
                                   int32_t* count, int32_t* codes, int32_t reuse,
-                                  void* split_done, void* workspace, size_t workspace_bytes,
-                                  void* stream);
+                                  void* split_done, void* split_stream, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
  * a2ats_code_attention_topk -- the attention score of the decode query with

@@ -74,7 +74,7 @@ _SIGS = {
     "a2ats_code_attention_topk": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _P,
                                   _I32, _D, _P, _P, _P, _P, _SZ, _P],
     "a2ats_rope_split_plain_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P,
-                                      _I64, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P],
+                                      _I64, _P, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P],
     "a2ats_cholesky_rows_workspace_size": [_I64, _I64, _I64],
     "a2ats_cholesky_rows": [_P, _I32, _I64, _I64, _I64, _P, _P, _P, _SZ, _P],
     "a2ats_cholesky_solve_rows": [_P, _I64, _I64, _I64, _P, _P, _P],
@@ -393,12 +393,15 @@ def a2ats_select_retrieval_set_rotated(keys, query=None, fraction: float = 0.2, 
 
 def a2ats_rope_split_plain_assign(keys, codebook, query=None, fraction: float = 0.2, *, rope,
                                   lengths=None, out=None, perm=None, count=None, codes=None,
-                                  reuse=False, split_done=None, workspace=None, stream=None):
+                                  reuse=False, split_done=None, split_stream=None, workspace=None,
+                                  stream=None):
     """Windowed RoPE, the retrieval split and plain VQ of every row in one
     call over the pre-RoPE keys; returns (out, perm, count, codes).
     split_done: a torch.cuda.Event, recorded on the stream once out, perm and
-    count are written (the codes follow).  reuse=True takes the codebook side
-    from `workspace` as the previous call on it left it."""
+    count are written (the codes follow).  split_stream: a torch.cuda.Stream
+    (with split_done) that runs the split beside the rest of the call.
+    reuse=True takes the codebook side from `workspace` as the previous call
+    on it left it."""
     _dev(keys, codebook, query, lengths, out, perm, count, codes)
     k4, cb, K, codes = _assign_common(keys, codebook, codes)
     B, H, N, d = k4.shape
@@ -428,7 +431,8 @@ def a2ats_rope_split_plain_assign(keys, codebook, query=None, fraction: float = 
     _check("a2ats_rope_split_plain_assign", lib.a2ats_rope_split_plain_assign(
         _ptr(k4), _dt(k4), B, H, N, d, _ptr(_lens(lengths)), _ptr(query), float(fraction),
         ctypes.byref(rp), _ptr(cb), K, _ptr(o4), _ptr(perm), _ptr(count), _ptr(codes),
-        int(bool(reuse)), ev, _ptr(ws), nb, _stream(stream)))
+        int(bool(reuse)), ev, _stream(split_stream) if split_stream is not None else None,
+        _ptr(ws), nb, _stream(stream)))
     return out, perm, count, codes
 
 

@@ -169,8 +169,11 @@ AssignWs carve_assign(Carve& c, int64_t B, int64_t H, int64_t Ncap, int64_t d, i
     w.tc.exact_list = c.take<int64_t>(rows);
     w.tc.exact_best = c.take<unsigned long long>(rows);
     w.tc.exact_done = c.take<int32_t>(rows);
-    w.tc.exact_count = c.take<int32_t>(4);
-    w.tc.head_count = c.take<int32_t>((size_t)H);
+    // the counters, the per-head list lengths and the compact tiles' flags
+    // are adjacent: one memset
+    w.tc.exact_count = c.take<int32_t>((size_t)(4 + H + B * H * ((Ncap + 127) / 128)));
+    w.tc.head_count = w.tc.exact_count + 4;
+    w.tc.tile_rot = w.tc.head_count + H;
     return w;
 }
 
@@ -568,12 +571,29 @@ struct SplitAfter {
     int32_t* perm;
     int32_t* count;
     cudaEvent_t done;
+    cudaStream_t side;  // or null: the split runs on the call's stream
 };
 
+// With a side stream the split forks there through `done` (recorded on st
+// once the scores are written, waited on by side) and `done` is recorded
+// again on side after it; the call's stream joins it at the end.
 cudaError_t split_after_natural(void* ctx, cudaStream_t st) {
     const SplitAfter* a = static_cast<const SplitAfter*>(ctx);
-    cudaError_t e = launch_select(a->scores, a->sh, a->len, a->fraction, a->perm, a->count, st);
-    if (e == cudaSuccess && a->done) e = cudaEventRecord(a->done, st);
+    cudaStream_t on = st;
+    cudaError_t e = cudaSuccess;
+    if (a->side) {
+        e = cudaEventRecord(a->done, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(a->side, a->done, 0);
+        on = a->side;
+    }
+    if (e == cudaSuccess)
+        e = launch_select(a->scores, a->sh, a->len, a->fraction, a->perm, a->count, on);
+    if (e == cudaSuccess && a->done) e = cudaEventRecord(a->done, on);
+    return e;
+}
+
+cudaError_t join_split(const SplitAfter& a, cudaStream_t st, cudaError_t e) {
+    if (e == cudaSuccess && a.side) e = cudaStreamWaitEvent(st, a.done, 0);
     return e;
 }
 }  // namespace
@@ -583,14 +603,15 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
                                   double fraction, const a2ats_rope_params* rope,
                                   const void* codebook, int64_t K, void* k_out, int32_t* perm,
                                   int32_t* count, int32_t* codes, int32_t reuse,
-                                  void* split_done, void* workspace, size_t workspace_bytes,
-                                  void* stream) {
+                                  void* split_done, void* split_stream, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
     if (!dtype_ok(dtype)) return A2ATS_ERR_DTYPE;
     int st = check_shape(B, H, Ncap, d);
     if (st) return st;
     if (K < 1 || K > (int64_t(1) << 24)) return A2ATS_ERR_SHAPE;
     if (!unit_interval(fraction)) return A2ATS_ERR_INVALID_ARG;
     if (!rope) return A2ATS_ERR_INVALID_ARG;
+    if (split_stream && (!split_done || split_stream == stream)) return A2ATS_ERR_INVALID_ARG;
     RopeArgs ra;
     if ((st = make_rope(rope, d, ra))) return st;
     if (B * H == 0) return A2ATS_OK;
@@ -610,10 +631,11 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
     SelectWs sw = carve_select(c, B, H, Ncap, d);
     cudaStream_t s = (cudaStream_t)stream;
     const Shape sh{B, H, Ncap, d};
-    SplitAfter after{sw.scores, sh, len, fraction, perm, count, (cudaEvent_t)split_done};
+    SplitAfter after{sw.scores, sh, len, fraction, perm, count, (cudaEvent_t)split_done,
+                     (cudaStream_t)split_stream};
     cudaError_t e;
     if (Ncap == 0) {
-        e = split_after_natural(&after, s);
+        e = join_split(after, s, split_after_natural(&after, s));
         return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
     }
     const bool tc = tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30);
@@ -660,6 +682,7 @@ int a2ats_rope_split_plain_assign(const void* keys, int32_t dtype, int64_t B, in
         e = launch_assign_exact(keys, dtype, sh, len, ra, all, nullptr, w.cp, w.half_norm, K,
                                 codes, s);
     }
+    e = join_split(after, s, e);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
 }
 

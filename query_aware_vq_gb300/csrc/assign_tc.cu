@@ -67,6 +67,11 @@ struct Params {
     int64_t plane_rows;        // rows of one A plane in the A tensor map
     const int32_t* len;        // [B] or null
     const int32_t* count;      // compact list: rows per (b, h); null = natural order
+    // compact list, two row planes: per 128-row tile, nonzero when a row of
+    // it was rotated (else every second plane is zero and its MMAs are
+    // skipped), [num_bh, tiles128]; or null
+    const int32_t* tile_rot;
+    int32_t tiles128;
     const int32_t* row_map;    // compact list: row of the keys each entry stands for,
                                // | kUnrotated when it was not rotated (its second
                                // plane is zero: the row operand is exact)
@@ -204,17 +209,17 @@ struct Geo {
     static constexpr int kRows = BM * RB;             // rows per tile
 };
 
-// The ring of -|c'|^2/2 per chunk, filled by the codebook producer.  Folded
-// (bf16 operands): per chunk the B operand of one more K = 16 step, kBN rows
-// of 32 bytes holding -h_j as three bf16 planes (elements 0-2, zeros after),
-// which the MMA issuer multiplies by a constant tile of ones so that each
-// accumulator starts at -h_j; the ring only has to stay ahead of the MMAs.
-// Else kBN floats per chunk, added by the epilogue, and a deeper ring that
-// lets the codebook stream run ahead of the epilogue.
+// -|c'|^2/2 per chunk.  Folded (bf16 operands): the B operand of one more
+// K = 16 step, kBN rows of 32 bytes holding -h_j as three bf16 planes
+// (elements 0-2, zeros after), copied into the chunk's first codebook stage;
+// the MMA issuer multiplies it by a constant tile of ones so that each
+// accumulator starts at -h_j.  Else kBN floats per chunk in a ring of their
+// own, added by the epilogue, which lets the codebook stream run ahead of
+// the epilogue.
 template <bool FOLD, int RB>
 struct HRing {
-    static constexpr int kSlots = FOLD ? (RB == 2 ? 4 : 2) : 8;
-    static constexpr int kSlotBytes = Geo<RB>::kBN * (FOLD ? 32 : 4);
+    static constexpr int kSlots = FOLD ? 0 : 8;
+    static constexpr int kSlotBytes = Geo<RB>::kBN * 4;
 };
 
 template <bool FOLD, int DK, int PA, int AST, int BST, int RB>
@@ -222,10 +227,16 @@ struct Smem {
     using G = Geo<RB>;
     using R = HRing<FOLD, RB>;
     static constexpr int kA = BM * 128;        // one 64-element k-block of one A plane
-    static constexpr int kB = G::kBN * 128;    // one B stage
+    // a codebook stage holds KS k-blocks of one plane (all of them up to
+    // d = 128: one handshake per chunk and plane), and in a chunk's first
+    // stage the folded -h tile after them
+    static constexpr int KS = DK <= 2 ? DK : 1;
+    static constexpr int kBk = G::kBN * 128;   // one k-block of one plane
+    static constexpr int kHT = FOLD ? G::kBN * 32 : 0;
+    static constexpr int kB = (KS * kBk + kHT + 1023) / 1024 * 1024;  // one B stage
     static constexpr int kABytes = AST * RB * PA * DK * kA;
     static constexpr int kBBytes = BST * kB;
-    static constexpr int kHOff = kABytes + kBBytes;          // the -h ring
+    static constexpr int kHOff = kABytes + kBBytes;          // the -h ring (unfolded)
     static constexpr int kOnesOff = kHOff + R::kSlots * R::kSlotBytes;  // folded: BM x 32 bytes
     static constexpr int kBarOff = kOnesOff + (FOLD ? BM * 32 : 0);
     static constexpr int kBars = 2 * AST + 2 * BST + 10 + 2 * R::kSlots;
@@ -242,10 +253,13 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // bf16 operands take -h_j into the MMAs (an exact three-plane split);
     // fp16 planes carry a per-head scale, and their epilogue adds -h_j
     constexpr bool FOLD = BF16;
+    static_assert(PA == 1 || RB == 1, "two row planes take one row block per tile");
     using S = Smem<FOLD, DK, PA, AST, BST, RB>;
     using G = Geo<RB>;
     constexpr int BN = G::kBN, kParts = G::kParts, kSubs = G::kSubs, kRows = G::kRows;
     constexpr int kHS = HRing<FOLD, RB>::kSlots, kHBytes = HRing<FOLD, RB>::kSlotBytes;
+    constexpr int KS = S::KS, kGroups = DK / KS;  // k-blocks per stage, stages per plane
+    constexpr int kHSd = kHS > 0 ? kHS : 1;       // the h ring's size as a divisor
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -375,27 +389,39 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (ti.skip) continue;
                 const int h = ti.bh % p.H;
                 for (int c = 0; c < p.nchunks && ok; c++) {
-                    const int hs = h_it % kHS;
-                    ok = mbar_wait(&h_empty[hs], ((h_it / kHS) & 1) ^ 1, p.status, 11);
-                    if (!ok) break;
-                    mbar_expect_tx(&h_full[hs], kHBytes);
                     const int64_t hrow = (int64_t)h * p.kpad + c * BN;
-                    const void* hsrc = FOLD ? static_cast<const void*>(p.hplanes + hrow * 16)
-                                            : static_cast<const void*>(p.hneg + hrow);
-                    asm volatile(
-                        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], "
-                        "%2, [%3];" ::"r"(su32(smH + hs * kHBytes)),
-                        "l"(hsrc), "r"(kHBytes), "r"(su32(&h_full[hs]))
-                        : "memory");
-                    h_it++;
+                    if constexpr (!FOLD) {
+                        const int hs = h_it % kHSd;
+                        ok = mbar_wait(&h_empty[hs], ((h_it / kHSd) & 1) ^ 1, p.status, 11);
+                        if (!ok) break;
+                        mbar_expect_tx(&h_full[hs], kHBytes);
+                        asm volatile(
+                            "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], "
+                            "[%1], %2, [%3];" ::"r"(su32(smH + hs * kHBytes)),
+                            "l"(p.hneg + hrow), "r"(kHBytes), "r"(su32(&h_full[hs]))
+                            : "memory");
+                        h_it++;
+                    }
                     for (int pl = 0; pl < p.P && ok; pl++)
-                        for (int kb = 0; kb < DK; kb++) {
+                        for (int g = 0; g < kGroups; g++) {
                             const int sb = b_it % BST;
                             ok = mbar_wait(&b_empty[sb], ((b_it / BST) & 1) ^ 1, p.status, 2);
                             if (!ok) break;
-                            mbar_expect_tx(&b_full[sb], S::kB);
-                            tma_3d(smB + sb * S::kB, &tmB, &b_full[sb], kb * BK, c * BN,
-                                   h * p.pstride + pl);
+                            // the chunk's first stage also carries the -h tile
+                            const bool with_h = FOLD && pl == 0 && g == 0;
+                            mbar_expect_tx(&b_full[sb], KS * S::kBk + (with_h ? S::kHT : 0));
+                            uint8_t* stage = smB + sb * S::kB;
+#pragma unroll
+                            for (int k = 0; k < KS; k++)
+                                tma_3d(stage + k * S::kBk, &tmB, &b_full[sb], (g * KS + k) * BK,
+                                       c * BN, h * p.pstride + pl);
+                            if (with_h)
+                                asm volatile(
+                                    "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes "
+                                    "[%0], [%1], %2, [%3];" ::"r"(su32(stage + KS * S::kBk)),
+                                    "l"(p.hplanes + hrow * 16), "r"(S::kHT),
+                                    "r"(su32(&b_full[sb]))
+                                    : "memory");
                             b_it++;
                         }
                 }
@@ -408,8 +434,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
             for (int s = 0; s < kHS; s++)
                 if (h_it > (uint32_t)s) {
-                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % kHS);
-                    mbar_wait(&h_full[last % kHS], (last / kHS) & 1, p.status, 3);
+                    const uint32_t last = h_it - 1 - ((h_it - 1 - s) % kHSd);
+                    mbar_wait(&h_full[last % kHSd], (last / kHSd) & 1, p.status, 3);
                 }
         }
     } else if (warp == 1) {
@@ -452,6 +478,11 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     }
                     if (stored) bulk_commit();
                 }
+                // the row's second plane is needed only when the tile holds a
+                // rotated row (one 128-row block per tile with two planes)
+                const bool lo_needed =
+                    PA == 1 || !p.tile_rot ||
+                    p.tile_rot[(int64_t)ti.bh * p.tiles128 + ti.r0 / BM] != 0;
                 for (int c = 0; c < p.nchunks && ok; c++) {
                     const int acc = acc_it & 1;
                     ok = mbar_wait(&acc_empty[acc], ((acc_it >> 1) & 1) ^ 1, p.status, 5);
@@ -460,47 +491,49 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     uint32_t accumulate[RB];
 #pragma unroll
                     for (int rb = 0; rb < RB; rb++) accumulate[rb] = 0;
-                    if constexpr (FOLD) {
-                        // D = ones x (-h planes)^T starts each accumulator at
-                        // -h_j; the slot is free once these MMAs have read it
-                        const int hs = acc_it % kHS;
-                        ok = mbar_wait(&h_full[hs], (acc_it / kHS) & 1, p.status, 12);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t od = sw32_desc(su32(sm + S::kOnesOff));
-                        const uint64_t hd = sw32_desc(su32(smH + hs * kHBytes));
-#pragma unroll
-                        for (int rb = 0; rb < RB; rb++) {
-                            tc_mma(tmem + (uint32_t)((acc * RB + rb) * BN), od, hd, idesc, 0u);
-                            accumulate[rb] = 1;
-                        }
-                        tc_commit(&h_empty[hs]);
-                    }
                     for (int pl = 0; pl < p.P && ok; pl++)
 #pragma unroll
-                        for (int kb = 0; kb < DK; kb++) {
+                        for (int g = 0; g < kGroups; g++) {
                             const int sb = b_it % BST;
                             ok = mbar_wait(&b_full[sb], (b_it / BST) & 1, p.status, 6);
                             if (!ok) break;
                             tc_fence_after();
-                            // descriptors of the stage's start; the k-steps of 16
-                            // elements are 32 bytes apart, i.e. +2 in the address
-                            // field (no carry: shared addresses are below 2^18)
-                            const uint64_t bd = sw128_desc(su32(smB + sb * S::kB));
+                            uint8_t* stage = smB + sb * S::kB;
+                            if (FOLD && pl == 0 && g == 0) {
+                                // D = ones x (-h planes)^T starts each
+                                // accumulator at -h_j
+                                const uint64_t od = sw32_desc(su32(sm + S::kOnesOff));
+                                const uint64_t hd = sw32_desc(su32(stage + KS * S::kBk));
 #pragma unroll
-                            for (int rb = 0; rb < RB; rb++) {
-                                const uint32_t d_tmem = tmem + (uint32_t)((acc * RB + rb) * BN);
+                                for (int rb = 0; rb < RB; rb++) {
+                                    tc_mma(tmem + (uint32_t)((acc * RB + rb) * BN), od, hd, idesc,
+                                           0u);
+                                    accumulate[rb] = 1;
+                                }
+                            }
 #pragma unroll
-                                for (int pa = 0; pa < PA; pa++) {
-                                    // the row's second plane multiplies chat's
-                                    // first only (the bound counts the rest)
-                                    if (pa > 0 && pl > 0) continue;
-                                    const uint64_t ad = a_desc[rb][pa][kb];
+                            for (int k = 0; k < KS; k++) {
+                                const int kb = g * KS + k;
+                                // descriptors of the k-block's start; the k-steps of
+                                // 16 elements are 32 bytes apart, i.e. +2 in the
+                                // address field (no carry: shared addresses are
+                                // below 2^18)
+                                const uint64_t bd = sw128_desc(su32(stage + k * S::kBk));
 #pragma unroll
-                                    for (int ks = 0; ks < BK / 16; ks++) {
-                                        tc_mma(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
-                                               accumulate[rb]);
-                                        accumulate[rb] = 1;
+                                for (int rb = 0; rb < RB; rb++) {
+                                    const uint32_t d_tmem = tmem + (uint32_t)((acc * RB + rb) * BN);
+#pragma unroll
+                                    for (int pa = 0; pa < PA; pa++) {
+                                        // the row's second plane multiplies chat's
+                                        // first only (the bound counts the rest)
+                                        if (pa > 0 && (pl > 0 || !lo_needed)) continue;
+                                        const uint64_t ad = a_desc[rb][pa][kb];
+#pragma unroll
+                                        for (int ks = 0; ks < BK / 16; ks++) {
+                                            tc_mma(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc,
+                                                   accumulate[rb]);
+                                            accumulate[rb] = 1;
+                                        }
                                     }
                                 }
                             }
@@ -647,8 +680,8 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const float2 gs = __ldg(gst + g0 + i);
                     sg[i] = fmaf(alpha, gs.x, beta * gs.y);
                 }
-                const int hs = acc_it % kHS;
-                ok = (FOLD || mbar_wait(&h_full[hs], (acc_it / kHS) & 1, p.status, 12)) &&
+                const int hs = acc_it % kHSd;
+                ok = (FOLD || mbar_wait(&h_full[hs], (acc_it / kHSd) & 1, p.status, 12)) &&
                      mbar_wait(&acc_full[acc], (acc_it >> 1) & 1, p.status, 8);
                 if (!ok) break;
                 tc_fence_after();
@@ -1011,7 +1044,7 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
                     const int32_t* __restrict__ perm, const int32_t* __restrict__ count,
                     uint16_t* __restrict__ planes, int32_t* __restrict__ row_map,
                     int32_t* __restrict__ ccount, int64_t* __restrict__ exact_list,
-                    int32_t* __restrict__ exact_count) {
+                    int32_t* __restrict__ exact_count, int32_t* __restrict__ tile_rot) {
     const int bh = blockIdx.y;
     const int32_t L = seq_len(len, bh / H, ncap);
     int32_t n;
@@ -1095,6 +1128,7 @@ compact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t
                 exact_list[atomicAdd(exact_count, 1)] = (int64_t)bh * ncap + j;
             } else {
                 row_map[(int64_t)bh * ncap + i] = j | (pos_row == 0 ? kUnrotated : 0);
+                if (pos_row != 0) tile_rot[(int64_t)bh * ((ncap + 127) / 128) + i / 128] = 1;
             }
         }
     }
@@ -1380,18 +1414,19 @@ cudaError_t launch_by_width(const CUtensorMap& ta, const CUtensorMap& tb, const 
             case 64:
                 return rb == 2 ? launch_kernel<BF16, 1, PA, 2, 6, 2>(ta, tb, tk, p, st)
                                : launch_kernel<BF16, 1, PA, 2, 4, 1>(ta, tb, tk, p, st);
-            case 128:
-                return rb == 2 ? launch_kernel<BF16, 2, PA, 2, 4, 2>(ta, tb, tk, p, st)
-                               : launch_kernel<BF16, 2, PA, 2, 4, 1>(ta, tb, tk, p, st);
+            case 128:  // stages of both k-blocks
+                return rb == 2 ? launch_kernel<BF16, 2, PA, 2, 2, 2>(ta, tb, tk, p, st)
+                               : launch_kernel<BF16, 2, PA, 2, 2, 1>(ta, tb, tk, p, st);
             case 192: return launch_kernel<BF16, 3, PA, 1, 4, 1>(ta, tb, tk, p, st);
-            default: return launch_kernel<BF16, 4, PA, 1, 4, 1>(ta, tb, tk, p, st);
+            // bf16 stages carry room for the -h tile: one stage fewer
+            default: return launch_kernel<BF16, 4, PA, 1, BF16 ? 3 : 4, 1>(ta, tb, tk, p, st);
         }
     }
     else {
         switch (p.d) {
-            case 64: return launch_kernel<BF16, 1, PA, 2, 4, 1>(ta, tb, tk, p, st);
-            case 128: return launch_kernel<BF16, 2, PA, 1, 4, 1>(ta, tb, tk, p, st);
-            case 192: return launch_kernel<BF16, 3, PA, 1, 3, 1>(ta, tb, tk, p, st);
+            case 64: return launch_kernel<BF16, 1, PA, 2, BF16 ? 3 : 4, 1>(ta, tb, tk, p, st);
+            case 128: return launch_kernel<BF16, 2, PA, 1, 2, 1>(ta, tb, tk, p, st);
+            case 192: return launch_kernel<BF16, 3, PA, 1, BF16 ? 2 : 3, 1>(ta, tb, tk, p, st);
             default: return launch_kernel<BF16, 4, PA, 1, 2, 1>(ta, tb, tk, p, st);
         }
     }
@@ -1498,6 +1533,8 @@ cudaError_t run_pass(const TcCall& c, const BSide& b, int PA, const void* asrc, 
     p.len = c.len;
     p.count = count;
     p.row_map = row_map;
+    p.tile_rot = PA == 2 && row_map ? c.tile_rot : nullptr;
+    p.tiles128 = (int32_t)((ncap + 127) / 128);
     p.skip = skip;
     p.skip_near = skip_near;
     p.hneg = c.hneg;
@@ -1577,9 +1614,10 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     const bool need_r = natural && rot;
     cudaError_t e;
 
-    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * 3, st);  // count, status, longest list
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(c.head_count, 0, sizeof(int32_t) * H, st);
+    // count, status, longest list, (unused), then the per-head list lengths
+    // and the compact tiles' flags (they follow exact_count in the workspace)
+    e = cudaMemsetAsync(c.exact_count, 0, sizeof(int32_t) * (4 + H + nbh * ((ncap + 127) / 128)),
+                        st);
     if (e != cudaSuccess) return e;
     // the codebook side, unless an earlier call left it in this workspace:
     // chat = c L L^T (c itself when L is the identity), -|c L|^2 / 2 padded,
@@ -1645,12 +1683,12 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
             compact_rows_kernel<kBF16><<<g, 256, 0, st>>>(
                 c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,
                 c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
-                c.exact_count);
+                c.exact_count, c.tile_rot);
         else
             compact_rows_kernel<kF16><<<g, 256, 0, st>>>(
                 c.x, (int32_t)H, (int32_t)ncap, (int32_t)d, c.len, c.ra, c.sel.mode == 2 ? 0 : c.sel.mode,
                 c.sel.perm, c.sel.count, c.compact, c.row_map, c.ccount, c.exact_list,
-                c.exact_count);
+                c.exact_count, c.tile_rot);
         note_launches(1);
         e = run_pass(c, bu, 2, c.compact, nbh * ncap, c.ccount, c.row_map, skip, 0, most, st);
         if (e != cudaSuccess) return e;

@@ -168,8 +168,10 @@ struct TcCall {
     int64_t* exact_list;  // [B*H*Ncap]
     unsigned long long* exact_best;  // [B*H*Ncap] (distance bits, index) of listed rows
     int32_t* exact_done;  // [B*H*Ncap] centroid slices finished per listed row
-    int32_t* exact_count; // [3]: count, status, longest compact list
-    int32_t* head_count;  // [H] listed rows per head (the exact path)
+    int32_t* exact_count; // [4]: count, status, longest compact list, unused
+    int32_t* head_count;  // [H] listed rows per head (the exact path): exact_count + 4
+    int32_t* tile_rot;    // [B*H, ceil(Ncap/128)] nonzero: that 128-row tile of the compact
+                          // list holds a rotated row (head_count + H; zeroed with them)
     // optional, for the pass over the stored keys in natural order (rows
     // outside the RoPE window, far_offset = 0): the cosine of each row with
     // score_q of its (b, h) into scores, and a copy of the row into kcopy

@@ -28,11 +28,12 @@ which gives exactly step 5 on the retrieval rows and step 6 on the others.
 By default (fused=True) steps 3, 4 and 6 are one call on the caller's
 stream, a2ats_rope_split_plain_assign: with far_offset = 0 the keys outside
 the RoPE window are their own k~, so the pass of the tensor-core assignment
-over them also copies them out and scores them for the split.  The call
-records an event once the split is written, and the second stream (after
-the calibration, when it is part of the step) starts the retrieval rule
-there, while the caller's stream finishes the window rows of step 6.  With
-fused=False the second stream runs steps 3-4 itself, beside step 6.
+over them also copies them out and scores them for the split.  The split
+itself runs on the second stream (on a third while the second calibrates),
+beside the window rows of step 6 on the caller's stream; the call records an
+event once it is written, and the second stream starts the retrieval rule
+there.  With fused=False the second stream runs steps 3-4 itself, beside
+step 6.
 
 Steps 1-2 may also run once, ahead of the steps that reuse their L
 (A2ATSStep.calibrate), as the pages do when H is calibrated offline.
@@ -87,6 +88,8 @@ class A2ATSStep:
                    lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K))
         self.side_workspace = torch.empty(side, dtype=torch.uint8, device=dev)
         self.side_stream = torch.cuda.Stream(device=dev)
+        # the split's stream while the second one calibrates
+        self.split_stream = torch.cuda.Stream(device=dev)
         self.calibrated = False
         self._inputs_ready = torch.cuda.Event()
         self._side_done = torch.cuda.Event()
@@ -161,7 +164,8 @@ class A2ATSStep:
             stage("rope_split_bulk", st, a2ats_rope_split_plain_assign, keys, codebook, None,
                   self.fraction, rope=self.rope, lengths=lengths, out=self.k_tilde,
                   perm=self.perm, count=self.count, codes=self.codes, reuse=reuse_codebook,
-                  split_done=self._split_done, workspace=ws)
+                  split_done=self._split_done,
+                  split_stream=self.split_stream if in_step else side, workspace=ws)
             side.wait_event(self._split_done)
         else:
             # second stream: steps 3-4 in one pass over the pre-RoPE cache

@@ -122,10 +122,10 @@ def test_rope_split_plain_assign_validation(lib):
     ws = 1 << 30
 
     def call(keys=FAKE, dt=1, K=256, k_out=FAKE + 4096, codes=FAKE + 8192, rp=rope, frac=0.2,
-             ws_ptr=FAKE, nb=ws, codebook=FAKE + 12288):
+             ws_ptr=FAKE, nb=ws, codebook=FAKE + 12288, split_stream=None):
         return f(keys, dt, 1, 2, 64, 128, None, None, frac,
                  ctypes.byref(rp) if rp is not None else None, codebook, K, k_out, FAKE, FAKE,
-                 codes, 0, None, ws_ptr, nb, None)
+                 codes, 0, None, split_stream, ws_ptr, nb, None)
 
     assert call(rp=None) == -1                 # rope is required
     assert call(k_out=FAKE) == -1              # k_out may not alias keys
@@ -134,6 +134,7 @@ def test_rope_split_plain_assign_validation(lib):
     assert call(frac=-0.1) == -1
     assert call(codes=None) == -1
     assert call(codebook=FAKE + 12290) == -4   # misaligned codebook
+    assert call(split_stream=FAKE) == -1       # a split stream needs split_done
     assert call(ws_ptr=None, nb=0) == -6
     # the workspace holds both the assignment's and the split's
     need = lib.a2ats_rope_split_plain_assign_workspace_size(1, 2, 64, 128, 256)
