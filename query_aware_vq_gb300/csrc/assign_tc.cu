@@ -152,23 +152,22 @@ __device__ __forceinline__ void top2_16(const float* k, float& t1, float& t2) {
 // (plus the absolute fp16 term), which is bounded group by group with the
 // group maxima of |chat_j| and h_j: s_g = alpha max|chat| + beta max h over
 // group g of kTcGroup centroids.  The row carries m1, its best value, at
-// centroid code (group code / kTcGroup); U, an upper bound of the exact value of every other
-// centroid (the largest t1_g + s_g over the other groups, and the second value
-// of the code's own group plus its s); the code is certified when m1 - s still
-// exceeds U, with room for the rounding of the comparison and the absolute
-// term, else the row joins the exact list.
-__device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int h,
-                                           float m1, float U, int32_t code, float xn,
-                                           float coef) {
+// centroid code (group code / kTcGroup) whose group bound is s1; U, an upper
+// bound of the exact value of every other centroid (the largest t1_g + s_g
+// over the other groups, and the second value of the code's own group plus
+// its s); the code is certified when m1 - s1 still exceeds U, with room for
+// the rounding of the comparison and the absolute term (abs_xn: the absolute
+// fp16 term for this row), else the row joins the exact list.  Lb: the
+// sequence length of the row's (b, h).
+__device__ __forceinline__ void decide_row(const Params& p, int32_t bh, int32_t ri, int32_t Lb,
+                                           float m1, float U, int32_t code, float s1,
+                                           float abs_xn) {
     const int32_t j = p.row_map ? (p.row_map[(int64_t)bh * p.seg + ri] & ~kUnrotated) : ri;
-    const int32_t Lb = seq_len(p.len, bh / p.H, p.out_ncap);
     if (j < 0 || j >= Lb) return;
     const int64_t out = (int64_t)bh * p.out_ncap + j;
     if (p.skip && p.skip[out]) return;
-    const float2 g1 = p.gstat[(int64_t)h * p.ngroups + code / kTcGroup];
-    const float e1 = coef * fmaf(xn, g1.x, g1.y);
     const float mag = fmaxf(fabsf(m1), fabsf(U));
-    const float tau = e1 + 2.f * p.head[h * 4 + 3] * xn + 4.f * mag * 1.1920929e-07f;
+    const float tau = s1 + 2.f * abs_xn + 4.f * mag * 1.1920929e-07f;
     if (!(m1 - U > tau)) {
         const int32_t slot = atomicAdd(p.exact_count, 1);
         p.exact_list[slot] = out;
@@ -654,7 +653,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             // and the group's second value are worked out once, after the sweep.
             constexpr int kG = kTcGroup;
             constexpr int kGroupsPerPart = kSubs * 32 / kG;
-            float m1 = -INFINITY, ub1 = -FLT_MAX, ub2 = -FLT_MAX;
+            float m1 = -INFINITY, ub1 = -FLT_MAX, ub2 = -FLT_MAX, s1 = 0.f;
             int32_t c1 = 0, gb1 = -1;
             float best[kG];
             const float xn = sqrtf(nrm) * p.norm_slack;
@@ -667,6 +666,9 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (rm >= 0 && (rm & kUnrotated)) coef = p.err_coef_unrot;
             }
             const float alpha = coef * xn, beta = coef;
+            // per-tile values of the decision, loaded ahead of the sweep
+            const int32_t Lb = seq_len(p.len, ti.bh / p.H, p.out_ncap);
+            const float abs_xn = p.head[h * 4 + 3] * xn;
             const float2* gst = p.gstat + (int64_t)h * p.ngroups;
             const float inv_scale = FOLD ? 1.f : p.head[h * 4 + 2];
             const float2 inv2 = make_float2(inv_scale, inv_scale);
@@ -745,6 +747,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         if (upd) {
                             m1 = t1;
                             c1 = g0 + gi;
+                            s1 = sg[gi];
                         }
                     }
                     if (sub + 1 < kSubs) {
@@ -773,18 +776,17 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 top2_16(key, k1, k2);
                 code = c1 * kG + (kG - 1 - (int32_t)(__float_as_uint(k1) & (kG - 1)));
                 // the second value is within 15 units in the last place of k2
-                const float2 gs = __ldg(gst + c1);
-                w2 = k2 + 16.f * 1.1920929e-07f * fabsf(k2) + fmaf(alpha, gs.x, beta * gs.y);
+                w2 = k2 + 16.f * 1.1920929e-07f * fabsf(k2) + s1;
             }
             if (kParts == 1) {
                 const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn, coef);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, Lb, m1, U, code, s1, abs_xn);
             } else if (part != 0) {
                 // merge the column parts of each row, then decide the row
                 ok = mbar_wait(merge_empty, (m_it & 1) ^ 1, p.status, 9);
                 if (!ok) break;
                 float4* mg = merge + (q * 32 + lane) * 2;
-                mg[0] = make_float4(m1, w2, __int_as_float(code), 0.f);
+                mg[0] = make_float4(m1, w2, __int_as_float(code), s1);
                 mg[1] = make_float4(ub1, ub2, __int_as_float(gb1), 0.f);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(merge_full);
@@ -801,6 +803,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     m1 = o0.x;
                     w2 = o0.y;
                     code = __float_as_int(o0.z);
+                    s1 = o0.w;
                 }
                 if (o1.x > ub1) {
                     ub2 = fmaxf(ub1, o1.y);
@@ -810,7 +813,7 @@ assign_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     ub2 = fmaxf(ub2, o1.x);
                 }
                 const float U = fmaxf(gb1 == code / kTcGroup ? ub2 : ub1, w2);
-                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, h, m1, U, code, xn, coef);
+                if (ri < ti.nvalid) decide_row(p, ti.bh, ri, Lb, m1, U, code, s1, abs_xn);
             }
             m_it++;
         }
