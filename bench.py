@@ -58,11 +58,11 @@ import synth  # noqa: E402
 METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of roofline"
 
 # DRAM bytes (read + write) of one stored-order contraction launch on the
-# default workload, from the ncu capture summarised in
-# profiles/assign_tc_kernel_llama32_3b_layer.md.  It holds only for the
-# contraction source it was taken on (the first 16 hex digits of the sha256 of
-# csrc/assign_tc.cu); for any other source the bench reports null.
-TC_TRAFFIC = {"llama32_3b_layer": ("2ef1434f86dd0e01", 87519744)}
+# default workload, from an ncu capture of this kernel (the summary under
+# profiles/ names the command).  It holds only for the contraction source it
+# was taken on (the first 16 hex digits of the sha256 of csrc/assign_tc.cu);
+# for any other source the bench reports null.
+TC_TRAFFIC = {"llama32_3b_layer": ("71532612ed968e4b", 87690240)}
 DEFAULT_WORKLOAD = "llama32_3b_layer"
 L2_FLUSH_BYTES = 256 << 20
 # the timed region lasts at least this long (untimed replays between the
