@@ -1716,12 +1716,13 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
         auto scan = S == 128 ? exact_scan_kernel<128> : exact_scan_kernel<64>;
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        // chunks of a head's rows run side by side in z: 4 to 8 (the blocks
-        // past a head's last chunk leave at once, and a block takes the
-        // chunks z, z + zc, ... of its head)
+        // chunks of a head's rows run side by side in z: up to 8, about 2048
+        // blocks in all (the blocks past a head's last chunk leave at once,
+        // and a block takes the chunks z, z + zc, ... of its head, staging
+        // its slice once)
         const int64_t slices = (K + S - 1) / S;
         int64_t zc = 2048 / (slices * H);
-        zc = zc < 4 ? 4 : (zc > 8 ? 8 : zc);
+        zc = zc < 1 ? 1 : (zc > 8 ? 8 : zc);
         dim3 g((unsigned)slices, (unsigned)H, (unsigned)zc);
         scan<<<g, kExactThreads, smem, st>>>((int32_t)d, c.cp, K, c.head_count, head_rows, head_cap,
                                              zbuf, c.exact_best, c.exact_done, c.exact_list,
