@@ -1238,15 +1238,96 @@ exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
     }
 }
 
-constexpr int kScanRows = 16;  // rows of a head per chunk: two per warp
+// Rows of a warp per chunk of a head's rows for long lists: eight with
+// 128-centroid slices, four with 64 (d > 128), so the staged rows stay near
+// 32 KB; a head whose list fits the grid's chunk groups in chunks of two rows
+// per warp takes those, for more blocks at work.
+template <int S> struct ScanTile { static constexpr int kRT = S == 128 ? 8 : 4; };
+
+// One warp's rows r0 .. r0 + nr - 1 of head list `rows` against the staged
+// slice (see exact_scan_kernel): z staged transposed in zT, then per pair of
+// centroids (l + 64 m, l + 64 m + 32) packed differences and squares.
+template <int S, int RT>
+__device__ __forceinline__ void scan_rows(const float* cT, float* zT, int d, int nc, int64_t j0,
+                                          const int32_t* rows, int r0, int nr, const float* zbuf,
+                                          unsigned long long* best, int32_t* done,
+                                          const int64_t* list, int32_t* codes, int lane) {
+    constexpr int CT = S / 32;
+    // z of the warp's rows, transposed (a missing row repeats the first)
+    for (int i = lane; i < RT * d; i += 32) {
+        const int r = i / d, a = i - r * d;
+        const int64_t e = rows[r0 + (r < nr ? r : 0)];
+        zT[a * RT + r] = __ldg(zbuf + e * d + a);
+    }
+    __syncwarp();
+    // acc[r][m]: distances of row r to l + 64 m and l + 64 m + 32
+    float2 acc[RT][CT / 2];
+#pragma unroll
+    for (int r = 0; r < RT; r++)
+#pragma unroll
+        for (int m = 0; m < CT / 2; m++) acc[r][m] = make_float2(0.f, 0.f);
+    const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll 2
+    for (int a = 0; a < d; a++) {
+        const float* col = cT + a * (S + 1) + lane;
+        float2 cv[CT / 2];
+#pragma unroll
+        for (int m = 0; m < CT / 2; m++) cv[m] = make_float2(col[64 * m], col[64 * m + 32]);
+        const float2* z2 = reinterpret_cast<const float2*>(zT + a * RT);
+#pragma unroll
+        for (int q = 0; q < RT / 2; q++) {
+            const float2 zq = z2[q];
+#pragma unroll
+            for (int u = 0; u < 2; u++) {
+                const float zr = u ? zq.y : zq.x;
+                const float2 za = make_float2(zr, zr);
+#pragma unroll
+                for (int m = 0; m < CT / 2; m++) {
+                    const float2 t = __ffma2_rn(cv[m], neg1, za);  // za - c, exact negation
+                    acc[2 * q + u][m] = __ffma2_rn(t, t, acc[2 * q + u][m]);
+                }
+            }
+        }
+    }
+    __syncwarp();  // zT is rewritten by the warp's next rows
+#pragma unroll
+    for (int r = 0; r < RT; r++) {
+        if (r >= nr) break;
+        const int64_t e = rows[r0 + r];
+        float bv = INFINITY;
+        int32_t bj = 0;
+#pragma unroll
+        for (int k = 0; k < CT; k++) {  // ascending j: strict < keeps the lowest
+            const float v = (k & 1) ? acc[r][k >> 1].y : acc[r][k >> 1].x;
+            const int c = lane + 32 * k;
+            if (c < nc && v < bv) {
+                bv = v;
+                bj = (int32_t)(j0 + c);
+            }
+        }
+        for (int m = 16; m; m >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
+            const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
+            if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
+        }
+        if (lane == 0) {
+            if (bv < INFINITY)
+                atomicMin(best + e, ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
+            __threadfence();
+            if (atomicAdd(done + e, 1) == (int)gridDim.x - 1)
+                codes[list[e]] = (int32_t)(uint32_t)(atomicOr(best + e, 0ull) & 0xffffffffull);
+        }
+    }
+}
 
 // The slice [j0, j0 + S) of head h's cp is staged transposed, cT[a][c] with a
 // padded stride S + 1 (few bank conflicts when it is written along a, none
-// when lanes read along c).  Each warp takes two rows of the chunk at a time
-// (rows w and w + 8), so every centroid value read from shared memory serves
-// both; lane l owns centroids l, l + 32, ... of the slice, in pairs
-// (l + 64 m, l + 64 m + 32) whose differences and squares run as packed
-// two-float instructions (each rounded as the scalar one).  The row's code is
+// when lanes read along c).  Each warp takes a few rows of the chunk at a
+// time, their z staged transposed (zT[a][r]: one vector load gives two rows'
+// element a to every lane), and lane l owns centroids l, l + 32, ... of the
+// slice, in pairs whose differences and squares run as packed two-float
+// instructions (each rounded as the scalar one); every centroid value read
+// from shared memory serves all of the warp's rows.  The row's code is
 // written by the slice block that adds the last of the gridDim.x partial
 // minima (a counter per row).
 template <int S>
@@ -1258,12 +1339,15 @@ exact_scan_kernel(int32_t d, const float* __restrict__ cp, int64_t K,
                   const int64_t* __restrict__ list, int32_t* __restrict__ codes) {
     static_assert(S % 64 == 0, "centroids come in pairs of lanes' columns");
     constexpr int kWarps = kExactThreads / 32;
-    static_assert(kScanRows == 2 * kWarps, "two rows per warp");
-    extern __shared__ float cT[];  // [d][S + 1], then [warps][2][d] for the rows' z
+    constexpr int RT = ScanTile<S>::kRT;
+    extern __shared__ float cT[];  // [d][S + 1], then [warps][d][RT] for the rows' z
     const int h = blockIdx.y;
     const int64_t j0 = (int64_t)blockIdx.x * S;
     const int n = head_count[h];
-    const int nchunks = (n + kScanRows - 1) / kScanRows;
+    // chunks of two rows per warp when they fit the chunk groups once
+    const bool narrow = n <= 2 * kWarps * (int)gridDim.z;
+    const int kChunk = kWarps * (narrow ? 2 : RT);
+    const int nchunks = (n + kChunk - 1) / kChunk;
     if ((int)blockIdx.z >= nchunks || j0 >= K) return;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nc = (int)(K - j0 < S ? K - j0 : S);
@@ -1293,70 +1377,16 @@ exact_scan_kernel(int32_t d, const float* __restrict__ cp, int64_t K,
     }
     __syncthreads();
     const int32_t* rows = head_rows + (int64_t)h * head_cap;
-    float* zs0 = cT + d * (S + 1) + 2 * w * d;  // this warp's two rows, staged once
-    float* zs1 = zs0 + d;
-    const float2 neg1 = make_float2(-1.f, -1.f);
+    float* zT = cT + d * (S + 1) + w * d * RT;  // this warp's rows, [a][r]
     for (int chunk = blockIdx.z; chunk < nchunks; chunk += gridDim.z) {
-        const int r_end = min(n, (chunk + 1) * kScanRows);
-        const int r0 = chunk * kScanRows + w, r1 = r0 + kWarps;
-        if (r0 >= r_end) continue;
-        const bool two = r1 < r_end;
-        const int64_t e0 = rows[r0];
-        const int64_t e1 = two ? rows[r1] : e0;
-        for (int a = lane; a < d; a += 32) {
-            zs0[a] = __ldg(zbuf + e0 * d + a);
-            zs1[a] = __ldg(zbuf + e1 * d + a);
-        }
-        __syncwarp();
-        // acc[r][m] = distances of row r to l + 64 m and l + 64 m + 32
-        float2 acc0[S / 64], acc1[S / 64];
-#pragma unroll
-        for (int m = 0; m < S / 64; m++) acc0[m] = acc1[m] = make_float2(0.f, 0.f);
-#pragma unroll 4
-        for (int a = 0; a < d; a++) {
-            const float2 za0 = make_float2(zs0[a], zs0[a]);
-            const float2 za1 = make_float2(zs1[a], zs1[a]);
-            const float* col = cT + a * (S + 1) + lane;
-#pragma unroll
-            for (int m = 0; m < S / 64; m++) {
-                const float2 cv = make_float2(col[64 * m], col[64 * m + 32]);
-                const float2 t0 = __ffma2_rn(cv, neg1, za0);  // za - c, exact negation
-                const float2 t1 = __ffma2_rn(cv, neg1, za1);
-                acc0[m] = __ffma2_rn(t0, t0, acc0[m]);
-                acc1[m] = __ffma2_rn(t1, t1, acc1[m]);
-            }
-        }
-        __syncwarp();  // zs is rewritten by the warp's next rows
-#pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-            if (rr == 1 && !two) break;
-            const float2* acc = rr == 0 ? acc0 : acc1;
-            const int64_t e = rr == 0 ? e0 : e1;
-            float bv = INFINITY;
-            int32_t bj = 0;
-#pragma unroll
-            for (int k = 0; k < S / 32; k++) {  // ascending j: strict < keeps the lowest
-                const float v = (k & 1) ? acc[k >> 1].y : acc[k >> 1].x;
-                const int c = lane + 32 * k;
-                if (c < nc && v < bv) {
-                    bv = v;
-                    bj = (int32_t)(j0 + c);
-                }
-            }
-            for (int m = 16; m; m >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
-                const int32_t oj = __shfl_xor_sync(0xffffffffu, bj, m);
-                if (ov < bv || (ov == bv && oj < bj)) { bv = ov; bj = oj; }
-            }
-            if (lane == 0) {
-                if (bv < INFINITY)
-                    atomicMin(best + e,
-                              ((unsigned long long)__float_as_uint(bv) << 32) | (uint32_t)bj);
-                __threadfence();
-                if (atomicAdd(done + e, 1) == (int)gridDim.x - 1)
-                    codes[list[e]] = (int32_t)(uint32_t)(atomicOr(best + e, 0ull) & 0xffffffffull);
-            }
-        }
+        const int rt = narrow ? 2 : RT;
+        const int r0 = chunk * kChunk + w * rt;
+        const int nr = min(rt, n - r0);  // the warp's rows in this chunk
+        if (nr <= 0) continue;
+        if (narrow)
+            scan_rows<S, 2>(cT, zT, d, nc, j0, rows, r0, nr, zbuf, best, done, list, codes, lane);
+        else
+            scan_rows<S, RT>(cT, zT, d, nc, j0, rows, r0, nr, zbuf, best, done, list, codes, lane);
     }
 }
 
@@ -1712,7 +1742,8 @@ cudaError_t launch_assign_tc(const TcCall& c, cudaStream_t st) {
     {
         // slices of 128 centroids (64 at d > 128) keep the staged slice near 66 KB
         const int S = d <= 128 ? 128 : 64;
-        const size_t smem = sizeof(float) * (size_t)d * (S + 1 + 2 * (kExactThreads / 32));
+        const int RT = S == 128 ? ScanTile<128>::kRT : ScanTile<64>::kRT;
+        const size_t smem = sizeof(float) * (size_t)d * (S + 1 + RT * (kExactThreads / 32));
         auto scan = S == 128 ? exact_scan_kernel<128> : exact_scan_kernel<64>;
         e = cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
