@@ -1164,7 +1164,6 @@ __global__ void mark_rows_kernel(int32_t H, int32_t ncap, const int32_t* __restr
 //                       slices, so ties go to the lowest index, and the
 //                       slice that finishes a row last writes its code
 constexpr int kExactThreads = 256;
-constexpr int kScanCents = 128;  // centroids per scan block (8 warps x 16)
 
 template <int DT>
 __global__ void __launch_bounds__(kExactThreads)

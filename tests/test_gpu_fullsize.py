@@ -1,11 +1,12 @@
 """GPU parity at the full sizes of the long-context and wide-head workloads,
 in the launch configuration the benchmark uses (one A2ATSStep over the whole
-batch), checked on sampled outputs the oracle computes one by one: H and L of
-sampled heads, the whole retrieval split of sampled (sequence, head) pairs,
-the codes of sampled retrieval and bulk rows, and the rotated keys: every
-RoPE-window row of every (sequence, head) in the storage format, and rows at
-the highest positions (up to 131071) rotated exactly in fp32 (deploy-preview
-page "A2ATS-adapted", "Windowed RoPE (Eq. 11-12)")."""
+batch), checked on outputs the oracle computes one by one: the whole
+retrieval split of every (sequence, head) and the codes of a few of its
+retrieval and bulk rows; H and L of sampled heads and the codes of many
+rows of sampled pairs; and the rotated keys: every RoPE-window row of every
+(sequence, head) in the storage format, and rows at the highest positions
+(up to 131071) rotated exactly in fp32 (deploy-preview page "A2ATS-adapted",
+"Windowed RoPE (Eq. 11-12)")."""
 import numpy as np
 import pytest
 import torch
@@ -24,7 +25,7 @@ def _rel(a, b):
     return np.linalg.norm(a - b) / np.linalg.norm(b)
 
 
-def _run(name, pairs, n_ret, n_bulk, h_tol):
+def _run(name, pairs, n_ret, n_bulk, h_tol, every=(16, 16)):
     w = synth.WORKLOADS[name]
     k, c = synth.keys(w), synth.codebook(w)
     Q = synth.queries(w) if not w.h_given else None
@@ -51,6 +52,29 @@ def _run(name, pairs, n_ret, n_bulk, h_tol):
             assert_storage_close(kt_win[b, h], want, synth.DTYPES[w.dtype])
     far = np.sort(rng.choice(n - w.W, 512, replace=False))
     assert torch.equal(step.k_tilde[:, :, far].cpu(), k[:, :, far])
+    # every (b, h): the whole retrieval split, and the codes of a few
+    # retrieval and bulk rows (H and L of the head as the sampled pairs below
+    # check them against the oracle)
+    Lh = {}
+    for h in range(w.H):
+        hm = (oracle.query_second_moment(Q[h], w.ridge).astype(np.float32).astype(np.float64)
+              if Q is not None else f64(Hg[h]))
+        Lo, info = oracle.cholesky(hm)
+        assert info == 0
+        Lh[h] = Lo.astype(np.float32).astype(np.float64)
+    n_r, n_b = every
+    for b in range(w.B):
+        for h in range(w.H):
+            v = oracle.windowed_rope(k[b, h], np.arange(n), n - 1, w.W, w.far_offset, w.rope_base)
+            _, cnt, scores, kth = oracle.select_retrieval_set(v, v[-1], w.fraction)
+            check_split(perm[b, h], int(count[b, h]), n, cnt, scores, kth)
+            ret, bulk = perm[b, h, :cnt], perm[b, h, cnt:n]
+            ret = np.sort(rng.choice(ret, min(n_r, len(ret)), replace=False))
+            bulk = np.sort(rng.choice(bulk, min(n_b, len(bulk)), replace=False))
+            code, d1, d2 = oracle.assign_cholesky(v[ret], c[h], Lh[h])
+            check_codes(codes[b, h, ret], code, (d2 - d1) / d2, "retrieval codes")
+            code, d1, d2 = oracle.assign_cholesky(v[bulk], c[h], None)
+            check_codes(codes[b, h, bulk], code, (d2 - d1) / d2, "bulk codes")
     for b, h in pairs:
         # calibration of this head, by the oracle, rounded to fp32 where the
         # pages' functions return float32 arrays
