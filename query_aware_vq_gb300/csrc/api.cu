@@ -314,7 +314,7 @@ int a2ats_append_rows(void* cache, int32_t dtype, int64_t B, int64_t H, int64_t 
 size_t a2ats_query_second_moment_workspace_size(int64_t H, int64_t M, int64_t d) {
     if (H < 0 || M < 1 || d < 1) return 0;
     Carve c(nullptr);
-    c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
+    c.take<float>((size_t)(2 * second_moment_splits(M, H) * H * d * d));
     c.take<int32_t>(4);
     return c.used + 256;
 }
@@ -332,7 +332,7 @@ int a2ats_query_second_moment(const void* queries, int32_t dtype, int64_t H, int
     if (!workspace || workspace_bytes < a2ats_query_second_moment_workspace_size(H, M, d))
         return A2ATS_ERR_WORKSPACE;
     Carve c(workspace);
-    float* partial = c.take<float>((size_t)(2 * second_moment_splits(M) * H * d * d));
+    float* partial = c.take<float>((size_t)(2 * second_moment_splits(M, H) * H * d * d));
     int32_t* status = c.take<int32_t>(4);
     cudaError_t e = launch_second_moment(queries, dtype, H, M, d, ridge, partial, status, h_out,
                                          (cudaStream_t)stream);

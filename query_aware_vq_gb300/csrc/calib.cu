@@ -420,17 +420,23 @@ __global__ void centroid_norm_kernel(const void* __restrict__ c, int64_t HK, int
 
 }  // namespace
 
-int64_t second_moment_splits(int64_t M) {
+// Slices of the M queries per head: about 256 queries each, at most 64;
+// halved while the grid would need more than one wave of three CTAs per SM
+// (about 448) and a slice stays within 2048 queries (the tensor-core
+// kernel's four accumulators of 512).
+int64_t second_moment_splits(int64_t M, int64_t H) {
     int64_t s = M / 256;
-    return s < 1 ? 1 : (s > 64 ? 64 : s);
+    s = s < 1 ? 1 : (s > 64 ? 64 : s);
+    while (s > 1 && s * H > 448 && (M + s / 2 - 1) / (s / 2) <= 2048) s /= 2;
+    return s;
 }
 
 cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, int64_t d,
                                  double ridge, float* partial, int32_t* status, float* h_out,
                                  cudaStream_t st) {
-    const int64_t splits = second_moment_splits(M);
+    const int64_t splits = second_moment_splits(M, H);
     cudaError_t e = cudaSuccess;
-    if (second_moment_tc_supported(dt, M, d)) {
+    if (second_moment_tc_supported(dt, H, M, d)) {
         e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
         if (e != cudaSuccess) return e;
         e = launch_second_moment_tc(q, dt, H, M, partial, status, st);

@@ -174,9 +174,9 @@ second_moment_tc_kernel(const uint16_t* __restrict__ q, int64_t M, int64_t split
 
 }  // namespace
 
-bool second_moment_tc_supported(int dt, int64_t M, int64_t d) {
+bool second_moment_tc_supported(int dt, int64_t H, int64_t M, int64_t d) {
     if ((dt != kBF16 && dt != kF16) || d != kQd || M < 1) return false;
-    const int64_t splits = second_moment_splits(M);
+    const int64_t splits = second_moment_splits(M, H);
     const int64_t rows = (M + splits - 1) / splits;
     const int64_t tiles = (rows + kQt - 1) / kQt;
     return (tiles + kNacc - 1) / kNacc * kQt <= kMaxAccRows;
@@ -184,7 +184,7 @@ bool second_moment_tc_supported(int dt, int64_t M, int64_t d) {
 
 cudaError_t launch_second_moment_tc(const void* q, int dt, int64_t H, int64_t M, float* partial,
                                     int32_t* status, cudaStream_t st) {
-    const int64_t splits = second_moment_splits(M);
+    const int64_t splits = second_moment_splits(M, H);
     auto k = dt == kBF16 ? second_moment_tc_kernel<true> : second_moment_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
     if (e != cudaSuccess) return e;

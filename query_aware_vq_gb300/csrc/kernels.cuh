@@ -77,7 +77,7 @@ cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* le
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st);
 
 // calib.cu ---------------------------------------------------------------
-int64_t second_moment_splits(int64_t M);
+int64_t second_moment_splits(int64_t M, int64_t H);
 // partial: [2][splits][H][d][d] (hi and lo planes); status: an int32 the
 // tensor-core kernel sets on a timed-out wait (zeroed here first).
 cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, int64_t d,
@@ -86,7 +86,7 @@ cudaError_t launch_second_moment(const void* q, int dt, int64_t H, int64_t M, in
 // calib_tc.cu: the slices' partial sums on the tensor cores (16-bit queries,
 // d = 128, slices short enough for fp32 accumulators); the same partial
 // layout as the SIMT kernel.
-bool second_moment_tc_supported(int dt, int64_t M, int64_t d);
+bool second_moment_tc_supported(int dt, int64_t H, int64_t M, int64_t d);
 cudaError_t launch_second_moment_tc(const void* q, int dt, int64_t H, int64_t M, float* partial,
                                     int32_t* status, cudaStream_t st);
 
