@@ -18,9 +18,11 @@
 //   warp 10    TMA producer of the key tiles (kept for all centroids), a tile
 //              ahead: 256 rows as two 128-row blocks at d <= 128 with one
 //              operand plane, else 128 rows;
-//   warp 0     TMA producer of the codebook, in stages of 64 elements by the
-//              accumulator width (128 centroids with two row blocks, else
-//              256), and of -|c'|^2/2 per chunk into a small ring;
+//   warp 0     TMA producer of the codebook by the accumulator width (128
+//              centroids with two row blocks, else 256): a stage holds both
+//              64-element k-blocks of a plane up to d = 128 (one k-block
+//              above), and a chunk's first stage also the bf16 planes of
+//              -|c'|^2/2 (fp16: a ring of its own, read by the epilogue);
 //   warp 1     TMEM allocation and tcgen05.mma issue (M = 128 per row
 //              block, bf16/fp16 -> fp32) into two accumulators per row block
 //              (the 512 TMEM columns), so the epilogue of one centroid chunk
@@ -1237,11 +1239,12 @@ exact_rows_kernel(const void* __restrict__ x, int32_t H, int32_t ncap, int32_t d
     }
 }
 
-// Rows of a warp per chunk of a head's rows for long lists: eight with
-// 128-centroid slices, four with 64 (d > 128), so the staged rows stay near
-// 32 KB; a head whose list fits the grid's chunk groups in chunks of two rows
-// per warp takes those, for more blocks at work.
-template <int S> struct ScanTile { static constexpr int kRT = S == 128 ? 8 : 4; };
+// Rows of a warp per chunk of a head's rows for long lists: four with the
+// 64-centroid slices of d > 128 (an LDS serves four rows); two with
+// 128-centroid slices, where more rows would cost a block per SM (eight were
+// slower on the long-context workload); a head whose list fits the grid's
+// chunk groups in chunks of two rows per warp takes those.
+template <int S> struct ScanTile { static constexpr int kRT = S == 128 ? 2 : 4; };
 
 // One warp's rows r0 .. r0 + nr - 1 of head list `rows` against the staged
 // slice (see exact_scan_kernel): z staged transposed in zT, then per pair of
@@ -1266,7 +1269,8 @@ __device__ __forceinline__ void scan_rows(const float* cT, float* zT, int d, int
 #pragma unroll
         for (int m = 0; m < CT / 2; m++) acc[r][m] = make_float2(0.f, 0.f);
     const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll 2
+    constexpr int kUnroll = RT <= 2 ? 4 : 2;  // registers of the row tile
+#pragma unroll kUnroll
     for (int a = 0; a < d; a++) {
         const float* col = cT + a * (S + 1) + lane;
         float2 cv[CT / 2];

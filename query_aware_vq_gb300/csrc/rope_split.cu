@@ -538,13 +538,14 @@ __device__ __forceinline__ int block_scan(int v, int& excl, int* warp_tot) {
 // Exact top-n_r per (b, h) by radix select on order-preserving keys of the
 // scores, ties on the threshold broken by lower index, then a stable
 // two-sided compaction: retrieval rows ascending, then bulk rows ascending.
-// One cluster of kSelCluster CTAs per (b, h): each CTA owns a contiguous
+// One cluster of kCl CTAs per (b, h) (kSelCluster, or half of it when many
+// (b, h) fill the GPU): each CTA owns a contiguous
 // segment of the row (its keys cached in shared memory when they fit); the
 // per-pass histograms and the compaction offsets are combined through
 // distributed shared memory.  In the compaction each thread owns a contiguous
 // run of the segment, so two block scans place every row.
-template <int kSelThreads>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+template <int kSelThreads, int kCl>
+__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kSelThreads)
 select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
               const int32_t* __restrict__ len, double fraction, int32_t* __restrict__ perm,
               int32_t* __restrict__ count) {
@@ -563,7 +564,7 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     __shared__ int warp_tot[65];
     __shared__ uint32_t sel_prefix, sel_need, sel_all;
     const int rank = (int)cluster.block_rank();
-    const int bh = blockIdx.x / kSelCluster;
+    const int bh = blockIdx.x / kCl;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int32_t n = seq_len(len, bh / H, ncap);
     const float* s = scores + (int64_t)bh * ncap;
@@ -571,11 +572,11 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     const double kd = ceil(fraction * (double)n);
     const int32_t k = kd < 0.0 ? 0 : (kd > (double)n ? n : (int32_t)kd);
     if (rank == 0 && tid == 0) count[bh] = k;
-    const int32_t seg = (n + kSelCluster - 1) / kSelCluster;
+    const int32_t seg = (n + kCl - 1) / kCl;
     const int32_t lo = min(n, rank * seg), hi = min(n, lo + seg);
     const int32_t m = hi - lo;
     // the launch gives ks room for a segment of the capacity when that fits
-    const bool cached = (ncap + kSelCluster - 1) / kSelCluster <= kSelCache;
+    const bool cached = (ncap + kCl - 1) / kCl <= kSelCache;
     const bool partial = k > 0 && k < n;
     // key i of the segment sits at ks[i + i / 32], so the contiguous runs of
     // the compaction (thread t reads t * per + e) fall on distinct banks
@@ -607,12 +608,12 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
             cluster.sync();
             // every CTA sums the cluster's histograms and takes the same digit
             if (tid < 256) {
-                uint32_t part[kSelCluster];
+                uint32_t part[kCl];
 #pragma unroll
-                for (int r = 0; r < kSelCluster; r++) part[r] = cluster.map_shared_rank(hb, r)[tid];
+                for (int r = 0; r < kCl; r++) part[r] = cluster.map_shared_rank(hb, r)[tid];
                 uint32_t t = 0;
 #pragma unroll
-                for (int r = 0; r < kSelCluster; r++) t += part[r];
+                for (int r = 0; r < kCl; r++) t += part[r];
                 tot[tid] = t;
             }
             __syncthreads();
@@ -680,15 +681,15 @@ select_kernel(const float* __restrict__ scores, int32_t H, int32_t ncap,
     cluster.sync();
     int gt_before = 0, eq_before = 0;
     {
-        int g[kSelCluster], q[kSelCluster];
+        int g[kCl], q[kCl];
 #pragma unroll
-        for (int r = 0; r < kSelCluster; r++) {
+        for (int r = 0; r < kCl; r++) {
             const int* other = cluster.map_shared_rank(seg_counts, r);
             g[r] = r < rank ? other[0] : 0;
             q[r] = r < rank ? other[1] : 0;
         }
 #pragma unroll
-        for (int r = 0; r < kSelCluster; r++) {
+        for (int r = 0; r < kCl; r++) {
             gt_before += g[r];
             eq_before += q[r];
         }
@@ -1038,31 +1039,31 @@ cudaError_t launch_select(const float* scores, const Shape& s, const int32_t* le
                           double fraction, int32_t* perm, int32_t* count, cudaStream_t st) {
     const int nbh = (int)(s.B * s.H);
     if (nbh == 0) return cudaSuccess;
-    const int64_t seg = (s.Ncap + kSelCluster - 1) / kSelCluster;
-    const size_t smem = seg <= kSelCache ? sizeof(uint32_t) * (size_t)(seg + seg / 32 + 1) : 0;
-    const int cache_bytes = (int)(sizeof(uint32_t) * (kSelCache + kSelCache / 32 + 1));
-    cudaError_t e = cudaFuncSetAttribute(select_kernel<512>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, cache_bytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(select_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 cache_bytes);
-    if (e != cudaSuccess) return e;
-    // 512 threads per CTA for a few (b, h); with many (a decode batch, more
-    // clusters than about four CTAs per SM), 256, so more CTAs are resident
-    // and the chain of barriers of each runs in fewer waves
+    // 512 threads and clusters of kSelCluster CTAs for a few (b, h); with
+    // many (a decode batch, more clusters than about four CTAs per SM), 256
+    // threads and half the cluster, so fewer CTAs run the same chain of
+    // barriers
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool few = (int64_t)nbh * kSelCluster <= 4 * (int64_t)sms;
+    const int cl = few ? kSelCluster : kSelCluster / 2;
+    const int64_t seg = (s.Ncap + cl - 1) / cl;
+    const size_t smem = seg <= kSelCache ? sizeof(uint32_t) * (size_t)(seg + seg / 32 + 1) : 0;
+    const int cache_bytes = (int)(sizeof(uint32_t) * (kSelCache + kSelCache / 32 + 1));
+    cudaError_t e = cudaFuncSetAttribute(select_kernel<512, kSelCluster>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, cache_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(select_kernel<256, kSelCluster / 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, cache_bytes);
+    if (e != cudaSuccess) return e;
     if (few)
-        select_kernel<512><<<nbh * kSelCluster, 512, smem, st>>>(scores, (int32_t)s.H,
-                                                                 (int32_t)s.Ncap, len, fraction,
-                                                                 perm, count);
+        select_kernel<512, kSelCluster><<<nbh * kSelCluster, 512, smem, st>>>(
+            scores, (int32_t)s.H, (int32_t)s.Ncap, len, fraction, perm, count);
     else
-        select_kernel<256><<<nbh * kSelCluster, 256, smem, st>>>(scores, (int32_t)s.H,
-                                                                 (int32_t)s.Ncap, len, fraction,
-                                                                 perm, count);
-                                               note_launches(1);
+        select_kernel<256, kSelCluster / 2><<<nbh * (kSelCluster / 2), 256, smem, st>>>(
+            scores, (int32_t)s.H, (int32_t)s.Ncap, len, fraction, perm, count);
+    note_launches(1);
     return cudaGetLastError();
 }
 
