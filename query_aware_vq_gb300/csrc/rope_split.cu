@@ -199,6 +199,87 @@ cosine_score_bh_kernel(const void* __restrict__ keys, int32_t H, int32_t ncap, i
         qv1[4] = b1.x; qv1[5] = b1.y; qv1[6] = b1.z; qv1[7] = b1.w;
     }
     const float qn = qnorm[bh];
+    // Blocks whose rows are all far, with no far rotation (the keys as they
+    // are): four rows per thread per step, every row's loads issued before
+    // the first is used and 16-bit keys kept packed until then, so that
+    // enough bytes are in flight to cover the memory latency.
+    const bool plain = DT != kF32 && !far_rot &&
+                       !(ra.enabled && ra.window > 0 && (L - 1 - (jend - 1)) < ra.window);
+    if constexpr (DT != kF32) {
+        if (plain) {
+            constexpr int RPT = 4;
+            for (int32_t jb = jbeg; jb < jend; jb += RPT * rpb) {
+                int32_t jr[RPT];
+                bool valid[RPT];
+                uint4 raw0[RPT], raw1[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; u++) {
+                    jr[u] = jb + rl + u * rpb;
+                    valid[u] = jr[u] < jend;
+                    if (valid[u]) {
+                        const typename Elem<DT>::T* kr =
+                            reinterpret_cast<const typename Elem<DT>::T*>(keys) + (bh * ncap + jr[u]) * d;
+                        raw0[u] = *reinterpret_cast<const uint4*>(kr + e0);
+                        raw1[u] = *reinterpret_cast<const uint4*>(kr + e1);
+                    }
+                }
+                float dot[RPT], nn[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; u++) {
+                    dot[u] = 0.f;
+                    nn[u] = 0.f;
+                    if (!valid[u]) continue;
+                    if constexpr (OUT >= 0) {
+                        // the copy is the key itself (converted when OUT differs)
+                        const int64_t row = bh * ncap + jr[u];
+                        if constexpr (OUT == DT) {
+                            typename Elem<DT>::T* ko = reinterpret_cast<typename Elem<DT>::T*>(kout) + row * d;
+                            *reinterpret_cast<uint4*>(ko + e0) = raw0[u];
+                            *reinterpret_cast<uint4*>(ko + e1) = raw1[u];
+                        } else {
+                            float v[8];
+                            const typename Elem<DT>::T* a = reinterpret_cast<const typename Elem<DT>::T*>(&raw0[u]);
+#pragma unroll
+                            for (int k = 0; k < 8; k++) v[k] = to_f32<DT>(a[k]);
+                            store8<OUT>(kout, row * d + e0, v);
+                            const typename Elem<DT>::T* b = reinterpret_cast<const typename Elem<DT>::T*>(&raw1[u]);
+#pragma unroll
+                            for (int k = 0; k < 8; k++) v[k] = to_f32<DT>(b[k]);
+                            store8<OUT>(kout, row * d + e1, v);
+                        }
+                    }
+                    const typename Elem<DT>::T* a = reinterpret_cast<const typename Elem<DT>::T*>(&raw0[u]);
+                    const typename Elem<DT>::T* b = reinterpret_cast<const typename Elem<DT>::T*>(&raw1[u]);
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const float x = to_f32<DT>(a[k]);
+                        dot[u] = fmaf(x, qv0[k], dot[u]);
+                        nn[u] = fmaf(x, x, nn[u]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const float x = to_f32<DT>(b[k]);
+                        dot[u] = fmaf(x, qv1[k], dot[u]);
+                        nn[u] = fmaf(x, x, nn[u]);
+                    }
+                }
+                for (int m = lpr >> 1; m; m >>= 1) {
+#pragma unroll
+                    for (int u = 0; u < RPT; u++) {
+                        dot[u] += __shfl_xor_sync(0xffffffffu, dot[u], m);
+                        nn[u] += __shfl_xor_sync(0xffffffffu, nn[u], m);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < RPT; u++)
+                    if (valid[u] && lane == 0) {
+                        const float kn = sqrtf(nn[u]);
+                        scores[bh * ncap + jr[u]] = (kn > 0.f && qn > 0.f) ? dot[u] / (kn * qn) : 0.f;
+                    }
+            }
+            return;
+        }
+    }
     // the loop bounds are uniform over the warp (the shuffles take it whole)
     for (int32_t jb = jbeg; jb < jend; jb += 2 * rpb) {
         int32_t jr[2] = {jb + rl, jb + rl + rpb};
