@@ -80,10 +80,11 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--path", choices=["step", "hweighted", "attention", "dequantize",
-                                       "subvector", "calibrate"],
+                                       "subvector", "calibrate", "rope"],
                    default="step",
                    help="hweighted: time the H-weighted rule over every key of the cache "
                         "(L from the workload's calibration, windowed RoPE fused); "
+                        "rope: time the windowed RoPE of the whole cache on its own; "
                         "attention: time the code-based attention scores and top tokens; "
                         "dequantize: time the reconstruction of the keys from their codes "
                         "(both steps after the path); calibrate: time one layer's codebook "
@@ -866,6 +867,81 @@ def run_dequantize(a):
         }), flush=True)
 
 
+def run_rope(a):
+    """The windowed RoPE of every valid cached key on its own (API page,
+    a2ats_windowed_rope; the per-step re-rotation of the deploy-preview
+    page), 16-bit keys in and out.  HBM-bound: a row read and a row written
+    per key.  The decode workload's cache (its lengths) is far larger than
+    L2; smaller caches are flushed from L2 between calls."""
+    import query_aware_vq_gb300 as q
+
+    rank, local, world = _dist()
+    torch.cuda.set_device(local)
+    w = synth.WORKLOADS[a.workload]
+    if a.batch > 0:
+        w = synth.scaled(w, B=a.batch)
+    if w.decode_steps:
+        lens0 = synth.decode_lengths(w)
+        keys = synth.keys(synth.scaled(w, N=int(lens0.max())))
+        kd = torch.zeros((w.B, w.H, w.N, w.d), dtype=synth.DTYPES[w.dtype], device="cuda")
+        kd[:, :, :keys.shape[2]] = keys.cuda()
+        del keys
+        lengths = torch.from_numpy(lens0).cuda()
+        valid = w.H * int(lens0.sum())
+    else:
+        keys, _, _, _ = _inputs(w, rank)
+        kd = keys.cuda()
+        lengths = None
+        valid = w.B * w.H * w.N
+    out = torch.empty_like(kd)
+    rope = dict(window=w.W, far_offset=w.far_offset, rope_base=w.rope_base)
+    flush_needed = valid * w.d * kd.element_size() * 2 < 4 * L2_FLUSH_BYTES
+    flush = torch.empty(L2_FLUSH_BYTES if flush_needed else 1, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(a.warmup, 3)):
+        q.a2ats_windowed_rope(kd, lengths=lengths, out=out, **rope)
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches0 = q.kernel_launches()
+    evs = []
+    clocks = Clocks(local)
+    clocks.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q.a2ats_windowed_rope(kd, lengths=lengths, out=out, **rope)
+        e1.record(stream)
+        evs.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    ms = _max_over_ranks(sum(x.elapsed_time(y) for x, y in evs) / a.steps, world)
+    bytes_per_call = valid * w.d * (kd.element_size() + out.element_size())
+    hbm, _, src = _peaks()
+    achieved = bytes_per_call / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "keys rotated/sec (windowed RoPE of the cache)",
+            "value": world * valid / (ms * 1e-3), "unit": "keys/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; the workload's keys)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "window": w.W, "valid_keys": valid,
+                       "l2": "flushed between calls (256 MB write)" if flush_needed
+                             else "inputs larger than L2 (no flush)"},
+            "roofline": {"kernel": "windowed_rope_bh_kernel", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": None,
+                         "bytes_per_call": bytes_per_call, "peak_source": f"{src} (hbm_gbs)"},
+            "clocks": clk,
+            "gpu_launches": int(round((q.kernel_launches() - launches0) / a.steps)) * a.steps,
+        }), flush=True)
+
+
 def run_hweighted(a):
     """The H-weighted rule (API page, a2ats_h_weighted_assignment, Eq. 14-18)
     over every key of the workload's cache, with L from the workload's own
@@ -1098,6 +1174,8 @@ if __name__ == "__main__":
         run_subvector(args)
     elif args.path == "calibrate":
         run_calibrate(args)
+    elif args.path == "rope":
+        run_rope(args)
     elif synth.WORKLOADS[args.workload].decode_steps:
         run_decode(args)
     else:

@@ -336,6 +336,106 @@ cosine_score_bh_kernel(const void* __restrict__ keys, int32_t H, int32_t ncap, i
     }
 }
 
+// Windowed RoPE alone over (chunk of kBhRows rows, (b, h)) blocks for the
+// half-split pairing with d % 16 == 0: no thread walks the rows past a
+// sequence's length.  A block whose rows are all far with no far rotation
+// copies its rows (converted when the dtypes differ) four rows per thread
+// per step, every row's loads issued before the first store, so that enough
+// bytes are in flight to cover the memory latency; other blocks rotate row
+// by row as windowed_rope_kernel does, with the same arithmetic.
+template <int IN, int OUT>
+__global__ void __launch_bounds__(kRopeThreads, 3)
+windowed_rope_bh_kernel(const void* __restrict__ kin, void* __restrict__ kout, int32_t H,
+                        int32_t ncap, int32_t d, const int32_t* __restrict__ len,
+                        const RopeArgs ra) {
+    const int lpr = d / 16;
+    const int rpb = kRopeThreads / lpr;
+    const int lane = threadIdx.x % lpr;
+    const int rl = threadIdx.x / lpr;
+    const int e0 = lane * 8;
+    const int e1 = e0 + d / 2;
+    const int64_t bh = blockIdx.y;
+    const int32_t L = seq_len(len, (int32_t)(bh / H), ncap);
+    const int32_t jbeg = blockIdx.x * kBhRows;
+    if (jbeg >= L) return;  // uniform over the block
+    const int32_t jend = min(jbeg + kBhRows, L);
+    const bool far_rot = ra.enabled && ra.far_offset != 0;
+    const bool plain = !far_rot && !(ra.enabled && ra.window > 0 && (L - 1 - (jend - 1)) < ra.window);
+    if constexpr (IN != kF32) {
+        if (plain) {
+            constexpr int RPT = 4;
+            using TI = typename Elem<IN>::T;
+            for (int32_t jb = jbeg; jb < jend; jb += RPT * rpb) {
+                int32_t jr[RPT];
+                bool valid[RPT];
+                uint4 raw0[RPT], raw1[RPT];
+#pragma unroll
+                for (int u = 0; u < RPT; u++) {
+                    jr[u] = jb + rl + u * rpb;
+                    valid[u] = jr[u] < jend;
+                    if (valid[u]) {
+                        const TI* kr = reinterpret_cast<const TI*>(kin) + (bh * ncap + jr[u]) * d;
+                        raw0[u] = *reinterpret_cast<const uint4*>(kr + e0);
+                        raw1[u] = *reinterpret_cast<const uint4*>(kr + e1);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < RPT; u++) {
+                    if (!valid[u]) continue;
+                    const int64_t row = bh * ncap + jr[u];
+                    if constexpr (OUT == IN) {
+                        TI* ko = reinterpret_cast<TI*>(kout) + row * d;
+                        *reinterpret_cast<uint4*>(ko + e0) = raw0[u];
+                        *reinterpret_cast<uint4*>(ko + e1) = raw1[u];
+                    } else {
+                        float v[8];
+                        const TI* a = reinterpret_cast<const TI*>(&raw0[u]);
+#pragma unroll
+                        for (int k = 0; k < 8; k++) v[k] = to_f32<IN>(a[k]);
+                        store8<OUT>(kout, row * d + e0, v);
+                        const TI* b = reinterpret_cast<const TI*>(&raw1[u]);
+#pragma unroll
+                        for (int k = 0; k < 8; k++) v[k] = to_f32<IN>(b[k]);
+                        store8<OUT>(kout, row * d + e1, v);
+                    }
+                }
+            }
+            return;
+        }
+    }
+    float fc[8], fs[8];
+    if (far_rot) angles8<false>(ra.far_offset, e0, ra, fc, fs);
+    for (int32_t jb = jbeg; jb < jend; jb += 2 * rpb) {
+        int32_t jr[2] = {jb + rl, jb + rl + rpb};
+        bool valid[2] = {jr[0] < jend, jr[1] < jend};
+        float v0[2][8], v1[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; u++)
+            if (valid[u]) {
+                const int64_t row = bh * ncap + jr[u];
+                load8<IN>(kin, row * d + e0, v0[u]);
+                load8<IN>(kin, row * d + e1, v1[u]);
+            }
+#pragma unroll
+        for (int u = 0; u < 2; u++) {
+            if (!valid[u]) continue;
+            const int64_t row = bh * ncap + jr[u];
+            if (ra.enabled) {
+                const bool near = ra.window > 0 && (L - 1 - jr[u]) < ra.window;
+                if (near) {
+                    float c[8], sn[8];
+                    angles8<false>(jr[u], e0, ra, c, sn);
+                    rotate8<false>(v0[u], v1[u], c, sn);
+                } else if (far_rot) {
+                    rotate8<false>(v0[u], v1[u], fc, fs);
+                }
+            }
+            store8<OUT>(kout, row * d + e0, v0[u]);
+            store8<OUT>(kout, row * d + e1, v1[u]);
+        }
+    }
+}
+
 int grid_for(int64_t work_items, int per_block) {
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
@@ -356,6 +456,11 @@ cudaError_t rope_dispatch_out(const void* kin, void* kout, const Shape& s, const
                                               st>>>(kin, kout, rows, (int32_t)s.H,
                                                     (int32_t)s.Ncap, d, len, ra);
                                                     note_launches(1);
+    } else if (d % 16 == 0 && d / 16 <= 32) {
+        dim3 grid((unsigned)((s.Ncap + kBhRows - 1) / kBhRows), (unsigned)(s.B * s.H));
+        windowed_rope_bh_kernel<IN, OUT><<<grid, kRopeThreads, 0, st>>>(
+            kin, kout, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra);
+        note_launches(1);
     } else if (d % 16 == 0) {
         const int lpr = d / 16;
         windowed_rope_kernel<IN, OUT, false><<<grid_for(rows, kRopeThreads / lpr), kRopeThreads,
