@@ -62,7 +62,7 @@ METRIC = "keys assigned/sec (windowed RoPE + H-weighted VQ argmin); % of rooflin
 # profiles/ names the command).  It holds only for the contraction source it
 # was taken on (the first 16 hex digits of the sha256 of csrc/assign_tc.cu);
 # for any other source the bench reports null.
-TC_TRAFFIC = {"llama32_3b_layer": ("74f90b6c4511056f", 87362048)}
+TC_TRAFFIC = {"llama32_3b_layer": ("658832b0770f7b11", 87563264)}
 DEFAULT_WORKLOAD = "llama32_3b_layer"
 L2_FLUSH_BYTES = 256 << 20
 # the timed region lasts at least this long (untimed replays between the
