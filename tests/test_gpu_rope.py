@@ -34,6 +34,10 @@ CASES = [
     (1, 1, 90, 32, "f32", 7, 5, 10000.0, True),
     (2, 2, 77, 24, "f32", 9, 0, 10000.0, False),
     (1, 1, 40, 8, "bf16", 3, 11, 100.0, True),
+    # several 1024-row chunks per (b, h): chunks of far rows only beside the
+    # chunk that holds the window, and far rows rotated by far_offset
+    (2, 2, 2600, 128, "bf16", 100, 0, 500000.0, False),
+    (2, 1, 2100, 64, "f16", 50, 7, 10000.0, False),
 ]
 
 

@@ -88,6 +88,11 @@ def test_split_full_size(name):
     (2, 1, 300, 128, "bf16", "bf16", 0.3, dict(window=40, rope_base=10000.0, interleaved=1)),
     (1, 2, 300, 24, "f32", "f32", 0.3, dict(window=8, rope_base=10000.0)),   # no fused form
     (1, 1, 5, 16, "bf16", "bf16", 0.5, dict(window=2, rope_base=10000.0)),
+    # several 1024-row chunks per (b, h): chunks of far rows only (copied
+    # as loaded, or converted) beside the chunk that holds the window
+    (2, 2, 2600, 128, "bf16", "bf16", 0.1, dict(window=64, rope_base=500000.0)),
+    (1, 1, 2600, 128, "bf16", "f32", 0.1, dict(window=64, rope_base=500000.0)),
+    (1, 1, 2100, 64, "f16", "f16", 0.2, dict(window=16, far_offset=5, rope_base=10000.0)),
 ])
 def test_rotated_split_equals_the_two_calls(case):
     """The one-pass call writes exactly what a2ats_windowed_rope and
