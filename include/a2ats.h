@@ -213,6 +213,27 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * a2ats_query_aware_assign_reuse -- a2ats_query_aware_assign without the
+ * codebook side (no counterpart on the pages: the codebook is a per-layer
+ * artifact, and a decode loop that assigns its new keys at every step needs
+ * the decoded centroids and their norms once).  It takes the decoded fp32
+ * centroids, |c|^2 / 2 and |c| (for beta = 1 also the contraction's planes
+ * and tables) from the workspace, where the last a2ats_query_aware_assign
+ * call on it left them.  The caller guarantees that that call had the same
+ * codebook contents, dtype, B, H, Ncap, d, K, beta (1 or not), fused_rope
+ * and rows, and that nothing but a2ats_query_aware_assign_reuse calls has
+ * used the workspace since; otherwise the codes are unspecified (no error is
+ * detected).  Arguments, results and errors are otherwise those of
+ * a2ats_query_aware_assign (codebook is only checked, not read).
+ * ------------------------------------------------------------------------ */
+int a2ats_query_aware_assign_reuse(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                   int64_t Ncap, int64_t d, const int32_t* len,
+                                   const void* codebook, int64_t K, const void* query,
+                                   double beta, const a2ats_rope_params* fused_rope, int32_t rows,
+                                   const int32_t* perm, const int32_t* count, int32_t* codes,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * a2ats_select_retrieval_set -- [API] a2ats_select_retrieval_set: per
  * (sequence, head), score s_i = cos(k~_i, query) (0 when a norm is 0) and
  * keep the top n_r = ceil(fraction * len) rows, ordered by (score desc,

@@ -61,6 +61,8 @@ _SIGS = {
     "a2ats_query_aware_assign_workspace_size": [_I64, _I64, _I64, _I64, _I64],
     "a2ats_query_aware_assign": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _D, _P,
                                  _I32, _P, _P, _P, _P, _SZ, _P],
+    "a2ats_query_aware_assign_reuse": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _I64, _P, _D,
+                                       _P, _I32, _P, _P, _P, _P, _SZ, _P],
     "a2ats_select_retrieval_set_workspace_size": [_I64, _I64, _I64, _I64],
     "a2ats_select_retrieval_set": [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _D, _P, _P, _P, _P,
                                    _SZ, _P],
@@ -319,9 +321,12 @@ def a2ats_h_weighted_assign(x, codebook, L=None, *, lengths=None, rope=None, row
 
 def a2ats_query_aware_assign(x, codebook, query=None, beta: float = 0.5, *, lengths=None,
                              rope=None, rows="all", perm=None, count=None, codes=None,
-                             workspace=None, stream=None):
+                             workspace=None, stream=None, reuse=False):
     """Cosine-blend assignment; query [B, H, d], or None for the proxy query
-    (the key at the decode position after windowed RoPE)."""
+    (the key at the decode position after windowed RoPE).  reuse=True calls
+    a2ats_query_aware_assign_reuse: the codebook side is the one the last
+    call on `workspace` left (same codebook, shapes, beta = 1 or not, rope
+    and rows), so a workspace must be given."""
     _dev(x, codebook, query, lengths, perm, count, codes)
     x4, cb, K, codes = _assign_common(x, codebook, codes)
     B, H, N, d = x4.shape
@@ -331,7 +336,10 @@ def a2ats_query_aware_assign(x, codebook, query=None, beta: float = 0.5, *, leng
     ws, nb = _workspace(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K), x.device,
                         workspace, stream)
     rp = _rope(rope)
-    _check("a2ats_query_aware_assign", lib.a2ats_query_aware_assign(
+    if reuse and workspace is None:
+        raise ValueError("reuse=True needs the workspace the codebook side was built in")
+    name = "a2ats_query_aware_assign_reuse" if reuse else "a2ats_query_aware_assign"
+    _check(name, getattr(lib, name)(
         _ptr(x4), _dt(x4), B, H, N, d, _ptr(_lens(lengths)), _ptr(cb), K, _ptr(query),
         float(beta), ctypes.byref(rp) if rp is not None else None, A2ATS_ROWS[rows], _ptr(perm),
         _ptr(count), _ptr(codes), _ptr(ws), nb, _stream(stream)))

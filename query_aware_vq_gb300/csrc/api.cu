@@ -425,12 +425,15 @@ size_t a2ats_query_aware_assign_workspace_size(int64_t B, int64_t H, int64_t Nca
     return a2ats_h_weighted_assign_workspace_size(B, H, Ncap, d, K);
 }
 
-int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
-                             int64_t d, const int32_t* len, const void* codebook, int64_t K,
-                             const void* query, double beta, const a2ats_rope_params* fused_rope,
-                             int32_t rows, const int32_t* perm, const int32_t* count,
-                             int32_t* codes, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+namespace {
+// The cosine blend; reuse: the codebook side (decoded centroids, their
+// norms and |c|^2 / 2, and for beta = 1 the contraction's planes and
+// tables) is the one the last call on this workspace left.
+int query_aware(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap, int64_t d,
+                const int32_t* len, const void* codebook, int64_t K, const void* query,
+                double beta, const a2ats_rope_params* fused_rope, int32_t rows,
+                const int32_t* perm, const int32_t* count, int32_t* codes, void* workspace,
+                size_t workspace_bytes, void* stream, bool reuse) {
     int st = check_assign_common(x, dtype, B, H, Ncap, d, codebook, K, rows, perm, count, codes);
     if (st) return st;
     if (!unit_interval(beta)) return A2ATS_ERR_INVALID_ARG;
@@ -446,28 +449,56 @@ int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H,
     cudaStream_t s = (cudaStream_t)stream;
     const Shape sh{B, H, Ncap, d};
     // decoded fp32 centroids (and |c|^2 / 2) for either rule
-    cudaError_t e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, nullptr, w.cp,
-                                              w.half_norm, nullptr, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    cudaError_t e = cudaSuccess;
+    if (!reuse) {
+        e = launch_codebook_transform(codebook, dtype, H, K, d, nullptr, nullptr, w.cp,
+                                      w.half_norm, nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     if (beta == 1.0) {
         // beta = 1 is plain nearest-centroid VQ: the same argmin as the
         // H-weighted rule with L = I, so it reduces exactly by construction
-        if (tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30))
+        if (tc_supported(dtype, d) && 2 * B * H * Ncap < (int64_t(1) << 30)) {
+            w.tc.prepared = reuse;
             e = assign_on_tensor_cores(w, dtype, sh, len, x, codebook, K, nullptr, ra,
                                        RowSel{rows, perm, count}, codes, s);
-        else
+        } else {
             e = launch_assign_exact(x, dtype, sh, len, ra, RowSel{rows, perm, count}, nullptr,
                                     w.cp, w.half_norm, K, codes, s);
+        }
         return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
     }
-    e = launch_centroid_norms(codebook, dtype, H, K, d, w.cnorm, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (!reuse) {
+        e = launch_centroid_norms(codebook, dtype, H, K, d, w.cnorm, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     // the per-(b, h) query: decoded as given, or the proxy k~ at t
     e = launch_prepare_query(x, query, dtype, sh, len, ra, w.q, w.qnorm, s);
     if (e != cudaSuccess) return cuda_fail(e);
     e = launch_assign_blend(x, w.cp, dtype, sh, len, ra, RowSel{rows, perm, count}, w.q,
                             w.qnorm, (float)beta, K, w.cnorm, codes, s);
     return e == cudaSuccess ? A2ATS_OK : cuda_fail(e);
+}
+}  // namespace
+
+int a2ats_query_aware_assign(const void* x, int32_t dtype, int64_t B, int64_t H, int64_t Ncap,
+                             int64_t d, const int32_t* len, const void* codebook, int64_t K,
+                             const void* query, double beta, const a2ats_rope_params* fused_rope,
+                             int32_t rows, const int32_t* perm, const int32_t* count,
+                             int32_t* codes, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    return query_aware(x, dtype, B, H, Ncap, d, len, codebook, K, query, beta, fused_rope, rows,
+                       perm, count, codes, workspace, workspace_bytes, stream, false);
+}
+
+int a2ats_query_aware_assign_reuse(const void* x, int32_t dtype, int64_t B, int64_t H,
+                                   int64_t Ncap, int64_t d, const int32_t* len,
+                                   const void* codebook, int64_t K, const void* query,
+                                   double beta, const a2ats_rope_params* fused_rope, int32_t rows,
+                                   const int32_t* perm, const int32_t* count, int32_t* codes,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    return query_aware(x, dtype, B, H, Ncap, d, len, codebook, K, query, beta, fused_rope, rows,
+                       perm, count, codes, workspace, workspace_bytes, stream, true);
 }
 
 size_t a2ats_select_retrieval_set_workspace_size(int64_t B, int64_t H, int64_t Ncap, int64_t d) {

@@ -243,14 +243,21 @@ class A2ATSDecodeStep:
         self.perm = torch.empty((B, H, N), dtype=torch.int32, device=dev)
         self.count = torch.empty((B, H), dtype=torch.int32, device=dev)
         self.codes = torch.full((B, H, N), -1, dtype=torch.int32, device=dev)
+        # the split's scratch and the assignment's (which keeps the codebook
+        # side between steps) in workspaces of their own
+        self.workspace = torch.empty(lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d),
+                                     dtype=torch.uint8, device=dev)
         ws = max(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
-                 lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K),
-                 lib.a2ats_select_retrieval_set_workspace_size(B, H, N, d))
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+                 lib.a2ats_h_weighted_assign_workspace_size(B, H, N, d, K))
+        self.assign_workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
 
-    def __call__(self, cache, lengths, new_keys, codebook, L=None, stream=None, events=None):
+    def __call__(self, cache, lengths, new_keys, codebook, L=None, stream=None, events=None,
+                 reuse_codebook=False):
+        """reuse_codebook=True takes the codebook side (decoded centroids,
+        norms; with L its transform and planes) that the previous call built:
+        the caller guarantees the same codebook (and L) as that call."""
         st = stream if stream is not None else torch.cuda.current_stream()
-        ws = self.workspace
+        ws, wa = self.workspace, self.assign_workspace
 
         def stage(name, fn, *a, **kw):
             if events is None:
@@ -268,11 +275,12 @@ class A2ATSDecodeStep:
               count=self.count, workspace=ws, stream=st)
         if L is not None:
             stage("assign_new", a2ats_h_weighted_assign, cache, codebook, L, lengths=lengths,
-                  rope=self.rope, rows="last", codes=self.codes, workspace=ws, stream=st)
+                  rope=self.rope, rows="last", codes=self.codes, workspace=wa, stream=st,
+                  reuse=reuse_codebook)
         else:
             stage("assign_new", a2ats_query_aware_assign, cache, codebook, None, self.beta,
-                  lengths=lengths, rope=self.rope, rows="last", codes=self.codes, workspace=ws,
-                  stream=st)
+                  lengths=lengths, rope=self.rope, rows="last", codes=self.codes, workspace=wa,
+                  stream=st, reuse=reuse_codebook)
         return self
 
 

@@ -75,11 +75,12 @@ def test_assign_validation(lib):
     assert f(*args(x=FAKE + 4)) == -4
     assert f(*args(ws=None)) == -6
     assert f(*args(wsb=16)) == -6
-    g = lib.a2ats_query_aware_assign
-    base = [FAKE, 1, 1, 2, 64, 128, None, FAKE, 16, None]
-    tail = [None, 0, None, None, FAKE, FAKE, 1 << 30, None]
-    for beta in (-0.1, 1.5, float("nan")):
-        assert g(*base, beta, *tail) == -1
+    for g in (lib.a2ats_query_aware_assign, lib.a2ats_query_aware_assign_reuse):
+        base = [FAKE, 1, 1, 2, 64, 128, None, FAKE, 16, None]
+        tail = [None, 0, None, None, FAKE, FAKE, 1 << 30, None]
+        for beta in (-0.1, 1.5, float("nan")):
+            assert g(*base, beta, *tail) == -1
+        assert g(*base, 0.5, None, 0, None, None, FAKE, None, 0, None) == -6  # no workspace
 
 
 def test_split_and_calibration_validation(lib):

@@ -220,3 +220,35 @@ def test_reuse_takes_the_codebook_side_from_the_workspace(dt, d, withL, rows, ro
                     n, cnt = int(lens[b]), int(count[b, h])
                     sel = perm[b, h, :cnt] if rows == "retrieval" else perm[b, h, cnt:n]
                     assert torch.equal(got[b, h, sel.long()], want[b, h, sel.long()])
+
+
+@pytest.mark.parametrize("dt,d,beta,rows,rope", [
+    ("bf16", 128, 0.7, "last", dict(window=40, far_offset=0, rope_base=500000.0)),
+    ("bf16", 128, 0.7, "all", dict(window=40, far_offset=0, rope_base=500000.0)),
+    ("bf16", 128, 1.0, "all", dict(window=40, far_offset=0, rope_base=500000.0)),  # tensor cores
+    ("f32", 48, 0.5, "all", None),
+])
+def test_blend_reuse_takes_the_codebook_side_from_the_workspace(dt, d, beta, rows, rope):
+    """The cosine blend with reuse gives, on new keys, the codes a full call
+    gives (the decoded centroids and norms, or for beta = 1 the planes, come
+    from the workspace)."""
+    B, H, N, K = 2, 2, 400, 90
+    c = dev(synth.gaussian((H, K, d), seed=51, dtype=dt, scale=2.0))
+    lens = dev(torch.tensor([N, N - 33], dtype=torch.int32))
+    lib = q.library()
+    ws = torch.empty(lib.a2ats_query_aware_assign_workspace_size(B, H, N, d, K),
+                     dtype=torch.uint8, device="cuda")
+    for step, seed in enumerate((53, 54, 55)):
+        x = dev(synth.gaussian((B, H, N, d), seed=seed, dtype=dt, scale=2.0))
+        kw = dict(lengths=lens, rope=rope, rows=rows)
+        want = q.a2ats_query_aware_assign(x, c, None, beta, **kw)
+        got = torch.full_like(want, -5)
+        got = q.a2ats_query_aware_assign(x, c, None, beta, codes=got, workspace=ws,
+                                         reuse=step > 0, **kw)
+        torch.cuda.synchronize()
+        for b in range(B):
+            n = int(lens[b])
+            if rows == "last":
+                assert torch.equal(got[b, :, n - 1], want[b, :, n - 1])
+            else:
+                assert torch.equal(got[b, :, :n], want[b, :, :n])
