@@ -71,7 +71,8 @@ __device__ __forceinline__ void angles8(int32_t pos, int pair0, const RopeArgs& 
         rope_angle(pos, ra.omega_hi[pair0 + k], ra.omega_lo[pair0 + k], ra, s[k], c[k]);
 }
 
-// One pass over every valid row: k_out = windowed RoPE of k_in.
+// One pass over every valid row: k_out = windowed RoPE of k_in (launched for
+// the interleaved pairing; the half-split one takes windowed_rope_bh_kernel).
 template <int IN, int OUT, bool INTERLEAVED>
 __global__ void __launch_bounds__(kRopeThreads)
 windowed_rope_kernel(const void* __restrict__ kin, void* __restrict__ kout, int64_t rows,
@@ -456,17 +457,11 @@ cudaError_t rope_dispatch_out(const void* kin, void* kout, const Shape& s, const
                                               st>>>(kin, kout, rows, (int32_t)s.H,
                                                     (int32_t)s.Ncap, d, len, ra);
                                                     note_launches(1);
-    } else if (d % 16 == 0 && d / 16 <= 32) {
+    } else if (d % 16 == 0) {  // d <= kMaxD: d / 16 lanes per row fit a warp
         dim3 grid((unsigned)((s.Ncap + kBhRows - 1) / kBhRows), (unsigned)(s.B * s.H));
         windowed_rope_bh_kernel<IN, OUT><<<grid, kRopeThreads, 0, st>>>(
             kin, kout, (int32_t)s.H, (int32_t)s.Ncap, d, len, ra);
         note_launches(1);
-    } else if (d % 16 == 0) {
-        const int lpr = d / 16;
-        windowed_rope_kernel<IN, OUT, false><<<grid_for(rows, kRopeThreads / lpr), kRopeThreads,
-                                               0, st>>>(kin, kout, rows, (int32_t)s.H,
-                                                        (int32_t)s.Ncap, d, len, ra);
-                                                        note_launches(1);
     } else {
         windowed_rope_scalar_kernel<IN, OUT><<<grid_for(rows * (d / 2), kRopeThreads),
                                                kRopeThreads, 0, st>>>(
